@@ -1,0 +1,163 @@
+"""float64 CPU oracle for the projection operators (test infrastructure).
+
+This package is a checker, not part of the product: only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it.  The arithmetic lives in ``tp_oracle.c`` (plain C, OpenMP); this
+module compiles it with gcc on first use and marshals numpy arrays.
+
+All inputs are up-cast to float64 / complex128 before the call, so the oracle
+sees the same values as the CUDA path and evaluates them in double precision.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tp_oracle.c")
+_LIB = os.path.join(_HERE, "libtp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+LINEAR, CUBIC = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile tp_oracle.c into libtp_oracle.so next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-Wall",
+             "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # TP_ORACLE_LIB lets the oracle's own mutation test load a
+            # deliberately broken build; nothing else sets it.
+            lib = ctypes.CDLL(os.environ.get("TP_ORACLE_LIB") or build())
+            d, i, p = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+            lib.oracle_project.argtypes = [i, p, i, i, p, i, i, p, i, i, i, d, d, p]
+            lib.oracle_backproject.argtypes = [i, p, p, i, i, i, p, i, p, i, i, i, i, d, d, p, p]
+            lib.oracle_project_backward.argtypes = [i, p, p, i, i, p, i, i, p, i, i, i, d, d, p, p, p]
+            for f in (lib.oracle_project, lib.oracle_backproject, lib.oracle_project_backward):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _c(a, dtype):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _interp(interp):
+    if interp in ("linear", LINEAR):
+        return LINEAR
+    if interp in ("cubic", CUBIC):
+        return CUBIC
+    raise ValueError(f"unknown interpolation {interp!r}")
+
+
+def _batch(*bs):
+    B = max(bs)
+    for b in bs:
+        if b not in (1, B):
+            raise ValueError(f"batch sizes {bs} do not broadcast")
+    return B
+
+
+def _check(rc):
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+
+
+def project(dim, src, rot, shift=None, N=None, interp="linear", oversampling=1.0, radius=-1.0):
+    """Forward projection of a (Bsrc, M[, M], M, M/2+1) spectrum.
+
+    dim=3: 3D->2D central slices; dim=2: 2D->2D rotation.  rot is
+    (Bp, P, dim, dim), shift (Bs, P, 2) or None.  Returns (B, P, N, N/2+1)
+    complex128.
+    """
+    src = _c(src, np.complex128)
+    rot = _c(rot, np.float64)
+    shift = _c(shift, np.float64)
+    Bsrc, M = src.shape[0], src.shape[1]
+    Bp, P = rot.shape[0], rot.shape[1]
+    Bs = shift.shape[0] if shift is not None else 1
+    N = M if N is None else int(N)
+    B = _batch(Bsrc, Bp, Bs)
+    out = np.zeros((B, P, N, N // 2 + 1), np.complex128)
+    _check(_load().oracle_project(dim, _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs,
+                                  N, _interp(interp), float(oversampling), float(radius), _ptr(out)))
+    return out
+
+
+def backproject(dim, img, rot, shift=None, M=None, weights=None, interp="linear",
+                oversampling=1.0, radius=-1.0, Bdst=1, want_weights=True):
+    """Adjoint of project(): scatter (B, P, N, N/2+1) images into a spectrum.
+
+    Returns (data, weight) with shapes (Bdst, M[, M], M, M/2+1); weight is
+    None when want_weights is False.
+    """
+    img = _c(img, np.complex128)
+    rot = _c(rot, np.float64)
+    shift = _c(shift, np.float64)
+    weights = _c(weights, np.float64)
+    B, P, N = img.shape[0], img.shape[1], img.shape[2]
+    M = N if M is None else int(M)
+    Bp = rot.shape[0]
+    Bs = shift.shape[0] if shift is not None else 1
+    X = M // 2 + 1
+    shp = (Bdst, M, M, X) if dim == 3 else (Bdst, M, X)
+    data = np.zeros(shp, np.complex128)
+    wt = np.zeros(shp, np.float64) if want_weights else None
+    _check(_load().oracle_backproject(dim, _ptr(img), _ptr(weights), B, P, N, _ptr(rot), Bp,
+                                      _ptr(shift), Bs, Bdst, M, _interp(interp),
+                                      float(oversampling), float(radius), _ptr(data), _ptr(wt)))
+    return data, wt
+
+
+def project_backward(dim, grad_out, src, rot, shift=None, interp="linear", oversampling=1.0,
+                     radius=-1.0, need_src=True, need_rot=True, need_shift=True):
+    """Gradients through project() for upstream grad_out (B, P, N, N/2+1).
+
+    Returns (grad_src, grad_rot, grad_shift); entries not requested (or
+    grad_shift without a shift) are None.
+    """
+    grad_out = _c(grad_out, np.complex128)
+    src = _c(src, np.complex128)
+    rot = _c(rot, np.float64)
+    shift = _c(shift, np.float64)
+    B, P, N = grad_out.shape[0], grad_out.shape[1], grad_out.shape[2]
+    Bsrc, M = src.shape[0], src.shape[1]
+    Bp = rot.shape[0]
+    Bs = shift.shape[0] if shift is not None else 1
+    gsrc = np.zeros_like(src) if need_src else None
+    grot = np.zeros_like(rot) if need_rot else None
+    gshift = np.zeros_like(shift) if (need_shift and shift is not None) else None
+    _check(_load().oracle_project_backward(dim, _ptr(grad_out), _ptr(src), Bsrc, M, _ptr(rot), Bp, P,
+                                           _ptr(shift), Bs, N, _interp(interp),
+                                           float(oversampling), float(radius),
+                                           _ptr(gsrc), _ptr(grot), _ptr(gshift)))
+    return gsrc, grot, gshift

@@ -1,0 +1,55 @@
+"""The oracle's pins reject plausible mistakes.
+
+Each case compiles a copy of the oracle with one planted error (on the CPU,
+in a temporary directory) and runs the pin suite against it in a child
+process; every mutant must make the pins fail.  This shows that the pins
+constrain the oracle rather than restate it.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "tp_oracle.c")
+
+MUTANTS = {
+    "rotation-transposed": ("p[j] = s * (R[0 * dim + j] * kx + R[1 * dim + j] * ky);",
+                            "p[j] = s * (R[j * dim + 0] * kx + R[j * dim + 1] * ky);"),
+    "phase-sign": ("double ang = -2.0 * M_PI", "double ang = 2.0 * M_PI"),
+    "friedel-read-no-conj": ("if (cj)\n                    v = cconj(v);", ""),
+    "friedel-reflect-x-only": ("m[1] = -m[1];\n        m[2] = -m[2];", ""),
+    "cubic-tap-offset": ("tap[j] = x0 - 1 + j;", "tap[j] = x0 + j;"),
+    "keys-a": ("const double a = -0.5;\n    double u = fabs(t);\n    if (u <= 1.0)\n        return (a + 2.0)",
+               "const double a = -0.75;\n    double u = fabs(t);\n    if (u <= 1.0)\n        return (a + 2.0)"),
+    "adjoint-friedel-no-conj": ("double im = wt * (cj ? -c.im : c.im);", "double im = wt * c.im;"),
+    "adjoint-phase-not-conj": ("cplx c = cmul(cconj(phase_of(t, kx, ky, N)), yk);",
+                               "cplx c = cmul(phase_of(t, kx, ky, N), yk);"),
+    "grad-shift-sign": ("cplx dy = {0.0, -2.0 * M_PI * k[a] / (double)N};",
+                        "cplx dy = {0.0, 2.0 * M_PI * k[a] / (double)N};"),
+    "linear-derivative": ("dw[0] = -1.0;\n    dw[1] = 1.0;", "dw[0] = 1.0;\n    dw[1] = -1.0;"),
+    "keys-derivative": ("return sg * (3.0 * (a + 2.0) * u * u - 2.0 * (a + 3.0) * u);",
+                        "return sg * (3.0 * (a + 2.0) * u * u - 1.0 * (a + 3.0) * u);"),
+    "radius-exclusive": ("if (kx * kx + ky * ky > r * r)\n                    continue;\n                double p[3];\n                sample_position(R, dim, s, kx, ky, p);\n                cplx S",
+                         "if (kx * kx + ky * ky >= r * r)\n                    continue;\n                double p[3];\n                sample_position(R, dim, s, kx, ky, p);\n                cplx S"),
+    "weight-ignores-omega": ("W[e] += wt * omega;", "W[e] += wt;"),
+    "grad-rot-no-scale": ("gR[i * dim + j] += s * k[i] * d.re;", "gR[i * dim + j] += k[i] * d.re;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutant = tmp_path / "mutant.c"
+    mutant.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o", str(lib),
+                    str(mutant), "-lm"], check=True)
+    env = dict(os.environ, TP_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins accepted mutant {name}:\n{r.stdout[-2000:]}"
