@@ -1,0 +1,238 @@
+"""Python binding of libtp_b300.so, the B300 Fourier-space projection library.
+
+Argument marshalling only: every function checks tensor types, derives the
+sizes the C ABI asks for, allocates outputs with PyTorch when the caller
+passes none, and calls the ``tp_*`` entry point of the same name on the
+current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there
+is no CPU path, and importing this package fails if the library is missing.
+
+Layouts follow ``include/tp.h``: spectra are complex64 half-spectra in
+``torch.fft.rfftn`` order, rotations float32 ``(Bp, P, d, d)``, shifts float32
+``(Bs, P, 2)``.  Backward and backprojection outputs are accumulated (+=)
+into the tensors passed in (fresh zeros otherwise).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TPError", "lib", "tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
+    "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version",
+    "LINEAR", "CUBIC",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtp_b300.so")
+LINEAR, CUBIC = 0, 1
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with "
+        "`python -m backprojection_tp_project_gather_b300.build` (nvcc, sm_103a)")
+
+
+class TPOptions(ctypes.Structure):
+    _fields_ = [("interp", ctypes.c_int), ("oversampling", ctypes.c_float),
+                ("radius", ctypes.c_float), ("flags", ctypes.c_uint)]
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"tp status {status}: {message}")
+        self.status = status
+
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P, _I = ctypes.c_void_p, ctypes.c_int
+_SIGS = {
+    "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
+    "tp_project_2d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
+    "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
+    "tp_project_2d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
+    "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.tp_last_error.restype = ctypes.c_char_p
+_lib.tp_version.restype = ctypes.c_char_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ctypes handle of libtp_b300.so."""
+    return _lib
+
+
+def tp_last_error() -> str:
+    return _lib.tp_last_error().decode()
+
+
+def tp_version() -> str:
+    return _lib.tp_version().decode()
+
+
+def _opts(interp, oversampling, radius):
+    if isinstance(interp, str):
+        interp = {"linear": LINEAR, "cubic": CUBIC}[interp]
+    return TPOptions(int(interp), float(oversampling), float(radius), 0)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions (got shape {tuple(t.shape)})")
+    return t
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _call(name, *args):
+    st = getattr(_lib, name)(*args)
+    if st != 0:
+        raise TPError(st, tp_last_error())
+
+
+def _batch(*bs):
+    return max(bs)
+
+
+def _poses(rot, shift, d):
+    _need(rot, "rot", torch.float32, 4)
+    if rot.shape[2:] != (d, d):
+        raise ValueError(f"rot must be (Bp, P, {d}, {d})")
+    if shift is not None:
+        _need(shift, "shift", torch.float32, 3)
+        if shift.shape[1] != rot.shape[1] or shift.shape[2] != 2:
+            raise ValueError("shift must be (Bs, P, 2) with the rotations' P")
+    return rot.shape[0], rot.shape[1], (shift.shape[0] if shift is not None else 1)
+
+
+def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, stream):
+    _need(src, "source", torch.complex64, dim + 1)
+    Bsrc, M = src.shape[0], src.shape[1]
+    Bp, P, Bs = _poses(rot, shift, dim)
+    N = M if N is None else int(N)
+    B = _batch(Bsrc, Bp, Bs)
+    if out is None:
+        out = torch.empty((B, P, N, N // 2 + 1), dtype=torch.complex64, device=src.device)
+    _need(out, "out", torch.complex64, 4)
+    if tuple(out.shape) != (B, P, N, N // 2 + 1):
+        raise ValueError(f"out must be {(B, P, N, N // 2 + 1)}")
+    _call(name, _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+          _opts(interp, oversampling, radius), _ptr(out), _stream(stream))
+    return out
+
+
+def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius, grad_src,
+              grad_rot, grad_shift, want_src, want_rot, want_shift, stream):
+    _need(grad_out, "grad_out", torch.complex64, 4)
+    _need(src, "source", torch.complex64, dim + 1)
+    Bsrc, M = src.shape[0], src.shape[1]
+    Bp, P, Bs = _poses(rot, shift, dim)
+    N = grad_out.shape[2]
+    if want_src and grad_src is None:
+        grad_src = torch.zeros_like(src)
+    if want_rot and grad_rot is None:
+        grad_rot = torch.zeros_like(rot)
+    if want_shift and shift is not None and grad_shift is None:
+        grad_shift = torch.zeros_like(shift)
+    if grad_src is not None:
+        _need(grad_src, "grad_src", torch.complex64, dim + 1)
+        if grad_src.shape != src.shape:
+            raise ValueError("grad of the source must have the source's shape")
+    if grad_rot is not None:
+        _need(grad_rot, "grad_rot", torch.float32, 4)
+        if grad_rot.shape != rot.shape:
+            raise ValueError("grad_rot must have rot's shape")
+    if grad_shift is not None:
+        _need(grad_shift, "grad_shift", torch.float32, 3)
+        if shift is None or grad_shift.shape != shift.shape:
+            raise ValueError("grad_shift must have shift's shape")
+    _call(name, _ptr(grad_out), _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+          _opts(interp, oversampling, radius), _ptr(grad_src), _ptr(grad_rot), _ptr(grad_shift),
+          _stream(stream))
+    return grad_src, grad_rot, grad_shift
+
+
+def tp_project_3d_2d(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
+                     radius=-1.0, out=None, stream=None):
+    """Central slices (B, P, N, N/2+1) of vol (Bv, Nv, Nv, Nv/2+1); see tp.h."""
+    return _forward("tp_project_3d_2d", 3, vol, rot, shift, N, interp, oversampling, radius, out,
+                    stream)
+
+
+def tp_project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
+                     radius=-1.0, out=None, stream=None):
+    """Rotated / shifted spectra (B, P, N, N/2+1) of img (Bi, Ni, Ni/2+1); see tp.h."""
+    return _forward("tp_project_2d_2d", 2, img, rot, shift, N, interp, oversampling, radius, out,
+                    stream)
+
+
+def tp_project_3d_2d_backward(grad_out, vol, rot, shift=None, *, interp="cubic",
+                              oversampling=1.0, radius=-1.0, grad_vol=None, grad_rot=None,
+                              grad_shift=None, want_vol=True, want_rot=True, want_shift=True,
+                              stream=None):
+    """(grad_vol, grad_rot, grad_shift), accumulated into the given tensors; see tp.h."""
+    return _backward("tp_project_3d_2d_backward", 3, grad_out, vol, rot, shift, interp,
+                     oversampling, radius, grad_vol, grad_rot, grad_shift, want_vol, want_rot,
+                     want_shift, stream)
+
+
+def tp_project_2d_2d_backward(grad_out, img, rot, shift=None, *, interp="cubic",
+                              oversampling=1.0, radius=-1.0, grad_img=None, grad_rot=None,
+                              grad_shift=None, want_img=True, want_rot=True, want_shift=True,
+                              stream=None):
+    """(grad_img, grad_rot, grad_shift), accumulated into the given tensors; see tp.h."""
+    return _backward("tp_project_2d_2d_backward", 2, grad_out, img, rot, shift, interp,
+                     oversampling, radius, grad_img, grad_rot, grad_shift, want_img, want_rot,
+                     want_shift, stream)
+
+
+def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, interp="cubic",
+                         oversampling=1.0, radius=-1.0, data_vol=None, weight_vol=None,
+                         want_weights=True, stream=None):
+    """Scatter proj (B, P, N, N/2+1) into (data_vol, weight_vol) of box Nv (+=); see tp.h."""
+    _need(proj, "proj", torch.complex64, 4)
+    B, P, N = proj.shape[0], proj.shape[1], proj.shape[2]
+    Bp, Pr, Bs = _poses(rot, shift, 3)
+    if Pr != P:
+        raise ValueError("rot must have the projections' P")
+    Nv = N if Nv is None else int(Nv)
+    shape = (Bv, Nv, Nv, Nv // 2 + 1)
+    if weights is not None:
+        _need(weights, "weights", torch.float32, 4)
+        if weights.shape != proj.shape:
+            raise ValueError("weights must have proj's shape")
+    if data_vol is None:
+        data_vol = torch.zeros(shape, dtype=torch.complex64, device=proj.device)
+    if want_weights and weight_vol is None:
+        weight_vol = torch.zeros(shape, dtype=torch.float32, device=proj.device)
+    _need(data_vol, "data_vol", torch.complex64, 4)
+    if tuple(data_vol.shape) != shape:
+        raise ValueError(f"data_vol must be {shape}")
+    if weight_vol is not None:
+        _need(weight_vol, "weight_vol", torch.float32, 4)
+        if tuple(weight_vol.shape) != shape:
+            raise ValueError(f"weight_vol must be {shape}")
+    _call("tp_backproject_2d_3d", _ptr(proj), _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift),
+          Bs, Bv, Nv, _opts(interp, oversampling, radius), _ptr(data_vol), _ptr(weight_vol),
+          _stream(stream))
+    return data_vol, weight_vol

@@ -1,0 +1,218 @@
+// tp_api.cu -- the exported C ABI (include/tp.h): argument validation,
+// launch geometry and error reporting.  Every entry point validates first,
+// then enqueues its kernels on the caller's stream and returns without
+// synchronising.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/tp.h"
+#include "tp_launch.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+tp_status fail(tp_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+tp_status ok() {
+    g_err[0] = '\0';
+    return TP_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared checks and parameter set-up for every operator.
+struct Geometry {
+    tp::Params q{};
+    int dim = 3;
+    bool cubic = false;
+};
+
+tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const float *shift,
+                int Bs, int N, const tp_options &o, int Bout, Geometry &g) {
+    if (!rot) return fail(TP_ERR_NULL, "rotation pointer is NULL");
+    if (o.flags != 0) return fail(TP_ERR_UNSUPPORTED, "tp_options.flags must be 0 (got %u)", o.flags);
+    if (o.interp != TP_LINEAR && o.interp != TP_CUBIC)
+        return fail(TP_ERR_UNSUPPORTED, "interp must be TP_LINEAR or TP_CUBIC (got %d)", o.interp);
+    if (!(o.oversampling > 0.0f) || !std::isfinite(o.oversampling))
+        return fail(TP_ERR_UNSUPPORTED, "oversampling must be finite and > 0");
+    if (!std::isfinite(o.radius)) return fail(TP_ERR_UNSUPPORTED, "radius must be finite");
+    if (M < 2 || (M & 1) || N < 2 || (N & 1))
+        return fail(TP_ERR_SHAPE, "box sizes must be even and >= 2 (source %d, output %d)", M, N);
+    if (M > 4096 || N > 4096) return fail(TP_ERR_SHAPE, "box sizes above 4096 are not supported");
+    if (P < 0 || Bsrc < 1 || Bp < 1 || Bs < 1 || Bout < 1)
+        return fail(TP_ERR_SHAPE, "batch sizes must be >= 1 and P >= 0");
+    int B = Bout;
+    if (Bsrc > B) B = Bsrc;
+    if (Bp > B) B = Bp;
+    if (shift && Bs > B) B = Bs;
+    auto bc = [B](int b) { return b == 1 || b == B; };
+    if (!bc(Bsrc) || !bc(Bp) || (shift && !bc(Bs)) || !bc(Bout))
+        return fail(TP_ERR_SHAPE, "batch sizes do not broadcast (source %d, rot %d, shift %d, out %d)",
+                    Bsrc, Bp, shift ? Bs : 1, Bout);
+    if (!aligned(rot, 4) || (shift && !aligned(shift, 4)))
+        return fail(TP_ERR_ALIGN, "rotation / shift pointers must be 4-byte aligned");
+    const long long Xs = M / 2 + 1, Xo = N / 2 + 1;
+    const long long src_elems = (dim == 3 ? (long long)M * M : (long long)M) * Xs;
+    if (src_elems >= (1LL << 31)) return fail(TP_ERR_SHAPE, "source spectrum too large");
+    const long long plane = (long long)N * Xo;
+    const int threads = tp::kSampleBlock;
+    const long long tiles = (plane + threads - 1) / threads;
+    if ((long long)B * P * tiles >= (1LL << 31))
+        return fail(TP_ERR_SHAPE, "too many samples for one launch (B*P*tiles = %lld)",
+                    (long long)B * P * tiles);
+    const double r = (o.radius < 0.0f) ? 0.5 * N : (double)o.radius;
+    const double r2 = std::floor(r * r);
+    tp::Params &q = g.q;
+    q.src_stride = src_elems;
+    q.Bsrc = Bsrc;
+    q.M = M;
+    q.Xs = (int)Xs;
+    q.rot = rot;
+    q.Bp = Bp;
+    q.shift = shift;
+    q.Bs = shift ? Bs : 1;
+    q.P = P;
+    q.B = B;
+    q.N = N;
+    q.Xo = (int)Xo;
+    q.plane = (int)plane;
+    q.tiles = (int)tiles;
+    q.s = o.oversampling;
+    q.fN = (float)N;
+    q.invN = 1.0f / (float)N;
+    q.r2max = r2 > 2e9 ? 2000000000 : (int)r2;
+    g.dim = dim;
+    g.cubic = o.interp == TP_CUBIC;
+    return TP_OK;
+}
+
+tp_status launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess)
+        return fail(TP_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+tp_status check_complex(const float *p, const char *name) {
+    if (!aligned(p, 8)) return fail(TP_ERR_ALIGN, "%s must be 8-byte aligned (complex64)", name);
+    return TP_OK;
+}
+
+tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, int Bp, int P,
+                  const float *shift, int Bs, int N, tp_options opts, float *out, void *stream) {
+    if (!src || !out) return fail(TP_ERR_NULL, "source and output pointers are required");
+    Geometry g;
+    tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
+    if (st != TP_OK) return st;
+    if ((st = check_complex(src, "source")) != TP_OK || (st = check_complex(out, "out")) != TP_OK)
+        return st;
+    if (P == 0) return ok();
+    g.q.src = reinterpret_cast<const float2 *>(src);
+    return launched(tp::launch_project(dim, g.cubic, g.q, reinterpret_cast<float2 *>(out),
+                                       static_cast<cudaStream_t>(stream)),
+                    "project");
+}
+
+tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, int M,
+                   const float *rot, int Bp, int P, const float *shift, int Bs, int N,
+                   tp_options opts, float *grad_src, float *grad_rot, float *grad_shift,
+                   void *stream) {
+    if (!grad_out) return fail(TP_ERR_NULL, "grad_out is required");
+    if ((grad_rot || grad_shift) && !src)
+        return fail(TP_ERR_NULL, "the source spectrum is required for rotation / shift gradients");
+    if (grad_shift && !shift) return fail(TP_ERR_NULL, "grad_shift requested without a shift tensor");
+    Geometry g;
+    tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
+    if (st != TP_OK) return st;
+    if ((st = check_complex(grad_out, "grad_out")) != TP_OK) return st;
+    if (src && (st = check_complex(src, "source")) != TP_OK) return st;
+    if (grad_src && (st = check_complex(grad_src, "grad of the source")) != TP_OK) return st;
+    if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
+        return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
+    if (P == 0) return ok();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (grad_rot || grad_shift) {
+        g.q.src = reinterpret_cast<const float2 *>(src);
+        cudaError_t e = tp::launch_pose_grad(dim, g.cubic, g.q,
+                                             reinterpret_cast<const float2 *>(grad_out), grad_rot,
+                                             grad_shift, s);
+        if (e != cudaSuccess) return launched(e, "pose gradient");
+    }
+    if (grad_src) {
+        g.q.src = nullptr;
+        cudaError_t e = tp::launch_scatter(dim, g.cubic, g.q,
+                                           reinterpret_cast<const float2 *>(grad_out), nullptr,
+                                           reinterpret_cast<float2 *>(grad_src), nullptr, s);
+        if (e != cudaSuccess) return launched(e, "spectrum gradient");
+    }
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
+                           const float *shift, int Bs, int N, tp_options opts, float *out,
+                           void *stream) {
+    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, stream);
+}
+
+tp_status tp_project_2d_2d(const float *img, int Bi, int Ni, const float *rot, int Bp, int P,
+                           const float *shift, int Bs, int N, tp_options opts, float *out,
+                           void *stream) {
+    return forward(2, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, out, stream);
+}
+
+tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int Bv, int Nv,
+                                    const float *rot, int Bp, int P, const float *shift, int Bs,
+                                    int N, tp_options opts, float *grad_vol, float *grad_rot,
+                                    float *grad_shift, void *stream) {
+    return backward(3, grad_out, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, grad_vol, grad_rot,
+                    grad_shift, stream);
+}
+
+tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int Bi, int Ni,
+                                    const float *rot, int Bp, int P, const float *shift, int Bs,
+                                    int N, tp_options opts, float *grad_img, float *grad_rot,
+                                    float *grad_shift, void *stream) {
+    return backward(2, grad_out, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, grad_img, grad_rot,
+                    grad_shift, stream);
+}
+
+tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, int P, int N,
+                               const float *rot, int Bp, const float *shift, int Bs, int Bv,
+                               int Nv, tp_options opts, float *data_vol, float *weight_vol,
+                               void *stream) {
+    if (!proj || !data_vol) return fail(TP_ERR_NULL, "proj and data_vol are required");
+    Geometry g;
+    tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
+    if (st != TP_OK) return st;
+    if (g.q.B != B)
+        return fail(TP_ERR_SHAPE, "operand batches (%d) exceed the image batch B = %d", g.q.B, B);
+    if ((st = check_complex(proj, "proj")) != TP_OK ||
+        (st = check_complex(data_vol, "data_vol")) != TP_OK)
+        return st;
+    if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
+        return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
+    if (P == 0) return ok();
+    return launched(tp::launch_scatter(3, g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
+                                       weights, reinterpret_cast<float2 *>(data_vol), weight_vol,
+                                       static_cast<cudaStream_t>(stream)),
+                    "backproject");
+}
+
+const char *tp_last_error(void) { return g_err; }
+
+const char *tp_version(void) { return "0.1.0"; }
+
+}  // extern "C"

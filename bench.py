@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the differentiable projection step at box 256 (cubic).
+
+One step is the whole hot path over one batch: forward 3D->2D projection of a
+256^3 spectrum for 512 poses with shifts (cubic, radius 128), the L2-loss
+gradient g = 2 (y - target) against seeded noisy targets (SNR 0.1), and the
+backward pass producing dL/dR, dL/dshift and dL/dvolume.  The metric is
+Fourier samples per second (one sample = one stored output RFFT pixel) over
+forward + backward, in Gsamples/s.
+
+  python bench.py [--gpus N --steps K --warmup W]   # this library, one JSON line
+  python bench.py --impl reference                   # the float64 CPU oracle arm
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+512-pose problem against its own volume (weak scaling, no collective on the
+data path); rank 0 prints the aggregate.  The L2 is flushed (a 256 MB write)
+between timed steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = 5
+METRIC = "Fourier samples/sec (Gsamples/s) fwd+bwd at box 256 cubic; % of mem roofline"
+UNIT = "Gsamples/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample-poses", type=int, default=64,
+                    help="poses of the workload the CPU-baseline oracle leg processes")
+    ap.add_argument("--ref-poses", type=int, default=1,
+                    help="poses per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def config_dict(w, P):
+    c = synth.CONFIGS[WORKLOAD]
+    return {"workload": c["name"], "box": c["box"], "poses": P, "interp": c["interp"],
+            "oversampling": 1.0, "radius": c["radius"], "shift_px": c["shift_lim"],
+            "loss": "L2 vs noisy targets, SNR 0.1", "l2_cache": "flushed between steps (256 MB write)",
+            "samples_per_step": P * c["box"] * (c["box"] // 2 + 1)}
+
+
+def in_radius_count(N, r):
+    kx = np.arange(N // 2 + 1)[None, :]
+    ky = np.fft.fftfreq(N, 1.0 / N)[:, None]
+    return int((kx * kx + ky * ky <= r * r).sum())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline leg).
+def oracle_step(w, P):
+    import oracle
+    kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
+    vol, R, t = w["vol"], w["rot"][:, :P], w["shift"][:, :P]
+    y = oracle.project(3, vol, R, shift=t, **kw)
+    g = 2.0 * (y - w["target"][:, :P])
+    oracle.project_backward(3, g, vol, R, shift=t, **kw)
+
+
+def oracle_sample_workload(P):
+    w = synth.workload(WORKLOAD, poses=P)
+    rng = synth.streams(7000 + WORKLOAD, 1)[0]
+    w["target"] = synth.complex_normal(w["grad"].shape, rng)   # any target: the cost is the same
+    return w
+
+
+def cpu_baseline(P):
+    import oracle
+    w = oracle_sample_workload(P)
+    t0 = time.perf_counter()
+    oracle_step(w, P)
+    dt = time.perf_counter() - t0
+    samples = P * w["box"] * (w["box"] // 2 + 1)
+    return {"value": samples / dt / 1e9, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{P} of 512 poses of the box-256 step (fwd + L2 grad + bwd), float64, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    P = args.ref_poses
+    w = oracle_sample_workload(P)
+    samples = P * w["box"] * (w["box"] // 2 + 1)
+    for _ in range(args.warmup):
+        oracle_step(w, P)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, P)
+        times.append(time.perf_counter() - t0)
+    value = samples * len(times) / sum(times) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, 512),
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": value,
+                             "unit": UNIT,
+                             "sample": f"each step: {P} of the 512 poses (fwd + L2 grad + bwd)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region (NVML, read-only).
+class ClockSampler:
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4}
+
+    def __init__(self, index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            try:  # the CUDA device's own NVML handle (indices can differ)
+                uuid = str(torch.cuda.get_device_properties(index).uuid)
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(
+                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:  # noqa: BLE001
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self._reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:  # noqa: BLE001  (no NVML: report no clock record)
+            self.nv = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self._reasons(self.h)
+                for k, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(k)
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(0.01)
+
+    def __enter__(self):
+        if self.nv:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.nv:
+            self._stop.set()
+            self.t.join()
+
+    def record(self):
+        if not self.nv or not self.samples:
+            return None
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "n_samples": len(self.samples)}
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 6400.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "backprojection_tp_project_gather_b300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the sources still match."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_sha") != kernel_source_sha():
+            return None
+        return d["kernels"][kernel]["dram_bytes_per_launch"]
+    except Exception:  # noqa: BLE001
+        return None
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cpu_line = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_line = cpu_baseline(args.cpu_sample_poses)
+
+    import backprojection_tp_project_gather_b300 as tp
+
+    seed = 1000 + WORKLOAD + 100 * rank           # rank 0 = the single-GPU workload
+    w = synth.workload(WORKLOAD, seed=seed)
+    P, N = w["P"], w["box"]
+    kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
+    dev = torch.device("cuda", local)
+    vol = torch.from_numpy(w["vol"]).to(dev)
+    # Current estimates = the true poses perturbed (small rotation, ~1 px shift).
+    rng = synth.streams(seed + 50, 3)
+    R_true = torch.from_numpy(w["rot"]).to(dev)
+    t_true = torch.from_numpy(w["shift"]).to(dev)
+    axis = rng[0].standard_normal((P, 3))
+    axis /= np.linalg.norm(axis, axis=1, keepdims=True)
+    ang = np.deg2rad(2.0) * rng[0].standard_normal(P)
+    K = np.zeros((P, 3, 3))
+    K[:, 0, 1], K[:, 0, 2], K[:, 1, 2] = -axis[:, 2], axis[:, 1], -axis[:, 0]
+    K = K - K.transpose(0, 2, 1)
+    dR = (np.eye(3) + np.sin(ang)[:, None, None] * K
+          + (1 - np.cos(ang))[:, None, None] * (K @ K))
+    rot = torch.from_numpy((w["rot"][0].astype(np.float64) @ dR).astype(np.float32)[None]).to(dev)
+    shift = (t_true + torch.from_numpy(rng[1].normal(0, 1, (1, P, 2)).astype(np.float32)).to(dev))
+    # Targets: clean projections at the true poses plus noise of 10x the signal power.
+    clean = tp.tp_project_3d_2d(vol, R_true, t_true, **kw)
+    noise = torch.from_numpy(synth.complex_normal((1, P, N, N // 2 + 1), rng[2])).to(dev)
+    mask = torch.from_numpy(np.fft.fftfreq(N, 1.0 / N)[:, None] ** 2
+                            + np.arange(N // 2 + 1)[None, :] ** 2 <= w["radius"] ** 2).to(dev)
+    n_in = float(mask.sum())
+    sig_pow = (clean.abs() ** 2 * mask).sum((2, 3), keepdim=True) / n_in
+    target = clean + noise * torch.sqrt(10.0 * sig_pow) * mask
+    m2t = (-2.0 * target).contiguous()
+    del clean, noise
+
+    y = torch.empty_like(target)
+    g = torch.empty_like(target)
+    grad_vol = torch.zeros_like(vol)
+    grad_rot = torch.zeros_like(rot)
+    grad_shift = torch.zeros_like(shift)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        tp.tp_project_3d_2d(vol, rot, shift, out=y, **kw)
+        if ev:
+            ev[1].record(stream)
+        torch.add(m2t, y, alpha=2.0, out=g)                       # g = 2 (y - target)
+        grad_vol.zero_()
+        grad_rot.zero_()
+        grad_shift.zero_()
+        if ev:
+            ev[2].record(stream)
+        tp.tp_project_3d_2d_backward(g, vol, rot, shift, grad_rot=grad_rot, grad_shift=grad_shift,
+                                     want_vol=False, **kw)
+        if ev:
+            ev[3].record(stream)
+        tp.tp_project_3d_2d_backward(g, vol, rot, shift, grad_vol=grad_vol, want_rot=False,
+                                     want_shift=False, **kw)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()                                            # L2 flush, untimed
+            step(events[i])
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)]
+                    for i in range(args.steps)])                        # ms
+    step_ms = seg.sum(1)
+    total_ms = float(step_ms.sum())
+    if dist:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    samples = P * N * (N // 2 + 1)
+    value = world * samples * args.steps / (total_ms * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers: pinned inputs
+    # copied in, the step, gradients copied out, every step.
+    h_vol = vol.cpu().pin_memory()
+    h_rot, h_shift = rot.cpu().pin_memory(), shift.cpu().pin_memory()
+    h_m2t = m2t.cpu().pin_memory()
+    o_vol = torch.empty_like(h_vol).pin_memory()
+    o_rot, o_shift = torch.empty_like(h_rot).pin_memory(), torch.empty_like(h_shift).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_vol, h_rot, h_shift, h_m2t))
+    d2h = sum(t.numel() * t.element_size() for t in (o_vol, o_rot, o_shift))
+
+    def e2e_step():
+        vol.copy_(h_vol, non_blocking=True)
+        rot.copy_(h_rot, non_blocking=True)
+        shift.copy_(h_shift, non_blocking=True)
+        m2t.copy_(h_m2t, non_blocking=True)
+        step()
+        o_vol.copy_(grad_vol, non_blocking=True)
+        o_rot.copy_(grad_rot, non_blocking=True)
+        o_shift.copy_(grad_shift, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * samples * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
+
+    if rank == 0:
+        names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_gather", "volume_grad_scatter"]
+        mean_seg = seg.mean(0)
+        kern = {"project_3d_2d": (mean_seg[0], samples * 8 + vol.numel() * 8),
+                "pose_grad_gather": (mean_seg[2], samples * 8 + vol.numel() * 8),
+                "volume_grad_scatter": (mean_seg[3], samples * 8 + 2 * vol.numel() * 8)}
+        dom = max(kern, key=lambda k: kern[k][0])
+        t_ms, nbytes = kern[dom]
+        peak, peak_src = measured_peak_hbm()
+        achieved = nbytes / (t_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Gaussian-blob volume, uniform SO(3) poses, noisy targets)",
+            "config": config_dict(w, P),
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": ncu_traffic(dom),
+                         "algorithmic_bytes_per_launch": nbytes},
+            "breakdown_ms": {n: float(mean_seg[i]) for i, n in enumerate(names)},
+            "fwd_gsamples_s": samples / (mean_seg[0] * 1e-3) / 1e9,
+            "bwd_gsamples_s": samples / ((mean_seg[2] + mean_seg[3]) * 1e-3) / 1e9,
+            "in_radius_samples_per_step": P * in_radius_count(N, w["radius"]),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks.record(),
+            "cpu_baseline": cpu_line,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * tp.h -- C ABI of the B300 Fourier-space projection library (libtp_b300.so).
+ *
+ * The operators are the ones named on the summary pages of "torch-projectors:
+ * A High-Performance Differentiable Projection Library for PyTorch"
+ * (D. Tegunov, 2026), cited by language and by the section of each page's
+ * technical summary ([de §2] = German page, section 2, and so on).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions shared by every entry point
+ * ---------------------------------------------------------------------------
+ * Memory.  Every array argument is a DEVICE pointer to C-contiguous memory
+ * owned by the caller.  The library allocates nothing, keeps no state between
+ * calls except a per-thread error message, and never synchronises: each call
+ * enqueues its kernels on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) and returns.  Results are ready when the stream reaches that point.
+ *
+ * Complex arrays are interleaved (re, im) float pairs (PyTorch complex64) and
+ * must be 8-byte aligned; real arrays are float32 and 4-byte aligned.
+ *
+ * Half-spectrum layout [it §2 "Spazio di Fourier e Formati"; ar §2]:
+ *   3D spectrum of box M: (M, M, M/2+1) indexed [z][y][x];
+ *   2D spectrum / image of box N: (N, N/2+1) indexed [y][x];
+ * exactly the output of torch.fft.rfftn / rfft2 (no fftshift).  Row i of a
+ * box-M axis holds frequency i for i < M/2, else i - M.  Box sizes are even.
+ *
+ * Geometry.  Output pixel (iy, ix) has frequency k = (ix, ky(iy)).  It is
+ * sampled at p = s * R^T k (p_j = s * sum_i R[i][j] k_i, k_z = 0 in 3D): the
+ * coordinates go through the inverse rotation [ko §2 "Forward Projection"].
+ * R is row-major (3x3 or 2x2) and need not be orthogonal.  s is
+ * tp_options.oversampling.  Pixels with kx^2 + ky^2 > radius^2 are zero and
+ * scatter nothing.
+ *
+ * Interpolation [it §2 "Interpolazione"; ko §2 "보간법"]: per axis, linear
+ * (taps floor(p), floor(p)+1, w = 1-|t|) or Catmull-Rom cubic (Keys kernel,
+ * a = -1/2, taps floor(p)-1 .. floor(p)+2), t = p - tap, weight = product
+ * over axes.  Friedel reads [ar §2 "التمرير الأمامي"]: a tap n with n_x < 0
+ * reads conj(V[-n]).  Taps outside the stored range (0 <= n_x <= M/2,
+ * -M/2 <= n_y, n_z <= M/2-1) read zero.
+ *
+ * Shift [de §2 "Interpolation"; ar §2]: the sample is multiplied by
+ * exp(-2 pi i (kx sx + ky sy) / N), a real-space shift by (sx, sy) pixels.
+ *
+ * Batches [de §3 item 3].  B = max of the operand batch sizes; each operand
+ * batch (Bv / Bi, Bp, Bs) is 1 (shared by all) or B.  P poses per batch
+ * element.  Rotations are (Bp, P, d, d), shifts (Bs, P, 2) or NULL (= 0).
+ *
+ * Outputs.  Forward outputs are overwritten.  Backprojection and gradient
+ * outputs are ACCUMULATED (+=) into caller-initialised memory, so that
+ * several calls can add into one volume.  A NULL gradient pointer means
+ * "not requested".  Gradients of a broadcast operand sum over the batch.
+ * Gradients are with respect to the matrix entries and shift components
+ * [de §3 item 4]; angle or quaternion chain rules belong to the caller.
+ * Complex gradients follow PyTorch's convention: for a real loss L,
+ * grad = dL/dRe + i dL/dIm, and each backward entry point applies the real
+ * adjoint of the forward map's Jacobian.
+ *
+ * Errors.  Each call returns a tp_status.  Argument errors are detected
+ * before anything is enqueued; TP_ERR_CUDA reports a launch failure.  No
+ * C++ exception crosses this interface.  tp_last_error() returns a message
+ * for the calling thread's most recent failure.  Empty problems (P == 0)
+ * succeed without launching anything.
+ */
+#ifndef TP_B300_H
+#define TP_B300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_NULL = 1,        /* a required pointer is NULL */
+    TP_ERR_SHAPE = 2,       /* bad size, odd box, batch that does not broadcast */
+    TP_ERR_ALIGN = 3,       /* pointer not aligned to its element type */
+    TP_ERR_UNSUPPORTED = 4, /* option value not supported */
+    TP_ERR_CUDA = 5,        /* a kernel launch failed (message has the CUDA error) */
+    TP_ERR_INTERNAL = 6
+} tp_status;
+
+enum { TP_LINEAR = 0, TP_CUBIC = 1 };
+
+typedef struct {
+    int interp;         /* TP_LINEAR or TP_CUBIC */
+    float oversampling; /* s > 0: sample position p = s * R^T k */
+    float radius;       /* cutoff in output-pixel frequency units; < 0 means N/2 */
+    unsigned flags;     /* reserved, must be 0 */
+} tp_options;
+
+/*
+ * 3D -> 2D forward projection: central slices of a 3D half-spectrum
+ * [it §2 "Operazioni Supportate"; de §2 "Unterstützte Operationen" item 3;
+ * ja §2 "演算の種類"].
+ *   vol    (Bv, Nv, Nv, Nv/2+1) complex        in
+ *   rot    (Bp, P, 3, 3) float                  in
+ *   shift  (Bs, P, 2) float, or NULL            in
+ *   out    (B, P, N, N/2+1) complex             out, overwritten
+ */
+tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv,
+                           const float *rot, int Bp, int P,
+                           const float *shift, int Bs,
+                           int N, tp_options opts, float *out, void *stream);
+
+/*
+ * Gradients through tp_project_3d_2d for an upstream gradient grad_out
+ * (B, P, N, N/2+1) complex [de §2 "Differentiable Backpropagation"; ko §2
+ * "그라디언트 계산"; ar §2 "الإزاحات والدورات"].
+ *   grad_vol    (Bv, Nv, Nv, Nv/2+1) complex, += adjoint applied to grad_out
+ *   grad_rot    (Bp, P, 3, 3) float, += dL/dR (row 3 is always 0: k_z = 0)
+ *   grad_shift  (Bs, P, 2) float, += dL/dshift; requires shift != NULL
+ * Any of the three may be NULL.
+ */
+tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int Bv, int Nv,
+                                    const float *rot, int Bp, int P,
+                                    const float *shift, int Bs, int N, tp_options opts,
+                                    float *grad_vol, float *grad_rot, float *grad_shift,
+                                    void *stream);
+
+/*
+ * 2D -> 3D backprojection: the adjoint of tp_project_3d_2d scattered into a
+ * data spectrum, plus an optional real weight spectrum [it §2 "accumulo di
+ * pesi"; de §2 "Dual-Volumen-Ansatz"; ko §2 "Backward Projection"].
+ *   proj        (B, P, N, N/2+1) complex                      in
+ *   weights     (B, P, N, N/2+1) float, or NULL (= 1)         in
+ *   rot         (Bp, P, 3, 3);  shift (Bs, P, 2) or NULL      in
+ *   data_vol    (Bv, Nv, Nv, Nv/2+1) complex, +=              out
+ *   weight_vol  (Bv, Nv, Nv, Nv/2+1) float, +=, or NULL       out
+ * A direct tap adds w * conj(phase) * proj to data_vol[n]; a Friedel tap adds
+ * the conjugate of that to data_vol[-n]; weight_vol gets w * weight at the
+ * same location.  Bv is 1 (all batch elements add into one volume) or B.
+ */
+tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, int P, int N,
+                               const float *rot, int Bp, const float *shift, int Bs,
+                               int Bv, int Nv, tp_options opts,
+                               float *data_vol, float *weight_vol, void *stream);
+
+/*
+ * 2D -> 2D forward: rotated and shifted 2D half-spectra
+ * [it §2 "Operazioni Supportate"; de §2 item 1; ja §2].
+ *   img    (Bi, Ni, Ni/2+1) complex;  rot (Bp, P, 2, 2);  shift (Bs, P, 2) or NULL
+ *   out    (B, P, N, N/2+1) complex, overwritten
+ */
+tp_status tp_project_2d_2d(const float *img, int Bi, int Ni,
+                           const float *rot, int Bp, int P,
+                           const float *shift, int Bs,
+                           int N, tp_options opts, float *out, void *stream);
+
+/*
+ * Gradients through tp_project_2d_2d [de §2 item 4 "2D -> 2D Backward"].
+ *   grad_img    (Bi, Ni, Ni/2+1) complex, +=
+ *   grad_rot    (Bp, P, 2, 2) float, +=
+ *   grad_shift  (Bs, P, 2) float, +=; requires shift != NULL
+ */
+tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int Bi, int Ni,
+                                    const float *rot, int Bp, int P,
+                                    const float *shift, int Bs, int N, tp_options opts,
+                                    float *grad_img, float *grad_rot, float *grad_shift,
+                                    void *stream);
+
+/* Message for the calling thread's most recent failure ("" if none). */
+const char *tp_last_error(void);
+
+/* Library version as "major.minor.patch". */
+const char *tp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_B300_H */

@@ -122,6 +122,18 @@ def blob_volume(box: int, n_blobs: int, rng):
     return centred_rfft(blob_density(box, c, s, a, 3)).astype(np.complex64)[None]
 
 
+def padded_blob_volume(box: int, n_blobs: int, rng, factor: int = 2):
+    """(1, f*box, f*box, f*box/2+1) spectrum of the same blob density zero-padded
+    in real space to f times the box (draws exactly what blob_volume draws)."""
+    c, s, a = blob_params(box, n_blobs, rng, 3)
+    d = blob_density(box, c, s, a, 3)
+    big = factor * box
+    o = big // 2 - box // 2
+    dp = np.zeros((big,) * 3, np.float64)
+    dp[o:o + box, o:o + box, o:o + box] = d
+    return centred_rfft(dp).astype(np.complex64)[None]
+
+
 def blob_images(n: int, box: int, n_blobs: int, rng):
     """(n, box, box/2+1) complex64 spectra of 2D blob images (one rng draw per image)."""
     out = np.empty((n, box, box // 2 + 1), np.complex64)
@@ -131,7 +143,8 @@ def blob_images(n: int, box: int, n_blobs: int, rng):
     return out
 
 
-def workload(cfg: int, *, poses: int | None = None, seed: int | None = None):
+def workload(cfg: int, *, poses: int | None = None, seed: int | None = None,
+             oversampling: int = 1):
     """Inputs of configuration cfg as numpy arrays (seed 1000 + cfg by default).
 
     ``poses`` truncates the pose / image count.  Every per-pose draw is made
@@ -139,7 +152,9 @@ def workload(cfg: int, *, poses: int | None = None, seed: int | None = None):
     the leading prefix of the full one.
     Keys: name, box, radius, interp, oversampling, P, rot, shift (or None),
     and vol (cfg 1, 3, 5), img (cfg 2) or proj (cfg 4); grad is a seeded
-    upstream gradient for the backward checks.
+    upstream gradient for the backward checks.  For cfg 3, ``oversampling=2``
+    returns the same blob density zero-padded to twice the box (the volume the
+    operator then samples at p = 2 R^T k).
     """
     c = CONFIGS[cfg]
     seed = 1000 + cfg if seed is None else seed
@@ -148,7 +163,9 @@ def workload(cfg: int, *, poses: int | None = None, seed: int | None = None):
     out = dict(cfg=cfg, name=c["name"], box=box, radius=c["radius"], oversampling=1.0)
     if cfg in (1, 3, 5):
         P = c["poses"] if poses is None else int(poses)
-        out.update(vol=blob_volume(box, c["blobs"], r_vol), rot=random_rotations(P, r_rot)[None],
+        vol = (padded_blob_volume(box, c["blobs"], r_vol, oversampling) if oversampling > 1
+               else blob_volume(box, c["blobs"], r_vol))
+        out.update(vol=vol, rot=random_rotations(P, r_rot)[None], oversampling=float(oversampling),
                    interp=c["interp"], P=P,
                    shift=(uniform_shifts(P, c["shift_lim"], r_shift)[None] if "shift_lim" in c else None),
                    grad=noise_images(1, P, box, r_grad))

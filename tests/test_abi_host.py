@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every entry point include/tp.h declares, and
+reject bad arguments with the documented status before touching the GPU:
+every call here fails validation (or has P == 0), so nothing is launched and
+the fake pointers are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp.h")
+
+TP_OK, TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_ALIGN, TP_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from backprojection_tp_project_gather_b300 import build
+    build.build()
+    import backprojection_tp_project_gather_b300 as m
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_operator_set():
+    syms = declared_symbols()
+    for name in ("tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
+                 "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(tp):
+    lib = tp.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert re.fullmatch(r"\d+\.\d+\.\d+", tp.tp_version())
+
+
+# Fake, well-aligned device addresses: validation rejects each call first.
+A = 0x10000
+MIS = 0x10004      # 4-byte aligned, not 8-byte aligned (bad for complex64)
+
+
+def opts(tp, interp=1, s=1.0, r=-1.0, flags=0):
+    return tp.TPOptions(interp, s, r, flags)
+
+
+def proj3(tp, **kw):
+    a = dict(vol=A, Bv=1, Nv=16, rot=A, Bp=1, P=4, shift=None, Bs=1, N=16, o=opts(tp), out=A)
+    a.update(kw)
+    return tp.lib().tp_project_3d_2d(a["vol"], a["Bv"], a["Nv"], a["rot"], a["Bp"], a["P"],
+                                     a["shift"], a["Bs"], a["N"], a["o"], a["out"], None)
+
+
+def test_forward_validation(tp):
+    assert proj3(tp, vol=None) == TP_ERR_NULL
+    assert proj3(tp, out=None) == TP_ERR_NULL
+    assert proj3(tp, rot=None) == TP_ERR_NULL
+    assert proj3(tp, N=15) == TP_ERR_SHAPE
+    assert proj3(tp, Nv=17) == TP_ERR_SHAPE
+    assert proj3(tp, Nv=0) == TP_ERR_SHAPE
+    assert proj3(tp, P=-1) == TP_ERR_SHAPE
+    assert proj3(tp, Bv=2, Bp=3) == TP_ERR_SHAPE
+    assert proj3(tp, Bv=2, shift=A, Bs=3) == TP_ERR_SHAPE
+    assert proj3(tp, Nv=8192) == TP_ERR_SHAPE
+    assert proj3(tp, vol=MIS) == TP_ERR_ALIGN
+    assert proj3(tp, out=MIS) == TP_ERR_ALIGN
+    assert proj3(tp, rot=A + 2) == TP_ERR_ALIGN
+    assert proj3(tp, o=opts(tp, interp=7)) == TP_ERR_UNSUPPORTED
+    assert proj3(tp, o=opts(tp, s=0.0)) == TP_ERR_UNSUPPORTED
+    assert proj3(tp, o=opts(tp, s=float("nan"))) == TP_ERR_UNSUPPORTED
+    assert proj3(tp, o=opts(tp, r=float("inf"))) == TP_ERR_UNSUPPORTED
+    assert proj3(tp, o=opts(tp, flags=1)) == TP_ERR_UNSUPPORTED
+    assert "flags" in tp.tp_last_error()
+    # An empty problem succeeds without launching anything.
+    assert proj3(tp, P=0) == TP_OK
+    assert tp.tp_last_error() == ""
+
+
+def test_backward_validation(tp):
+    lib = tp.lib()
+    o = opts(tp)
+
+    def bwd(go=A, vol=A, shift=None, gv=A, gr=A, gs=None, P=4):
+        return lib.tp_project_3d_2d_backward(go, vol, 1, 16, A, 1, P, shift, 1, 16, o, gv, gr, gs,
+                                             None)
+    assert bwd(go=None) == TP_ERR_NULL
+    assert bwd(vol=None) == TP_ERR_NULL                 # needed for grad_rot
+    assert bwd(gs=A) == TP_ERR_NULL                     # grad_shift without shift
+    assert bwd(gv=MIS) == TP_ERR_ALIGN
+    assert bwd(P=0) == TP_OK
+    assert lib.tp_project_2d_2d_backward(A, A, 1, 15, A, 1, 4, None, 1, 16, o, A, A, None,
+                                         None) == TP_ERR_SHAPE
+
+
+def test_backprojection_validation(tp):
+    lib = tp.lib()
+    o = opts(tp)
+
+    def bp(proj=A, B=2, Bp=1, Bv=1, data=A, wv=A, P=4, weights=None):
+        return lib.tp_backproject_2d_3d(proj, weights, B, P, 16, A, Bp, None, 1, Bv, 16, o, data,
+                                        wv, None)
+    assert bp(proj=None) == TP_ERR_NULL
+    assert bp(data=None) == TP_ERR_NULL
+    assert bp(Bv=3) == TP_ERR_SHAPE                     # Bv must be 1 or B
+    assert bp(Bp=4) == TP_ERR_SHAPE                     # rotations batch larger than B
+    assert bp(data=MIS) == TP_ERR_ALIGN
+    assert bp(weights=A + 2) == TP_ERR_ALIGN
+    assert bp(P=0) == TP_OK
+    assert bp(wv=None, P=0) == TP_OK
+
+
+def test_binding_rejects_cpu_tensors(tp):
+    import torch
+    vol = torch.zeros((1, 8, 8, 5), dtype=torch.complex64)
+    rot = torch.eye(3).reshape(1, 1, 3, 3)
+    with pytest.raises(ValueError, match="CUDA"):
+        tp.tp_project_3d_2d(vol, rot)
