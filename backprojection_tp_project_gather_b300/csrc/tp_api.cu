@@ -39,7 +39,6 @@ struct Geometry {
 
 tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const float *shift,
                 int Bs, int N, const tp_options &o, int Bout, Geometry &g) {
-    if (!rot) return fail(TP_ERR_NULL, "rotation pointer is NULL");
     if (o.flags != 0) return fail(TP_ERR_UNSUPPORTED, "tp_options.flags must be 0 (got %u)", o.flags);
     if (o.interp != TP_LINEAR && o.interp != TP_CUBIC)
         return fail(TP_ERR_UNSUPPORTED, "interp must be TP_LINEAR or TP_CUBIC (got %d)", o.interp);
@@ -109,13 +108,13 @@ tp_status check_complex(const float *p, const char *name) {
 
 tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, int Bp, int P,
                   const float *shift, int Bs, int N, tp_options opts, float *out, void *stream) {
-    if (!src || !out) return fail(TP_ERR_NULL, "source and output pointers are required");
     Geometry g;
     tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
     if (st != TP_OK) return st;
+    if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
+    if (!src || !out || !rot) return fail(TP_ERR_NULL, "source, rotation and output pointers are required");
     if ((st = check_complex(src, "source")) != TP_OK || (st = check_complex(out, "out")) != TP_OK)
         return st;
-    if (P == 0) return ok();
     g.q.src = reinterpret_cast<const float2 *>(src);
     return launched(tp::launch_project(dim, g.cubic, g.q, reinterpret_cast<float2 *>(out),
                                        static_cast<cudaStream_t>(stream)),
@@ -126,19 +125,19 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
                    const float *rot, int Bp, int P, const float *shift, int Bs, int N,
                    tp_options opts, float *grad_src, float *grad_rot, float *grad_shift,
                    void *stream) {
-    if (!grad_out) return fail(TP_ERR_NULL, "grad_out is required");
-    if ((grad_rot || grad_shift) && !src)
-        return fail(TP_ERR_NULL, "the source spectrum is required for rotation / shift gradients");
-    if (grad_shift && !shift) return fail(TP_ERR_NULL, "grad_shift requested without a shift tensor");
     Geometry g;
     tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
     if (st != TP_OK) return st;
+    if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
+    if (!grad_out || !rot) return fail(TP_ERR_NULL, "grad_out and rotation pointers are required");
+    if ((grad_rot || grad_shift) && !src)
+        return fail(TP_ERR_NULL, "the source spectrum is required for rotation / shift gradients");
+    if (grad_shift && !shift) return fail(TP_ERR_NULL, "grad_shift requested without a shift tensor");
     if ((st = check_complex(grad_out, "grad_out")) != TP_OK) return st;
     if (src && (st = check_complex(src, "source")) != TP_OK) return st;
     if (grad_src && (st = check_complex(grad_src, "grad of the source")) != TP_OK) return st;
     if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
-    if (P == 0) return ok();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (grad_rot || grad_shift) {
         g.q.src = reinterpret_cast<const float2 *>(src);
@@ -193,18 +192,19 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
                                const float *rot, int Bp, const float *shift, int Bs, int Bv,
                                int Nv, tp_options opts, float *data_vol, float *weight_vol,
                                void *stream) {
-    if (!proj || !data_vol) return fail(TP_ERR_NULL, "proj and data_vol are required");
     Geometry g;
     tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
     if (st != TP_OK) return st;
     if (g.q.B != B)
         return fail(TP_ERR_SHAPE, "operand batches (%d) exceed the image batch B = %d", g.q.B, B);
+    if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
+    if (!proj || !data_vol || !rot)
+        return fail(TP_ERR_NULL, "proj, rotation and data_vol pointers are required");
     if ((st = check_complex(proj, "proj")) != TP_OK ||
         (st = check_complex(data_vol, "data_vol")) != TP_OK)
         return st;
     if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
         return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
-    if (P == 0) return ok();
     return launched(tp::launch_scatter(3, g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
                                        weights, reinterpret_cast<float2 *>(data_vol), weight_vol,
                                        static_cast<cudaStream_t>(stream)),
