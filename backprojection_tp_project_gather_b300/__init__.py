@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "TPError", "lib", "tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
     "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version",
-    "LINEAR", "CUBIC",
+    "tp_workspace_bytes", "LINEAR", "CUBIC",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -46,18 +46,22 @@ class TPError(RuntimeError):
 
 
 _lib = ctypes.CDLL(LIB_PATH)
-_P, _I = ctypes.c_void_p, ctypes.c_int
+_P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
-    "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
+    "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _Z, _P],
     "tp_project_2d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
-    "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
+    "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P,
+                                  _P, _Z, _P],
     "tp_project_2d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
-    "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P],
+    "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P, _Z,
+                             _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+_lib.tp_workspace_bytes.argtypes = [_I, _I, _I, _I, TPOptions]
+_lib.tp_workspace_bytes.restype = ctypes.c_size_t
 _lib.tp_last_error.restype = ctypes.c_char_p
 _lib.tp_version.restype = ctypes.c_char_p
 
@@ -73,6 +77,21 @@ def tp_last_error() -> str:
 
 def tp_version() -> str:
     return _lib.tp_version().decode()
+
+
+def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic"):
+    """Workspace bytes the 3D entry points need (see include/tp.h)."""
+    return int(_lib.tp_workspace_bytes(int(Bv), int(B), int(P), int(Nv), _opts(interp, 1.0, -1.0)))
+
+
+def _workspace(ws, Bv, B, P, Nv, interp, device):
+    need = tp_workspace_bytes(Bv, B, P, Nv, interp)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    if ws.device.type != "cuda" or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = ws.numel() * ws.element_size()
+    return ws, nbytes
 
 
 def _opts(interp, oversampling, radius):
@@ -125,7 +144,8 @@ def _poses(rot, shift, d):
     return rot.shape[0], rot.shape[1], (shift.shape[0] if shift is not None else 1)
 
 
-def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, stream):
+def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, stream,
+             workspace=None):
     _need(src, "source", torch.complex64, dim + 1)
     Bsrc, M = src.shape[0], src.shape[1]
     Bp, P, Bs = _poses(rot, shift, dim)
@@ -136,13 +156,17 @@ def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, s
     _need(out, "out", torch.complex64, 4)
     if tuple(out.shape) != (B, P, N, N // 2 + 1):
         raise ValueError(f"out must be {(B, P, N, N // 2 + 1)}")
-    _call(name, _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
-          _opts(interp, oversampling, radius), _ptr(out), _stream(stream))
+    args = [_ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+            _opts(interp, oversampling, radius), _ptr(out)]
+    if dim == 3:
+        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, interp, src.device)
+        args += [_ptr(ws), nbytes]
+    _call(name, *args, _stream(stream))
     return out
 
 
 def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius, grad_src,
-              grad_rot, grad_shift, want_src, want_rot, want_shift, stream):
+              grad_rot, grad_shift, want_src, want_rot, want_shift, stream, workspace=None):
     _need(grad_out, "grad_out", torch.complex64, 4)
     _need(src, "source", torch.complex64, dim + 1)
     Bsrc, M = src.shape[0], src.shape[1]
@@ -166,17 +190,24 @@ def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius
         _need(grad_shift, "grad_shift", torch.float32, 3)
         if shift is None or grad_shift.shape != shift.shape:
             raise ValueError("grad_shift must have shift's shape")
-    _call(name, _ptr(grad_out), _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
-          _opts(interp, oversampling, radius), _ptr(grad_src), _ptr(grad_rot), _ptr(grad_shift),
-          _stream(stream))
+    args = [_ptr(grad_out), _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+            _opts(interp, oversampling, radius), _ptr(grad_src), _ptr(grad_rot), _ptr(grad_shift)]
+    if dim == 3:
+        B = grad_out.shape[0]
+        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, interp, grad_out.device)
+        args += [_ptr(ws), nbytes]
+    _call(name, *args, _stream(stream))
     return grad_src, grad_rot, grad_shift
 
 
 def tp_project_3d_2d(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
-                     radius=-1.0, out=None, stream=None):
-    """Central slices (B, P, N, N/2+1) of vol (Bv, Nv, Nv, Nv/2+1); see tp.h."""
+                     radius=-1.0, out=None, workspace=None, stream=None):
+    """Central slices (B, P, N, N/2+1) of vol (Bv, Nv, Nv, Nv/2+1); see tp.h.
+
+    workspace: optional uint8 CUDA tensor of at least tp_workspace_bytes() bytes
+    (allocated per call when omitted)."""
     return _forward("tp_project_3d_2d", 3, vol, rot, shift, N, interp, oversampling, radius, out,
-                    stream)
+                    stream, workspace)
 
 
 def tp_project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
@@ -189,11 +220,11 @@ def tp_project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampli
 def tp_project_3d_2d_backward(grad_out, vol, rot, shift=None, *, interp="cubic",
                               oversampling=1.0, radius=-1.0, grad_vol=None, grad_rot=None,
                               grad_shift=None, want_vol=True, want_rot=True, want_shift=True,
-                              stream=None):
+                              workspace=None, stream=None):
     """(grad_vol, grad_rot, grad_shift), accumulated into the given tensors; see tp.h."""
     return _backward("tp_project_3d_2d_backward", 3, grad_out, vol, rot, shift, interp,
                      oversampling, radius, grad_vol, grad_rot, grad_shift, want_vol, want_rot,
-                     want_shift, stream)
+                     want_shift, stream, workspace)
 
 
 def tp_project_2d_2d_backward(grad_out, img, rot, shift=None, *, interp="cubic",
@@ -208,7 +239,7 @@ def tp_project_2d_2d_backward(grad_out, img, rot, shift=None, *, interp="cubic",
 
 def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, interp="cubic",
                          oversampling=1.0, radius=-1.0, data_vol=None, weight_vol=None,
-                         want_weights=True, stream=None):
+                         want_weights=True, workspace=None, stream=None):
     """Scatter proj (B, P, N, N/2+1) into (data_vol, weight_vol) of box Nv (+=); see tp.h."""
     _need(proj, "proj", torch.complex64, 4)
     B, P, N = proj.shape[0], proj.shape[1], proj.shape[2]
@@ -232,7 +263,8 @@ def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, 
         _need(weight_vol, "weight_vol", torch.float32, 4)
         if tuple(weight_vol.shape) != shape:
             raise ValueError(f"weight_vol must be {shape}")
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, proj.device)
     _call("tp_backproject_2d_3d", _ptr(proj), _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift),
           Bs, Bv, Nv, _opts(interp, oversampling, radius), _ptr(data_vol), _ptr(weight_vol),
-          _stream(stream))
+          _ptr(ws), nbytes, _stream(stream))
     return data_vol, weight_vol

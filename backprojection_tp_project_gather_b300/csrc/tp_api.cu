@@ -50,6 +50,8 @@ tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const
     if (M > 4096 || N > 4096) return fail(TP_ERR_SHAPE, "box sizes above 4096 are not supported");
     if (P < 0 || Bsrc < 1 || Bp < 1 || Bs < 1 || Bout < 1)
         return fail(TP_ERR_SHAPE, "batch sizes must be >= 1 and P >= 0");
+    if (dim == 3 && Bsrc > 65535)
+        return fail(TP_ERR_SHAPE, "at most 65535 distinct volumes per call (got %d)", Bsrc);
     int B = Bout;
     if (Bsrc > B) B = Bsrc;
     if (Bp > B) B = Bp;
@@ -106,8 +108,20 @@ tp_status check_complex(const float *p, const char *name) {
     return TP_OK;
 }
 
+// Workspace check for the 3D operators (the 2D ones need none).
+tp_status check_workspace(const Geometry &g, void *ws, size_t ws_bytes) {
+    if (g.dim != 3) return TP_OK;
+    const size_t need = tp::brick_workspace_bytes(g.q, g.cubic);
+    if (!ws) return fail(TP_ERR_NULL, "workspace is required (%zu bytes, see tp_workspace_bytes)", need);
+    if (!aligned(ws, 16)) return fail(TP_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (ws_bytes < need)
+        return fail(TP_ERR_SHAPE, "workspace too small: %zu bytes given, %zu needed", ws_bytes, need);
+    return TP_OK;
+}
+
 tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, int Bp, int P,
-                  const float *shift, int Bs, int N, tp_options opts, float *out, void *stream) {
+                  const float *shift, int Bs, int N, tp_options opts, float *out, void *ws,
+                  size_t ws_bytes, void *stream) {
     Geometry g;
     tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
     if (st != TP_OK) return st;
@@ -115,16 +129,19 @@ tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, 
     if (!src || !out || !rot) return fail(TP_ERR_NULL, "source, rotation and output pointers are required");
     if ((st = check_complex(src, "source")) != TP_OK || (st = check_complex(out, "out")) != TP_OK)
         return st;
+    if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
     g.q.src = reinterpret_cast<const float2 *>(src);
-    return launched(tp::launch_project(dim, g.cubic, g.q, reinterpret_cast<float2 *>(out),
-                                       static_cast<cudaStream_t>(stream)),
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2 *o = reinterpret_cast<float2 *>(out);
+    return launched(dim == 3 ? tp::launch_brick_project(g.cubic, g.q, o, ws, s)
+                             : tp::launch_project(dim, g.cubic, g.q, o, s),
                     "project");
 }
 
 tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, int M,
                    const float *rot, int Bp, int P, const float *shift, int Bs, int N,
-                   tp_options opts, float *grad_src, float *grad_rot, float *grad_shift,
-                   void *stream) {
+                   tp_options opts, float *grad_src, float *grad_rot, float *grad_shift, void *ws,
+                   size_t ws_bytes, void *stream) {
     Geometry g;
     tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
     if (st != TP_OK) return st;
@@ -138,19 +155,27 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
     if (grad_src && (st = check_complex(grad_src, "grad of the source")) != TP_OK) return st;
     if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
+    if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool binned = false;
     if (grad_rot || grad_shift) {
         g.q.src = reinterpret_cast<const float2 *>(src);
-        cudaError_t e = tp::launch_pose_grad(dim, g.cubic, g.q,
-                                             reinterpret_cast<const float2 *>(grad_out), grad_rot,
-                                             grad_shift, s);
+        const float2 *go = reinterpret_cast<const float2 *>(grad_out);
+        cudaError_t e = dim == 3
+                            ? tp::launch_brick_pose_grad(g.cubic, g.q, go, grad_rot, grad_shift, ws,
+                                                         false, s)
+                            : tp::launch_pose_grad(dim, g.cubic, g.q, go, grad_rot, grad_shift, s);
         if (e != cudaSuccess) return launched(e, "pose gradient");
+        binned = true;
     }
     if (grad_src) {
         g.q.src = nullptr;
-        cudaError_t e = tp::launch_scatter(dim, g.cubic, g.q,
-                                           reinterpret_cast<const float2 *>(grad_out), nullptr,
-                                           reinterpret_cast<float2 *>(grad_src), nullptr, s);
+        const float2 *go = reinterpret_cast<const float2 *>(grad_out);
+        float2 *gs = reinterpret_cast<float2 *>(grad_src);
+        cudaError_t e = dim == 3
+                            ? tp::launch_brick_scatter(g.cubic, g.q, go, nullptr, gs, nullptr, ws,
+                                                       binned, s)
+                            : tp::launch_scatter(dim, g.cubic, g.q, go, nullptr, gs, nullptr, s);
         if (e != cudaSuccess) return launched(e, "spectrum gradient");
     }
     return ok();
@@ -160,24 +185,36 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
 
 extern "C" {
 
+size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts) {
+    if (Bv < 1 || B < 1 || P < 1 || Nv < 2 || (Nv & 1) || Nv > 4096 || Bv > B) return 0;
+    tp::Params q{};
+    q.Bsrc = Bv;
+    q.B = B;
+    q.P = P;
+    q.M = Nv;
+    return tp::brick_workspace_bytes(q, opts.interp == TP_CUBIC);
+}
+
 tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
                            const float *shift, int Bs, int N, tp_options opts, float *out,
-                           void *stream) {
-    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, stream);
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, workspace,
+                   workspace_bytes, stream);
 }
 
 tp_status tp_project_2d_2d(const float *img, int Bi, int Ni, const float *rot, int Bp, int P,
                            const float *shift, int Bs, int N, tp_options opts, float *out,
                            void *stream) {
-    return forward(2, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, out, stream);
+    return forward(2, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, out, nullptr, 0, stream);
 }
 
 tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int Bv, int Nv,
                                     const float *rot, int Bp, int P, const float *shift, int Bs,
                                     int N, tp_options opts, float *grad_vol, float *grad_rot,
-                                    float *grad_shift, void *stream) {
+                                    float *grad_shift, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
     return backward(3, grad_out, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, grad_vol, grad_rot,
-                    grad_shift, stream);
+                    grad_shift, workspace, workspace_bytes, stream);
 }
 
 tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int Bi, int Ni,
@@ -185,13 +222,13 @@ tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int
                                     int N, tp_options opts, float *grad_img, float *grad_rot,
                                     float *grad_shift, void *stream) {
     return backward(2, grad_out, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, grad_img, grad_rot,
-                    grad_shift, stream);
+                    grad_shift, nullptr, 0, stream);
 }
 
 tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, int P, int N,
                                const float *rot, int Bp, const float *shift, int Bs, int Bv,
                                int Nv, tp_options opts, float *data_vol, float *weight_vol,
-                               void *stream) {
+                               void *workspace, size_t workspace_bytes, void *stream) {
     Geometry g;
     tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
     if (st != TP_OK) return st;
@@ -205,9 +242,11 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
         return st;
     if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
         return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
-    return launched(tp::launch_scatter(3, g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
-                                       weights, reinterpret_cast<float2 *>(data_vol), weight_vol,
-                                       static_cast<cudaStream_t>(stream)),
+    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    return launched(tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
+                                             weights, reinterpret_cast<float2 *>(data_vol),
+                                             weight_vol, workspace, false,
+                                             static_cast<cudaStream_t>(stream)),
                     "backproject");
 }
 

@@ -1,0 +1,845 @@
+// tp_brick.cu -- brick-binned kernels for the 3D operators (forward central
+// slices, rotation/shift gradients, backprojection / spectrum gradient).
+//
+// Design.  The 3D half-spectrum is viewed as a "virtual" full spectrum
+// F(n) = V[n] for n_x >= 0 and conj(V[-n]) for n_x < 0 (zero outside the
+// stored range): exactly the per-tap Friedel rule of the method
+// [ar §2 "التمرير الأمامي"; ko §2 "Friedel 대칭성 처리"].  It is tiled
+// into bricks of kBS^3 voxels.  Every output pixel q whose sample position
+// p(q) = s R^T q has floor(p) inside a brick belongs to that brick, so each
+// pixel has exactly one owner and its whole stencil (taps floor(p)-LO ..
+// floor(p)+HI) lies in the brick plus a halo of LO+HI voxels.
+//
+//  - gather (forward, pose gradients): a block stages brick+halo of F in
+//    shared memory, then every owned sample reads its 8 or 64 taps from
+//    shared memory with one branch-free code path;
+//  - scatter (backprojection, spectrum gradient): a block accumulates its
+//    samples' contributions into brick+halo accumulators in shared memory
+//    and adds them to the stored half-spectrum once per work unit (Friedel
+//    positions conjugated at -n), with vector atomics because halos of
+//    neighbouring bricks and other work units overlap.
+//
+// Binning.  Two small passes precede every operator: one thread per pose
+// computes the pose's geometry once (into the caller's workspace), then one
+// warp per (brick, 32-pose chunk) marks with a ballot which poses can reach
+// the brick: the plane spanned by a = s R[0], b = s R[1] must meet it, the
+// half-plane qx >= 0 must touch it and it must lie within the pose's reach.
+// A work unit is one brick and kGroup chunks of poses; persistent blocks take
+// units from a global counter, skip empty ones at the cost of kGroup mask
+// loads, and keep the staged brick when consecutive units share it.  For one
+// (pose, brick) pair the owned pixels form a convex polygon in k-space: its
+// rows come from the pseudo-inverse of [a b] and each row's qx interval from
+// the three slab constraints; the enumeration is a small superset and the
+// exact floor(p) test decides ownership.
+//
+// Method: "torch-projectors: A High-Performance Differentiable Projection
+// Library for PyTorch", 3D->2D projection and 2D->3D backprojection
+// [it §2 "Operazioni Supportate"; de §2 "Unterstützte Operationen"] with the
+// weight spectrum [de §2 "Dual-Volumen-Ansatz"].
+#include "tp_device.cuh"
+#include "tp_launch.h"
+
+namespace tp {
+
+namespace {
+
+constexpr int kBS = 16;          // brick edge (voxels)
+constexpr int kWarps = 8;        // warps per block
+constexpr int kThreads = 32 * kWarps;
+constexpr int kGroup = 4;        // 32-pose chunks per work unit
+constexpr int kUnitPoses = 32 * kGroup;
+constexpr float kMargin = 0.01f; // enumeration margin in voxel units
+
+template <bool CUBIC>
+struct Halo {
+    using St = Stencil<CUBIC>;
+    static constexpr int S = kBS + St::LO + St::HI;  // staged edge (19 or 17)
+    static constexpr int PX = 20;                     // shared-memory pitches
+    static constexpr int PY = 20;
+    static constexpr int ELEMS = PX * PY * S;
+};
+
+// Per-pose geometry, computed once per call.
+struct PoseGeo {
+    float a[3], b[3];   // p = a*qx + b*qy
+    float ia[3];        // 1/a_d (0 when |a_d| is negligible)
+    float u[3];         // qy = u . p for p on the plane
+    float v[3];         // qx = v . p for p on the plane
+    float n[3];         // a x b, the plane normal (unnormalised)
+    float reach;        // largest |p| of an in-radius sample
+    float sx, sy;
+    int ridx, sidx;     // pose position in rot / shift
+    int bp;             // output image index (b * P + p)
+    int degenerate;     // a and b (nearly) parallel: no pseudo-inverse
+};
+constexpr int kGeoWords = sizeof(PoseGeo) / 4;
+
+// Scratch layout inside the caller's workspace.
+struct Scratch {
+    unsigned *counters;   // work counters of the main kernels
+    PoseGeo *geo;         // B*P poses
+    unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
+    int nchunks;          // 32-pose chunks per volume
+};
+
+__device__ __forceinline__ void pose_geo(const Params &q, int b, int pi, PoseGeo &g) {
+    const Pose<3> ps = load_pose<3>(q, b, pi);
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        g.a[d] = ps.a[d];
+        g.b[d] = ps.b[d];
+        g.ia[d] = fabsf(ps.a[d]) > 1e-6f ? 1.0f / ps.a[d] : 0.0f;
+    }
+    g.n[0] = g.a[1] * g.b[2] - g.a[2] * g.b[1];
+    g.n[1] = g.a[2] * g.b[0] - g.a[0] * g.b[2];
+    g.n[2] = g.a[0] * g.b[1] - g.a[1] * g.b[0];
+    const float aa = g.a[0] * g.a[0] + g.a[1] * g.a[1] + g.a[2] * g.a[2];
+    const float bb = g.b[0] * g.b[0] + g.b[1] * g.b[1] + g.b[2] * g.b[2];
+    const float ab = g.a[0] * g.b[0] + g.a[1] * g.b[1] + g.a[2] * g.b[2];
+    const float det = aa * bb - ab * ab;
+    const bool degenerate = !(det > 1e-6f * aa * bb) || !(aa > 0.f);
+    const float id = degenerate ? 0.f : 1.0f / det;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        g.u[d] = (aa * g.b[d] - ab * g.a[d]) * id;
+        g.v[d] = (bb * g.a[d] - ab * g.b[d]) * id;
+    }
+    // |p| <= sigma_max([a b]) |q| and |q|^2 <= r2max for in-radius pixels.
+    const float hs = 0.5f * (aa + bb), hd = 0.5f * (aa - bb);
+    const float smax2 = hs + sqrtf(hd * hd + ab * ab);
+    g.reach = sqrtf(smax2 * (float)q.r2max) * 1.001f + 0.01f;
+    g.sx = ps.sx;
+    g.sy = ps.sy;
+    g.ridx = ps.ridx;
+    g.sidx = ps.sidx;
+    g.bp = b * q.P + pi;
+    g.degenerate = degenerate;
+}
+
+struct BrickBox {
+    int o[3];           // brick origin (virtual spectrum coordinates)
+    float lo[3], hi[3]; // box with margin
+};
+
+// Brick placement: index i in [0, 2S) of an axis maps centre-out to the
+// brick coordinate 0, -1, 1, -2, ... so low brick indices are the busiest
+// (central) bricks and are handed out first.
+__device__ __forceinline__ int brick_coord(int i) { return (i & 1) ? -((i + 1) >> 1) : (i >> 1); }
+
+__device__ __forceinline__ BrickBox brick_box(int linear, int nb) {
+    BrickBox bx;
+    const int ix = linear % nb, iy = (linear / nb) % nb, iz = linear / (nb * nb);
+    bx.o[0] = brick_coord(ix) * kBS;
+    bx.o[1] = brick_coord(iy) * kBS;
+    bx.o[2] = brick_coord(iz) * kBS;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        bx.lo[d] = (float)bx.o[d] - kMargin;
+        bx.hi[d] = (float)(bx.o[d] + kBS) + kMargin;
+    }
+    return bx;
+}
+
+// Can an in-radius sample of the pose have its position p in the box?  The
+// plane must meet the box, the half-plane qx >= 0 must reach it, and the box
+// must come within the pose's reach of the origin.
+__device__ __forceinline__ bool pose_reaches(const PoseGeo &g, const BrickBox &bx) {
+    float c[3], h[3], dist2 = 0.f;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        c[d] = 0.5f * (bx.lo[d] + bx.hi[d]);
+        h[d] = 0.5f * (bx.hi[d] - bx.lo[d]);
+        const float e = fmaxf(fabsf(c[d]) - h[d], 0.f);
+        dist2 += e * e;
+    }
+    if (dist2 > g.reach * g.reach) return false;
+    if (g.degenerate) return true;
+    const float cn = g.n[0] * c[0] + g.n[1] * c[1] + g.n[2] * c[2];
+    const float hn = fabsf(g.n[0]) * h[0] + fabsf(g.n[1]) * h[1] + fabsf(g.n[2]) * h[2];
+    if (fabsf(cn) > hn * 1.0001f + 1e-6f) return false;
+    const float cv = g.v[0] * c[0] + g.v[1] * c[1] + g.v[2] * c[2];
+    const float hv = fabsf(g.v[0]) * h[0] + fabsf(g.v[1]) * h[1] + fabsf(g.v[2]) * h[2];
+    return cv + hv >= -0.01f;
+}
+
+// Calls f(qx, qy, active) on every lane for groups of 32 candidate pixels:
+// a superset of the image pixels (inside the radius) whose sample position
+// lies in the box; active is false on lanes without a candidate.  Must be
+// called by a whole warp with warp-uniform arguments (f may use warp
+// collectives).
+template <class F>
+__device__ __forceinline__ void for_pixels_in_box(const PoseGeo &g, const BrickBox &bx, int N,
+                                                  int r2max, F &&f) {
+    const int lane = threadIdx.x & 31;
+    const float *lo = bx.lo, *hi = bx.hi;
+    int qy0, qy1;
+    if (g.degenerate) {
+        qy0 = -(N >> 1);
+        qy1 = (N >> 1) - 1;
+    } else {
+        float m = 0.f, e = 0.f;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            m += g.u[d] * 0.5f * (lo[d] + hi[d]);
+            e += fabsf(g.u[d]) * 0.5f * (hi[d] - lo[d]);
+        }
+        const float lo_y = fmaxf(m - e - 0.01f, -1e7f), hi_y = fminf(m + e + 0.01f, 1e7f);
+        qy0 = max((int)ceilf(lo_y), -(N >> 1));
+        qy1 = min((int)floorf(hi_y), (N >> 1) - 1);
+    }
+    const int rmax = (int)floorf(sqrtf((float)r2max));
+    qy0 = max(qy0, -rmax);
+    qy1 = min(qy1, rmax);
+    for (int base = qy0; base <= qy1; base += 32) {
+        const int qy = base + lane;
+        int xs = 0, cnt = 0;
+        if (qy <= qy1) {
+            float xl = 0.f, xh = (float)(N >> 1);
+            bool empty = false;
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                const float bd = (float)qy * g.b[d];
+                if (g.ia[d] != 0.f) {
+                    const float t1 = (lo[d] - bd) * g.ia[d], t2 = (hi[d] - bd) * g.ia[d];
+                    xl = fmaxf(xl, fminf(t1, t2));
+                    xh = fminf(xh, fmaxf(t1, t2));
+                } else if (bd < lo[d] || bd > hi[d]) {
+                    empty = true;
+                }
+            }
+            const int rr = r2max - qy * qy;
+            if (rr < 0) empty = true;
+            xh = fminf(xh, floorf(sqrtf((float)max(rr, 0))));
+            if (!empty && xl <= xh) {
+                xs = (int)ceilf(xl);
+                cnt = max(0, (int)floorf(xh) - xs + 1);
+            }
+        }
+        // Inclusive scan of the row counts across the warp.
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        const int excl = incl - cnt;
+        for (int i0 = 0; i0 < total; i0 += 32) {
+            const int i = i0 + lane;
+            // Row holding candidate i: the first lane whose inclusive count exceeds i.
+            int r = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const int t = __shfl_sync(0xffffffffu, incl, r + step - 1);
+                if (t <= i) r += step;
+            }
+            r = min(r, 31);
+            const int rx = __shfl_sync(0xffffffffu, xs, r);
+            const int re = __shfl_sync(0xffffffffu, excl, r);
+            f(rx + (i - re), base + r, i < total);
+        }
+    }
+}
+
+__device__ __forceinline__ int poses_of_volume(const Params &q) {
+    return (q.Bsrc == 1) ? q.B * q.P : q.P;
+}
+
+// Output-image index of pose i of the pose list of spectrum v.
+__device__ __forceinline__ int pose_id(const Params &q, int v, int i) {
+    return (q.Bsrc == 1) ? i : v * q.P + i;
+}
+
+// ---------------------------------------------------------------------------
+// Binning passes.
+__global__ void __launch_bounds__(256) k_pose_geometry(Params q, PoseGeo *__restrict__ geo,
+                                                       unsigned *__restrict__ counters) {
+    const int id = blockIdx.x * 256 + threadIdx.x;
+    if (id == 0)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) counters[k] = 0u;
+    if (id >= q.B * q.P) return;
+    const int b = id / q.P, pi = id - b * q.P;
+    PoseGeo g;
+    pose_geo(q, b, pi, g);
+    geo[id] = g;
+}
+
+// One warp per (volume, brick, chunk): bit l of the mask = pose 32*chunk + l
+// of the volume's list can reach the brick.
+__global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, int nchunks,
+                                                     const PoseGeo *__restrict__ geo,
+                                                     unsigned *__restrict__ masks) {
+    const int nbr = nb * nb * nb;
+    const long long total = (long long)q.Bsrc * nbr * nchunks;
+    const int Pv = poses_of_volume(q);
+    const int lane = threadIdx.x & 31;
+    for (long long w = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; w < total;
+         w += ((long long)gridDim.x * 256) >> 5) {
+        const int c = (int)(w % nchunks);
+        const long long r = w / nchunks;
+        const int j = (int)(r % nbr), v = (int)(r / nbr);
+        const int i = c * 32 + lane;
+        bool hit = false;
+        if (i < Pv) {
+            const BrickBox bx = brick_box(j, nb);
+            hit = pose_reaches(geo[pose_id(q, v, i)], bx);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (lane == 0) masks[w] = m;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shared pieces of the main kernels.
+
+// The block's current work unit: the poses that reach its brick, with their
+// geometry copied into shared memory.
+struct UnitTable {
+    PoseGeo pose[kUnitPoses];
+    int nhit;     // entries of pose[]
+    int next;     // work counter for the warps
+    int unit;     // unit index handed out by the global counter
+};
+
+// Fetch the next non-empty unit from the global counter and load its poses
+// (block-wide).  Returns false when the units are exhausted.
+__device__ __forceinline__ bool fetch_unit(const Params &q, const Scratch &sc, int nb, int slot,
+                                           UnitTable &t, int &v, int &brick) {
+    const int nbr = nb * nb * nb;
+    const int ngrp = (sc.nchunks + kGroup - 1) / kGroup;
+    const long long nunits = (long long)q.Bsrc * nbr * ngrp;
+    for (;;) {
+        if (threadIdx.x == 0) {
+            t.unit = (int)atomicAdd(sc.counters + slot, 1u);
+            t.nhit = 0;
+            t.next = 0;
+        }
+        __syncthreads();
+        const int u = t.unit;
+        if (u >= nunits) return false;
+        const int grp = u % ngrp;
+        const int r = u / ngrp;
+        brick = r % nbr;
+        v = r / nbr;
+        // Warp w lists the set bits of chunk grp * kGroup + w.
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (warp < kGroup) {
+            const int c = grp * kGroup + warp;
+            unsigned m = 0u;
+            if (c < sc.nchunks) m = __ldg(sc.masks + ((size_t)v * nbr + brick) * sc.nchunks + c);
+            int base = 0;
+            if (lane == 0 && m) base = atomicAdd(&t.nhit, __popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if ((m >> lane) & 1u) {
+                const int at = base + __popc(m & ((1u << lane) - 1u));
+                const int *src = reinterpret_cast<const int *>(sc.geo + pose_id(q, v, c * 32 + lane));
+                int *dst = reinterpret_cast<int *>(&t.pose[at]);
+                for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+            }
+        }
+        __syncthreads();
+        if (t.nhit > 0) return true;
+        __syncthreads();   // everyone has read nhit before thread 0 resets it
+    }
+}
+
+// Next listed pose for the calling warp, or -1 when the list is exhausted.
+__device__ __forceinline__ int next_pose(UnitTable &t) {
+    int k = 0;
+    if ((threadIdx.x & 31) == 0) k = atomicAdd(&t.next, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    return k < t.nhit ? k : -1;
+}
+
+__device__ __forceinline__ bool stored(int x, int y, int z, int half) {
+    return x >= 0 && x <= half && y >= -half && y < half && z >= -half && z < half;
+}
+
+// Stage brick + halo of the virtual spectrum into shared memory.  Every
+// element is one 8-byte cp.async (zero-filled outside the stored range), so
+// all copies of the block are in flight at once; elements on the Friedel
+// side (n_x < 0) are conjugated in a second pass.
+template <bool CUBIC>
+__device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X, const BrickBox &bx,
+                                      float2 *s) {
+    using H = Halo<CUBIC>;
+    const int half = M >> 1;
+    const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
+              z0 = bx.o[2] - Stencil<CUBIC>::LO;
+    for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
+        const int lx = e % H::S, ly = (e / H::S) % H::S, lz = e / (H::S * H::S);
+        int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
+        if (nx < 0) {
+            nx = -nx;
+            ny = -ny;
+            nz = -nz;
+        }
+        const bool ok = stored(nx, ny, nz, half);
+        const float2 *src = ok ? V + ((size_t)wrap_row(nz, M) * M + wrap_row(ny, M)) * X + nx : V;
+        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + (lz * H::PY + ly) * H::PX + lx);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src),
+                     "r"(ok ? 8 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    if (x0 < 0) {
+        __syncthreads();
+        const int nneg = min(-x0, H::S);   // staged columns lx < -x0 hold n_x < 0
+        for (int e = threadIdx.x; e < nneg * H::S * H::S; e += kThreads) {
+            const int lx = e % nneg, r = e / nneg;
+            const int ly = r % H::S, lz = r / H::S;
+            float2 *p = s + (lz * H::PY + ly) * H::PX + lx;
+            p->y = -p->y;
+        }
+    }
+}
+
+// Weighted sum over the stencil from staged shared memory (and derivatives).
+template <bool CUBIC, bool DERIV>
+__device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float (*w)[4],
+                                            float (*d)[4], float2 &S, float2 *dS) {
+    using H = Halo<CUBIC>;
+    constexpr int T = Stencil<CUBIC>::TAPS;
+    S = make_float2(0.f, 0.f);
+    if (DERIV)
+#pragma unroll
+        for (int a = 0; a < 3; ++a) dS[a] = make_float2(0.f, 0.f);
+    const float2 *base = s + (l[2] * H::PY + l[1]) * H::PX + l[0];
+#pragma unroll
+    for (int jz = 0; jz < T; ++jz) {
+        float2 ay = make_float2(0.f, 0.f), ayx = ay, ayy = ay;
+#pragma unroll
+        for (int jy = 0; jy < T; ++jy) {
+            const float2 *row = base + (jz * H::PY + jy) * H::PX;
+            float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+#pragma unroll
+            for (int jx = 0; jx < T; ++jx) {
+                const float2 val = row[jx];
+                cfma(w[0][jx], val, r0);
+                if (DERIV) cfma(d[0][jx], val, r1);
+            }
+            cfma(w[1][jy], r0, ay);
+            if (DERIV) {
+                cfma(w[1][jy], r1, ayx);
+                cfma(d[1][jy], r0, ayy);
+            }
+        }
+        cfma(w[2][jz], ay, S);
+        if (DERIV) {
+            cfma(w[2][jz], ayx, dS[0]);
+            cfma(w[2][jz], ayy, dS[1]);
+            cfma(d[2][jz], ay, dS[2]);
+        }
+    }
+}
+
+// Owned-sample set-up: position, ownership and stencil of pixel (qx, qy).
+template <bool CUBIC, bool DERIV>
+__device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx, int qx, int qy,
+                                           int *l, float (*w)[4], float (*d)[4]) {
+    bool own = true;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const float p = fmaf(g.a[a], (float)qx, g.b[a] * (float)qy);
+        float t;
+        const int x0 = split_coord(p, t);
+        l[a] = x0 - bx.o[a];
+        own = own && (unsigned)l[a] < (unsigned)kBS;
+        Stencil<CUBIC>::weights(t, w[a]);
+        if (DERIV) Stencil<CUBIC>::derivs(t, d[a]);
+    }
+    return own;
+}
+
+// ---------------------------------------------------------------------------
+// Forward projection.
+template <bool CUBIC>
+__global__ void __launch_bounds__(kThreads, 3) k_brick_project(Params q, int nb, Scratch sc,
+                                                               float2 *__restrict__ out) {
+    extern __shared__ float2 s_vol[];
+    __shared__ UnitTable s_tab;
+    int staged = -1;   // (volume, brick) held in s_vol
+    int v, brick;
+    while (fetch_unit(q, sc, nb, 0, s_tab, v, brick)) {
+        const BrickBox bx = brick_box(brick, nb);
+        const int key = v * nb * nb * nb + brick;
+        if (staged != key) {
+            stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+            staged = key;
+            __syncthreads();
+        }
+        for (int k; (k = next_pose(s_tab)) >= 0;) {
+            const PoseGeo &g = s_tab.pose[k];
+            float2 *o = out + (size_t)g.bp * q.plane;
+            const float sx = g.sx, sy = g.sy;
+            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                int l[3];
+                float w[3][4], d[3][4];
+                if (!active || !own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d)) return;
+                float2 S;
+                gather_smem<CUBIC, false>(s_vol, l, w, d, S, nullptr);
+                if (q.shift) S = cmul(shift_phase(qx, qy, sx, sy, q.fN, q.invN), S);
+                const int iy = qy < 0 ? qy + q.N : qy;
+                o[iy * q.Xo + qx] = S;
+            });
+        }
+        __syncthreads();
+    }
+}
+
+// Zeros for the pixels no brick owns: outside the radius, or with floor(p)
+// outside the brick grid (all taps there lie outside the stored range).
+__global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, float2 *__restrict__ out) {
+    const int bp = blockIdx.x / q.tiles;
+    const int rem = (blockIdx.x - bp * q.tiles) * 256 + threadIdx.x;
+    if (rem >= q.plane) return;
+    const int iy = rem / q.Xo;
+    const int kx = rem - iy * q.Xo;
+    const int ky = row_freq(iy, q.N);
+    bool zero = kx * kx + ky * ky > q.r2max;
+    if (!zero) {
+        const int b = bp / q.P, pi = bp - b * q.P;
+        const Pose<3> ps = load_pose<3>(q, b, pi);
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            float t;
+            const int x0 = split_coord(fmaf(ps.a[a], (float)kx, ps.b[a] * (float)ky), t);
+            zero = zero || x0 < -G || x0 >= G;
+        }
+    }
+    if (zero) out[(size_t)bp * q.plane + rem] = make_float2(0.f, 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// Rotation / shift gradients: per warp and (pose, brick), sums over the
+// owned samples, reduced across the warp and added to grad_rot / grad_shift.
+template <bool CUBIC>
+__global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int nb, Scratch sc,
+                                                                 const float2 *__restrict__ g_out,
+                                                                 float *__restrict__ grad_rot,
+                                                                 float *__restrict__ grad_shift) {
+    extern __shared__ float2 s_vol[];
+    __shared__ UnitTable s_tab;
+    int staged = -1;
+    int v, brick;
+    while (fetch_unit(q, sc, nb, 1, s_tab, v, brick)) {
+        const BrickBox bx = brick_box(brick, nb);
+        const int key = v * nb * nb * nb + brick;
+        if (staged != key) {
+            stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+            staged = key;
+            __syncthreads();
+        }
+        for (int k; (k = next_pose(s_tab)) >= 0;) {
+            const PoseGeo &g = s_tab.pose[k];
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            const float2 *gp = g_out + (size_t)g.bp * q.plane;
+            const float sx = g.sx, sy = g.sy;
+            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                int l[3];
+                float w[3][4], d[3][4];
+                if (!active || !own_sample<CUBIC, true>(g, bx, qx, qy, l, w, d)) return;
+                float2 S, dS[3];
+                gather_smem<CUBIC, true>(s_vol, l, w, d, S, dS);
+                const int iy = qy < 0 ? qy + q.N : qy;
+                const float2 gv = __ldg(gp + iy * q.Xo + qx);
+                float2 ph = make_float2(1.f, 0.f);
+                if (q.shift) ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
+                const float2 gq = cmul_conj_a(ph, gv);   // conj(phase) * g
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const float dl = gq.x * dS[i].x + gq.y * dS[i].y;   // dL/dp_i
+                    acc[i] = fmaf(q.s * (float)qx, dl, acc[i]);
+                    acc[3 + i] = fmaf(q.s * (float)qy, dl, acc[3 + i]);
+                }
+                const float2 y = cmul(ph, S);
+                const float qv = 6.283185307179586f * q.invN * (gv.x * y.y - gv.y * y.x);
+                acc[6] = fmaf((float)qx, qv, acc[6]);
+                acc[7] = fmaf((float)qy, qv, acc[7]);
+            });
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float t = acc[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                acc[i] = t;
+            }
+            if ((threadIdx.x & 31) == 0) {
+                if (grad_rot)
+#pragma unroll
+                    for (int i = 0; i < 6; ++i)
+                        if (acc[i] != 0.f) atomicAdd(grad_rot + (size_t)g.ridx * 9 + i, acc[i]);
+                if (grad_shift) {
+                    if (acc[6] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx, acc[6]);
+                    if (acc[7] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx + 1, acc[7]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backprojection / spectrum gradient (adjoint of the forward projection).
+//
+// Each group of 32 candidates is set up one sample per lane (ownership,
+// stencil weights, conj(phase) * y); the owned samples are queued in shared
+// memory and then spread cooperatively: in the cubic case the 32 lanes of
+// the warp take 32 of a sample's 64 taps per round.  With the accumulator
+// pitches 20 x 20 the taps (jx, jy, jz) of a 4 x 4 x 2 block fall into 32
+// distinct banks, so the shared-memory atomics of a round never conflict.
+struct Queue {
+    float w[12][32];   // stencil weights (x, y, z; 4 each) per queued sample
+    float c[2][32];    // conj(phase) * y
+    float om[32];      // weight-spectrum factor
+    int base[32];      // accumulator offset of the first tap
+};
+
+template <bool CUBIC, bool WEIGHTS>
+__global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Scratch sc,
+                                                            const float2 *__restrict__ img,
+                                                            const float *__restrict__ omega,
+                                                            float2 *__restrict__ dst,
+                                                            float *__restrict__ wdst) {
+    using H = Halo<CUBIC>;
+    static_assert(H::PX == 20 && H::PY == 20, "bank-conflict-free spreading assumes 20 x 20 pitches");
+    constexpr int T = Stencil<CUBIC>::TAPS;
+    constexpr int NACC = WEIGHTS ? 3 : 2;
+    extern __shared__ float s_dyn[];
+    __shared__ UnitTable s_tab;
+    float *s_re = s_dyn, *s_im = s_dyn + H::ELEMS, *s_w = s_dyn + 2 * H::ELEMS;
+    Queue &Q = reinterpret_cast<Queue *>(s_dyn + NACC * H::ELEMS)[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    // Tap of this lane in a spreading round.
+    int tx, ty, tz, tsub;
+    if (CUBIC) {
+        tx = lane & 3;
+        ty = (lane >> 2) & 3;
+        tz = lane >> 4;          // plus 2 in the second round
+        tsub = 0;
+    } else {
+        tx = lane & 1;
+        ty = (lane >> 1) & 1;
+        tz = (lane >> 2) & 1;
+        tsub = lane >> 3;        // which of 4 samples this lane serves
+    }
+    const int toff = tx + H::PX * ty + H::PX * H::PY * tz;
+    const int half = q.M >> 1;
+    int v, brick;
+    while (fetch_unit(q, sc, nb, 2, s_tab, v, brick)) {
+        const BrickBox bx = brick_box(brick, nb);
+        for (int e = threadIdx.x; e < NACC * H::ELEMS; e += kThreads) s_dyn[e] = 0.f;
+        __syncthreads();
+        for (int k; (k = next_pose(s_tab)) >= 0;) {
+            const PoseGeo &g = s_tab.pose[k];
+            const size_t ib = (size_t)g.bp * q.plane;
+            const float sx = g.sx, sy = g.sy;
+            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                int l[3];
+                float w[3][4], d[3][4];
+                const bool own = active && own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d);
+                const unsigned mask = __ballot_sync(0xffffffffu, own);
+                if (own) {
+                    const int slot = __popc(mask & ((1u << lane) - 1u));
+                    const int iy = qy < 0 ? qy + q.N : qy;
+                    float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                    if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, sx, sy, q.fN, q.invN), cv);
+#pragma unroll
+                    for (int a = 0; a < 3; ++a)
+#pragma unroll
+                        for (int i = 0; i < T; ++i) Q.w[4 * a + i][slot] = w[a][i];
+                    Q.c[0][slot] = cv.x;
+                    Q.c[1][slot] = cv.y;
+                    if (WEIGHTS) Q.om[slot] = omega ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                    Q.base[slot] = (l[2] * H::PY + l[1]) * H::PX + l[0];
+                }
+                __syncwarp();
+                const int nq = __popc(mask);
+                if (CUBIC) {
+                    for (int sq = 0; sq < nq; ++sq) {
+                        const float wxy = Q.w[tx][sq] * Q.w[4 + ty][sq];
+                        const float cr = Q.c[0][sq], ci = Q.c[1][sq];
+                        const int b0 = Q.base[sq] + toff;
+                        const float om = WEIGHTS ? Q.om[sq] : 0.f;
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const float wt = wxy * Q.w[8 + tz + 2 * r][sq];
+                            const int idx = b0 + r * 2 * H::PX * H::PY;
+                            atomicAdd(s_re + idx, wt * cr);
+                            atomicAdd(s_im + idx, wt * ci);
+                            if (WEIGHTS) atomicAdd(s_w + idx, wt * om);
+                        }
+                    }
+                } else {
+                    for (int s0 = 0; s0 < nq; s0 += 4) {
+                        const int sq = s0 + tsub;
+                        if (sq < nq) {
+                            const float wt = Q.w[tx][sq] * Q.w[4 + ty][sq] * Q.w[8 + tz][sq];
+                            const int idx = Q.base[sq] + toff;
+                            atomicAdd(s_re + idx, wt * Q.c[0][sq]);
+                            atomicAdd(s_im + idx, wt * Q.c[1][sq]);
+                            if (WEIGHTS) atomicAdd(s_w + idx, wt * Q.om[sq]);
+                        }
+                    }
+                }
+                __syncwarp();
+            });
+        }
+        __syncthreads();
+        // Fold brick + halo into the stored half-spectrum.
+        float2 *Vd = dst + (size_t)v * q.src_stride;
+        float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
+        const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
+                  z0 = bx.o[2] - Stencil<CUBIC>::LO;
+        for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
+            const int lx = e % H::S, ly = (e / H::S) % H::S, lz = e / (H::S * H::S);
+            const int k = (lz * H::PY + ly) * H::PX + lx;
+            const float re = s_re[k], im = s_im[k];
+            const float wv = WEIGHTS ? s_w[k] : 0.f;
+            if (re == 0.f && im == 0.f && wv == 0.f) continue;
+            int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
+            const bool cj = nx < 0;
+            if (cj) {
+                nx = -nx;
+                ny = -ny;
+                nz = -nz;
+            }
+            if (!stored(nx, ny, nz, half)) continue;
+            const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
+            if (re != 0.f || im != 0.f) atomicAdd(Vd + idx, make_float2(re, cj ? -im : im));
+            if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launch geometry and scratch layout.
+int bricks_per_axis(int M, bool cubic) {
+    const int need = (M >> 1) + (cubic ? Stencil<true>::HI : Stencil<false>::HI);
+    return 2 * ((need + kBS - 1) / kBS);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t geo, masks, total;
+    int nb, nchunks;
+};
+
+Layout layout(const Params &q, bool cubic) {
+    Layout L;
+    L.nb = bricks_per_axis(q.M, cubic);
+    const long long Pv = (q.Bsrc == 1) ? (long long)q.B * q.P : q.P;
+    L.nchunks = (int)((Pv + 31) / 32);
+    L.geo = 256;   // counters first
+    L.masks = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
+    L.total = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * L.nb * L.nb * L.nb * L.nchunks);
+    return L;
+}
+
+Scratch scratch_in(void *ws, const Layout &L) {
+    Scratch sc;
+    char *base = static_cast<char *>(ws);
+    sc.counters = reinterpret_cast<unsigned *>(base);
+    sc.geo = reinterpret_cast<PoseGeo *>(base + L.geo);
+    sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
+    sc.nchunks = L.nchunks;
+    return sc;
+}
+
+int resident_blocks(const void *kern, size_t smem) {
+    int dev = 0, sms = 148, per_sm = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    return sms * per_sm;
+}
+
+// Pose geometry and brick masks for the poses of q (shared by the main kernels).
+cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_t st) {
+    const int pb = (q.B * q.P + 255) / 256;
+    k_pose_geometry<<<pb, 256, 0, st>>>(q, sc.geo, sc.counters);
+    const long long warps = (long long)q.Bsrc * L.nb * L.nb * L.nb * L.nchunks;
+    long long blocks = (warps + 7) / 8;
+    if (blocks > 65535LL * 32) blocks = 65535LL * 32;
+    k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, L.nchunks, sc.geo, sc.masks);
+    return cudaGetLastError();
+}
+
+template <bool CUBIC>
+cudaError_t project_t(const Params &q, float2 *out, void *ws, cudaStream_t st) {
+    const Layout L = layout(q, CUBIC);
+    const Scratch sc = scratch_in(ws, L);
+    const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
+    auto kern = k_brick_project<CUBIC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if ((e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    const long long zb = (long long)q.B * q.P * q.tiles;
+    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, out);
+    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out);
+    return cudaGetLastError();
+}
+
+template <bool CUBIC>
+cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gshift, void *ws,
+                        bool binned, cudaStream_t st) {
+    const Layout L = layout(q, CUBIC);
+    const Scratch sc = scratch_in(ws, L);
+    const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
+    auto kern = k_brick_pose_grad<CUBIC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, g, grot,
+                                                                          gshift);
+    return cudaGetLastError();
+}
+
+template <bool CUBIC, bool WEIGHTS>
+cudaError_t scatter_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
+                      float *wdst, void *ws, bool binned, cudaStream_t st) {
+    const Layout L = layout(q, CUBIC);
+    const Scratch sc = scratch_in(ws, L);
+    const size_t smem = sizeof(float) * Halo<CUBIC>::ELEMS * (WEIGHTS ? 3 : 2) + sizeof(Queue) * kWarps;
+    auto kern = k_brick_scatter<CUBIC, WEIGHTS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
+                                                                          dst, wdst);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t brick_workspace_bytes(const Params &q, bool cubic) { return layout(q, cubic).total; }
+
+cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, void *ws,
+                                 cudaStream_t st) {
+    return cubic ? project_t<true>(q, out, ws, st) : project_t<false>(q, out, ws, st);
+}
+
+cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *g, float *grot,
+                                   float *gshift, void *ws, bool binned, cudaStream_t st) {
+    return cubic ? pose_grad_t<true>(q, g, grot, gshift, ws, binned, st)
+                 : pose_grad_t<false>(q, g, grot, gshift, ws, binned, st);
+}
+
+cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
+                                 float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st) {
+    if (wdst)
+        return cubic ? scatter_t<true, true>(q, img, omega, dst, wdst, ws, binned, st)
+                     : scatter_t<false, true>(q, img, omega, dst, wdst, ws, binned, st);
+    return cubic ? scatter_t<true, false>(q, img, omega, dst, nullptr, ws, binned, st)
+                 : scatter_t<false, false>(q, img, omega, dst, nullptr, ws, binned, st);
+}
+
+}  // namespace tp

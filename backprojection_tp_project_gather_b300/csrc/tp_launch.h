@@ -20,4 +20,17 @@ cudaError_t launch_pose_grad(int dim, bool cubic, const Params &q, const float2 
 cudaError_t launch_scatter(int dim, bool cubic, const Params &q, const float2 *img,
                            const float *omega, float2 *dst, float *wdst, cudaStream_t st);
 
+// 3D brick-binned kernels (tp_brick.cu): forward, pose gradients and
+// scatter.  ws is the caller's workspace of brick_workspace_bytes() bytes;
+// with binned = true the pose binning of an earlier launch on the same
+// stream, for the same poses, is reused.
+size_t brick_workspace_bytes(const Params &q, bool cubic);
+cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, void *ws,
+                                 cudaStream_t st);
+cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
+                                   float *grad_rot, float *grad_shift, void *ws, bool binned,
+                                   cudaStream_t st);
+cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
+                                 float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st);
+
 }  // namespace tp

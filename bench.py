@@ -52,6 +52,8 @@ def parse_args():
                     help="poses per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--poses", type=int, default=None,
+                    help="pose count (default: the workload's 512); smaller runs are for profiling")
     return ap.parse_args()
 
 
@@ -237,7 +239,7 @@ def run_ours(args):
     import backprojection_tp_project_gather_b300 as tp
 
     seed = 1000 + WORKLOAD + 100 * rank           # rank 0 = the single-GPU workload
-    w = synth.workload(WORKLOAD, seed=seed)
+    w = synth.workload(WORKLOAD, seed=seed, poses=args.poses)
     P, N = w["P"], w["box"]
     kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
     dev = torch.device("cuda", local)
@@ -257,7 +259,7 @@ def run_ours(args):
     rot = torch.from_numpy((w["rot"][0].astype(np.float64) @ dR).astype(np.float32)[None]).to(dev)
     shift = (t_true + torch.from_numpy(rng[1].normal(0, 1, (1, P, 2)).astype(np.float32)).to(dev))
     # Targets: clean projections at the true poses plus noise of 10x the signal power.
-    clean = tp.tp_project_3d_2d(vol, R_true, t_true, **kw)
+    clean = tp.tp_project_3d_2d(vol, R_true, t_true, **kw)  # (workspace allocated per call here)
     noise = torch.from_numpy(synth.complex_normal((1, P, N, N // 2 + 1), rng[2])).to(dev)
     mask = torch.from_numpy(np.fft.fftfreq(N, 1.0 / N)[:, None] ** 2
                             + np.arange(N // 2 + 1)[None, :] ** 2 <= w["radius"] ** 2).to(dev)
@@ -273,6 +275,8 @@ def run_ours(args):
     grad_rot = torch.zeros_like(rot)
     grad_shift = torch.zeros_like(shift)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ws = torch.empty(tp.tp_workspace_bytes(1, 1, P, N, w["interp"]), dtype=torch.uint8, device=dev)
+    kw["workspace"] = ws
     stream = torch.cuda.current_stream()
 
     def step(ev=None):

@@ -55,6 +55,13 @@
  * grad = dL/dRe + i dL/dIm, and each backward entry point applies the real
  * adjoint of the forward map's Jacobian.
  *
+ * Workspace.  The 3D entry points bin poses against bricks of the volume in
+ * a scratch area the caller provides: `workspace` must point to at least
+ * tp_workspace_bytes(...) bytes of device memory, 16-byte aligned, owned by
+ * the caller.  Its contents need no initialisation and are meaningless
+ * between calls; it must not be used by two calls that can run at the same
+ * time (one workspace per stream).
+ *
  * Errors.  Each call returns a tp_status.  Argument errors are detected
  * before anything is enqueued; TP_ERR_CUDA reports a launch failure.  No
  * C++ exception crosses this interface.  tp_last_error() returns a message
@@ -63,6 +70,8 @@
  */
 #ifndef TP_B300_H
 #define TP_B300_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -99,7 +108,8 @@ typedef struct {
 tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv,
                            const float *rot, int Bp, int P,
                            const float *shift, int Bs,
-                           int N, tp_options opts, float *out, void *stream);
+                           int N, tp_options opts, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Gradients through tp_project_3d_2d for an upstream gradient grad_out
@@ -114,7 +124,7 @@ tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int
                                     const float *rot, int Bp, int P,
                                     const float *shift, int Bs, int N, tp_options opts,
                                     float *grad_vol, float *grad_rot, float *grad_shift,
-                                    void *stream);
+                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * 2D -> 3D backprojection: the adjoint of tp_project_3d_2d scattered into a
@@ -132,7 +142,8 @@ tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int
 tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, int P, int N,
                                const float *rot, int Bp, const float *shift, int Bs,
                                int Bv, int Nv, tp_options opts,
-                               float *data_vol, float *weight_vol, void *stream);
+                               float *data_vol, float *weight_vol,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * 2D -> 2D forward: rotated and shifted 2D half-spectra
@@ -156,6 +167,14 @@ tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int
                                     const float *shift, int Bs, int N, tp_options opts,
                                     float *grad_img, float *grad_rot, float *grad_shift,
                                     void *stream);
+
+/*
+ * Bytes of workspace the 3D entry points need for a volume batch Bv, batch
+ * B (Bv is 1 or B), P poses per batch element, volume box Nv and the
+ * interpolation of opts; the same for all three of them (the backward uses
+ * it for both of its passes).  Returns 0 for invalid sizes.
+ */
+size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts);
 
 /* Message for the calling thread's most recent failure ("" if none). */
 const char *tp_last_error(void);

@@ -54,11 +54,17 @@ def opts(tp, interp=1, s=1.0, r=-1.0, flags=0):
     return tp.TPOptions(interp, s, r, flags)
 
 
+WS = 0x20000       # fake workspace address
+WSB = 1 << 30      # claimed workspace size
+
+
 def proj3(tp, **kw):
-    a = dict(vol=A, Bv=1, Nv=16, rot=A, Bp=1, P=4, shift=None, Bs=1, N=16, o=opts(tp), out=A)
+    a = dict(vol=A, Bv=1, Nv=16, rot=A, Bp=1, P=4, shift=None, Bs=1, N=16, o=opts(tp), out=A,
+             ws=WS, wsb=WSB)
     a.update(kw)
     return tp.lib().tp_project_3d_2d(a["vol"], a["Bv"], a["Nv"], a["rot"], a["Bp"], a["P"],
-                                     a["shift"], a["Bs"], a["N"], a["o"], a["out"], None)
+                                     a["shift"], a["Bs"], a["N"], a["o"], a["out"], a["ws"],
+                                     a["wsb"], None)
 
 
 def test_forward_validation(tp):
@@ -81,6 +87,10 @@ def test_forward_validation(tp):
     assert proj3(tp, o=opts(tp, r=float("inf"))) == TP_ERR_UNSUPPORTED
     assert proj3(tp, o=opts(tp, flags=1)) == TP_ERR_UNSUPPORTED
     assert "flags" in tp.tp_last_error()
+    assert proj3(tp, ws=None) == TP_ERR_NULL
+    assert proj3(tp, ws=WS + 4) == TP_ERR_ALIGN
+    assert proj3(tp, wsb=16) == TP_ERR_SHAPE
+    assert "workspace" in tp.tp_last_error()
     # An empty problem succeeds without launching anything.
     assert proj3(tp, P=0) == TP_OK
     assert tp.tp_last_error() == ""
@@ -92,7 +102,7 @@ def test_backward_validation(tp):
 
     def bwd(go=A, vol=A, shift=None, gv=A, gr=A, gs=None, P=4):
         return lib.tp_project_3d_2d_backward(go, vol, 1, 16, A, 1, P, shift, 1, 16, o, gv, gr, gs,
-                                             None)
+                                             WS, WSB, None)
     assert bwd(go=None) == TP_ERR_NULL
     assert bwd(vol=None) == TP_ERR_NULL                 # needed for grad_rot
     assert bwd(gs=A) == TP_ERR_NULL                     # grad_shift without shift
@@ -108,7 +118,7 @@ def test_backprojection_validation(tp):
 
     def bp(proj=A, B=2, Bp=1, Bv=1, data=A, wv=A, P=4, weights=None):
         return lib.tp_backproject_2d_3d(proj, weights, B, P, 16, A, Bp, None, 1, Bv, 16, o, data,
-                                        wv, None)
+                                        wv, WS, WSB, None)
     assert bp(proj=None) == TP_ERR_NULL
     assert bp(data=None) == TP_ERR_NULL
     assert bp(Bv=3) == TP_ERR_SHAPE                     # Bv must be 1 or B
@@ -117,6 +127,14 @@ def test_backprojection_validation(tp):
     assert bp(weights=A + 2) == TP_ERR_ALIGN
     assert bp(P=0) == TP_OK
     assert bp(wv=None, P=0) == TP_OK
+
+
+def test_workspace_size_query(tp):
+    small = tp.tp_workspace_bytes(1, 1, 8, 32, "cubic")
+    big = tp.tp_workspace_bytes(1, 1, 512, 256, "cubic")
+    assert 0 < small < big
+    assert tp.tp_workspace_bytes(1, 1, 8, 31, "cubic") == 0      # odd box
+    assert tp.tp_workspace_bytes(2, 1, 8, 32, "cubic") == 0      # Bv > B
 
 
 def test_binding_rejects_cpu_tensors(tp):
