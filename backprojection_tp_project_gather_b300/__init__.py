@@ -56,14 +56,23 @@ _SIGS = {
     "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P, _Z,
                              _P],
 }
-for _name, _args in _SIGS.items():
-    _f = getattr(_lib, _name)
-    _f.argtypes = _args
-    _f.restype = ctypes.c_int
-_lib.tp_workspace_bytes.argtypes = [_I, _I, _I, _I, TPOptions]
-_lib.tp_workspace_bytes.restype = ctypes.c_size_t
-_lib.tp_last_error.restype = ctypes.c_char_p
-_lib.tp_version.restype = ctypes.c_char_p
+_SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, TPOptions]
+_RESTYPES = {"tp_workspace_bytes": ctypes.c_size_t, "tp_last_error": ctypes.c_char_p,
+             "tp_version": ctypes.c_char_p}
+_bound = {}
+
+
+def _fn(name):
+    """Entry point `name` with its C signature (bound on first use, so a
+    rebuild can run while an older library is on disk)."""
+    f = _bound.get(name)
+    if f is None:
+        f = getattr(_lib, name)
+        if name in _SIGS:
+            f.argtypes = _SIGS[name]
+        f.restype = _RESTYPES.get(name, ctypes.c_int)
+        _bound[name] = f
+    return f
 
 
 def lib() -> ctypes.CDLL:
@@ -72,16 +81,17 @@ def lib() -> ctypes.CDLL:
 
 
 def tp_last_error() -> str:
-    return _lib.tp_last_error().decode()
+    return _fn("tp_last_error")().decode()
 
 
 def tp_version() -> str:
-    return _lib.tp_version().decode()
+    return _fn("tp_version")().decode()
 
 
 def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic"):
     """Workspace bytes the 3D entry points need (see include/tp.h)."""
-    return int(_lib.tp_workspace_bytes(int(Bv), int(B), int(P), int(Nv), _opts(interp, 1.0, -1.0)))
+    return int(_fn("tp_workspace_bytes")(int(Bv), int(B), int(P), int(Nv),
+                                         _opts(interp, 1.0, -1.0)))
 
 
 def _workspace(ws, Bv, B, P, Nv, interp, device):
@@ -124,7 +134,7 @@ def _stream(stream):
 
 
 def _call(name, *args):
-    st = getattr(_lib, name)(*args)
+    st = _fn(name)(*args)
     if st != 0:
         raise TPError(st, tp_last_error())
 

@@ -62,7 +62,7 @@ def proj3(tp, **kw):
     a = dict(vol=A, Bv=1, Nv=16, rot=A, Bp=1, P=4, shift=None, Bs=1, N=16, o=opts(tp), out=A,
              ws=WS, wsb=WSB)
     a.update(kw)
-    return tp.lib().tp_project_3d_2d(a["vol"], a["Bv"], a["Nv"], a["rot"], a["Bp"], a["P"],
+    return tp._fn("tp_project_3d_2d")(a["vol"], a["Bv"], a["Nv"], a["rot"], a["Bp"], a["P"],
                                      a["shift"], a["Bs"], a["N"], a["o"], a["out"], a["ws"],
                                      a["wsb"], None)
 
@@ -101,14 +101,14 @@ def test_backward_validation(tp):
     o = opts(tp)
 
     def bwd(go=A, vol=A, shift=None, gv=A, gr=A, gs=None, P=4):
-        return lib.tp_project_3d_2d_backward(go, vol, 1, 16, A, 1, P, shift, 1, 16, o, gv, gr, gs,
+        return tp._fn("tp_project_3d_2d_backward")(go, vol, 1, 16, A, 1, P, shift, 1, 16, o, gv, gr, gs,
                                              WS, WSB, None)
     assert bwd(go=None) == TP_ERR_NULL
     assert bwd(vol=None) == TP_ERR_NULL                 # needed for grad_rot
     assert bwd(gs=A) == TP_ERR_NULL                     # grad_shift without shift
     assert bwd(gv=MIS) == TP_ERR_ALIGN
     assert bwd(P=0) == TP_OK
-    assert lib.tp_project_2d_2d_backward(A, A, 1, 15, A, 1, 4, None, 1, 16, o, A, A, None,
+    assert tp._fn("tp_project_2d_2d_backward")(A, A, 1, 15, A, 1, 4, None, 1, 16, o, A, A, None,
                                          None) == TP_ERR_SHAPE
 
 
@@ -117,7 +117,7 @@ def test_backprojection_validation(tp):
     o = opts(tp)
 
     def bp(proj=A, B=2, Bp=1, Bv=1, data=A, wv=A, P=4, weights=None):
-        return lib.tp_backproject_2d_3d(proj, weights, B, P, 16, A, Bp, None, 1, Bv, 16, o, data,
+        return tp._fn("tp_backproject_2d_3d")(proj, weights, B, P, 16, A, Bp, None, 1, Bv, 16, o, data,
                                         wv, WS, WSB, None)
     assert bp(proj=None) == TP_ERR_NULL
     assert bp(data=None) == TP_ERR_NULL
