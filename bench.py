@@ -133,59 +133,64 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
-# Clock sampling during the timed region (NVML, read-only).
+# Clock sampling during the timed region (nvidia-smi query loop, read-only).
 class ClockSampler:
-    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-               "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4}
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self._stop = threading.Event()
+        import torch
+        self.bus = None
         try:
-            import pynvml
-            import torch
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            try:  # the CUDA device's own NVML handle (indices can differ)
-                uuid = str(torch.cuda.get_device_properties(index).uuid)
-                self.h = pynvml.nvmlDeviceGetHandleByUUID(
-                    uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            except Exception:  # noqa: BLE001
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self._reasons = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
-        except Exception:  # noqa: BLE001  (no NVML: report no clock record)
-            self.nv = None
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self._reasons(self.h)
-                for k, bit in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(k)
-            except Exception:  # noqa: BLE001
-                pass
-            time.sleep(0.01)
+            p = torch.cuda.get_device_properties(index)
+            self.bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:  # noqa: BLE001
+            pass
+        self.proc, self.error = None, None
 
     def __enter__(self):
-        if self.nv:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        import tempfile
+        self.out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception as e:  # noqa: BLE001
+            self.error = str(e)
+        time.sleep(0.2)
         return self
 
     def __exit__(self, *exc):
-        if self.nv:
-            self._stop.set()
-            self.t.join()
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            self.proc.wait()
 
     def record(self):
-        if not self.nv or not self.samples:
-            return None
-        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "n_samples": len(self.samples)}
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi unavailable"}
+        self.out.seek(0)
+        rows = [r.split(", ") for r in self.out.read().strip().splitlines() if r.strip()]
+        if self.bus:
+            mine = [r for r in rows if r[0].upper().endswith(self.bus[-7:])]
+            rows = mine or rows
+        sm, mx, reasons = [], None, set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, flag in zip(self.REASONS, r[3:7]):
+                    if flag.strip() == "Active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"error": "no clock samples"}
+        return {"sm_mhz": float(statistics.median(sm)), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "n_samples": len(sm)}
 
 
 def measured_peak_hbm():
@@ -392,7 +397,10 @@ def run_ours(args):
             "in_radius_samples_per_step": P * in_radius_count(N, w["radius"]),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": 3 * args.steps,
+            # per step: forward (pose geometry, brick masks, zero fill, gather), then the
+            # pose-gradient call (geometry, masks, gather) and the volume-gradient call
+            # (geometry, masks, scatter) -- all kernels of this library
+            "gpu_launches": 10 * args.steps,
             "clocks": clocks.record(),
             "cpu_baseline": cpu_line,
         }
