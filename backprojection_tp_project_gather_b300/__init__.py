@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "TPError", "lib", "tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
     "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version",
-    "tp_workspace_bytes", "LINEAR", "CUBIC",
+    "tp_workspace_bytes", "tp_project_3d_2d_noalloc", "LINEAR", "CUBIC",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +50,7 @@ _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
     "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _Z, _P],
     "tp_project_2d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
+    "tp_project_3d_2d_noalloc": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
     "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P,
                                   _P, _Z, _P],
     "tp_project_2d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
@@ -218,6 +219,30 @@ def tp_project_3d_2d(vol, rot, shift=None, *, N=None, interp="cubic", oversampli
     (allocated per call when omitted)."""
     return _forward("tp_project_3d_2d", 3, vol, rot, shift, N, interp, oversampling, radius, out,
                     stream, workspace)
+
+
+def tp_project_3d_2d_noalloc(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
+                             radius=-1.0, out=None, stream=None):
+    """tp_project_3d_2d for callers that cannot allocate device scratch.
+
+    The library keeps the scratch in a fixed array of its own instead of a
+    caller workspace; include/tp.h gives its size limit and the rule that such
+    calls must not overlap on the GPU.  Pass `out` to avoid the one output
+    allocation this wrapper would otherwise make.
+    """
+    _need(vol, "vol", torch.complex64, 4)
+    Bv, Nv = vol.shape[0], vol.shape[1]
+    Bp, P, Bs = _poses(rot, shift, 3)
+    N = Nv if N is None else int(N)
+    B = _batch(Bv, Bp, Bs)
+    if out is None:
+        out = torch.empty((B, P, N, N // 2 + 1), dtype=torch.complex64, device=vol.device)
+    _need(out, "out", torch.complex64, 4)
+    if tuple(out.shape) != (B, P, N, N // 2 + 1):
+        raise ValueError(f"out must be {(B, P, N, N // 2 + 1)}")
+    _call("tp_project_3d_2d_noalloc", _ptr(vol), Bv, Nv, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+          _opts(interp, oversampling, radius), _ptr(out), _stream(stream))
+    return out
 
 
 def tp_project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,

@@ -176,6 +176,25 @@ tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int
  */
 size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts);
 
+/*
+ * tp_project_3d_2d without a workspace, for callers that cannot allocate
+ * device memory (no cudaMalloc allowed where they run, e.g. during a graph
+ * capture or under a foreign allocator).  The paper has no counterpart: it
+ * is an interface convenience of this library.  Arguments and results are
+ * those of tp_project_3d_2d.  The scratch lives in a fixed 16 MiB array in
+ * the library's device memory, reserved on every GPU that loads the
+ * library until the process exits; problems needing more scratch than that
+ * (tp_workspace_bytes) fail with TP_ERR_SHAPE and a message on stderr.
+ * All calls share the array: calls that can overlap on the GPU race and
+ * must be serialised by the caller.  The first call on each device looks
+ * the array up (and may load the module); make it before any stream
+ * capture.  No memory is allocated.
+ */
+tp_status tp_project_3d_2d_noalloc(const float *vol, int Bv, int Nv,
+                                   const float *rot, int Bp, int P,
+                                   const float *shift, int Bs,
+                                   int N, tp_options opts, float *out, void *stream);
+
 /* Message for the calling thread's most recent failure ("" if none). */
 const char *tp_last_error(void);
 
