@@ -19,18 +19,21 @@
 //    positions conjugated at -n), with vector atomics because halos of
 //    neighbouring bricks and other work units overlap.
 //
-// Binning.  Two small passes precede every operator: one thread per pose
-// computes the pose's geometry once (into the caller's workspace), then one
-// warp per (brick, 32-pose chunk) marks with a ballot which poses can reach
-// the brick: the plane spanned by a = s R[0], b = s R[1] must meet it, the
-// half-plane qx >= 0 must touch it and it must lie within the pose's reach.
-// A work unit is one brick and kGroup chunks of poses; persistent blocks take
-// units from a global counter, skip empty ones at the cost of kGroup mask
-// loads, and keep the staged brick when consecutive units share it.  For one
-// (pose, brick) pair the owned pixels form a convex polygon in k-space: its
-// rows come from the pseudo-inverse of [a b] and each row's qx interval from
-// the three slab constraints; the enumeration is a small superset and the
-// exact floor(p) test decides ownership.
+// Binning.  Three small passes precede every operator: one thread per pose
+// computes the pose's geometry once (into the caller's workspace); one warp
+// per (brick, 32-pose chunk) marks with a ballot which poses can reach the
+// brick (the plane spanned by a = s R[0], b = s R[1] must meet it, the
+// half-plane qx >= 0 must touch it and it must lie within the pose's reach)
+// and counts them per brick; one block per volume then turns the counts
+// into a compact list of work units -- a brick and a range of chunks holding
+// about kUnitHits reaching poses, so busy bricks near the origin are split
+// and empty bricks vanish.  Persistent blocks take units from a global
+// counter in brick order (busiest first), stage the brick once per unit and
+// walk its poses in batches of up to 128.  For one (pose, brick) pair the
+// owned pixels form a convex polygon in k-space: its rows come from the
+// pseudo-inverse of [a b] and each row's qx interval from the three slab
+// constraints; the enumeration is a small superset and the exact floor(p)
+// test decides ownership.
 //
 // Method: "torch-projectors: A High-Performance Differentiable Projection
 // Library for PyTorch", 3D->2D projection and 2D->3D backprojection
@@ -46,8 +49,10 @@ namespace {
 constexpr int kBS = 16;          // brick edge (voxels)
 constexpr int kWarps = 8;        // warps per block
 constexpr int kThreads = 32 * kWarps;
-constexpr int kGroup = 4;        // 32-pose chunks per work unit
+constexpr int kGroup = 4;        // 32-pose chunks per batch of a work unit
 constexpr int kUnitPoses = 32 * kGroup;
+constexpr int kUnitHits = 64;    // reaching poses per work unit (load-balance target)
+constexpr int kQueueStride = 21; // floats per queued scatter sample (odd: no bank conflicts)
 constexpr float kMargin = 0.01f; // enumeration margin in voxel units
 
 template <bool CUBIC>
@@ -76,9 +81,11 @@ constexpr int kGeoWords = sizeof(PoseGeo) / 4;
 
 // Scratch layout inside the caller's workspace.
 struct Scratch {
-    unsigned *counters;   // work counters of the main kernels
+    unsigned *counters;   // [4][Bsrc]: work counters of the three main kernels, unit counts
     PoseGeo *geo;         // B*P poses
     unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
+    int *hits;            // [Bsrc][bricks] reaching poses per brick
+    int4 *units;          // [Bsrc][bricks * chunks] work units (brick, first chunk, end chunk)
     int nchunks;          // 32-pose chunks per volume
 };
 
@@ -252,25 +259,24 @@ __device__ __forceinline__ int pose_id(const Params &q, int v, int i) {
 
 // ---------------------------------------------------------------------------
 // Binning passes.
-__global__ void __launch_bounds__(256) k_pose_geometry(Params q, PoseGeo *__restrict__ geo,
-                                                       unsigned *__restrict__ counters) {
+__global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratch sc) {
     const int id = blockIdx.x * 256 + threadIdx.x;
-    if (id == 0)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) counters[k] = 0u;
+    const int stride = gridDim.x * 256;
+    for (int k = id; k < 4 * q.Bsrc; k += stride) sc.counters[k] = 0u;
+    for (long long k = id; k < (long long)q.Bsrc * nbr; k += stride) sc.hits[k] = 0;
     if (id >= q.B * q.P) return;
     const int b = id / q.P, pi = id - b * q.P;
     PoseGeo g;
     pose_geo(q, b, pi, g);
-    geo[id] = g;
+    sc.geo[id] = g;
 }
 
 // One warp per (volume, brick, chunk): bit l of the mask = pose 32*chunk + l
-// of the volume's list can reach the brick.
-__global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, int nchunks,
-                                                     const PoseGeo *__restrict__ geo,
-                                                     unsigned *__restrict__ masks) {
+// of the volume's list can reach the brick; the brick's count grows by the
+// number of set bits.
+__global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
     const int nbr = nb * nb * nb;
+    const int nchunks = sc.nchunks;
     const long long total = (long long)q.Bsrc * nbr * nchunks;
     const int Pv = poses_of_volume(q);
     const int lane = threadIdx.x & 31;
@@ -283,65 +289,135 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, int nchun
         bool hit = false;
         if (i < Pv) {
             const BrickBox bx = brick_box(j, nb);
-            hit = pose_reaches(geo[pose_id(q, v, i)], bx);
+            hit = pose_reaches(sc.geo[pose_id(q, v, i)], bx);
         }
         const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (lane == 0) masks[w] = m;
+        if (lane == 0) {
+            sc.masks[w] = m;
+            if (m) atomicAdd(sc.hits + r, __popc(m));
+        }
+    }
+}
+
+// One block per volume: split every brick with reaching poses into
+// ceil(hits / kUnitHits) units over equal chunk ranges, and list the units
+// in brick order (a block-wide exclusive scan gives each brick its slots).
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc) {
+    __shared__ int warp_sum[kPlanThreads / 32];
+    const int v = blockIdx.x;
+    const int nch = sc.nchunks;
+    const int per = (nbr + kPlanThreads - 1) / kPlanThreads;
+    const int j0 = threadIdx.x * per, j1 = min(nbr, j0 + per);
+    const int *hits = sc.hits + (size_t)v * nbr;
+    int mine = 0;
+    for (int j = j0; j < j1; ++j) {
+        const int h = hits[j];
+        mine += h ? min(nch, (h + kUnitHits - 1) / kUnitHits) : 0;
+    }
+    // Block-wide exclusive scan of the per-thread unit counts.
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int x = warp_sum[lane];
+        int y = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += t;
+        }
+        warp_sum[lane] = y - x;   // exclusive prefix of the warp totals
+        if (lane == 31) sc.counters[3 * gridDim.x + v] = (unsigned)y;
+    }
+    __syncthreads();
+    int at = warp_sum[warp] + incl - mine;
+    int4 *out = sc.units + (size_t)v * nbr * nch;
+    for (int j = j0; j < j1; ++j) {
+        const int h = hits[j];
+        if (!h) continue;
+        const int n = min(nch, (h + kUnitHits - 1) / kUnitHits);
+        for (int i = 0; i < n; ++i)
+            out[at++] = make_int4(j, (int)((long long)nch * i / n), (int)((long long)nch * (i + 1) / n), 0);
     }
 }
 
 // ---------------------------------------------------------------------------
 // Shared pieces of the main kernels.
 
-// The block's current work unit: the poses that reach its brick, with their
-// geometry copied into shared memory.
+// A batch of the block's current work unit: the poses that reach its
+// brick, with their geometry copied into shared memory.
 struct UnitTable {
     PoseGeo pose[kUnitPoses];
-    int nhit;     // entries of pose[]
-    int next;     // work counter for the warps
-    int unit;     // unit index handed out by the global counter
+    unsigned mask[32];   // masks of the batch's chunks
+    int base[32];        // table offset of each chunk's first pose
+    int nhit;            // entries of pose[]
+    int nchunk;          // chunks in the batch
+    int next;            // work counter for the warps
+    int unit;            // unit index handed out by the global counter
 };
 
-// Fetch the next non-empty unit from the global counter and load its poses
-// (block-wide).  Returns false when the units are exhausted.
-__device__ __forceinline__ bool fetch_unit(const Params &q, const Scratch &sc, int nb, int slot,
-                                           UnitTable &t, int &v, int &brick) {
-    const int nbr = nb * nb * nb;
-    const int ngrp = (sc.nchunks + kGroup - 1) / kGroup;
-    const long long nunits = (long long)q.Bsrc * nbr * ngrp;
-    for (;;) {
-        if (threadIdx.x == 0) {
-            t.unit = (int)atomicAdd(sc.counters + slot, 1u);
-            t.nhit = 0;
+// Take the next unit of volume v from the global counter (block-wide).
+// Returns false when the volume's units are exhausted.
+__device__ __forceinline__ bool next_unit(const Scratch &sc, int slot, int v, int nbr,
+                                          UnitTable &t, int4 &rec) {
+    const int nvol = gridDim.z;
+    if (threadIdx.x == 0) t.unit = (int)atomicAdd(sc.counters + slot * nvol + v, 1u);
+    __syncthreads();
+    const int u = t.unit;
+    __syncthreads();   // everyone has read t.unit before the next request
+    if (u >= (int)__ldg(sc.counters + 3 * nvol + v)) return false;
+    rec = __ldg(sc.units + (size_t)v * nbr * sc.nchunks + u);
+    return true;
+}
+
+// Load the reaching poses of the unit's chunks, from chunk c on, into the
+// table (block-wide): as many whole chunks (at most 32) as fit into its
+// kUnitPoses entries.  Returns the first chunk not loaded; t.nhit holds the
+// number of poses loaded.
+__device__ __forceinline__ int load_batch(const Params &q, const Scratch &sc, int nbr, int v,
+                                          int brick, int c, int c1, UnitTable &t) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned *masks = sc.masks + ((size_t)v * nbr + brick) * sc.nchunks;
+    if (warp == 0) {
+        const unsigned m = (c + lane < c1) ? __ldg(masks + c + lane) : 0u;
+        const int n = __popc(m);
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        // Chunks 0..k-1 fit (a single chunk always does: 32 <= kUnitPoses).
+        const int k = max(1, __popc(__ballot_sync(0xffffffffu, incl <= kUnitPoses)));
+        t.mask[lane] = m;
+        t.base[lane] = incl - n;
+        if (lane == k - 1) t.nhit = incl;
+        if (lane == 0) {
+            t.nchunk = min(k, c1 - c);
             t.next = 0;
         }
-        __syncthreads();
-        const int u = t.unit;
-        if (u >= nunits) return false;
-        const int grp = u % ngrp;
-        const int r = u / ngrp;
-        brick = r % nbr;
-        v = r / nbr;
-        // Warp w lists the set bits of chunk grp * kGroup + w.
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (warp < kGroup) {
-            const int c = grp * kGroup + warp;
-            unsigned m = 0u;
-            if (c < sc.nchunks) m = __ldg(sc.masks + ((size_t)v * nbr + brick) * sc.nchunks + c);
-            int base = 0;
-            if (lane == 0 && m) base = atomicAdd(&t.nhit, __popc(m));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if ((m >> lane) & 1u) {
-                const int at = base + __popc(m & ((1u << lane) - 1u));
-                const int *src = reinterpret_cast<const int *>(sc.geo + pose_id(q, v, c * 32 + lane));
-                int *dst = reinterpret_cast<int *>(&t.pose[at]);
-                for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
-            }
-        }
-        __syncthreads();
-        if (t.nhit > 0) return true;
-        __syncthreads();   // everyone has read nhit before thread 0 resets it
     }
+    __syncthreads();
+    const int nchunk = t.nchunk;
+    for (int i = warp; i < nchunk; i += kWarps) {
+        const unsigned m = t.mask[i];
+        if ((m >> lane) & 1u) {
+            const int at = t.base[i] + __popc(m & ((1u << lane) - 1u));
+            const int *src = reinterpret_cast<const int *>(sc.geo + pose_id(q, v, (c + i) * 32 + lane));
+            int *dst = reinterpret_cast<int *>(&t.pose[at]);
+            for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+        }
+    }
+    __syncthreads();
+    return c + nchunk;
 }
 
 // Next listed pose for the calling warp, or -1 when the list is exhausted.
@@ -460,56 +536,64 @@ __global__ void __launch_bounds__(kThreads, 3) k_brick_project(Params q, int nb,
                                                                float2 *__restrict__ out) {
     extern __shared__ float2 s_vol[];
     __shared__ UnitTable s_tab;
-    int staged = -1;   // (volume, brick) held in s_vol
-    int v, brick;
-    while (fetch_unit(q, sc, nb, 0, s_tab, v, brick)) {
-        const BrickBox bx = brick_box(brick, nb);
-        const int key = v * nb * nb * nb + brick;
-        if (staged != key) {
-            stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
-            staged = key;
+    const int v = blockIdx.z, nbr = nb * nb * nb;
+    int4 rec;
+    while (next_unit(sc, 0, v, nbr, s_tab, rec)) {
+        const BrickBox bx = brick_box(rec.x, nb);
+        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+        for (int c0 = rec.y; c0 < rec.z;) {
+            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
+            for (int k; (k = next_pose(s_tab)) >= 0;) {
+                const PoseGeo &g = s_tab.pose[k];
+                float2 *o = out + (size_t)g.bp * q.plane;
+                const float sx = g.sx, sy = g.sy;
+                for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                    int l[3];
+                    float w[3][4], d[3][4];
+                    if (!active || !own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d)) return;
+                    float2 S;
+                    gather_smem<CUBIC, false>(s_vol, l, w, d, S, nullptr);
+                    if (q.shift) S = cmul(shift_phase(qx, qy, sx, sy, q.fN, q.invN), S);
+                    const int iy = qy < 0 ? qy + q.N : qy;
+                    o[iy * q.Xo + qx] = S;
+                });
+            }
             __syncthreads();
         }
-        for (int k; (k = next_pose(s_tab)) >= 0;) {
-            const PoseGeo &g = s_tab.pose[k];
-            float2 *o = out + (size_t)g.bp * q.plane;
-            const float sx = g.sx, sy = g.sy;
-            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                int l[3];
-                float w[3][4], d[3][4];
-                if (!active || !own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d)) return;
-                float2 S;
-                gather_smem<CUBIC, false>(s_vol, l, w, d, S, nullptr);
-                if (q.shift) S = cmul(shift_phase(qx, qy, sx, sy, q.fN, q.invN), S);
-                const int iy = qy < 0 ? qy + q.N : qy;
-                o[iy * q.Xo + qx] = S;
-            });
-        }
-        __syncthreads();
     }
 }
 
-// Zeros for the pixels no brick owns: outside the radius, or with floor(p)
-// outside the brick grid (all taps there lie outside the stored range).
-__global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, float2 *__restrict__ out) {
-    const int bp = blockIdx.x / q.tiles;
-    const int rem = (blockIdx.x - bp * q.tiles) * 256 + threadIdx.x;
-    if (rem >= q.plane) return;
-    const int iy = rem / q.Xo;
-    const int kx = rem - iy * q.Xo;
-    const int ky = row_freq(iy, q.N);
-    bool zero = kx * kx + ky * ky > q.r2max;
-    if (!zero) {
-        const int b = bp / q.P, pi = bp - b * q.P;
-        const Pose<3> ps = load_pose<3>(q, b, pi);
+// Zeros for the pixels no brick owns: outside the radius (one warp per
+// output row writes the tail of the row beyond the radius), and, for poses
+// whose reach exceeds the brick grid, in-radius pixels with floor(p) outside
+// it (all their taps lie outside the stored range).
+__global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, const PoseGeo *__restrict__ geo,
+                                                      float2 *__restrict__ out) {
+    const long long rows = (long long)q.B * q.P * q.N;
+    const int lane = threadIdx.x & 31;
+    const int half = q.N >> 1;
+    for (long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; row < rows;
+         row += ((long long)gridDim.x * 256) >> 5) {
+        const int bp = (int)(row / q.N), iy = (int)(row - (long long)bp * q.N);
+        const int ky = row_freq(iy, q.N);
+        const int rr = q.r2max - ky * ky;
+        const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
+        float2 *o = out + (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        for (int x = xcut + 1 + lane; x <= half; x += 32) o[x] = make_float2(0.f, 0.f);
+        if (xcut >= 0 && geo[bp].reach >= (float)G - 0.5f) {
+            const PoseGeo &g = geo[bp];
+            for (int x = lane; x <= xcut; x += 32) {
+                bool outside = false;
 #pragma unroll
-        for (int a = 0; a < 3; ++a) {
-            float t;
-            const int x0 = split_coord(fmaf(ps.a[a], (float)kx, ps.b[a] * (float)ky), t);
-            zero = zero || x0 < -G || x0 >= G;
+                for (int a = 0; a < 3; ++a) {
+                    float t;
+                    const int x0 = split_coord(fmaf(g.a[a], (float)x, g.b[a] * (float)ky), t);
+                    outside = outside || x0 < -G || x0 >= G;
+                }
+                if (outside) o[x] = make_float2(0.f, 0.f);
+            }
         }
     }
-    if (zero) out[(size_t)bp * q.plane + rem] = make_float2(0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -522,64 +606,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
                                                                  float *__restrict__ grad_shift) {
     extern __shared__ float2 s_vol[];
     __shared__ UnitTable s_tab;
-    int staged = -1;
-    int v, brick;
-    while (fetch_unit(q, sc, nb, 1, s_tab, v, brick)) {
-        const BrickBox bx = brick_box(brick, nb);
-        const int key = v * nb * nb * nb + brick;
-        if (staged != key) {
-            stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
-            staged = key;
+    const int v = blockIdx.z, nbr = nb * nb * nb;
+    int4 rec;
+    while (next_unit(sc, 1, v, nbr, s_tab, rec)) {
+        const BrickBox bx = brick_box(rec.x, nb);
+        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+        for (int c0 = rec.y; c0 < rec.z;) {
+            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
+            for (int k; (k = next_pose(s_tab)) >= 0;) {
+                const PoseGeo &g = s_tab.pose[k];
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                const float2 *gp = g_out + (size_t)g.bp * q.plane;
+                const float sx = g.sx, sy = g.sy;
+                for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                    int l[3];
+                    float w[3][4], d[3][4];
+                    if (!active || !own_sample<CUBIC, true>(g, bx, qx, qy, l, w, d)) return;
+                    float2 S, dS[3];
+                    gather_smem<CUBIC, true>(s_vol, l, w, d, S, dS);
+                    const int iy = qy < 0 ? qy + q.N : qy;
+                    const float2 gv = __ldg(gp + iy * q.Xo + qx);
+                    float2 ph = make_float2(1.f, 0.f);
+                    if (q.shift) ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
+                    const float2 gq = cmul_conj_a(ph, gv);   // conj(phase) * g
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) {
+                        const float dl = gq.x * dS[i].x + gq.y * dS[i].y;   // dL/dp_i
+                        acc[i] = fmaf(q.s * (float)qx, dl, acc[i]);
+                        acc[3 + i] = fmaf(q.s * (float)qy, dl, acc[3 + i]);
+                    }
+                    const float2 y = cmul(ph, S);
+                    const float qv = 6.283185307179586f * q.invN * (gv.x * y.y - gv.y * y.x);
+                    acc[6] = fmaf((float)qx, qv, acc[6]);
+                    acc[7] = fmaf((float)qy, qv, acc[7]);
+                });
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float t = acc[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                    acc[i] = t;
+                }
+                if ((threadIdx.x & 31) == 0) {
+                    if (grad_rot)
+#pragma unroll
+                        for (int i = 0; i < 6; ++i)
+                            if (acc[i] != 0.f) atomicAdd(grad_rot + (size_t)g.ridx * 9 + i, acc[i]);
+                    if (grad_shift) {
+                        if (acc[6] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx, acc[6]);
+                        if (acc[7] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx + 1, acc[7]);
+                    }
+                }
+            }
             __syncthreads();
         }
-        for (int k; (k = next_pose(s_tab)) >= 0;) {
-            const PoseGeo &g = s_tab.pose[k];
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            const float2 *gp = g_out + (size_t)g.bp * q.plane;
-            const float sx = g.sx, sy = g.sy;
-            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                int l[3];
-                float w[3][4], d[3][4];
-                if (!active || !own_sample<CUBIC, true>(g, bx, qx, qy, l, w, d)) return;
-                float2 S, dS[3];
-                gather_smem<CUBIC, true>(s_vol, l, w, d, S, dS);
-                const int iy = qy < 0 ? qy + q.N : qy;
-                const float2 gv = __ldg(gp + iy * q.Xo + qx);
-                float2 ph = make_float2(1.f, 0.f);
-                if (q.shift) ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
-                const float2 gq = cmul_conj_a(ph, gv);   // conj(phase) * g
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    const float dl = gq.x * dS[i].x + gq.y * dS[i].y;   // dL/dp_i
-                    acc[i] = fmaf(q.s * (float)qx, dl, acc[i]);
-                    acc[3 + i] = fmaf(q.s * (float)qy, dl, acc[3 + i]);
-                }
-                const float2 y = cmul(ph, S);
-                const float qv = 6.283185307179586f * q.invN * (gv.x * y.y - gv.y * y.x);
-                acc[6] = fmaf((float)qx, qv, acc[6]);
-                acc[7] = fmaf((float)qy, qv, acc[7]);
-            });
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float t = acc[i];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                acc[i] = t;
-            }
-            if ((threadIdx.x & 31) == 0) {
-                if (grad_rot)
-#pragma unroll
-                    for (int i = 0; i < 6; ++i)
-                        if (acc[i] != 0.f) atomicAdd(grad_rot + (size_t)g.ridx * 9 + i, acc[i]);
-                if (grad_shift) {
-                    if (acc[6] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx, acc[6]);
-                    if (acc[7] != 0.f) atomicAdd(grad_shift + 2 * (size_t)g.sidx + 1, acc[7]);
-                }
-            }
-        }
-        __syncthreads();
     }
 }
 
@@ -593,10 +675,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // pitches 20 x 20 the taps (jx, jy, jz) of a 4 x 4 x 2 block fall into 32
 // distinct banks, so the shared-memory atomics of a round never conflict.
 struct Queue {
-    float w[12][32];   // stencil weights (x, y, z; 4 each) per queued sample
-    float c[2][32];    // conj(phase) * y
-    float om[32];      // weight-spectrum factor
-    int base[32];      // accumulator offset of the first tap
+    float w[32][kQueueStride];   // per sample: wx*wy products (16), wz (4); odd stride
+    float4 rec[32];              // per sample: conj(phase) * y (re, im), omega, first tap
 };
 
 template <bool CUBIC, bool WEIGHTS>
@@ -609,90 +689,113 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
     static_assert(H::PX == 20 && H::PY == 20, "bank-conflict-free spreading assumes 20 x 20 pitches");
     constexpr int T = Stencil<CUBIC>::TAPS;
     constexpr int NACC = WEIGHTS ? 3 : 2;
+    constexpr int ZSTEP = 2 * H::PX * H::PY;   // accumulator offset of taps jz + 2
     extern __shared__ float s_dyn[];
     __shared__ UnitTable s_tab;
     float *s_re = s_dyn, *s_im = s_dyn + H::ELEMS, *s_w = s_dyn + 2 * H::ELEMS;
     Queue &Q = reinterpret_cast<Queue *>(s_dyn + NACC * H::ELEMS)[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
-    // Tap of this lane in a spreading round.
-    int tx, ty, tz, tsub;
+    // Tap of this lane in a spreading round: cubic, 32 of a sample's 64 taps
+    // (x, y from the lane, z = tz and tz + 2); linear, the 8 taps of one of
+    // four samples.
+    int txy, tz, tsub;
     if (CUBIC) {
-        tx = lane & 3;
-        ty = (lane >> 2) & 3;
-        tz = lane >> 4;          // plus 2 in the second round
+        txy = lane & 15;
+        tz = lane >> 4;
         tsub = 0;
     } else {
-        tx = lane & 1;
-        ty = (lane >> 1) & 1;
+        txy = (lane & 1) + 4 * ((lane >> 1) & 1);
         tz = (lane >> 2) & 1;
-        tsub = lane >> 3;        // which of 4 samples this lane serves
+        tsub = lane >> 3;
     }
-    const int toff = tx + H::PX * ty + H::PX * H::PY * tz;
+    const int toff = (txy & 3) + H::PX * (txy >> 2) + H::PX * H::PY * tz;
     const int half = q.M >> 1;
-    int v, brick;
-    while (fetch_unit(q, sc, nb, 2, s_tab, v, brick)) {
-        const BrickBox bx = brick_box(brick, nb);
+    const int v = blockIdx.z, nbr = nb * nb * nb;
+    float2 *Vd = dst + (size_t)v * q.src_stride;
+    float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
+    int4 rec;
+    while (next_unit(sc, 2, v, nbr, s_tab, rec)) {
+        const BrickBox bx = brick_box(rec.x, nb);
         for (int e = threadIdx.x; e < NACC * H::ELEMS; e += kThreads) s_dyn[e] = 0.f;
         __syncthreads();
-        for (int k; (k = next_pose(s_tab)) >= 0;) {
-            const PoseGeo &g = s_tab.pose[k];
-            const size_t ib = (size_t)g.bp * q.plane;
-            const float sx = g.sx, sy = g.sy;
-            for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                int l[3];
-                float w[3][4], d[3][4];
-                const bool own = active && own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d);
-                const unsigned mask = __ballot_sync(0xffffffffu, own);
-                if (own) {
-                    const int slot = __popc(mask & ((1u << lane) - 1u));
-                    const int iy = qy < 0 ? qy + q.N : qy;
-                    float2 cv = __ldg(img + ib + iy * q.Xo + qx);
-                    if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, sx, sy, q.fN, q.invN), cv);
+        for (int c0 = rec.y; c0 < rec.z;) {
+            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
+            for (int k; (k = next_pose(s_tab)) >= 0;) {
+                const PoseGeo &g = s_tab.pose[k];
+                const size_t ib = (size_t)g.bp * q.plane;
+                const float sx = g.sx, sy = g.sy;
+                for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                    int l[3];
+                    float w[3][4], d[3][4];
+                    const bool own = active && own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d);
+                    const unsigned mask = __ballot_sync(0xffffffffu, own);
+                    if (own) {
+                        const int slot = __popc(mask & ((1u << lane) - 1u));
+                        const int iy = qy < 0 ? qy + q.N : qy;
+                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, sx, sy, q.fN, q.invN), cv);
+                        float *wq = Q.w[slot];
 #pragma unroll
-                    for (int a = 0; a < 3; ++a)
+                        for (int jy = 0; jy < T; ++jy)
 #pragma unroll
-                        for (int i = 0; i < T; ++i) Q.w[4 * a + i][slot] = w[a][i];
-                    Q.c[0][slot] = cv.x;
-                    Q.c[1][slot] = cv.y;
-                    if (WEIGHTS) Q.om[slot] = omega ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
-                    Q.base[slot] = (l[2] * H::PY + l[1]) * H::PX + l[0];
-                }
-                __syncwarp();
-                const int nq = __popc(mask);
-                if (CUBIC) {
-                    for (int sq = 0; sq < nq; ++sq) {
-                        const float wxy = Q.w[tx][sq] * Q.w[4 + ty][sq];
-                        const float cr = Q.c[0][sq], ci = Q.c[1][sq];
-                        const int b0 = Q.base[sq] + toff;
-                        const float om = WEIGHTS ? Q.om[sq] : 0.f;
+                            for (int jx = 0; jx < T; ++jx) wq[jx + 4 * jy] = w[0][jx] * w[1][jy];
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const float wt = wxy * Q.w[8 + tz + 2 * r][sq];
-                            const int idx = b0 + r * 2 * H::PX * H::PY;
-                            atomicAdd(s_re + idx, wt * cr);
-                            atomicAdd(s_im + idx, wt * ci);
-                            if (WEIGHTS) atomicAdd(s_w + idx, wt * om);
+                        for (int jz = 0; jz < T; ++jz) wq[16 + jz] = w[2][jz];
+                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
+                                                  __int_as_float((l[2] * H::PY + l[1]) * H::PX + l[0]));
+                    }
+                    __syncwarp();
+                    const int nq = __popc(mask);
+                    if (CUBIC) {
+                        // The next sample's queue entries are read before this
+                        // sample's atomics are issued, hiding their latency.
+                        float wxy = 0.f, wz0 = 0.f, wz1 = 0.f;
+                        float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (nq > 0) {
+                            wxy = Q.w[0][txy];
+                            wz0 = Q.w[0][16 + tz];
+                            wz1 = Q.w[0][18 + tz];
+                            r4 = Q.rec[0];
+                        }
+                        for (int sq = 0; sq < nq; ++sq) {
+                            const float wt0 = wxy * wz0, wt1 = wxy * wz1;
+                            const float4 cur = r4;
+                            if (sq + 1 < nq) {
+                                wxy = Q.w[sq + 1][txy];
+                                wz0 = Q.w[sq + 1][16 + tz];
+                                wz1 = Q.w[sq + 1][18 + tz];
+                                r4 = Q.rec[sq + 1];
+                            }
+                            const int idx = __float_as_int(cur.w) + toff;
+                            atomicAdd(s_re + idx, wt0 * cur.x);
+                            atomicAdd(s_im + idx, wt0 * cur.y);
+                            atomicAdd(s_re + idx + ZSTEP, wt1 * cur.x);
+                            atomicAdd(s_im + idx + ZSTEP, wt1 * cur.y);
+                            if (WEIGHTS) {
+                                atomicAdd(s_w + idx, wt0 * cur.z);
+                                atomicAdd(s_w + idx + ZSTEP, wt1 * cur.z);
+                            }
+                        }
+                    } else {
+                        for (int s0 = 0; s0 < nq; s0 += 4) {
+                            const int sq = s0 + tsub;
+                            if (sq < nq) {
+                                const float wt = Q.w[sq][txy] * Q.w[sq][16 + tz];
+                                const float4 r4 = Q.rec[sq];
+                                const int idx = __float_as_int(r4.w) + toff;
+                                atomicAdd(s_re + idx, wt * r4.x);
+                                atomicAdd(s_im + idx, wt * r4.y);
+                                if (WEIGHTS) atomicAdd(s_w + idx, wt * r4.z);
+                            }
                         }
                     }
-                } else {
-                    for (int s0 = 0; s0 < nq; s0 += 4) {
-                        const int sq = s0 + tsub;
-                        if (sq < nq) {
-                            const float wt = Q.w[tx][sq] * Q.w[4 + ty][sq] * Q.w[8 + tz][sq];
-                            const int idx = Q.base[sq] + toff;
-                            atomicAdd(s_re + idx, wt * Q.c[0][sq]);
-                            atomicAdd(s_im + idx, wt * Q.c[1][sq]);
-                            if (WEIGHTS) atomicAdd(s_w + idx, wt * Q.om[sq]);
-                        }
-                    }
-                }
-                __syncwarp();
-            });
+                    __syncwarp();
+                });
+            }
+            __syncthreads();
         }
-        __syncthreads();
         // Fold brick + halo into the stored half-spectrum.
-        float2 *Vd = dst + (size_t)v * q.src_stride;
-        float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
         const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
                   z0 = bx.o[2] - Stencil<CUBIC>::LO;
         for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
@@ -727,18 +830,21 @@ int bricks_per_axis(int M, bool cubic) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t geo, masks, total;
+    size_t geo, masks, hits, units, total;
     int nb, nchunks;
 };
 
 Layout layout(const Params &q, bool cubic) {
     Layout L;
     L.nb = bricks_per_axis(q.M, cubic);
+    const size_t nbr = (size_t)L.nb * L.nb * L.nb;
     const long long Pv = (q.Bsrc == 1) ? (long long)q.B * q.P : q.P;
     L.nchunks = (int)((Pv + 31) / 32);
-    L.geo = 256;   // counters first
+    L.geo = align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);   // counters first
     L.masks = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
-    L.total = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * L.nb * L.nb * L.nb * L.nchunks);
+    L.hits = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * L.nchunks);
+    L.units = L.hits + align256(sizeof(int) * (size_t)q.Bsrc * nbr);
+    L.total = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
     return L;
 }
 
@@ -748,6 +854,8 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.counters = reinterpret_cast<unsigned *>(base);
     sc.geo = reinterpret_cast<PoseGeo *>(base + L.geo);
     sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
+    sc.hits = reinterpret_cast<int *>(base + L.hits);
+    sc.units = reinterpret_cast<int4 *>(base + L.units);
     sc.nchunks = L.nchunks;
     return sc;
 }
@@ -762,15 +870,27 @@ int resident_blocks(const void *kern, size_t smem) {
     return sms * per_sm;
 }
 
-// Pose geometry and brick masks for the poses of q (shared by the main kernels).
+// Pose geometry, brick masks and work units for the poses of q (shared by
+// the main kernels of one call).
 cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_t st) {
-    const int pb = (q.B * q.P + 255) / 256;
-    k_pose_geometry<<<pb, 256, 0, st>>>(q, sc.geo, sc.counters);
-    const long long warps = (long long)q.Bsrc * L.nb * L.nb * L.nb * L.nchunks;
+    const int nbr = L.nb * L.nb * L.nb;
+    const int pb = (int)((q.B * (long long)q.P + 255) / 256);
+    k_pose_geometry<<<pb, 256, 0, st>>>(q, nbr, sc);
+    const long long warps = (long long)q.Bsrc * nbr * L.nchunks;
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 32) blocks = 65535LL * 32;
-    k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, L.nchunks, sc.geo, sc.masks);
+    k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, sc);
+    k_plan_units<<<q.Bsrc, kPlanThreads, 0, st>>>(nbr, sc);
     return cudaGetLastError();
+}
+
+// Blocks of a main kernel: the resident ones, shared out over the volumes
+// (each volume has its own unit list and counter, indexed by blockIdx.z).
+dim3 main_grid(const Params &q, const void *kern, size_t smem) {
+    const long long res = resident_blocks(kern, smem);
+    long long per = (res + q.Bsrc - 1) / q.Bsrc;
+    if (per < 1) per = 1;
+    return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
 }
 
 template <bool CUBIC>
@@ -782,9 +902,10 @@ cudaError_t project_t(const Params &q, float2 *out, void *ws, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = bin(q, L, sc, st)) != cudaSuccess) return e;
-    const long long zb = (long long)q.B * q.P * q.tiles;
-    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, out);
-    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out);
+    const long long zrows = (long long)q.B * q.P * q.N;
+    const long long zb = (zrows + 7) / 8 < 65535LL * 32 ? (zrows + 7) / 8 : 65535LL * 32;
+    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, sc.geo, out);
+    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out);
     return cudaGetLastError();
 }
 
@@ -798,8 +919,8 @@ cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gs
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
-    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, g, grot,
-                                                                          gshift);
+    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, g, grot,
+                                                                       gshift);
     return cudaGetLastError();
 }
 
@@ -813,8 +934,8 @@ cudaError_t scatter_t(const Params &q, const float2 *img, const float *omega, fl
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
-    kern<<<resident_blocks((const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
-                                                                          dst, wdst);
+    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
+                                                                       dst, wdst);
     return cudaGetLastError();
 }
 

@@ -397,10 +397,10 @@ def run_ours(args):
             "in_radius_samples_per_step": P * in_radius_count(N, w["radius"]),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            # per step: forward (pose geometry, brick masks, zero fill, gather), then the
-            # pose-gradient call (geometry, masks, gather) and the volume-gradient call
-            # (geometry, masks, scatter) -- all kernels of this library
-            "gpu_launches": 10 * args.steps,
+            # per step: forward (pose geometry, brick masks, unit plan, zero fill, gather),
+            # then the pose-gradient call (geometry, masks, plan, gather) and the
+            # volume-gradient call (geometry, masks, plan, scatter): all of this library
+            "gpu_launches": 13 * args.steps,
             "clocks": clocks.record(),
             "cpu_baseline": cpu_line,
         }
