@@ -674,6 +674,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // the warp take 32 of a sample's 64 taps per round.  With the accumulator
 // pitches 20 x 20 the taps (jx, jy, jz) of a 4 x 4 x 2 block fall into 32
 // distinct banks, so the shared-memory atomics of a round never conflict.
+// Adds v[i] to the shared-memory floats *a[i] as one batch of compare-and-
+// swap operations.  A float atomicAdd to shared memory is itself a
+// compare-and-swap retry loop on this architecture; issuing several of them
+// one after another serialises their round trips.  Here all old values are
+// read, all sums formed and all swaps issued before any result is examined,
+// and only a swap that lost a race is retried (each lost race is another
+// completed addition, so the loop terminates).  The words need not be
+// distinct: when two of them coincide the later swap sees the earlier one's
+// result, fails once and retries.
+template <int N>
+__device__ __forceinline__ void shared_add(float *const (&a)[N], const float (&v)[N]) {
+    unsigned seen[N], got[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) seen[i] = *reinterpret_cast<volatile unsigned *>(a[i]);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        got[i] = atomicCAS(reinterpret_cast<unsigned *>(a[i]), seen[i],
+                           __float_as_uint(__uint_as_float(seen[i]) + v[i]));
+    unsigned left = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (got[i] != seen[i]) left |= 1u << i;
+    while (left) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (!((left >> i) & 1u)) continue;
+            seen[i] = got[i];
+            got[i] = atomicCAS(reinterpret_cast<unsigned *>(a[i]), seen[i],
+                               __float_as_uint(__uint_as_float(seen[i]) + v[i]));
+            if (got[i] == seen[i]) left &= ~(1u << i);
+        }
+    }
+}
+
 struct Queue {
     float w[32][kQueueStride];   // per sample: wx*wy products (16), wz (4); odd stride
     float4 rec[32];              // per sample: conj(phase) * y (re, im), omega, first tap
@@ -749,7 +783,7 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
                     const int nq = __popc(mask);
                     if (CUBIC) {
                         // The next sample's queue entries are read before this
-                        // sample's atomics are issued, hiding their latency.
+                        // sample's additions are issued, hiding their latency.
                         float wxy = 0.f, wz0 = 0.f, wz1 = 0.f;
                         float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (nq > 0) {
@@ -768,13 +802,18 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
                                 r4 = Q.rec[sq + 1];
                             }
                             const int idx = __float_as_int(cur.w) + toff;
-                            atomicAdd(s_re + idx, wt0 * cur.x);
-                            atomicAdd(s_im + idx, wt0 * cur.y);
-                            atomicAdd(s_re + idx + ZSTEP, wt1 * cur.x);
-                            atomicAdd(s_im + idx + ZSTEP, wt1 * cur.y);
                             if (WEIGHTS) {
-                                atomicAdd(s_w + idx, wt0 * cur.z);
-                                atomicAdd(s_w + idx + ZSTEP, wt1 * cur.z);
+                                float *const a[6] = {s_re + idx, s_im + idx, s_re + idx + ZSTEP,
+                                                     s_im + idx + ZSTEP, s_w + idx, s_w + idx + ZSTEP};
+                                const float val[6] = {wt0 * cur.x, wt0 * cur.y, wt1 * cur.x,
+                                                      wt1 * cur.y, wt0 * cur.z, wt1 * cur.z};
+                                shared_add<6>(a, val);
+                            } else {
+                                float *const a[4] = {s_re + idx, s_im + idx, s_re + idx + ZSTEP,
+                                                     s_im + idx + ZSTEP};
+                                const float val[4] = {wt0 * cur.x, wt0 * cur.y, wt1 * cur.x,
+                                                      wt1 * cur.y};
+                                shared_add<4>(a, val);
                             }
                         }
                     } else {

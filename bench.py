@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--poses", type=int, default=None,
                     help="pose count (default: the workload's 512); smaller runs are for profiling")
+    ap.add_argument("--ncu-summary", metavar="RAW_CSV", default=None,
+                    help="write profiles/ncu_traffic.json from `ncu -i REP --page raw --csv` output")
     return ap.parse_args()
 
 
@@ -211,15 +213,64 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the sources still match."""
+# The three kernels that do the work of a step, by the bench's segment names.
+NCU_KERNELS = {"project_3d_2d": "k_brick_project", "pose_grad_gather": "k_brick_pose_grad",
+               "volume_grad_scatter": "k_brick_scatter"}
+NCU_METRICS = {"dram__bytes_read.sum": "dram_read_bytes", "dram__bytes_write.sum": "dram_write_bytes",
+               "gpu__time_duration.sum": "duration_ns",
+               "gpu__compute_memory_throughput.avg.pct_of_peak_sustained_elapsed": "mem_sol_pct",
+               "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed": "dram_pct",
+               "lts__throughput.avg.pct_of_peak_sustained_elapsed": "l2_pct",
+               "l1tex__throughput.avg.pct_of_peak_sustained_elapsed": "l1_pct",
+               "sm__warps_active.avg.pct_of_peak_sustained_active": "warps_active_pct",
+               "launch__registers_per_thread": "registers"}
+UNIT_SCALE = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9,
+              "ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1,
+              "%": 1, "register/thread": 1, "": 1}
+
+
+def ncu_summary(csv_path, out_path):
+    """Write profiles/ncu_traffic.json from `ncu -i <rep> --page raw --csv` output.
+
+    One entry per bench segment with the captured launch's DRAM bytes, duration
+    and throughput percentages, tagged with the hash of the kernel sources so
+    that a stale summary is never reported against changed kernels."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    names, units = rows[hdr], rows[hdr + 1]
+    col = {n: i for i, n in enumerate(names)}
+    kernels = {}
+    for r in rows[hdr + 2:]:
+        if len(r) != len(names):
+            continue
+        kname = r[col["Kernel Name"]]
+        seg = next((s for s, k in NCU_KERNELS.items() if k + "<" in kname or k + "(" in kname), None)
+        if seg is None or seg in kernels:
+            continue
+        d = {"kernel": kname.split("(")[0]}
+        for m, key in NCU_METRICS.items():
+            if m in col and r[col[m]] not in ("", "n/a"):
+                d[key] = float(r[col[m]].replace(",", "")) * UNIT_SCALE.get(units[col[m]], 1)
+        if "dram_read_bytes" in d and "dram_write_bytes" in d:
+            d["dram_bytes_per_launch"] = d["dram_read_bytes"] + d["dram_write_bytes"]
+        kernels[seg] = d
+    out = {"source_sha": kernel_source_sha(), "from": os.path.basename(csv_path), "kernels": kernels}
+    with open(out_path, "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    return out
+
+
+def ncu_profile():
+    """The committed ncu summary, if the kernel sources still match it."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         if d.get("source_sha") != kernel_source_sha():
             return None
-        return d["kernels"][kernel]["dram_bytes_per_launch"]
+        return d["kernels"]
     except Exception:  # noqa: BLE001
         return None
 
@@ -381,6 +432,21 @@ def run_ours(args):
         t_ms, nbytes = kern[dom]
         peak, peak_src = measured_peak_hbm()
         achieved = nbytes / (t_ms * 1e-3) / 1e9
+        prof = ncu_profile()
+        traffic, sol = None, None
+        if prof:
+            traffic = prof.get(dom, {}).get("dram_bytes_per_launch")
+            # Memory SOL % (max of DRAM, L2, L1 throughput) of the three
+            # kernels, weighted by their share of the step.
+            wsum = sum(kern[k][0] for k in kern if "mem_sol_pct" in prof.get(k, {}))
+            if wsum > 0:
+                sol = {"mem_sol_pct_time_weighted": sum(
+                    kern[k][0] * prof[k]["mem_sol_pct"] for k in kern
+                    if "mem_sol_pct" in prof.get(k, {})) / wsum,
+                       "per_kernel": {k: {m: prof[k].get(m) for m in
+                                          ("mem_sol_pct", "l1_pct", "l2_pct", "dram_pct")}
+                                      for k in kern if k in prof},
+                       "source": "profiles/ncu_traffic.json (ncu --set full, same sources)"}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -389,8 +455,9 @@ def run_ours(args):
             "config": config_dict(w, P),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": ncu_traffic(dom),
+                         "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes},
+            "ncu_memory_sol": sol,
             "breakdown_ms": {n: float(mean_seg[i]) for i, n in enumerate(names)},
             "fwd_gsamples_s": samples / (mean_seg[0] * 1e-3) / 1e9,
             "bwd_gsamples_s": samples / ((mean_seg[2] + mean_seg[3]) * 1e-3) / 1e9,
@@ -412,6 +479,10 @@ def run_ours(args):
 
 def main():
     args = parse_args()
+    if args.ncu_summary:
+        out = ncu_summary(args.ncu_summary, os.path.join(ROOT, "profiles", "ncu_traffic.json"))
+        print(json.dumps(out, indent=1))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
