@@ -512,7 +512,7 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
 }
 
 // Owned-sample set-up: position, ownership and stencil of pixel (qx, qy).
-template <bool CUBIC, bool DERIV>
+template <bool CUBIC, bool DERIV, int SIZE = kBS>
 __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx, int qx, int qy,
                                            int *l, float (*w)[4], float (*d)[4]) {
     bool own = true;
@@ -522,7 +522,7 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
         float t;
         const int x0 = split_coord(p, t);
         l[a] = x0 - bx.o[a];
-        own = own && (unsigned)l[a] < (unsigned)kBS;
+        own = own && (unsigned)l[a] < (unsigned)SIZE;
         Stencil<CUBIC>::weights(t, w[a]);
         if (DERIV) Stencil<CUBIC>::derivs(t, d[a]);
     }
@@ -668,80 +668,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // ---------------------------------------------------------------------------
 // Backprojection / spectrum gradient (adjoint of the forward projection).
 //
-// Each group of 32 candidates is set up one sample per lane (ownership,
-// stencil weights, conj(phase) * y); the owned samples are queued in shared
-// memory and then spread cooperatively: in the cubic case the 32 lanes of
-// the warp take 32 of a sample's 64 taps per round.  With the accumulator
-// pitches 20 x 20 the taps (jx, jy, jz) of a 4 x 4 x 2 block fall into 32
-// distinct banks, so the shared-memory atomics of a round never conflict.
-// Adds v[i] to the shared-memory floats *a[i] as one batch of compare-and-
-// swap operations.  A float atomicAdd to shared memory is itself a
-// compare-and-swap retry loop on this architecture; issuing several of them
-// one after another serialises their round trips.  Here all old values are
-// read, all sums formed and all swaps issued before any result is examined,
-// and only a swap that lost a race is retried (each lost race is another
-// completed addition, so the loop terminates).  The words need not be
-// distinct: when two of them coincide the later swap sees the earlier one's
-// result, fails once and retries.
-template <int N>
-__device__ __forceinline__ void shared_add(float *const (&a)[N], const float (&v)[N]) {
-    unsigned seen[N], got[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) seen[i] = *reinterpret_cast<volatile unsigned *>(a[i]);
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        got[i] = atomicCAS(reinterpret_cast<unsigned *>(a[i]), seen[i],
-                           __float_as_uint(__uint_as_float(seen[i]) + v[i]));
-    unsigned left = 0;
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (got[i] != seen[i]) left |= 1u << i;
-    while (left) {
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            if (!((left >> i) & 1u)) continue;
-            seen[i] = got[i];
-            got[i] = atomicCAS(reinterpret_cast<unsigned *>(a[i]), seen[i],
-                               __float_as_uint(__uint_as_float(seen[i]) + v[i]));
-            if (got[i] == seen[i]) left &= ~(1u << i);
-        }
-    }
-}
+// Both kernels set up each group of 32 candidates one sample per lane
+// (ownership, stencil weights, conj(phase) * y), queue the owned samples in
+// shared memory and then spread them cooperatively over the taps.
 
+// Linear: a block shares one accumulator for brick + halo; the warps work on
+// different poses of the unit and add with shared-memory atomics, the 32
+// lanes taking the 8 taps of each of four samples per round.
 struct Queue {
     float w[32][kQueueStride];   // per sample: wx*wy products (16), wz (4); odd stride
     float4 rec[32];              // per sample: conj(phase) * y (re, im), omega, first tap
 };
 
-template <bool CUBIC, bool WEIGHTS>
-__global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Scratch sc,
-                                                            const float2 *__restrict__ img,
-                                                            const float *__restrict__ omega,
-                                                            float2 *__restrict__ dst,
-                                                            float *__restrict__ wdst) {
-    using H = Halo<CUBIC>;
-    static_assert(H::PX == 20 && H::PY == 20, "bank-conflict-free spreading assumes 20 x 20 pitches");
-    constexpr int T = Stencil<CUBIC>::TAPS;
+template <bool WEIGHTS>
+__global__ void __launch_bounds__(kThreads, 2) k_brick_scatter_linear(Params q, int nb, Scratch sc,
+                                                                     const float2 *__restrict__ img,
+                                                                     const float *__restrict__ omega,
+                                                                     float2 *__restrict__ dst,
+                                                                     float *__restrict__ wdst) {
+    using H = Halo<false>;
     constexpr int NACC = WEIGHTS ? 3 : 2;
-    constexpr int ZSTEP = 2 * H::PX * H::PY;   // accumulator offset of taps jz + 2
     extern __shared__ float s_dyn[];
     __shared__ UnitTable s_tab;
     float *s_re = s_dyn, *s_im = s_dyn + H::ELEMS, *s_w = s_dyn + 2 * H::ELEMS;
     Queue &Q = reinterpret_cast<Queue *>(s_dyn + NACC * H::ELEMS)[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
-    // Tap of this lane in a spreading round: cubic, 32 of a sample's 64 taps
-    // (x, y from the lane, z = tz and tz + 2); linear, the 8 taps of one of
-    // four samples.
-    int txy, tz, tsub;
-    if (CUBIC) {
-        txy = lane & 15;
-        tz = lane >> 4;
-        tsub = 0;
-    } else {
-        txy = (lane & 1) + 4 * ((lane >> 1) & 1);
-        tz = (lane >> 2) & 1;
-        tsub = lane >> 3;
-    }
+    const int txy = (lane & 1) + 4 * ((lane >> 1) & 1), tz = (lane >> 2) & 1, tsub = lane >> 3;
     const int toff = (txy & 3) + H::PX * (txy >> 2) + H::PX * H::PY * tz;
     const int half = q.M >> 1;
     const int v = blockIdx.z, nbr = nb * nb * nb;
@@ -761,7 +713,7 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
                 for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
                     int l[3];
                     float w[3][4], d[3][4];
-                    const bool own = active && own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d);
+                    const bool own = active && own_sample<false, false>(g, bx, qx, qy, l, w, d);
                     const unsigned mask = __ballot_sync(0xffffffffu, own);
                     if (own) {
                         const int slot = __popc(mask & ((1u << lane) - 1u));
@@ -770,63 +722,26 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
                         if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, sx, sy, q.fN, q.invN), cv);
                         float *wq = Q.w[slot];
 #pragma unroll
-                        for (int jy = 0; jy < T; ++jy)
+                        for (int jy = 0; jy < 2; ++jy)
 #pragma unroll
-                            for (int jx = 0; jx < T; ++jx) wq[jx + 4 * jy] = w[0][jx] * w[1][jy];
-#pragma unroll
-                        for (int jz = 0; jz < T; ++jz) wq[16 + jz] = w[2][jz];
+                            for (int jx = 0; jx < 2; ++jx) wq[jx + 4 * jy] = w[0][jx] * w[1][jy];
+                        wq[16] = w[2][0];
+                        wq[17] = w[2][1];
                         const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * H::PY + l[1]) * H::PX + l[0]));
                     }
                     __syncwarp();
                     const int nq = __popc(mask);
-                    if (CUBIC) {
-                        // The next sample's queue entries are read before this
-                        // sample's additions are issued, hiding their latency.
-                        float wxy = 0.f, wz0 = 0.f, wz1 = 0.f;
-                        float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (nq > 0) {
-                            wxy = Q.w[0][txy];
-                            wz0 = Q.w[0][16 + tz];
-                            wz1 = Q.w[0][18 + tz];
-                            r4 = Q.rec[0];
-                        }
-                        for (int sq = 0; sq < nq; ++sq) {
-                            const float wt0 = wxy * wz0, wt1 = wxy * wz1;
-                            const float4 cur = r4;
-                            if (sq + 1 < nq) {
-                                wxy = Q.w[sq + 1][txy];
-                                wz0 = Q.w[sq + 1][16 + tz];
-                                wz1 = Q.w[sq + 1][18 + tz];
-                                r4 = Q.rec[sq + 1];
-                            }
-                            const int idx = __float_as_int(cur.w) + toff;
-                            if (WEIGHTS) {
-                                float *const a[6] = {s_re + idx, s_im + idx, s_re + idx + ZSTEP,
-                                                     s_im + idx + ZSTEP, s_w + idx, s_w + idx + ZSTEP};
-                                const float val[6] = {wt0 * cur.x, wt0 * cur.y, wt1 * cur.x,
-                                                      wt1 * cur.y, wt0 * cur.z, wt1 * cur.z};
-                                shared_add<6>(a, val);
-                            } else {
-                                float *const a[4] = {s_re + idx, s_im + idx, s_re + idx + ZSTEP,
-                                                     s_im + idx + ZSTEP};
-                                const float val[4] = {wt0 * cur.x, wt0 * cur.y, wt1 * cur.x,
-                                                      wt1 * cur.y};
-                                shared_add<4>(a, val);
-                            }
-                        }
-                    } else {
-                        for (int s0 = 0; s0 < nq; s0 += 4) {
-                            const int sq = s0 + tsub;
-                            if (sq < nq) {
-                                const float wt = Q.w[sq][txy] * Q.w[sq][16 + tz];
-                                const float4 r4 = Q.rec[sq];
-                                const int idx = __float_as_int(r4.w) + toff;
-                                atomicAdd(s_re + idx, wt * r4.x);
-                                atomicAdd(s_im + idx, wt * r4.y);
-                                if (WEIGHTS) atomicAdd(s_w + idx, wt * r4.z);
-                            }
+                    for (int s0 = 0; s0 < nq; s0 += 4) {
+                        const int sq = s0 + tsub;
+                        if (sq < nq) {
+                            const float wt = Q.w[sq][txy] * Q.w[sq][16 + tz];
+                            const float4 r4 = Q.rec[sq];
+                            const int idx = __float_as_int(r4.w) + toff;
+                            atomicAdd(s_re + idx, wt * r4.x);
+                            atomicAdd(s_im + idx, wt * r4.y);
+                            if (WEIGHTS) atomicAdd(s_w + idx, wt * r4.z);
                         }
                     }
                     __syncwarp();
@@ -835,8 +750,7 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
             __syncthreads();
         }
         // Fold brick + halo into the stored half-spectrum.
-        const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
-                  z0 = bx.o[2] - Stencil<CUBIC>::LO;
+        const int x0 = bx.o[0], y0 = bx.o[1], z0 = bx.o[2];
         for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
             const int lx = e % H::S, ly = (e / H::S) % H::S, lz = e / (H::S * H::S);
             const int k = (lz * H::PY + ly) * H::PX + lx;
@@ -856,6 +770,189 @@ __global__ void __launch_bounds__(kThreads) k_brick_scatter(Params q, int nb, Sc
             if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
         }
         __syncthreads();
+    }
+}
+
+// Cubic: every warp owns a private accumulator for one octant (8^3) of a
+// brick plus the stencil's halo, so the spreading needs no atomics.  A warp
+// takes (work unit, octant) items from the global counter on its own, runs
+// through all poses of the unit that reach its octant and enumerates only
+// the samples whose floor(p) lies in it; each sample is spread by the whole
+// warp, the lanes taking its taps (jx, jy, jz) and (jx, jy, jz + 2) with
+// x, y from the lane and jz from the half-warp.  With the tile's x pitch of
+// 12 complex words the 16 lanes of a half-warp fall into distinct bank
+// pairs, so the 64-bit reads and writes of a round never conflict.  The
+// tile is folded into the stored half-spectrum with vector global atomics
+// when the item is done.
+constexpr int kOct = kBS / 2;              // octant edge
+constexpr int kOS = kOct + 3;              // octant + cubic halo (taps x0 - 1 .. x0 + 2)
+constexpr int kOPX = 12;                   // x pitch of the tile (complex words)
+constexpr int kOElems = kOS * kOS * kOPX;  // complex words of the tile
+constexpr int kOQW = 13;                   // floats per queued weight row (odd: no bank conflicts)
+
+struct OctQueue {
+    float w[32][kOQW];   // per sample: wx (4), wy (4), wz (4)
+    float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
+};
+
+template <bool WEIGHTS>
+struct OctLayout {
+    static constexpr int WARPS = WEIGHTS ? 2 : 4;   // warps per block (blocks only share an SM)
+    static constexpr size_t TILE = sizeof(float2) * kOElems;
+    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * kOElems : 0;
+    static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(OctQueue);
+    static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned queue");
+};
+
+__device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct) {
+    BrickBox ob;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        ob.o[d] = bx.o[d] + kOct * ((oct >> d) & 1);
+        ob.lo[d] = (float)ob.o[d] - kMargin;
+        ob.hi[d] = (float)(ob.o[d] + kOct) + kMargin;
+    }
+    return ob;
+}
+
+__device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
+    PoseGeo g;
+    const int *src = reinterpret_cast<const int *>(p);
+    int *dst = reinterpret_cast<int *>(&g);
+#pragma unroll
+    for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+    return g;
+}
+
+template <bool WEIGHTS>
+__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 4)
+    k_brick_scatter_cubic(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
+                          const float *__restrict__ omega, float2 *__restrict__ dst,
+                          float *__restrict__ wdst) {
+    using OL = OctLayout<WEIGHTS>;
+    extern __shared__ float4 s_oct[];
+    const int lane = threadIdx.x & 31;
+    char *mine = reinterpret_cast<char *>(s_oct) + (threadIdx.x >> 5) * OL::WARP_BYTES;
+    float2 *acc = reinterpret_cast<float2 *>(mine);
+    float *wacc = reinterpret_cast<float *>(mine + OL::TILE);
+    OctQueue &Q = *reinterpret_cast<OctQueue *>(mine + OL::TILE + OL::WTILE);
+    const int jx = lane & 3, jy = (lane >> 2) & 3, tz = lane >> 4;
+    const int toff = jx + kOPX * (jy + kOS * tz);
+    constexpr int ZSTEP = 2 * kOPX * kOS;   // tile offset of taps jz + 2
+    const int half = q.M >> 1;
+    const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
+    const int items = 8 * (int)__ldg(sc.counters + 3 * nvol + v);
+    const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
+    float2 *Vd = dst + (size_t)v * q.src_stride;
+    float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
+    for (int e = lane; e < kOElems; e += 32) {
+        acc[e] = make_float2(0.f, 0.f);
+        if (WEIGHTS) wacc[e] = 0.f;
+    }
+    __syncwarp();
+    for (;;) {
+        int item = 0;
+        if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= items) break;
+        const int4 rec = __ldg(units + (item >> 3));
+        const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
+        const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
+        bool touched = false;
+        for (int c = rec.y; c < rec.z; ++c) {
+            for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
+                const PoseGeo g = load_geo(sc.geo + pose_id(q, v, c * 32 + __ffs(m) - 1));
+                if (!pose_reaches(g, ob)) continue;
+                touched = true;
+                const size_t ib = (size_t)g.bp * q.plane;
+                for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                    int l[3];
+                    float w[3][4], d[3][4];
+                    const bool own = active && own_sample<true, false, kOct>(g, ob, qx, qy, l, w, d);
+                    const unsigned mask = __ballot_sync(0xffffffffu, own);
+                    if (own) {
+                        const int slot = __popc(mask & ((1u << lane) - 1u));
+                        const int iy = qy < 0 ? qy + q.N : qy;
+                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
+                        float *wq = Q.w[slot];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            wq[j] = w[0][j];
+                            wq[4 + j] = w[1][j];
+                            wq[8 + j] = w[2][j];
+                        }
+                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
+                                                  __int_as_float((l[2] * kOS + l[1]) * kOPX + l[0]));
+                    }
+                    __syncwarp();
+                    const int nq = __popc(mask);
+                    // The next sample's queue entries are read before this
+                    // sample's tile words, hiding their latency.
+                    float wx = 0.f, wy = 0.f, wz0 = 0.f, wz1 = 0.f;
+                    float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (nq > 0) {
+                        wx = Q.w[0][jx];
+                        wy = Q.w[0][4 + jy];
+                        wz0 = Q.w[0][8 + tz];
+                        wz1 = Q.w[0][10 + tz];
+                        r4 = Q.rec[0];
+                    }
+                    for (int sq = 0; sq < nq; ++sq) {
+                        const float wxy = wx * wy;
+                        const float wt0 = wxy * wz0, wt1 = wxy * wz1;
+                        const float4 cur = r4;
+                        if (sq + 1 < nq) {
+                            wx = Q.w[sq + 1][jx];
+                            wy = Q.w[sq + 1][4 + jy];
+                            wz0 = Q.w[sq + 1][8 + tz];
+                            wz1 = Q.w[sq + 1][10 + tz];
+                            r4 = Q.rec[sq + 1];
+                        }
+                        const int idx = __float_as_int(cur.w) + toff;
+                        float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
+                        a0.x = fmaf(wt0, cur.x, a0.x);
+                        a0.y = fmaf(wt0, cur.y, a0.y);
+                        a1.x = fmaf(wt1, cur.x, a1.x);
+                        a1.y = fmaf(wt1, cur.y, a1.y);
+                        acc[idx] = a0;
+                        acc[idx + ZSTEP] = a1;
+                        if (WEIGHTS) {
+                            wacc[idx] = fmaf(wt0, cur.z, wacc[idx]);
+                            wacc[idx + ZSTEP] = fmaf(wt1, cur.z, wacc[idx + ZSTEP]);
+                        }
+                        // The lanes' words of a sample are distinct, but the
+                        // next sample's taps may reuse another lane's words.
+                        __syncwarp();
+                    }
+                });
+            }
+        }
+        if (!touched) continue;
+        // Fold the tile into the stored half-spectrum and clear it.
+        const int x0 = ob.o[0] - 1, y0 = ob.o[1] - 1, z0 = ob.o[2] - 1;
+        for (int e = lane; e < kOS * kOS * kOS; e += 32) {
+            const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
+            const int k = (lz * kOS + ly) * kOPX + lx;
+            const float2 cv = acc[k];
+            const float wv = WEIGHTS ? wacc[k] : 0.f;
+            if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
+            acc[k] = make_float2(0.f, 0.f);
+            if (WEIGHTS) wacc[k] = 0.f;
+            int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
+            const bool cj = nx < 0;
+            if (cj) {
+                nx = -nx;
+                ny = -ny;
+                nz = -nz;
+            }
+            if (!stored(nx, ny, nz, half)) continue;
+            const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
+            if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, cj ? -cv.y : cv.y));
+            if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
+        }
+        __syncwarp();
     }
 }
 
@@ -963,18 +1060,42 @@ cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gs
     return cudaGetLastError();
 }
 
-template <bool CUBIC, bool WEIGHTS>
-cudaError_t scatter_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
-                      float *wdst, void *ws, bool binned, cudaStream_t st) {
-    const Layout L = layout(q, CUBIC);
+template <bool WEIGHTS>
+cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
+                             float *wdst, void *ws, bool binned, cudaStream_t st) {
+    const Layout L = layout(q, false);
     const Scratch sc = scratch_in(ws, L);
-    const size_t smem = sizeof(float) * Halo<CUBIC>::ELEMS * (WEIGHTS ? 3 : 2) + sizeof(Queue) * kWarps;
-    auto kern = k_brick_scatter<CUBIC, WEIGHTS>;
+    const size_t smem = sizeof(float) * Halo<false>::ELEMS * (WEIGHTS ? 3 : 2) + sizeof(Queue) * kWarps;
+    auto kern = k_brick_scatter_linear<WEIGHTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
     kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
                                                                        dst, wdst);
+    return cudaGetLastError();
+}
+
+template <bool WEIGHTS>
+cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
+                            float *wdst, void *ws, bool binned, cudaStream_t st) {
+    using OL = OctLayout<WEIGHTS>;
+    const Layout L = layout(q, true);
+    const Scratch sc = scratch_in(ws, L);
+    const int threads = 32 * OL::WARPS;
+    const size_t smem = OL::WARP_BYTES * OL::WARPS;
+    auto kern = k_brick_scatter_cubic<WEIGHTS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    int dev = 0, sms = 148, per_sm = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const long long per = ((long long)sms * per_sm + q.Bsrc - 1) / q.Bsrc;
+    kern<<<dim3((unsigned)per, 1, (unsigned)q.Bsrc), threads, smem, st>>>(q, L.nb, sc, img, omega,
+                                                                        dst, wdst);
     return cudaGetLastError();
 }
 
@@ -996,10 +1117,10 @@ cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *g,
 cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
                                  float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st) {
     if (wdst)
-        return cubic ? scatter_t<true, true>(q, img, omega, dst, wdst, ws, binned, st)
-                     : scatter_t<false, true>(q, img, omega, dst, wdst, ws, binned, st);
-    return cubic ? scatter_t<true, false>(q, img, omega, dst, nullptr, ws, binned, st)
-                 : scatter_t<false, false>(q, img, omega, dst, nullptr, ws, binned, st);
+        return cubic ? scatter_cubic_t<true>(q, img, omega, dst, wdst, ws, binned, st)
+                     : scatter_linear_t<true>(q, img, omega, dst, wdst, ws, binned, st);
+    return cubic ? scatter_cubic_t<false>(q, img, omega, dst, nullptr, ws, binned, st)
+                 : scatter_linear_t<false>(q, img, omega, dst, nullptr, ws, binned, st);
 }
 
 }  // namespace tp
