@@ -51,8 +51,10 @@ _SIGS = {
     "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _Z, _P],
     "tp_project_2d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
     "tp_project_3d_2d_noalloc": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
+    "tp_project_3d_2d_save": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _Z, _P],
     "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P,
                                   _P, _Z, _P],
+    "tp_project_3d_2d_backward_saved": [_P, _P, _P, _I, _I, _I, _I, _I, TPOptions, _P, _P, _P],
     "tp_project_2d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
     "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P, _Z,
                              _P],
@@ -219,6 +221,62 @@ def tp_project_3d_2d(vol, rot, shift=None, *, N=None, interp="cubic", oversampli
     (allocated per call when omitted)."""
     return _forward("tp_project_3d_2d", 3, vol, rot, shift, N, interp, oversampling, radius, out,
                     stream, workspace)
+
+
+def tp_project_3d_2d_save(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
+                          radius=-1.0, out=None, dout=None, workspace=None, stream=None):
+    """tp_project_3d_2d that also returns dout (B, P, N, N/2+1, 3) complex:
+    phase * dS/dp_a per pixel, for tp_project_3d_2d_backward_saved; see tp.h."""
+    _need(vol, "vol", torch.complex64, 4)
+    Bv, Nv = vol.shape[0], vol.shape[1]
+    Bp, P, Bs = _poses(rot, shift, 3)
+    N = Nv if N is None else int(N)
+    B = _batch(Bv, Bp, Bs)
+    shape = (B, P, N, N // 2 + 1)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.complex64, device=vol.device)
+    if dout is None:
+        dout = torch.empty(shape + (3,), dtype=torch.complex64, device=vol.device)
+    _need(out, "out", torch.complex64, 4)
+    _need(dout, "dout", torch.complex64, 5)
+    if tuple(out.shape) != shape or tuple(dout.shape) != shape + (3,):
+        raise ValueError(f"out must be {shape} and dout {shape + (3,)}")
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, vol.device)
+    _call("tp_project_3d_2d_save", _ptr(vol), Bv, Nv, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+          _opts(interp, oversampling, radius), _ptr(out), _ptr(dout), _ptr(ws), nbytes,
+          _stream(stream))
+    return out, dout
+
+
+def tp_project_3d_2d_backward_saved(grad_out, out, dout, rot, shift=None, *, interp="cubic",
+                                    oversampling=1.0, radius=-1.0, grad_rot=None,
+                                    grad_shift=None, want_rot=True, want_shift=True, stream=None):
+    """dL/dR and dL/dshift (accumulated) from a tp_project_3d_2d_save forward's
+    out and dout; rot and shift only give the gradients' shapes and batches."""
+    _need(grad_out, "grad_out", torch.complex64, 4)
+    _need(out, "out", torch.complex64, 4)
+    _need(dout, "dout", torch.complex64, 5)
+    B, P, N = grad_out.shape[0], grad_out.shape[1], grad_out.shape[2]
+    if tuple(out.shape) != tuple(grad_out.shape) or tuple(dout.shape) != tuple(grad_out.shape) + (3,):
+        raise ValueError("grad_out, out and dout (with a trailing 3) must have the same shape")
+    Bp, Pr, Bs = _poses(rot, shift, 3)
+    if Pr != P:
+        raise ValueError("rot must have grad_out's P")
+    if want_rot and grad_rot is None:
+        grad_rot = torch.zeros_like(rot)
+    if want_shift and shift is not None and grad_shift is None:
+        grad_shift = torch.zeros_like(shift)
+    if grad_rot is not None:
+        _need(grad_rot, "grad_rot", torch.float32, 4)
+        if grad_rot.shape != rot.shape:
+            raise ValueError("grad_rot must have rot's shape")
+    if grad_shift is not None:
+        _need(grad_shift, "grad_shift", torch.float32, 3)
+        if shift is None or grad_shift.shape != shift.shape:
+            raise ValueError("grad_shift must have shift's shape")
+    _call("tp_project_3d_2d_backward_saved", _ptr(grad_out), _ptr(out), _ptr(dout), B, P, N, Bp, Bs,
+          _opts(interp, oversampling, radius), _ptr(grad_rot), _ptr(grad_shift), _stream(stream))
+    return grad_rot, grad_shift
 
 
 def tp_project_3d_2d_noalloc(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,

@@ -119,9 +119,10 @@ tp_status check_workspace(const Geometry &g, void *ws, size_t ws_bytes) {
     return TP_OK;
 }
 
+// dout (3D only, may be NULL): also save D_a = phase * dS/dp_a per pixel.
 tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, int Bp, int P,
-                  const float *shift, int Bs, int N, tp_options opts, float *out, void *ws,
-                  size_t ws_bytes, void *stream) {
+                  const float *shift, int Bs, int N, tp_options opts, float *out, float *dout,
+                  void *ws, size_t ws_bytes, void *stream) {
     Geometry g;
     tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
     if (st != TP_OK) return st;
@@ -129,11 +130,13 @@ tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, 
     if (!src || !out || !rot) return fail(TP_ERR_NULL, "source, rotation and output pointers are required");
     if ((st = check_complex(src, "source")) != TP_OK || (st = check_complex(out, "out")) != TP_OK)
         return st;
+    if (dout && (st = check_complex(dout, "dout")) != TP_OK) return st;
     if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
     g.q.src = reinterpret_cast<const float2 *>(src);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float2 *o = reinterpret_cast<float2 *>(out);
-    return launched(dim == 3 ? tp::launch_brick_project(g.cubic, g.q, o, ws, s)
+    return launched(dim == 3 ? tp::launch_brick_project(g.cubic, g.q, o, reinterpret_cast<float2 *>(dout),
+                                                        ws, s)
                              : tp::launch_project(dim, g.cubic, g.q, o, s),
                     "project");
 }
@@ -198,14 +201,70 @@ size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts) {
 tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
                            const float *shift, int Bs, int N, tp_options opts, float *out,
                            void *workspace, size_t workspace_bytes, void *stream) {
-    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, workspace,
+    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, nullptr, workspace,
                    workspace_bytes, stream);
+}
+
+tp_status tp_project_3d_2d_save(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
+                                const float *shift, int Bs, int N, tp_options opts, float *out,
+                                float *dout, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    if (!dout && P > 0) return fail(TP_ERR_NULL, "dout is required");
+    return forward(3, vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, dout, workspace,
+                   workspace_bytes, stream);
+}
+
+tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *out,
+                                          const float *dout, int B, int P, int N, int Bp, int Bs,
+                                          tp_options opts, float *grad_rot, float *grad_shift,
+                                          void *stream) {
+    if (opts.flags != 0) return fail(TP_ERR_UNSUPPORTED, "tp_options.flags must be 0 (got %u)", opts.flags);
+    if (opts.interp != TP_LINEAR && opts.interp != TP_CUBIC)
+        return fail(TP_ERR_UNSUPPORTED, "interp must be TP_LINEAR or TP_CUBIC (got %d)", opts.interp);
+    if (!(opts.oversampling > 0.0f) || !std::isfinite(opts.oversampling))
+        return fail(TP_ERR_UNSUPPORTED, "oversampling must be finite and > 0");
+    if (!std::isfinite(opts.radius)) return fail(TP_ERR_UNSUPPORTED, "radius must be finite");
+    if (N < 2 || (N & 1) || N > 4096) return fail(TP_ERR_SHAPE, "output box must be even, 2..4096 (got %d)", N);
+    if (B < 1 || P < 0 || (Bp != 1 && Bp != B) || (Bs != 1 && Bs != B))
+        return fail(TP_ERR_SHAPE, "batch sizes do not broadcast (B %d, rot %d, shift %d, P %d)", B, Bp,
+                    Bs, P);
+    const long long Xo = N / 2 + 1;
+    if ((long long)B * P >= (1LL << 31) || (long long)B * P * N * Xo * 3 >= (1LL << 62))
+        return fail(TP_ERR_SHAPE, "too many images (B*P = %lld)", (long long)B * P);
+    if (P == 0 || (!grad_rot && !grad_shift)) return ok();
+    if (!grad_out || !out || !dout)
+        return fail(TP_ERR_NULL, "grad_out, out and dout pointers are required");
+    tp_status st;
+    if ((st = check_complex(grad_out, "grad_out")) != TP_OK || (st = check_complex(out, "out")) != TP_OK ||
+        (st = check_complex(dout, "dout")) != TP_OK)
+        return st;
+    if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
+        return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
+    tp::Params q{};
+    q.B = B;
+    q.P = P;
+    q.Bp = Bp;
+    q.Bs = Bs;
+    q.N = N;
+    q.Xo = (int)Xo;
+    q.plane = (int)(N * Xo);
+    q.s = opts.oversampling;
+    q.fN = (float)N;
+    q.invN = 1.0f / (float)N;
+    const double r = (opts.radius < 0.0f) ? 0.5 * N : (double)opts.radius;
+    const double r2 = std::floor(r * r);
+    q.r2max = r2 > 2e9 ? 2000000000 : (int)r2;
+    return launched(tp::launch_pose_grad_saved(q, reinterpret_cast<const float2 *>(grad_out),
+                                               reinterpret_cast<const float2 *>(out),
+                                               reinterpret_cast<const float2 *>(dout), grad_rot,
+                                               grad_shift, static_cast<cudaStream_t>(stream)),
+                    "pose gradient (saved)");
 }
 
 tp_status tp_project_2d_2d(const float *img, int Bi, int Ni, const float *rot, int Bp, int P,
                            const float *shift, int Bs, int N, tp_options opts, float *out,
                            void *stream) {
-    return forward(2, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, out, nullptr, 0, stream);
+    return forward(2, img, Bi, Ni, rot, Bp, P, shift, Bs, N, opts, out, nullptr, nullptr, 0, stream);
 }
 
 tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int Bv, int Nv,

@@ -530,10 +530,14 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
 }
 
 // ---------------------------------------------------------------------------
-// Forward projection.
-template <bool CUBIC>
-__global__ void __launch_bounds__(kThreads, 3) k_brick_project(Params q, int nb, Scratch sc,
-                                                               float2 *__restrict__ out) {
+// Forward projection.  With SAVE the stencil's derivative weights are
+// gathered too and D_a = phase * dS/dp_a (the derivative of the output with
+// respect to the sample position) is written next to the output, three
+// complex values per pixel.
+template <bool CUBIC, bool SAVE>
+__global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params q, int nb, Scratch sc,
+                                                                         float2 *__restrict__ out,
+                                                                         float2 *__restrict__ dout) {
     extern __shared__ float2 s_vol[];
     __shared__ UnitTable s_tab;
     const int v = blockIdx.z, nbr = nb * nb * nb;
@@ -545,17 +549,27 @@ __global__ void __launch_bounds__(kThreads, 3) k_brick_project(Params q, int nb,
             c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
             for (int k; (k = next_pose(s_tab)) >= 0;) {
                 const PoseGeo &g = s_tab.pose[k];
-                float2 *o = out + (size_t)g.bp * q.plane;
+                const size_t ob = (size_t)g.bp * q.plane;
                 const float sx = g.sx, sy = g.sy;
                 for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
                     int l[3];
                     float w[3][4], d[3][4];
-                    if (!active || !own_sample<CUBIC, false>(g, bx, qx, qy, l, w, d)) return;
-                    float2 S;
-                    gather_smem<CUBIC, false>(s_vol, l, w, d, S, nullptr);
-                    if (q.shift) S = cmul(shift_phase(qx, qy, sx, sy, q.fN, q.invN), S);
+                    if (!active || !own_sample<CUBIC, SAVE>(g, bx, qx, qy, l, w, d)) return;
+                    float2 S, dS[3];
+                    gather_smem<CUBIC, SAVE>(s_vol, l, w, d, S, dS);
                     const int iy = qy < 0 ? qy + q.N : qy;
-                    o[iy * q.Xo + qx] = S;
+                    const size_t e = ob + (size_t)iy * q.Xo + qx;
+                    if (q.shift) {
+                        const float2 ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
+                        S = cmul(ph, S);
+                        if (SAVE)
+#pragma unroll
+                            for (int a = 0; a < 3; ++a) dS[a] = cmul(ph, dS[a]);
+                    }
+                    out[e] = S;
+                    if (SAVE)
+#pragma unroll
+                        for (int a = 0; a < 3; ++a) dout[3 * e + a] = dS[a];
                 });
             }
             __syncthreads();
@@ -566,20 +580,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_brick_project(Params q, int nb,
 // Zeros for the pixels no brick owns: outside the radius (one warp per
 // output row writes the tail of the row beyond the radius), and, for poses
 // whose reach exceeds the brick grid, in-radius pixels with floor(p) outside
-// it (all their taps lie outside the stored range).
+// it (all their taps lie outside the stored range).  dout, when given,
+// receives the matching zeros (three complex values per pixel).
 __global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, const PoseGeo *__restrict__ geo,
-                                                      float2 *__restrict__ out) {
+                                                      float2 *__restrict__ out,
+                                                      float2 *__restrict__ dout) {
     const long long rows = (long long)q.B * q.P * q.N;
     const int lane = threadIdx.x & 31;
     const int half = q.N >> 1;
+    const float2 zero = make_float2(0.f, 0.f);
     for (long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; row < rows;
          row += ((long long)gridDim.x * 256) >> 5) {
         const int bp = (int)(row / q.N), iy = (int)(row - (long long)bp * q.N);
         const int ky = row_freq(iy, q.N);
         const int rr = q.r2max - ky * ky;
         const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
-        float2 *o = out + (size_t)bp * q.plane + (size_t)iy * q.Xo;
-        for (int x = xcut + 1 + lane; x <= half; x += 32) o[x] = make_float2(0.f, 0.f);
+        const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
+        if (dout)
+            for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
         if (xcut >= 0 && geo[bp].reach >= (float)G - 0.5f) {
             const PoseGeo &g = geo[bp];
             for (int x = lane; x <= xcut; x += 32) {
@@ -590,7 +609,12 @@ __global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, const Pos
                     const int x0 = split_coord(fmaf(g.a[a], (float)x, g.b[a] * (float)ky), t);
                     outside = outside || x0 < -G || x0 >= G;
                 }
-                if (outside) o[x] = make_float2(0.f, 0.f);
+                if (outside) {
+                    out[r0 + x] = zero;
+                    if (dout)
+#pragma unroll
+                        for (int a = 0; a < 3; ++a) dout[3 * (r0 + x) + a] = zero;
+                }
             }
         }
     }
@@ -1029,19 +1053,19 @@ dim3 main_grid(const Params &q, const void *kern, size_t smem) {
     return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
 }
 
-template <bool CUBIC>
-cudaError_t project_t(const Params &q, float2 *out, void *ws, cudaStream_t st) {
+template <bool CUBIC, bool SAVE>
+cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, cudaStream_t st) {
     const Layout L = layout(q, CUBIC);
     const Scratch sc = scratch_in(ws, L);
     const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
-    auto kern = k_brick_project<CUBIC>;
+    auto kern = k_brick_project<CUBIC, SAVE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = bin(q, L, sc, st)) != cudaSuccess) return e;
     const long long zrows = (long long)q.B * q.P * q.N;
     const long long zb = (zrows + 7) / 8 < 65535LL * 32 ? (zrows + 7) / 8 : 65535LL * 32;
-    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, sc.geo, out);
-    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out);
+    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, sc.geo, out, dout);
+    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out, dout);
     return cudaGetLastError();
 }
 
@@ -1103,9 +1127,13 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
 
 size_t brick_workspace_bytes(const Params &q, bool cubic) { return layout(q, cubic).total; }
 
-cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, void *ws,
+cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  cudaStream_t st) {
-    return cubic ? project_t<true>(q, out, ws, st) : project_t<false>(q, out, ws, st);
+    if (dout)
+        return cubic ? project_t<true, true>(q, out, dout, ws, st)
+                     : project_t<false, true>(q, out, dout, ws, st);
+    return cubic ? project_t<true, false>(q, out, nullptr, ws, st)
+                 : project_t<false, false>(q, out, nullptr, ws, st);
 }
 
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *g, float *grot,

@@ -23,14 +23,21 @@ cudaError_t launch_scatter(int dim, bool cubic, const Params &q, const float2 *i
 // 3D brick-binned kernels (tp_brick.cu): forward, pose gradients and
 // scatter.  ws is the caller's workspace of brick_workspace_bytes() bytes;
 // with binned = true the pose binning of an earlier launch on the same
-// stream, for the same poses, is reused.
+// stream, for the same poses, is reused.  With dout the forward also writes
+// D_a = phase * dS/dp_a, three complex values per output pixel.
 size_t brick_workspace_bytes(const Params &q, bool cubic);
-cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, void *ws,
+cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  cudaStream_t st);
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
                                    float *grad_rot, float *grad_shift, void *ws, bool binned,
                                    cudaStream_t st);
 cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
                                  float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st);
+
+// dL/dR (rows 0 and 1) and dL/dshift of the 3D forward from its output y and
+// saved derivatives D (tp_saved.cu), accumulated with atomics.
+cudaError_t launch_pose_grad_saved(const Params &q, const float2 *grad_out, const float2 *y,
+                                   const float2 *D, float *grad_rot, float *grad_shift,
+                                   cudaStream_t st);
 
 }  // namespace tp

@@ -4,7 +4,10 @@
 One step is the whole hot path over one batch: forward 3D->2D projection of a
 256^3 spectrum for 512 poses with shifts (cubic, radius 128), the L2-loss
 gradient g = 2 (y - target) against seeded noisy targets (SNR 0.1), and the
-backward pass producing dL/dR, dL/dshift and dL/dvolume.  The metric is
+backward pass producing dL/dR, dL/dshift and dL/dvolume.  The forward saves
+D = phase * dS/dp per pixel, so the rotation and shift gradients are a
+streaming reduction over (g, y, D); the volume gradient is the brick scatter
+of g.  The metric is
 Fourier samples per second (one sample = one stored output RFFT pixel) over
 forward + backward, in Gsamples/s.
 
@@ -214,8 +217,8 @@ def kernel_source_sha():
 
 
 # The three kernels that do the work of a step, by the bench's segment names.
-NCU_KERNELS = {"project_3d_2d": "k_brick_project", "pose_grad_gather": "k_brick_pose_grad",
-               "volume_grad_scatter": "k_brick_scatter"}
+NCU_KERNELS = {"project_3d_2d": "k_brick_project", "pose_grad_saved": "k_pose_grad_saved",
+               "volume_grad_scatter": "k_brick_scatter_cubic"}
 NCU_METRICS = {"dram__bytes_read.sum": "dram_read_bytes", "dram__bytes_write.sum": "dram_write_bytes",
                "gpu__time_duration.sum": "duration_ns",
                "gpu__compute_memory_throughput.avg.pct_of_peak_sustained_elapsed": "mem_sol_pct",
@@ -326,6 +329,7 @@ def run_ours(args):
     del clean, noise
 
     y = torch.empty_like(target)
+    D = torch.empty(tuple(target.shape) + (3,), dtype=torch.complex64, device=dev)
     g = torch.empty_like(target)
     grad_vol = torch.zeros_like(vol)
     grad_rot = torch.zeros_like(rot)
@@ -335,10 +339,13 @@ def run_ours(args):
     kw["workspace"] = ws
     stream = torch.cuda.current_stream()
 
+    kw_saved = {k: kw[k] for k in ("interp", "oversampling", "radius")}
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        tp.tp_project_3d_2d(vol, rot, shift, out=y, **kw)
+        # Forward; it also saves D = phase * dS/dp for the pose gradients.
+        tp.tp_project_3d_2d_save(vol, rot, shift, out=y, dout=D, **kw)
         if ev:
             ev[1].record(stream)
         torch.add(m2t, y, alpha=2.0, out=g)                       # g = 2 (y - target)
@@ -347,8 +354,8 @@ def run_ours(args):
         grad_shift.zero_()
         if ev:
             ev[2].record(stream)
-        tp.tp_project_3d_2d_backward(g, vol, rot, shift, grad_rot=grad_rot, grad_shift=grad_shift,
-                                     want_vol=False, **kw)
+        tp.tp_project_3d_2d_backward_saved(g, y, D, rot, shift, grad_rot=grad_rot,
+                                           grad_shift=grad_shift, **kw_saved)
         if ev:
             ev[3].record(stream)
         tp.tp_project_3d_2d_backward(g, vol, rot, shift, grad_vol=grad_vol, want_rot=False,
@@ -423,10 +430,15 @@ def run_ours(args):
     e2e_value = world * samples * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
 
     if rank == 0:
-        names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_gather", "volume_grad_scatter"]
+        names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_saved", "volume_grad_scatter"]
         mean_seg = seg.mean(0)
-        kern = {"project_3d_2d": (mean_seg[0], samples * 8 + vol.numel() * 8),
-                "pose_grad_gather": (mean_seg[2], samples * 8 + vol.numel() * 8),
+        n_in = P * in_radius_count(N, w["radius"])
+        # Algorithmic HBM bytes per launch: the forward reads the volume once
+        # and writes y (8 B) and D (24 B) per stored pixel; the pose gradient
+        # reads g, y and D (40 B) per in-radius pixel; the scatter reads g
+        # (8 B per stored pixel) and reads and writes the volume gradient once.
+        kern = {"project_3d_2d": (mean_seg[0], samples * 32 + vol.numel() * 8),
+                "pose_grad_saved": (mean_seg[2], n_in * 40),
                 "volume_grad_scatter": (mean_seg[3], samples * 8 + 2 * vol.numel() * 8)}
         dom = max(kern, key=lambda k: kern[k][0])
         t_ms, nbytes = kern[dom]
@@ -461,13 +473,13 @@ def run_ours(args):
             "breakdown_ms": {n: float(mean_seg[i]) for i, n in enumerate(names)},
             "fwd_gsamples_s": samples / (mean_seg[0] * 1e-3) / 1e9,
             "bwd_gsamples_s": samples / ((mean_seg[2] + mean_seg[3]) * 1e-3) / 1e9,
-            "in_radius_samples_per_step": P * in_radius_count(N, w["radius"]),
+            "in_radius_samples_per_step": n_in,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            # per step: forward (pose geometry, brick masks, unit plan, zero fill, gather),
-            # then the pose-gradient call (geometry, masks, plan, gather) and the
-            # volume-gradient call (geometry, masks, plan, scatter): all of this library
-            "gpu_launches": 13 * args.steps,
+            # per step: forward (pose geometry, brick masks, unit plan, zero fill, gather
+            # with saved derivatives), the saved-path pose gradient (one streaming
+            # kernel) and the volume-gradient call (geometry, masks, plan, scatter)
+            "gpu_launches": 10 * args.steps,
             "clocks": clocks.record(),
             "cpu_baseline": cpu_line,
         }

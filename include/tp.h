@@ -127,6 +127,41 @@ tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int
                                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * tp_project_3d_2d that also saves what the rotation and shift gradients
+ * need, so that tp_project_3d_2d_backward_saved gets them without touching
+ * the volume again (a save-for-backward split of the gradients of [de §2
+ * "Differentiable Backpropagation"; ar §2 "الإزاحات والدورات"]; the pages
+ * recompute instead).  Arguments, out and errors as tp_project_3d_2d, plus
+ *   dout   (B, P, N, N/2+1, 3) complex          out, overwritten
+ * with dout[b][p][y][x][a] = phase * dS/dp_a, the derivative of out[b][p][y][x]
+ * with respect to component a of the pixel's sample position p = s R^T k
+ * (zero where out is zero by the radius).  dout must be 8-byte aligned.
+ */
+tp_status tp_project_3d_2d_save(const float *vol, int Bv, int Nv,
+                                const float *rot, int Bp, int P,
+                                const float *shift, int Bs,
+                                int N, tp_options opts, float *out, float *dout,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Rotation and shift gradients of a tp_project_3d_2d_save forward for an
+ * upstream gradient grad_out, from its out and dout alone (no volume and no
+ * workspace): per pixel dL/dp_a = Re(conj(grad_out) dout_a), then
+ *   grad_rot    (Bp, P, 3, 3) float, += s k_i dL/dp_a at [i][a] (row 3 is 0)
+ *   grad_shift  (Bs, P, 2) float, += (2 pi k_a / N) Im(conj(grad_out) out)
+ * the same values as tp_project_3d_2d_backward.  grad_out, out (B, P, N,
+ * N/2+1) and dout are complex; B is the output batch, Bp and Bs (each 1 or
+ * B) the rotation and shift batches of the forward (Bs = 1 when it had no
+ * shift; grad_shift is then the gradient at zero shift).  opts must be the
+ * forward's (oversampling and radius are used).  Either gradient may be
+ * NULL; with both NULL the call does nothing.
+ */
+tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *out,
+                                          const float *dout, int B, int P, int N,
+                                          int Bp, int Bs, tp_options opts,
+                                          float *grad_rot, float *grad_shift, void *stream);
+
+/*
  * 2D -> 3D backprojection: the adjoint of tp_project_3d_2d scattered into a
  * data spectrum, plus an optional real weight spectrum [it §2 "accumulo di
  * pesi"; de §2 "Dual-Volumen-Ansatz"; ko §2 "Backward Projection"].

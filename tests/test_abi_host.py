@@ -34,7 +34,8 @@ def declared_symbols():
 def test_header_declares_the_operator_set():
     syms = declared_symbols()
     for name in ("tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
-                 "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version"):
+                 "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_project_3d_2d_save",
+                 "tp_project_3d_2d_backward_saved", "tp_last_error", "tp_version"):
         assert name in syms
 
 
@@ -127,6 +128,38 @@ def test_backprojection_validation(tp):
     assert bp(weights=A + 2) == TP_ERR_ALIGN
     assert bp(P=0) == TP_OK
     assert bp(wv=None, P=0) == TP_OK
+
+
+def test_saved_forward_validation(tp):
+    def save(dout=A, P=4, vol=A, ws=WS):
+        return tp._fn("tp_project_3d_2d_save")(vol, 1, 16, A, 1, P, None, 1, 16, opts(tp), A, dout,
+                                               ws, WSB, None)
+    assert save(dout=None) == TP_ERR_NULL
+    assert "dout" in tp.tp_last_error()
+    assert save(dout=MIS) == TP_ERR_ALIGN
+    assert save(vol=None) == TP_ERR_NULL
+    assert save(ws=None) == TP_ERR_NULL
+    assert save(P=0, dout=None) == TP_OK
+
+
+def test_saved_backward_validation(tp):
+    def bs(go=A, out=A, dout=A, B=2, P=4, N=16, Bp=1, Bs=1, o=None, gr=A, gs=None):
+        return tp._fn("tp_project_3d_2d_backward_saved")(go, out, dout, B, P, N, Bp, Bs,
+                                                         o or opts(tp), gr, gs, None)
+    assert bs(N=15) == TP_ERR_SHAPE
+    assert bs(N=8192) == TP_ERR_SHAPE
+    assert bs(B=0) == TP_ERR_SHAPE
+    assert bs(Bp=3) == TP_ERR_SHAPE                     # rotations batch must be 1 or B
+    assert bs(Bs=3) == TP_ERR_SHAPE
+    assert bs(P=-1) == TP_ERR_SHAPE
+    assert bs(o=opts(tp, flags=2)) == TP_ERR_UNSUPPORTED
+    assert bs(o=opts(tp, s=-1.0)) == TP_ERR_UNSUPPORTED
+    assert bs(go=None) == TP_ERR_NULL
+    assert bs(dout=None) == TP_ERR_NULL
+    assert bs(out=MIS) == TP_ERR_ALIGN
+    assert bs(gr=A + 2) == TP_ERR_ALIGN
+    assert bs(gr=None, gs=None, go=None) == TP_OK       # nothing requested: no work, no checks
+    assert bs(P=0, go=None) == TP_OK
 
 
 def test_workspace_size_query(tp):
