@@ -49,8 +49,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-sample-poses", type=int, default=64,
-                    help="poses of the workload the CPU-baseline oracle leg processes")
+    ap.add_argument("--cpu-sample-poses", type=int, default=512,
+                    help="poses of the workload one CPU-baseline oracle step processes")
+    ap.add_argument("--cpu-min-seconds", type=float, default=10.0,
+                    help="the CPU-baseline leg repeats oracle steps until this much time has passed")
     ap.add_argument("--ref-poses", type=int, default=1,
                     help="poses per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -94,17 +96,22 @@ def oracle_sample_workload(P):
     return w
 
 
-def cpu_baseline(P):
+def cpu_baseline(P, min_seconds):
+    """The oracle, as it stands, on this host's cores: whole steps over the
+    first P poses, repeated (at most 10 times) until min_seconds passed."""
     import oracle
     w = oracle_sample_workload(P)
-    t0 = time.perf_counter()
-    oracle_step(w, P)
-    dt = time.perf_counter() - t0
-    samples = P * w["box"] * (w["box"] // 2 + 1)
+    reps, dt = 0, 0.0
+    while reps < 10 and (reps == 0 or dt < min_seconds):
+        t0 = time.perf_counter()
+        oracle_step(w, P)
+        dt += time.perf_counter() - t0
+        reps += 1
+    samples = reps * P * w["box"] * (w["box"] // 2 + 1)
     return {"value": samples / dt / 1e9, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{P} of 512 poses of the box-256 step (fwd + L2 grad + bwd), float64, "
-                      f"{dt:.1f} s"}
+            "sample": f"{reps} x {P} of the 512 poses of the box-256 step (fwd + L2 grad + bwd), "
+                      f"float64, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -279,6 +286,22 @@ def ncu_profile():
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank aggregation: every rank times its own steps; the job's time is
+# the slowest rank's and its throughput counts the samples of all ranks.
+def max_over_ranks(value, dist=None, device=None):
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, samples_per_rank_step, steps, job_ms):
+    """Gsamples/s of the whole job: all ranks' samples over the slowest rank's time."""
+    return world * samples_per_rank_step * steps / (job_ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
 
@@ -293,7 +316,7 @@ def run_ours(args):
 
     cpu_line = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu_line = cpu_baseline(args.cpu_sample_poses)
+        cpu_line = cpu_baseline(args.cpu_sample_poses, args.cpu_min_seconds)
 
     import backprojection_tp_project_gather_b300 as tp
 
@@ -384,13 +407,9 @@ def run_ours(args):
     seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)]
                     for i in range(args.steps)])                        # ms
     step_ms = seg.sum(1)
-    total_ms = float(step_ms.sum())
-    if dist:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(step_ms.sum(), dist, dev)
     samples = P * N * (N // 2 + 1)
-    value = world * samples * args.steps / (total_ms * 1e-3) / 1e9
+    value = whole_job_rate(world, samples, args.steps, total_ms)
 
     # End to end through the public API with host buffers: pinned inputs
     # copied in, the step, gradients copied out, every step.
@@ -422,12 +441,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * samples * args.e2e_steps / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = whole_job_rate(world, samples, args.e2e_steps, e2e_ms)
 
     if rank == 0:
         names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_saved", "volume_grad_scatter"]
