@@ -55,13 +55,21 @@ constexpr int kUnitHits = 64;    // reaching poses per work unit (load-balance t
 constexpr int kQueueStride = 21; // floats per queued scatter sample (odd: no bank conflicts)
 constexpr float kMargin = 0.01f; // enumeration margin in voxel units
 
+// Brick + halo in shared memory.  Linear: row-major with pitches 20 x 20.
+// Cubic: each z layer is a 5 x 5 grid of 4 x 4 (x, y) tiles of 16 complex
+// words (one full row of 32 banks), so element (x, y) sits in bank pair
+// (x mod 4) + 4 (y mod 4) whatever the tile; see gather_smem.
 template <bool CUBIC>
 struct Halo {
     using St = Stencil<CUBIC>;
     static constexpr int S = kBS + St::LO + St::HI;  // staged edge (19 or 17)
-    static constexpr int PX = 20;                     // shared-memory pitches
+    static constexpr int PX = 20;                     // pitches (the cubic tiles cover 20 x 20)
     static constexpr int PY = 20;
     static constexpr int ELEMS = PX * PY * S;
+    __device__ __forceinline__ static int index(int x, int y, int z) {
+        if (CUBIC) return z * (PX * PY) + ((y >> 2) * (PX / 4) + (x >> 2)) * 16 + (x & 3) + 4 * (y & 3);
+        return (z * PY + y) * PX + x;
+    }
 };
 
 // Per-pose geometry, computed once per call.
@@ -453,7 +461,7 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
         }
         const bool ok = stored(nx, ny, nz, half);
         const float2 *src = ok ? V + ((size_t)wrap_row(nz, M) * M + wrap_row(ny, M)) * X + nx : V;
-        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + (lz * H::PY + ly) * H::PX + lx);
+        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + H::index(lx, ly, lz));
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src),
                      "r"(ok ? 8 : 0)
                      : "memory");
@@ -466,13 +474,29 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
         for (int e = threadIdx.x; e < nneg * H::S * H::S; e += kThreads) {
             const int lx = e % nneg, r = e / nneg;
             const int ly = r % H::S, lz = r / H::S;
-            float2 *p = s + (lz * H::PY + ly) * H::PX + lx;
+            float2 *p = s + H::index(lx, ly, lz);
             p->y = -p->y;
         }
     }
 }
 
 // Weighted sum over the stencil from staged shared memory (and derivatives).
+//
+// Cubic: the 16 (x, y) taps of a layer cover all 16 bank pairs (the tile
+// layout of Halo<true>), and each lane visits them in its own order: at
+// step (sx, sy) lane L reads the tap in bank pair ((sx + L) mod 4) +
+// 4 ((sy + L / 4) mod 4).  The 16 lanes of a half-warp then never share a
+// bank pair, so every 64-bit load of the warp takes the minimum two
+// wavefronts.  The order rotates the x and y taps independently, so the
+// separable weights are rotated once per sample (rot4) and the row sums stay.
+__device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) {
+    float t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = (c & 1) ? v[(i + 1) & 3] : v[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = (c & 2) ? t[(i + 2) & 3] : t[i];
+}
+
 template <bool CUBIC, bool DERIV>
 __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float (*w)[4],
                                             float (*d)[4], float2 &S, float2 *dS) {
@@ -482,7 +506,53 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
     if (DERIV)
 #pragma unroll
         for (int a = 0; a < 3; ++a) dS[a] = make_float2(0.f, 0.f);
-    const float2 *base = s + (l[2] * H::PY + l[1]) * H::PX + l[0];
+    if (CUBIC) {
+        const int lane = threadIdx.x & 31;
+        const int cx = (lane - l[0]) & 3, cy = ((lane >> 2) - l[1]) & 3;
+        float wx[4], wy[4], dx[4], dy[4];
+        rot4(w[0], cx, wx);
+        rot4(w[1], cy, wy);
+        if (DERIV) {
+            rot4(d[0], cx, dx);
+            rot4(d[1], cy, dy);
+        }
+        int ox[4], oy[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int x = l[0] + ((i + cx) & 3), y = l[1] + ((i + cy) & 3);
+            ox[i] = (x >> 2) * 16 + (x & 3);
+            oy[i] = (y >> 2) * (16 * H::PX / 4) + 4 * (y & 3);
+        }
+        const float2 *base = s + l[2] * (H::PX * H::PY);
+#pragma unroll
+        for (int jz = 0; jz < 4; ++jz) {
+            float2 ay = make_float2(0.f, 0.f), ayx = ay, ayy = ay;
+#pragma unroll
+            for (int sy = 0; sy < 4; ++sy) {
+                const float2 *row = base + jz * (H::PX * H::PY) + oy[sy];
+                float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+#pragma unroll
+                for (int sx = 0; sx < 4; ++sx) {
+                    const float2 val = row[ox[sx]];
+                    cfma(wx[sx], val, r0);
+                    if (DERIV) cfma(dx[sx], val, r1);
+                }
+                cfma(wy[sy], r0, ay);
+                if (DERIV) {
+                    cfma(wy[sy], r1, ayx);
+                    cfma(dy[sy], r0, ayy);
+                }
+            }
+            cfma(w[2][jz], ay, S);
+            if (DERIV) {
+                cfma(w[2][jz], ayx, dS[0]);
+                cfma(w[2][jz], ayy, dS[1]);
+                cfma(d[2][jz], ay, dS[2]);
+            }
+        }
+        return;
+    }
+    const float2 *base = s + H::index(l[0], l[1], l[2]);
 #pragma unroll
     for (int jz = 0; jz < T; ++jz) {
         float2 ay = make_float2(0.f, 0.f), ayx = ay, ayy = ay;
