@@ -279,30 +279,46 @@ __global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratc
     sc.geo[id] = g;
 }
 
-// One warp per (volume, brick, chunk): bit l of the mask = pose 32*chunk + l
-// of the volume's list can reach the brick; the brick's count grows by the
-// number of set bits.
+__device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
+    PoseGeo g;
+    const int *src = reinterpret_cast<const int *>(p);
+    int *dst = reinterpret_cast<int *>(&g);
+#pragma unroll
+    for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+    return g;
+}
+
+// Bit l of mask (volume, brick, chunk) = pose 32*chunk + l of the volume's
+// list can reach the brick; the brick's count grows by the number of set
+// bits.  A warp keeps one chunk's 32 poses in registers and sweeps a range
+// of kMaskBricks bricks.
+constexpr int kMaskBricks = 8;
+
 __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
     const int nbr = nb * nb * nb;
     const int nchunks = sc.nchunks;
-    const long long total = (long long)q.Bsrc * nbr * nchunks;
+    const int ranges = (nbr + kMaskBricks - 1) / kMaskBricks;
+    const long long total = (long long)q.Bsrc * nchunks * ranges;
     const int Pv = poses_of_volume(q);
     const int lane = threadIdx.x & 31;
     for (long long w = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; w < total;
          w += ((long long)gridDim.x * 256) >> 5) {
-        const int c = (int)(w % nchunks);
-        const long long r = w / nchunks;
-        const int j = (int)(r % nbr), v = (int)(r / nbr);
+        const int rg = (int)(w % ranges);
+        const long long r = w / ranges;
+        const int c = (int)(r % nchunks), v = (int)(r / nchunks);
         const int i = c * 32 + lane;
-        bool hit = false;
-        if (i < Pv) {
-            const BrickBox bx = brick_box(j, nb);
-            hit = pose_reaches(sc.geo[pose_id(q, v, i)], bx);
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (lane == 0) {
-            sc.masks[w] = m;
-            if (m) atomicAdd(sc.hits + r, __popc(m));
+        const bool valid = i < Pv;
+        PoseGeo g;
+        if (valid) g = load_geo(sc.geo + pose_id(q, v, i));
+        const int j1 = min(nbr, (rg + 1) * kMaskBricks);
+        for (int j = rg * kMaskBricks; j < j1; ++j) {
+            const bool hit = valid && pose_reaches(g, brick_box(j, nb));
+            const unsigned m = __ballot_sync(0xffffffffu, hit);
+            if (lane == 0) {
+                const size_t vj = (size_t)v * nbr + j;
+                sc.masks[vj * nchunks + c] = m;
+                if (m) atomicAdd(sc.hits + vj, __popc(m));
+            }
         }
     }
 }
@@ -600,6 +616,50 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
 }
 
 // ---------------------------------------------------------------------------
+// Zeros for the pixels no brick owns: outside the radius (a warp writes the
+// tail of an output row beyond the radius), and, for poses whose reach
+// exceeds the brick grid of half-width G, in-radius pixels with floor(p)
+// outside it (all their taps lie outside the stored range).  dout, when
+// given, receives the matching zeros (three complex values per pixel).  The
+// rows are shared out over the nwarps warps of the grid.
+__device__ __forceinline__ void zero_unowned(const Params &q, int G, const PoseGeo *__restrict__ geo,
+                                             float2 *__restrict__ out, float2 *__restrict__ dout,
+                                             long long warp, long long nwarps) {
+    const long long rows = (long long)q.B * q.P * q.N;
+    const int lane = threadIdx.x & 31;
+    const int half = q.N >> 1;
+    const float2 zero = make_float2(0.f, 0.f);
+    for (long long row = warp; row < rows; row += nwarps) {
+        const int bp = (int)(row / q.N), iy = (int)(row - (long long)bp * q.N);
+        const int ky = row_freq(iy, q.N);
+        const int rr = q.r2max - ky * ky;
+        const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
+        const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
+        if (dout)
+            for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
+        if (xcut >= 0 && __ldg(&geo[bp].reach) >= (float)G - 0.5f) {
+            const PoseGeo g = load_geo(geo + bp);
+            for (int x = lane; x <= xcut; x += 32) {
+                bool outside = false;
+#pragma unroll
+                for (int a = 0; a < 3; ++a) {
+                    float t;
+                    const int x0 = split_coord(fmaf(g.a[a], (float)x, g.b[a] * (float)ky), t);
+                    outside = outside || x0 < -G || x0 >= G;
+                }
+                if (outside) {
+                    out[r0 + x] = zero;
+                    if (dout)
+#pragma unroll
+                        for (int a = 0; a < 3; ++a) dout[3 * (r0 + x) + a] = zero;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Forward projection.  With SAVE the stencil's derivative weights are
 // gathered too and D_a = phase * dS/dp_a (the derivative of the output with
 // respect to the sample position) is written next to the output, three
@@ -611,6 +671,10 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
     extern __shared__ float2 s_vol[];
     __shared__ UnitTable s_tab;
     const int v = blockIdx.z, nbr = nb * nb * nb;
+    // The zeros go out first: plain stores that overlap the gathers below.
+    zero_unowned(q, (nb / 2) * kBS, sc.geo, out, dout,
+                 ((long long)(blockIdx.z * gridDim.x + blockIdx.x) * kThreads + threadIdx.x) >> 5,
+                 (long long)gridDim.x * gridDim.z * kWarps);
     int4 rec;
     while (next_unit(sc, 0, v, nbr, s_tab, rec)) {
         const BrickBox bx = brick_box(rec.x, nb);
@@ -643,49 +707,6 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
                 });
             }
             __syncthreads();
-        }
-    }
-}
-
-// Zeros for the pixels no brick owns: outside the radius (one warp per
-// output row writes the tail of the row beyond the radius), and, for poses
-// whose reach exceeds the brick grid, in-radius pixels with floor(p) outside
-// it (all their taps lie outside the stored range).  dout, when given,
-// receives the matching zeros (three complex values per pixel).
-__global__ void __launch_bounds__(256) k_zero_unowned(Params q, int G, const PoseGeo *__restrict__ geo,
-                                                      float2 *__restrict__ out,
-                                                      float2 *__restrict__ dout) {
-    const long long rows = (long long)q.B * q.P * q.N;
-    const int lane = threadIdx.x & 31;
-    const int half = q.N >> 1;
-    const float2 zero = make_float2(0.f, 0.f);
-    for (long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; row < rows;
-         row += ((long long)gridDim.x * 256) >> 5) {
-        const int bp = (int)(row / q.N), iy = (int)(row - (long long)bp * q.N);
-        const int ky = row_freq(iy, q.N);
-        const int rr = q.r2max - ky * ky;
-        const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
-        const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
-        for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
-        if (dout)
-            for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
-        if (xcut >= 0 && geo[bp].reach >= (float)G - 0.5f) {
-            const PoseGeo &g = geo[bp];
-            for (int x = lane; x <= xcut; x += 32) {
-                bool outside = false;
-#pragma unroll
-                for (int a = 0; a < 3; ++a) {
-                    float t;
-                    const int x0 = split_coord(fmaf(g.a[a], (float)x, g.b[a] * (float)ky), t);
-                    outside = outside || x0 < -G || x0 >= G;
-                }
-                if (outside) {
-                    out[r0 + x] = zero;
-                    if (dout)
-#pragma unroll
-                        for (int a = 0; a < 3; ++a) dout[3 * (r0 + x) + a] = zero;
-                }
-            }
         }
     }
 }
@@ -909,14 +930,6 @@ __device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct) {
     return ob;
 }
 
-__device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
-    PoseGeo g;
-    const int *src = reinterpret_cast<const int *>(p);
-    int *dst = reinterpret_cast<int *>(&g);
-#pragma unroll
-    for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
-    return g;
-}
 
 template <bool WEIGHTS>
 __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 4)
@@ -1106,7 +1119,7 @@ cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_
     const int nbr = L.nb * L.nb * L.nb;
     const int pb = (int)((q.B * (long long)q.P + 255) / 256);
     k_pose_geometry<<<pb, 256, 0, st>>>(q, nbr, sc);
-    const long long warps = (long long)q.Bsrc * nbr * L.nchunks;
+    const long long warps = (long long)q.Bsrc * L.nchunks * ((nbr + kMaskBricks - 1) / kMaskBricks);
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 32) blocks = 65535LL * 32;
     k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, sc);
@@ -1132,9 +1145,6 @@ cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, cuda
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = bin(q, L, sc, st)) != cudaSuccess) return e;
-    const long long zrows = (long long)q.B * q.P * q.N;
-    const long long zb = (zrows + 7) / 8 < 65535LL * 32 ? (zrows + 7) / 8 : 65535LL * 32;
-    k_zero_unowned<<<(unsigned)zb, 256, 0, st>>>(q, (L.nb / 2) * kBS, sc.geo, out, dout);
     kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out, dout);
     return cudaGetLastError();
 }
