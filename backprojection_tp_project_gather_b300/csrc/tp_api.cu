@@ -136,7 +136,7 @@ tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float2 *o = reinterpret_cast<float2 *>(out);
     return launched(dim == 3 ? tp::launch_brick_project(g.cubic, g.q, o, reinterpret_cast<float2 *>(dout),
-                                                        ws, s)
+                                                        ws, tp::kBinNew, s)
                              : tp::launch_project(dim, g.cubic, g.q, o, s),
                     "project");
 }
@@ -160,16 +160,16 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
     if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    bool binned = false;
+    tp::BinMode mode = tp::kBinNew;
     if (grad_rot || grad_shift) {
         g.q.src = reinterpret_cast<const float2 *>(src);
         const float2 *go = reinterpret_cast<const float2 *>(grad_out);
         cudaError_t e = dim == 3
                             ? tp::launch_brick_pose_grad(g.cubic, g.q, go, grad_rot, grad_shift, ws,
-                                                         false, s)
+                                                         mode, s)
                             : tp::launch_pose_grad(dim, g.cubic, g.q, go, grad_rot, grad_shift, s);
         if (e != cudaSuccess) return launched(e, "pose gradient");
-        binned = true;
+        if (mode == tp::kBinNew) mode = tp::kBinSameCall;
     }
     if (grad_src) {
         g.q.src = nullptr;
@@ -177,7 +177,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
         float2 *gs = reinterpret_cast<float2 *>(grad_src);
         cudaError_t e = dim == 3
                             ? tp::launch_brick_scatter(g.cubic, g.q, go, nullptr, gs, nullptr, ws,
-                                                       binned, s)
+                                                       mode, s)
                             : tp::launch_scatter(dim, g.cubic, g.q, go, nullptr, gs, nullptr, s);
         if (e != cudaSuccess) return launched(e, "spectrum gradient");
     }
@@ -304,7 +304,8 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
     if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
     return launched(tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
                                              weights, reinterpret_cast<float2 *>(data_vol),
-                                             weight_vol, workspace, false,
+                                             weight_vol, workspace,
+                                             tp::kBinNew,
                                              static_cast<cudaStream_t>(stream)),
                     "backproject");
 }

@@ -88,7 +88,16 @@ struct PoseGeo {
 constexpr int kGeoWords = sizeof(PoseGeo) / 4;
 
 // Scratch layout inside the caller's workspace.
+// Identity of a binning: the sizes it was computed for.  Together with the
+// pose geometry it determines the masks and work units completely.
+constexpr int kKeyWords = 12;
+struct BinKey {
+    unsigned w[kKeyWords];
+};
+
 struct Scratch {
+    unsigned *key;        // BinKey of the binning held in the workspace
+    unsigned *changed;    // set by k_pose_geometry when key or geometry differ
     unsigned *counters;   // [4][Bsrc]: work counters of the three main kernels, unit counts
     PoseGeo *geo;         // B*P poses
     unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
@@ -267,16 +276,39 @@ __device__ __forceinline__ int pose_id(const Params &q, int v, int i) {
 
 // ---------------------------------------------------------------------------
 // Binning passes.
-__global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratch sc) {
+// Pose geometry, and whether the binning held in the workspace still fits:
+// *sc.changed (cleared before the launch) is set when the key or any pose's
+// geometry differs bit for bit from what is stored, and the masks and units
+// are then recomputed; otherwise the two passes after this one return at
+// once.  The work counters of the main kernels are cleared either way.
+__global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratch sc, BinKey key) {
     const int id = blockIdx.x * 256 + threadIdx.x;
     const int stride = gridDim.x * 256;
-    for (int k = id; k < 4 * q.Bsrc; k += stride) sc.counters[k] = 0u;
+    for (int k = id; k < 3 * q.Bsrc; k += stride) sc.counters[k] = 0u;
     for (long long k = id; k < (long long)q.Bsrc * nbr; k += stride) sc.hits[k] = 0;
+    if (id == 0) {
+        bool same = true;
+#pragma unroll
+        for (int i = 0; i < kKeyWords; ++i) same = same && sc.key[i] == key.w[i];
+        if (!same) {
+#pragma unroll
+            for (int i = 0; i < kKeyWords; ++i) sc.key[i] = key.w[i];
+            atomicOr(sc.changed, 1u);
+        }
+    }
     if (id >= q.B * q.P) return;
     const int b = id / q.P, pi = id - b * q.P;
     PoseGeo g;
     pose_geo(q, b, pi, g);
-    sc.geo[id] = g;
+    const int *now = reinterpret_cast<const int *>(&g);
+    int *held = reinterpret_cast<int *>(sc.geo + id);
+    bool same = true;
+#pragma unroll
+    for (int k = 0; k < kGeoWords; ++k) same = same && held[k] == now[k];
+    if (!same) {
+        sc.geo[id] = g;
+        atomicOr(sc.changed, 1u);
+    }
 }
 
 __device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
@@ -295,6 +327,7 @@ __device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
 constexpr int kMaskBricks = 8;
 
 __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
+    if (*sc.changed == 0u) return;
     const int nbr = nb * nb * nb;
     const int nchunks = sc.nchunks;
     const int ranges = (nbr + kMaskBricks - 1) / kMaskBricks;
@@ -329,6 +362,7 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch s
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc) {
+    if (*sc.changed == 0u) return;
     __shared__ int warp_sum[kPlanThreads / 32];
     const int v = blockIdx.x;
     const int nch = sc.nchunks;
@@ -1073,7 +1107,7 @@ int bricks_per_axis(int M, bool cubic) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t geo, masks, hits, units, total;
+    size_t counters, geo, masks, hits, units, total;
     int nb, nchunks;
 };
 
@@ -1083,7 +1117,8 @@ Layout layout(const Params &q, bool cubic) {
     const size_t nbr = (size_t)L.nb * L.nb * L.nb;
     const long long Pv = (q.Bsrc == 1) ? (long long)q.B * q.P : q.P;
     L.nchunks = (int)((Pv + 31) / 32);
-    L.geo = align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);   // counters first
+    L.counters = 256;                                         // key and flag first
+    L.geo = L.counters + align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);
     L.masks = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
     L.hits = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.units = L.hits + align256(sizeof(int) * (size_t)q.Bsrc * nbr);
@@ -1094,7 +1129,9 @@ Layout layout(const Params &q, bool cubic) {
 Scratch scratch_in(void *ws, const Layout &L) {
     Scratch sc;
     char *base = static_cast<char *>(ws);
-    sc.counters = reinterpret_cast<unsigned *>(base);
+    sc.key = reinterpret_cast<unsigned *>(base);
+    sc.changed = sc.key + kKeyWords;
+    sc.counters = reinterpret_cast<unsigned *>(base + L.counters);
     sc.geo = reinterpret_cast<PoseGeo *>(base + L.geo);
     sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
     sc.hits = reinterpret_cast<int *>(base + L.hits);
@@ -1115,16 +1152,43 @@ int resident_blocks(const void *kern, size_t smem) {
 
 // Pose geometry, brick masks and work units for the poses of q (shared by
 // the main kernels of one call).
+BinKey bin_key(const Params &q, const Layout &L) {
+    BinKey k{};
+    k.w[0] = 0x6e696274u;   // tag: a binning of this library
+    k.w[1] = (unsigned)q.M;
+    k.w[2] = (unsigned)q.N;
+    k.w[3] = (unsigned)q.B;
+    k.w[4] = (unsigned)q.P;
+    k.w[5] = (unsigned)q.Bsrc;
+    k.w[6] = (unsigned)q.Bp;
+    k.w[7] = (unsigned)q.Bs;
+    k.w[8] = (unsigned)L.nb;
+    k.w[9] = (unsigned)L.nchunks;
+    k.w[10] = (unsigned)q.r2max;
+    k.w[11] = q.shift ? 1u : 0u;
+    return k;
+}
+
 cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_t st) {
     const int nbr = L.nb * L.nb * L.nb;
     const int pb = (int)((q.B * (long long)q.P + 255) / 256);
-    k_pose_geometry<<<pb, 256, 0, st>>>(q, nbr, sc);
+    cudaError_t e = cudaMemsetAsync(sc.changed, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    k_pose_geometry<<<pb, 256, 0, st>>>(q, nbr, sc, bin_key(q, L));
     const long long warps = (long long)q.Bsrc * L.nchunks * ((nbr + kMaskBricks - 1) / kMaskBricks);
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 32) blocks = 65535LL * 32;
     k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, sc);
     k_plan_units<<<q.Bsrc, kPlanThreads, 0, st>>>(nbr, sc);
     return cudaGetLastError();
+}
+
+// Binning for a main kernel whose work counter is `slot` (0 forward, 1 pose
+// gradient, 2 scatter).
+cudaError_t prepare(const Params &q, const Layout &L, const Scratch &sc, int slot, BinMode mode,
+                    cudaStream_t st) {
+    (void)slot;
+    return mode == kBinNew ? bin(q, L, sc, st) : cudaSuccess;
 }
 
 // Blocks of a main kernel: the resident ones, shared out over the volumes
@@ -1137,28 +1201,29 @@ dim3 main_grid(const Params &q, const void *kern, size_t smem) {
 }
 
 template <bool CUBIC, bool SAVE>
-cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, cudaStream_t st) {
+cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, BinMode mode,
+                      cudaStream_t st) {
     const Layout L = layout(q, CUBIC);
     const Scratch sc = scratch_in(ws, L);
     const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
     auto kern = k_brick_project<CUBIC, SAVE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if ((e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    if ((e = prepare(q, L, sc, 0, mode, st)) != cudaSuccess) return e;
     kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out, dout);
     return cudaGetLastError();
 }
 
 template <bool CUBIC>
 cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gshift, void *ws,
-                        bool binned, cudaStream_t st) {
+                        BinMode mode, cudaStream_t st) {
     const Layout L = layout(q, CUBIC);
     const Scratch sc = scratch_in(ws, L);
     const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
     auto kern = k_brick_pose_grad<CUBIC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    if ((e = prepare(q, L, sc, 1, mode, st)) != cudaSuccess) return e;
     kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, g, grot,
                                                                        gshift);
     return cudaGetLastError();
@@ -1166,14 +1231,14 @@ cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gs
 
 template <bool WEIGHTS>
 cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
-                             float *wdst, void *ws, bool binned, cudaStream_t st) {
+                             float *wdst, void *ws, BinMode mode, cudaStream_t st) {
     const Layout L = layout(q, false);
     const Scratch sc = scratch_in(ws, L);
     const size_t smem = sizeof(float) * Halo<false>::ELEMS * (WEIGHTS ? 3 : 2) + sizeof(Queue) * kWarps;
     auto kern = k_brick_scatter_linear<WEIGHTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
     kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
                                                                        dst, wdst);
     return cudaGetLastError();
@@ -1181,7 +1246,7 @@ cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *om
 
 template <bool WEIGHTS>
 cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
-                            float *wdst, void *ws, bool binned, cudaStream_t st) {
+                            float *wdst, void *ws, BinMode mode, cudaStream_t st) {
     using OL = OctLayout<WEIGHTS>;
     const Layout L = layout(q, true);
     const Scratch sc = scratch_in(ws, L);
@@ -1190,7 +1255,7 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
     auto kern = k_brick_scatter_cubic<WEIGHTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (!binned && (e = bin(q, L, sc, st)) != cudaSuccess) return e;
+    if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
     int dev = 0, sms = 148, per_sm = 1;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1208,27 +1273,27 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
 size_t brick_workspace_bytes(const Params &q, bool cubic) { return layout(q, cubic).total; }
 
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
-                                 cudaStream_t st) {
+                                 BinMode mode, cudaStream_t st) {
     if (dout)
-        return cubic ? project_t<true, true>(q, out, dout, ws, st)
-                     : project_t<false, true>(q, out, dout, ws, st);
-    return cubic ? project_t<true, false>(q, out, nullptr, ws, st)
-                 : project_t<false, false>(q, out, nullptr, ws, st);
+        return cubic ? project_t<true, true>(q, out, dout, ws, mode, st)
+                     : project_t<false, true>(q, out, dout, ws, mode, st);
+    return cubic ? project_t<true, false>(q, out, nullptr, ws, mode, st)
+                 : project_t<false, false>(q, out, nullptr, ws, mode, st);
 }
 
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *g, float *grot,
-                                   float *gshift, void *ws, bool binned, cudaStream_t st) {
-    return cubic ? pose_grad_t<true>(q, g, grot, gshift, ws, binned, st)
-                 : pose_grad_t<false>(q, g, grot, gshift, ws, binned, st);
+                                   float *gshift, void *ws, BinMode mode, cudaStream_t st) {
+    return cubic ? pose_grad_t<true>(q, g, grot, gshift, ws, mode, st)
+                 : pose_grad_t<false>(q, g, grot, gshift, ws, mode, st);
 }
 
 cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
-                                 float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st) {
+                                 float2 *dst, float *wdst, void *ws, BinMode mode, cudaStream_t st) {
     if (wdst)
-        return cubic ? scatter_cubic_t<true>(q, img, omega, dst, wdst, ws, binned, st)
-                     : scatter_linear_t<true>(q, img, omega, dst, wdst, ws, binned, st);
-    return cubic ? scatter_cubic_t<false>(q, img, omega, dst, nullptr, ws, binned, st)
-                 : scatter_linear_t<false>(q, img, omega, dst, nullptr, ws, binned, st);
+        return cubic ? scatter_cubic_t<true>(q, img, omega, dst, wdst, ws, mode, st)
+                     : scatter_linear_t<true>(q, img, omega, dst, wdst, ws, mode, st);
+    return cubic ? scatter_cubic_t<false>(q, img, omega, dst, nullptr, ws, mode, st)
+                 : scatter_linear_t<false>(q, img, omega, dst, nullptr, ws, mode, st);
 }
 
 }  // namespace tp

@@ -21,18 +21,21 @@ cudaError_t launch_scatter(int dim, bool cubic, const Params &q, const float2 *i
                            const float *omega, float2 *dst, float *wdst, cudaStream_t st);
 
 // 3D brick-binned kernels (tp_brick.cu): forward, pose gradients and
-// scatter.  ws is the caller's workspace of brick_workspace_bytes() bytes;
-// with binned = true the pose binning of an earlier launch on the same
-// stream, for the same poses, is reused.  With dout the forward also writes
-// D_a = phase * dS/dp_a, three complex values per output pixel.
+// scatter.  ws is the caller's workspace of brick_workspace_bytes() bytes.
+// With kBinNew the launch bins its poses first (pose geometry, brick masks,
+// work units; masks and units are kept when the workspace already holds the
+// binning of identical poses and sizes); with kBinSameCall it uses the
+// binning an earlier launch of the same call made.  With dout the forward
+// also writes D_a = phase * dS/dp_a, three complex values per output pixel.
+enum BinMode { kBinNew = 0, kBinSameCall = 1 };
 size_t brick_workspace_bytes(const Params &q, bool cubic);
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
-                                 cudaStream_t st);
+                                 BinMode mode, cudaStream_t st);
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
-                                   float *grad_rot, float *grad_shift, void *ws, bool binned,
+                                   float *grad_rot, float *grad_shift, void *ws, BinMode mode,
                                    cudaStream_t st);
 cudaError_t launch_brick_scatter(bool cubic, const Params &q, const float2 *img, const float *omega,
-                                 float2 *dst, float *wdst, void *ws, bool binned, cudaStream_t st);
+                                 float2 *dst, float *wdst, void *ws, BinMode mode, cudaStream_t st);
 
 // dL/dR (rows 0 and 1) and dL/dshift of the 3D forward from its output y and
 // saved derivatives D (tp_saved.cu), accumulated with atomics.

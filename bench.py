@@ -338,8 +338,17 @@ def run_ours(args):
     K = K - K.transpose(0, 2, 1)
     dR = (np.eye(3) + np.sin(ang)[:, None, None] * K
           + (1 - np.cos(ang))[:, None, None] * (K @ K))
-    rot = torch.from_numpy((w["rot"][0].astype(np.float64) @ dR).astype(np.float32)[None]).to(dev)
-    shift = (t_true + torch.from_numpy(rng[1].normal(0, 1, (1, P, 2)).astype(np.float32)).to(dev))
+    rot_a = torch.from_numpy((w["rot"][0].astype(np.float64) @ dR).astype(np.float32)[None]).to(dev)
+    shift_a = (t_true + torch.from_numpy(rng[1].normal(0, 1, (1, P, 2)).astype(np.float32)).to(dev))
+    # A second set of estimates (the first nudged by ~0.1 degree, ~0.05 px):
+    # steps alternate between the two, so that every step brings new poses
+    # (as the updated estimates of a refinement would) and the forward bins
+    # them; the backward of the same step reuses that binning.
+    eps = torch.from_numpy(0.002 * rng[1].standard_normal((1, P, 3, 3)).astype(np.float32)).to(dev)
+    rot_b = rot_a + eps
+    shift_b = shift_a + 0.05
+    pose_sets = [(rot_a, shift_a), (rot_b, shift_b)]
+    rot, shift = rot_a.clone(), shift_a.clone()
     # Targets: clean projections at the true poses plus noise of 10x the signal power.
     clean = tp.tp_project_3d_2d(vol, R_true, t_true, **kw)  # (workspace allocated per call here)
     noise = torch.from_numpy(synth.complex_normal((1, P, N, N // 2 + 1), rng[2])).to(dev)
@@ -364,7 +373,10 @@ def run_ours(args):
 
     kw_saved = {k: kw[k] for k in ("interp", "oversampling", "radius")}
 
-    def step(ev=None):
+    def step(ev=None, i=0):
+        # This step's pose estimates (an 18 KB device copy, untimed).
+        rot.copy_(pose_sets[i & 1][0])
+        shift.copy_(pose_sets[i & 1][1])
         if ev:
             ev[0].record(stream)
         # Forward; it also saves D = phase * dS/dp for the pose gradients.
@@ -386,9 +398,9 @@ def run_ours(args):
         if ev:
             ev[4].record(stream)
 
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         flush.zero_()
-        step()
+        step(i=i)
     torch.cuda.synchronize()
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -398,7 +410,7 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.zero_()                                            # L2 flush, untimed
-            step(events[i])
+            step(events[i], i=args.warmup + i)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -414,31 +426,32 @@ def run_ours(args):
     # End to end through the public API with host buffers: pinned inputs
     # copied in, the step, gradients copied out, every step.
     h_vol = vol.cpu().pin_memory()
-    h_rot, h_shift = rot.cpu().pin_memory(), shift.cpu().pin_memory()
+    h_poses = [(r.cpu().pin_memory(), t.cpu().pin_memory()) for r, t in pose_sets]
+    h_rot, h_shift = h_poses[0]
     h_m2t = m2t.cpu().pin_memory()
     o_vol = torch.empty_like(h_vol).pin_memory()
     o_rot, o_shift = torch.empty_like(h_rot).pin_memory(), torch.empty_like(h_shift).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (h_vol, h_rot, h_shift, h_m2t))
     d2h = sum(t.numel() * t.element_size() for t in (o_vol, o_rot, o_shift))
 
-    def e2e_step():
+    def e2e_step(i):
         vol.copy_(h_vol, non_blocking=True)
-        rot.copy_(h_rot, non_blocking=True)
-        shift.copy_(h_shift, non_blocking=True)
+        pose_sets[0][0].copy_(h_poses[i & 1][0], non_blocking=True)
+        pose_sets[0][1].copy_(h_poses[i & 1][1], non_blocking=True)
         m2t.copy_(h_m2t, non_blocking=True)
-        step()
+        step(i=0)
         o_vol.copy_(grad_vol, non_blocking=True)
         o_rot.copy_(grad_rot, non_blocking=True)
         o_shift.copy_(grad_shift, non_blocking=True)
 
-    e2e_step()
+    e2e_step(1)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)

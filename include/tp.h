@@ -58,9 +58,12 @@
  * Workspace.  The 3D entry points bin poses against bricks of the volume in
  * a scratch area the caller provides: `workspace` must point to at least
  * tp_workspace_bytes(...) bytes of device memory, 16-byte aligned, owned by
- * the caller.  Its contents need no initialisation and are meaningless
- * between calls; it must not be used by two calls that can run at the same
- * time (one workspace per stream).
+ * the caller.  Its contents need no initialisation.  A call that finds in it
+ * the binning of identical poses and sizes (compared on the device, bit for
+ * bit: for example the backward call after the forward call of one step)
+ * keeps the brick masks and work units instead of recomputing them; any
+ * difference, or a fresh workspace, recomputes them.  It must not be used by
+ * two calls that can run at the same time (one workspace per stream).
  *
  * Errors.  Each call returns a tp_status.  Argument errors are detected
  * before anything is enqueued; TP_ERR_CUDA reports a launch failure.  No
@@ -88,6 +91,7 @@ typedef enum {
 } tp_status;
 
 enum { TP_LINEAR = 0, TP_CUBIC = 1 };
+
 
 typedef struct {
     int interp;         /* TP_LINEAR or TP_CUBIC */
