@@ -161,3 +161,51 @@ def project_backward(dim, grad_out, src, rot, shift=None, interp="linear", overs
                                            float(oversampling), float(radius),
                                            _ptr(gsrc), _ptr(grot), _ptr(gshift)))
     return gsrc, grot, gshift
+
+
+def backproject_backward(dim, grad_data, img, rot, shift=None, grad_weight=None, weights=None,
+                         interp="linear", oversampling=1.0, radius=-1.0):
+    """Gradients of backproject() for upstream gradients of its two spectra.
+
+    backproject() is the real adjoint of project() (data: taps w times
+    conj(phase) times the image; weights: taps w times the image weights,
+    no phase).  With grad_data (complex) and grad_weight (real, or None) the
+    upstream gradients of the data and weight spectra:
+      grad_img     = project(grad_data)                 (adjoint of the adjoint)
+      grad_weights = Re project(grad_weight), no shift  (None without grad_weight)
+      grad_rot     = project()'s rotation gradient at spectrum grad_data for
+                     upstream img, plus, with grad_weight, that at spectrum
+                     grad_weight without shift for upstream weights (or 1)
+      grad_shift   = project()'s shift gradient at spectrum grad_data for
+                     upstream img (None without shift)
+    The tests pin this against finite differences of backproject() itself.
+    Returns (grad_img, grad_weights, grad_rot, grad_shift).
+    """
+    img = _c(img, np.complex128)
+    B, N = img.shape[0], img.shape[2]
+    kw = dict(interp=interp, oversampling=oversampling, radius=radius)
+
+    def upstream(a, *operands):
+        # project()'s batch is that of its operands; when they are all
+        # shared by the B images, the gradients (linear in the upstream)
+        # take the upstream summed over the images.
+        nb = max(o.shape[0] for o in operands if o is not None)
+        return a.sum(axis=0, keepdims=True) if nb < a.shape[0] else a
+
+    rot_ = _c(rot, np.float64)
+    shift_ = _c(shift, np.float64)
+    gd = _c(grad_data, np.complex128)
+    grad_img = np.broadcast_to(project(dim, gd, rot_, shift=shift_, N=N, **kw),
+                               img.shape).copy()
+    _, grad_rot, grad_shift = project_backward(dim, upstream(img, gd, rot_, shift_), gd, rot_,
+                                               shift=shift_, need_src=False, **kw)
+    grad_weights = None
+    if grad_weight is not None:
+        gw = _c(grad_weight, np.complex128)
+        grad_weights = np.broadcast_to(project(dim, gw, rot_, shift=None, N=N, **kw).real,
+                                       img.shape).copy()
+        om = np.ones(img.shape) if weights is None else _c(weights, np.float64)
+        _, gr_w, _ = project_backward(dim, upstream(om, gw, rot_).astype(np.complex128), gw, rot_,
+                                      shift=None, need_src=False, need_shift=False, **kw)
+        grad_rot = grad_rot + gr_w
+    return grad_img, grad_weights, grad_rot, grad_shift

@@ -435,3 +435,61 @@ def test_batch_broadcast_matches_separate_calls():
                                             interp="cubic")
         acc += gRb
     np.testing.assert_allclose(gR, acc, rtol=1e-12, atol=1e-12)
+
+
+# P16: gradients of the backprojection (data and weight spectra) against
+# finite differences of backproject() itself, for
+#   L = Re<G, data(y, w; R, t)> + <GW, weight(y, w; R, t)>.
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+@pytest.mark.parametrize("with_weights", [False, True])
+def test_backprojection_gradients_finite_differences(interp, with_weights):
+    rng = np.random.default_rng(16)
+    M, N, P = 18, 16, 2
+    s, r = 1.2, 7.0
+    y = crandn(rng, (2, P, N, N // 2 + 1))
+    om = rng.uniform(0.5, 1.5, y.shape) if with_weights else None
+    R = synth.random_rotations(P, rng).astype(np.float64)[None]          # broadcast over B = 2
+    t = rng.uniform(-3, 3, (2, P, 2))
+    G = crandn(rng, (1, M, M, M // 2 + 1))
+    GW = rng.standard_normal((1, M, M, M // 2 + 1))
+    kw = dict(interp=interp, oversampling=s, radius=r)
+
+    def loss(y_, om_, R_, t_):
+        data, wt = oracle.backproject(3, y_, R_, shift=t_, M=M, weights=om_, **kw)
+        return np.vdot(G, data).real + np.sum(GW * wt)
+
+    gy, gw, gR, gt = oracle.backproject_backward(3, G, y, R, shift=t, grad_weight=GW, weights=om,
+                                                 **kw)
+    h = 1e-6 if interp == "cubic" else 1e-7
+    for idx in itertools.product(range(P), range(3), range(3)):
+        Rp, Rm = R.copy(), R.copy()
+        Rp[(0,) + idx] += h
+        Rm[(0,) + idx] -= h
+        fd = (loss(y, om, Rp, t) - loss(y, om, Rm, t)) / (2 * h)
+        assert abs(fd - gR[(0,) + idx]) <= 1e-6 * (abs(fd) + np.abs(gR).max()), (idx, fd)
+    for idx in itertools.product(range(2), range(P), range(2)):
+        tp, tm = t.copy(), t.copy()
+        tp[idx] += h
+        tm[idx] -= h
+        fd = (loss(y, om, R, tp) - loss(y, om, R, tm)) / (2 * h)
+        assert abs(fd - gt[idx]) <= 1e-6 * (abs(fd) + np.abs(gt).max()), (idx, fd)
+    # The map is linear in the images and in the weights: unit differences are exact.
+    for _ in range(6):
+        e = tuple(rng.integers(0, n) for n in y.shape)
+        for dv in (1.0, 1j):
+            yp, ym = y.copy(), y.copy()
+            yp[e] += dv
+            ym[e] -= dv
+            fd = (loss(yp, om, R, t) - loss(ym, om, R, t)) / 2
+            want = gy[e].real if dv == 1.0 else gy[e].imag
+            assert abs(fd - want) <= 1e-10 * (1 + abs(fd))
+        if with_weights:
+            op, omm = om.copy(), om.copy()
+            op[e] += 1.0
+            omm[e] -= 1.0
+            fd = (loss(y, op, R, t) - loss(y, omm, R, t)) / 2
+            assert abs(fd - gw[e]) <= 1e-10 * (1 + abs(fd))
+    if not with_weights:
+        # The weight spectrum with unit image weights still depends on the poses.
+        gy1, gw1, gR1, _ = oracle.backproject_backward(3, G, y, R, shift=t, grad_weight=GW, **kw)
+        assert gw1.shape == y.shape
