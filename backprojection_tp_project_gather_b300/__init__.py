@@ -58,9 +58,13 @@ _SIGS = {
     "tp_project_2d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P],
     "tp_backproject_2d_3d": [_P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions, _P, _P, _P, _Z,
                              _P],
+    "tp_backproject_2d_3d_backward": [_P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I, _I, _I, TPOptions,
+                                      _P, _P, _P, _P, _P, _Z, _P, _Z, _P],
+    "tp_backproject_backward_scratch_bytes": [_I, _I, _I, _I, _I, _I],
 }
 _SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, TPOptions]
 _RESTYPES = {"tp_workspace_bytes": ctypes.c_size_t, "tp_last_error": ctypes.c_char_p,
+             "tp_backproject_backward_scratch_bytes": ctypes.c_size_t,
              "tp_version": ctypes.c_char_p}
 _bound = {}
 
@@ -361,3 +365,72 @@ def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, 
           Bs, Bv, Nv, _opts(interp, oversampling, radius), _ptr(data_vol), _ptr(weight_vol),
           _ptr(ws), nbytes, _stream(stream))
     return data_vol, weight_vol
+
+
+def tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, with_weight_grad=True):
+    """Scratch bytes tp_backproject_2d_3d_backward needs (see include/tp.h)."""
+    return int(_fn("tp_backproject_backward_scratch_bytes")(int(Bv), int(B), int(P), int(N), int(Nv),
+                                                            1 if with_weight_grad else 0))
+
+
+def tp_backproject_2d_3d_backward(grad_data_vol, proj, rot, shift=None, weights=None,
+                                  grad_weight_vol=None, *, interp="cubic", oversampling=1.0,
+                                  radius=-1.0, grad_proj=None, grad_weights=None, grad_rot=None,
+                                  grad_shift=None, want_proj=True, want_weights=True,
+                                  want_rot=True, want_shift=True, scratch=None, workspace=None,
+                                  stream=None):
+    """Gradients of tp_backproject_2d_3d: (grad_proj, grad_weights, grad_rot, grad_shift).
+
+    grad_proj and grad_weights are written; grad_rot and grad_shift are
+    accumulated into the given tensors (zeros when omitted); see tp.h."""
+    _need(grad_data_vol, "grad_data_vol", torch.complex64, 4)
+    _need(proj, "proj", torch.complex64, 4)
+    Bv, Nv = grad_data_vol.shape[0], grad_data_vol.shape[1]
+    B, P, N = proj.shape[0], proj.shape[1], proj.shape[2]
+    Bp, Pr, Bs = _poses(rot, shift, 3)
+    if Pr != P:
+        raise ValueError("rot must have the projections' P")
+    if weights is not None:
+        _need(weights, "weights", torch.float32, 4)
+        if weights.shape != proj.shape:
+            raise ValueError("weights must have proj's shape")
+    if grad_weight_vol is not None:
+        _need(grad_weight_vol, "grad_weight_vol", torch.float32, 4)
+        if grad_weight_vol.shape != grad_data_vol.shape:
+            raise ValueError("grad_weight_vol must have grad_data_vol's shape")
+    dev = proj.device
+    if want_proj and grad_proj is None:
+        grad_proj = torch.empty_like(proj)
+    if want_weights and grad_weight_vol is not None and grad_weights is None:
+        grad_weights = torch.empty(proj.shape, dtype=torch.float32, device=dev)
+    if want_rot and grad_rot is None:
+        grad_rot = torch.zeros_like(rot)
+    if want_shift and shift is not None and grad_shift is None:
+        grad_shift = torch.zeros_like(shift)
+    for t, name, dt in ((grad_proj, "grad_proj", torch.complex64),
+                        (grad_weights, "grad_weights", torch.float32)):
+        if t is not None:
+            _need(t, name, dt, 4)
+            if t.shape != proj.shape:
+                raise ValueError(f"{name} must have proj's shape")
+    if grad_rot is not None:
+        _need(grad_rot, "grad_rot", torch.float32, 4)
+        if grad_rot.shape != rot.shape:
+            raise ValueError("grad_rot must have rot's shape")
+    if grad_shift is not None:
+        _need(grad_shift, "grad_shift", torch.float32, 3)
+        if shift is None or grad_shift.shape != shift.shape:
+            raise ValueError("grad_shift must have shift's shape")
+    weight_terms = grad_weight_vol is not None and (grad_weights is not None or grad_rot is not None)
+    need = tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, weight_terms)
+    if scratch is None:
+        scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if scratch.device.type != "cuda" or not scratch.is_contiguous():
+        raise ValueError("scratch must be a contiguous CUDA tensor")
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, dev)
+    _call("tp_backproject_2d_3d_backward", _ptr(grad_data_vol), _ptr(grad_weight_vol), _ptr(proj),
+          _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift), Bs, Bv, Nv,
+          _opts(interp, oversampling, radius), _ptr(grad_proj), _ptr(grad_weights), _ptr(grad_rot),
+          _ptr(grad_shift), _ptr(scratch), scratch.numel() * scratch.element_size(), _ptr(ws),
+          nbytes, _stream(stream))
+    return grad_proj, grad_weights, grad_rot, grad_shift

@@ -310,6 +310,97 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
                     "backproject");
 }
 
+size_t tp_backproject_backward_scratch_bytes(int Bv, int B, int P, int N, int Nv,
+                                             int with_weight_grad) {
+    if (Bv < 1 || B < 1 || P < 1 || N < 2 || (N & 1) || Nv < 2 || (Nv & 1) || N > 4096 ||
+        Nv > 4096 || Bv > B)
+        return 0;
+    auto a256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t img = (size_t)B * P * N * (N / 2 + 1);
+    size_t bytes = a256(8 * img) + a256(24 * img);                        // y, D
+    if (with_weight_grad)
+        bytes += a256(8 * (size_t)Bv * Nv * Nv * (Nv / 2 + 1)) + a256(8 * img);   // GW + 0i, y_W
+    return bytes;
+}
+
+tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float *grad_weight_vol,
+                                        const float *proj, const float *weights, int B, int P,
+                                        int N, const float *rot, int Bp, const float *shift, int Bs,
+                                        int Bv, int Nv, tp_options opts, float *grad_proj,
+                                        float *grad_weights, float *grad_rot, float *grad_shift,
+                                        void *scratch, size_t scratch_bytes, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    Geometry g;
+    tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
+    if (st != TP_OK) return st;
+    if (g.q.B != B)
+        return fail(TP_ERR_SHAPE, "operand batches (%d) exceed the image batch B = %d", g.q.B, B);
+    if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
+    if (!rot) return fail(TP_ERR_NULL, "rotation pointer is required");
+    const bool data_terms = grad_proj || grad_shift || (grad_rot && grad_data_vol);
+    if (data_terms && !grad_data_vol)
+        return fail(TP_ERR_NULL, "grad_proj / grad_shift need grad_data_vol");
+    if (grad_weights && !grad_weight_vol)
+        return fail(TP_ERR_NULL, "grad_weights needs grad_weight_vol");
+    if ((grad_rot || grad_shift) && !proj)
+        return fail(TP_ERR_NULL, "rotation / shift gradients need proj");
+    if (grad_shift && !shift) return fail(TP_ERR_NULL, "grad_shift requested without a shift tensor");
+    if ((grad_data_vol && (st = check_complex(grad_data_vol, "grad_data_vol")) != TP_OK) ||
+        (proj && (st = check_complex(proj, "proj")) != TP_OK) ||
+        (grad_proj && (st = check_complex(grad_proj, "grad_proj")) != TP_OK))
+        return st;
+    if ((grad_weight_vol && !aligned(grad_weight_vol, 4)) || (weights && !aligned(weights, 4)) ||
+        (grad_weights && !aligned(grad_weights, 4)) || (grad_rot && !aligned(grad_rot, 4)) ||
+        (grad_shift && !aligned(grad_shift, 4)))
+        return fail(TP_ERR_ALIGN, "real arrays must be 4-byte aligned");
+    const bool weight_terms = grad_weight_vol && (grad_weights || grad_rot);
+    if (!data_terms && !weight_terms) return ok();
+    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    const size_t need = tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, weight_terms ? 1 : 0);
+    if (!scratch) return fail(TP_ERR_NULL, "scratch is required (%zu bytes)", need);
+    if (!aligned(scratch, 16)) return fail(TP_ERR_ALIGN, "scratch must be 16-byte aligned");
+    if (scratch_bytes < need)
+        return fail(TP_ERR_SHAPE, "scratch too small: %zu bytes given, %zu needed", scratch_bytes, need);
+    auto a256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t img = (size_t)B * P * N * (N / 2 + 1);
+    char *base = static_cast<char *>(scratch);
+    float2 *sy = reinterpret_cast<float2 *>(base);
+    float2 *sD = reinterpret_cast<float2 *>(base + a256(8 * img));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (data_terms) {
+        // P(G) (the images' gradient) and its saved derivatives, then the
+        // pose gradients with the images as the upstream gradient.
+        g.q.src = reinterpret_cast<const float2 *>(grad_data_vol);
+        float2 *y = grad_proj ? reinterpret_cast<float2 *>(grad_proj) : sy;
+        e = tp::launch_brick_project(g.cubic, g.q, y, (grad_rot || grad_shift) ? sD : nullptr,
+                                     workspace, tp::kBinNew, s);
+        if (e != cudaSuccess) return launched(e, "backprojection gradient (data)");
+        if (grad_rot || grad_shift) {
+            e = tp::launch_pose_grad_saved(g.q, reinterpret_cast<const float2 *>(proj), y, sD,
+                                           grad_rot, grad_shift, s);
+            if (e != cudaSuccess) return launched(e, "backprojection pose gradient (data)");
+        }
+    }
+    if (weight_terms) {
+        float2 *gw = reinterpret_cast<float2 *>(base + a256(8 * img) + a256(24 * img));
+        float2 *yw = reinterpret_cast<float2 *>(reinterpret_cast<char *>(gw) +
+                                                a256(8 * (size_t)Bv * Nv * Nv * (Nv / 2 + 1)));
+        e = tp::launch_real_to_complex(grad_weight_vol, gw, (long long)Bv * g.q.src_stride, s);
+        if (e != cudaSuccess) return launched(e, "backprojection gradient (weights)");
+        tp::Params qw = g.q;   // the weight spectrum has no phase
+        qw.src = gw;
+        qw.shift = nullptr;
+        qw.Bs = 1;
+        e = tp::launch_brick_project(g.cubic, qw, yw, grad_rot ? sD : nullptr, workspace,
+                                     tp::kBinNew, s);
+        if (e != cudaSuccess) return launched(e, "backprojection gradient (weights)");
+        e = tp::launch_weight_grads(qw, weights, yw, sD, grad_weights, grad_rot, s);
+        if (e != cudaSuccess) return launched(e, "backprojection gradient (weights)");
+    }
+    return ok();
+}
+
 const char *tp_last_error(void) { return g_err; }
 
 const char *tp_version(void) { return "0.1.0"; }

@@ -43,4 +43,13 @@ cudaError_t launch_pose_grad_saved(const Params &q, const float2 *grad_out, cons
                                    const float2 *D, float *grad_rot, float *grad_shift,
                                    cudaStream_t st);
 
+// Weight-spectrum gradients of the backprojection (tp_bpgrad.cu): dst = src
+// + 0i for n elements, and grad_weights = Re y (written) plus grad_rot +=
+// omega Re D_a s k_i from the unshifted projection y, D of the weight
+// spectrum's gradient.
+cudaError_t launch_real_to_complex(const float *src, float2 *dst, long long n, cudaStream_t st);
+cudaError_t launch_weight_grads(const Params &q, const float *omega, const float2 *y,
+                                const float2 *D, float *grad_weights, float *grad_rot,
+                                cudaStream_t st);
+
 }  // namespace tp

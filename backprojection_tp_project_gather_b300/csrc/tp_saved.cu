@@ -9,8 +9,8 @@
 //   dL/dp_a       = Re(conj(g) D_a)
 //   dL/dR[i][a]  += s k_i dL/dp_a           (i = 0, 1; row 2 stays 0)
 //   dL/dshift_a  += (2 pi k_a / N) Im(conj(g) y)
-// These are the analytic rotation and shift gradients of "torch-projectors:
-// Differentiable Fourier-Space Projection Library for PyTorch" [de §3 item 4;
+// These are the analytic rotation and shift gradients of "torch-projectors: A
+// High-Performance Differentiable Projection Library for PyTorch" [de §3 item 4;
 // ar §2], with the inverse rotation of [ko §2 "Forward Projection"] and the
 // shift phase exp(-2 pi i (kx sx + ky sy) / N) of [de §2 "Interpolation"].
 // This is a streaming reduction over (g, y, D): one block per output image,

@@ -185,6 +185,46 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Gradients of tp_backproject_2d_3d for upstream gradients of its data and
+ * weight spectra (the gradient of the backprojection "with respect to all
+ * inputs" [de §2 "Differentiable Backpropagation"] and through the weight
+ * spectrum [ar §2]).  The backprojection is the real adjoint of
+ * tp_project_3d_2d, so with G = grad_data_vol and GW = grad_weight_vol:
+ *   grad_proj     (B, P, N, N/2+1) complex = the projection of G (with the
+ *                 shift phase), WRITTEN, not accumulated;
+ *   grad_weights  (B, P, N, N/2+1) float = Re of the unshifted projection of
+ *                 GW, WRITTEN; needs grad_weight_vol;
+ *   grad_rot      (Bp, P, 3, 3) float, += the rotation gradient of the
+ *                 projection of G for upstream proj, plus (with GW) that of
+ *                 the unshifted projection of GW for upstream weights (1 when
+ *                 weights is NULL);
+ *   grad_shift    (Bs, P, 2) float, += the shift gradient of the projection
+ *                 of G for upstream proj; requires shift != NULL.
+ * Any output may be NULL.  grad_data_vol (Bv, Nv, Nv, Nv/2+1) complex is
+ * required for grad_proj and grad_shift, proj for grad_rot / grad_shift;
+ * grad_weight_vol (same shape, float) may be NULL (no weight terms).  The
+ * other arguments are those of tp_backproject_2d_3d.  scratch: at least
+ * tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, weight terms?) bytes
+ * of device memory, 16-byte aligned, owned by the caller; workspace as for
+ * the other 3D calls.
+ */
+tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float *grad_weight_vol,
+                                        const float *proj, const float *weights, int B, int P,
+                                        int N, const float *rot, int Bp, const float *shift, int Bs,
+                                        int Bv, int Nv, tp_options opts, float *grad_proj,
+                                        float *grad_weights, float *grad_rot, float *grad_shift,
+                                        void *scratch, size_t scratch_bytes, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
+ * Scratch bytes tp_backproject_2d_3d_backward needs (with_weight_grad != 0
+ * when grad_weight_vol is given and grad_weights or grad_rot is requested);
+ * 0 for invalid sizes.
+ */
+size_t tp_backproject_backward_scratch_bytes(int Bv, int B, int P, int N, int Nv,
+                                             int with_weight_grad);
+
+/*
  * 2D -> 2D forward: rotated and shifted 2D half-spectra
  * [it §2 "Operazioni Supportate"; de §2 item 1; ja §2].
  *   img    (Bi, Ni, Ni/2+1) complex;  rot (Bp, P, 2, 2);  shift (Bs, P, 2) or NULL

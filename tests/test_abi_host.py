@@ -35,7 +35,8 @@ def test_header_declares_the_operator_set():
     syms = declared_symbols()
     for name in ("tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
                  "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_project_3d_2d_save",
-                 "tp_project_3d_2d_backward_saved", "tp_last_error", "tp_version"):
+                 "tp_project_3d_2d_backward_saved", "tp_backproject_2d_3d_backward",
+                 "tp_backproject_backward_scratch_bytes", "tp_last_error", "tp_version"):
         assert name in syms
 
 
@@ -160,6 +161,31 @@ def test_saved_backward_validation(tp):
     assert bs(gr=A + 2) == TP_ERR_ALIGN
     assert bs(gr=None, gs=None, go=None) == TP_OK       # nothing requested: no work, no checks
     assert bs(P=0, go=None) == TP_OK
+
+
+def test_backprojection_backward_validation(tp):
+    SC = 0x40000
+
+    def bb(G=A, GW=None, proj=A, B=2, P=4, Bv=1, Bp=1, shift=None, gp=A, gw=None, gr=A, gs=None,
+           sc=SC, scb=WSB, ws=WS):
+        return tp._fn("tp_backproject_2d_3d_backward")(G, GW, proj, None, B, P, 16, A, Bp, shift, 1,
+                                                       Bv, 16, opts(tp), gp, gw, gr, gs, sc, scb,
+                                                       ws, WSB, None)
+    assert bb(G=None) == TP_ERR_NULL                    # grad_proj needs the data gradient
+    assert bb(gw=A) == TP_ERR_NULL                      # grad_weights needs grad_weight_vol
+    assert bb(proj=None) == TP_ERR_NULL                 # grad_rot needs the images
+    assert bb(gs=A) == TP_ERR_NULL                      # grad_shift without a shift
+    assert bb(sc=None) == TP_ERR_NULL
+    assert "scratch" in tp.tp_last_error()
+    assert bb(sc=SC + 8) == TP_ERR_ALIGN
+    assert bb(scb=64) == TP_ERR_SHAPE
+    assert bb(Bv=3) == TP_ERR_SHAPE
+    assert bb(gp=MIS) == TP_ERR_ALIGN
+    assert bb(gp=None, gr=None) == TP_OK                # nothing requested
+    assert bb(P=0, G=None) == TP_OK
+    small = tp.tp_backproject_backward_scratch_bytes(1, 2, 4, 16, 16, False)
+    assert 0 < small < tp.tp_backproject_backward_scratch_bytes(1, 2, 4, 16, 16, True)
+    assert tp.tp_backproject_backward_scratch_bytes(1, 2, 4, 15, 16, True) == 0
 
 
 def test_workspace_size_query(tp):
