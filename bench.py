@@ -59,6 +59,14 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--poses", type=int, default=None,
                     help="pose count (default: the workload's 512); smaller runs are for profiling")
+    ap.add_argument("--workload", default="fwdbwd",
+                    choices=["fwdbwd", "backproject", "backproject-backward", "oversampling"],
+                    help="fwdbwd: the differentiable step (the headline, default); backproject: "
+                         "2048 images into a 256^3 data + weight spectrum; backproject-backward: "
+                         "the gradients of that backprojection; oversampling: cubic at s = 1 "
+                         "against linear at s = 2 with the padding FFT, box 128, 4096 poses")
+    ap.add_argument("--interp", default="cubic", choices=["linear", "cubic"],
+                    help="interpolation of the backproject workloads")
     ap.add_argument("--ncu-summary", metavar="RAW_CSV", default=None,
                     help="write profiles/ncu_traffic.json from `ncu -i REP --page raw --csv` output")
     return ap.parse_args()
@@ -535,6 +543,175 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Further workloads (one GPU; not the headline line): each prints one JSON
+# line with CUDA-event timing of its step, inputs resident, L2 flushed.
+def _timed(step, steps, warmup, stream, flush):
+    import torch
+    for i in range(warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(warmup + i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = np.array([a.elapsed_time(b) for a, b in ev])
+    return ms, clocks.record()
+
+
+def run_workload(args):
+    import torch
+    import backprojection_tp_project_gather_b300 as tp
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peak, peak_src = measured_peak_hbm()
+    line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "impl": "ours", "workload": args.workload}
+
+    if args.workload in ("backproject", "backproject-backward"):
+        w = synth.workload(4)
+        n, N = w["P"], w["box"]
+        samples = n * N * (N // 2 + 1)
+        proj = torch.from_numpy(w["proj"]).to(dev)
+        rot = torch.from_numpy(w["rot"]).to(dev)
+        kw = dict(interp=args.interp, oversampling=1.0, radius=w["radius"])
+        shape = (1, N, N, N // 2 + 1)
+        ws = torch.empty(tp.tp_workspace_bytes(1, 1, n, N, args.interp), dtype=torch.uint8,
+                         device=dev)
+        vol_bytes = 8 * N * N * (N // 2 + 1)
+        cfg = {"workload": f"backproject-box{N}-{n}img-{args.interp}", "box": N, "images": n,
+               "interp": args.interp, "radius": w["radius"], "weights": "1 (default)",
+               "l2_cache": "flushed between steps (256 MB write)"}
+        if args.workload == "backproject":
+            data = torch.zeros(shape, dtype=torch.complex64, device=dev)
+            wvol = torch.zeros(shape, dtype=torch.float32, device=dev)
+
+            def step(i):
+                tp.tp_backproject_2d_3d(proj, rot, data_vol=data, weight_vol=wvol, workspace=ws,
+                                        **kw)
+            nbytes = samples * 8 + 2 * vol_bytes + 2 * vol_bytes // 2
+            metric = "backprojected Fourier samples/sec (Gsamples/s), data + weight spectra"
+        else:
+            rng = synth.streams(7004, 1)[0]
+            G = torch.from_numpy(synth.complex_normal(shape, rng)).to(dev)
+            GW = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(dev)
+            gp = torch.empty_like(proj)
+            gw = torch.empty(proj.shape, dtype=torch.float32, device=dev)
+            gr = torch.zeros_like(rot)
+            sc = torch.empty(tp.tp_backproject_backward_scratch_bytes(1, 1, n, N, N, True),
+                             dtype=torch.uint8, device=dev)
+
+            def step(i):
+                gr.zero_()
+                tp.tp_backproject_2d_3d_backward(G, proj, rot, grad_weight_vol=GW, grad_proj=gp,
+                                                 grad_weights=gw, grad_rot=gr, scratch=sc,
+                                                 workspace=ws, **kw)
+            # data: spectrum read, y and D written (32 B), images read with y and
+            # D (40 B); weights: spectrum read and converted, y_W and D_W written,
+            # read back with grad_weights written (4 B).
+            nbytes = (vol_bytes + samples * 32 + samples * 40
+                      + vol_bytes // 2 + vol_bytes + samples * 32 + samples * 36)
+            metric = ("Fourier samples/sec (Gsamples/s) of the backprojection's gradients "
+                      "(images, image weights, rotations)")
+            cfg["upstream"] = "random data (complex) and weight (real) spectrum gradients"
+        ms, clocks = _timed(step, args.steps, args.warmup, stream, flush)
+        t = float(ms.mean())
+        line.update(metric=metric, unit="Gsamples/s", value=samples / (t * 1e-3) / 1e9,
+                    ms_per_step=t, config=cfg, clocks=clocks,
+                    roofline={"bound": "hbm", "achieved": nbytes / (t * 1e-3) / 1e9, "peak": peak,
+                              "peak_source": peak_src, "unit": "GB/s",
+                              "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
+                              "algorithmic_bytes_per_step": nbytes,
+                              "timed": "whole call (binning + kernels)"})
+    elif args.workload == "oversampling":
+        c = synth.CONFIGS[3]
+        M, P = c["box"], c["poses"]
+        r_vol, r_rot = synth.streams(1003, 5)[:2]
+        cen, sig, amp = synth.blob_params(M, c["blobs"], r_vol, 3)
+        dens = torch.from_numpy(synth.blob_density(M, cen, sig, amp, 3).astype(np.float32)).to(dev)
+        rot = torch.from_numpy(synth.random_rotations(P, r_rot)[None]).to(dev)
+        radius = c["radius"]
+        out = torch.empty((1, P, M, M // 2 + 1), dtype=torch.complex64, device=dev)
+        ws1 = torch.empty(tp.tp_workspace_bytes(1, 1, P, M, "cubic"), dtype=torch.uint8, device=dev)
+        ws2 = torch.empty(tp.tp_workspace_bytes(1, 1, P, 2 * M, "linear"), dtype=torch.uint8,
+                          device=dev)
+        big = torch.zeros((2 * M,) * 3, dtype=torch.float32, device=dev)
+        o = M // 2
+
+        def spec(d):
+            return torch.fft.rfftn(torch.fft.ifftshift(d)).unsqueeze(0).contiguous()
+
+        def cubic1(i):
+            tp.tp_project_3d_2d(spec(dens), rot, out=out, interp="cubic", radius=radius,
+                                workspace=ws1)
+
+        def linear2(i):
+            big[o:o + M, o:o + M, o:o + M] = dens
+            tp.tp_project_3d_2d(spec(big), rot, N=M, out=out, interp="linear", oversampling=2.0,
+                                radius=radius, workspace=ws2)
+
+        def cubic2(i):
+            big[o:o + M, o:o + M, o:o + M] = dens
+            tp.tp_project_3d_2d(spec(big), rot, N=M, out=out, interp="cubic", oversampling=2.0,
+                                radius=radius, workspace=ws2)
+        res = {}
+        for name, fn in (("cubic_s1", cubic1), ("linear_s2", linear2), ("cubic_s2", cubic2)):
+            ms, clocks = _timed(fn, args.steps, args.warmup, stream, flush)
+            res[name] = {"ms": float(ms.mean())}
+        # Accuracy against the exact transform of the density at the sample
+        # positions p = R^T k (box-M units), on the first 4 poses: separable
+        # sums over x, y, z as batched complex products.
+        Q = 4
+        ky = torch.fft.fftfreq(M, 1.0 / M, device=dev, dtype=torch.float64)
+        kx = torch.arange(M // 2 + 1, device=dev, dtype=torch.float64)
+        KY, KX = torch.meshgrid(ky, kx, indexing="ij")
+        inside = (KX * KX + KY * KY <= radius * radius)
+        x = torch.arange(M, device=dev, dtype=torch.float64) - M // 2
+        d64 = dens.double().to(torch.complex128)
+        exact = torch.zeros((Q, M, M // 2 + 1), dtype=torch.complex128, device=dev)
+        R64 = rot[0, :Q].double()
+        for q in range(Q):
+            p = (R64[q, 0][:, None, None] * KX + R64[q, 1][:, None, None] * KY)   # (3, M, X)
+            pk = p.reshape(3, -1)                                                 # (3, S)
+            ex = torch.exp(-2j * np.pi * pk[0][:, None] * x[None, :] / M)        # (S, M)
+            ey = torch.exp(-2j * np.pi * pk[1][:, None] * x[None, :] / M)
+            ez = torch.exp(-2j * np.pi * pk[2][:, None] * x[None, :] / M)
+            vals = torch.empty(pk.shape[1], dtype=torch.complex128, device=dev)
+            for a in range(0, pk.shape[1], 1024):
+                sl = slice(a, a + 1024)
+                t1 = torch.einsum("zyx,sx->szy", d64, ex[sl])
+                t2 = torch.einsum("szy,sy->sz", t1, ey[sl])
+                vals[sl] = torch.einsum("sz,sz->s", t2, ez[sl])
+            exact[q] = vals.reshape(M, M // 2 + 1) * inside
+        for name, fn in (("cubic_s1", cubic1), ("linear_s2", linear2), ("cubic_s2", cubic2)):
+            fn(0)
+            torch.cuda.synchronize()
+            got = out[0, :Q].to(torch.complex128) * inside
+            res[name]["rel_l2_vs_exact"] = float(torch.linalg.vector_norm(got - exact)
+                                                 / torch.linalg.vector_norm(exact))
+        samples = P * M * (M // 2 + 1)
+        line.update(metric="box-128 forward incl. rfftn (and the 2x padding for s = 2): ms per "
+                           "4096 poses and rel. L2 error vs the exact transform",
+                    unit="ms", value=res["cubic_s1"]["ms"], higher_is_better=False,
+                    ms_per_step=res["cubic_s1"]["ms"], results=res, clocks=clocks,
+                    config={"workload": "oversampling-study-box128-4096poses",
+                            "radius": radius, "exact_subset": f"first {Q} poses, in-radius pixels",
+                            "samples_per_step": samples,
+                            "fft": "torch.fft.rfftn (cuFFT) inside the timed region"})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.ncu_summary:
@@ -543,6 +720,8 @@ def main():
         return 0
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "fwdbwd":
+        return run_workload(args)
     return run_ours(args)
 
 
