@@ -23,7 +23,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -222,11 +221,18 @@ def measured_peak_hbm():
         return 6400.0, "fallback"
 
 
+# The sources of the step's kernels (k_brick_project, k_pose_grad_saved,
+# k_brick_scatter_cubic and the binning passes): a committed ncu summary is
+# reported only while these files are unchanged.
+KERNEL_SOURCES = ("tp_brick.cu", "tp_saved.cu", "tp_device.cuh")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "backprojection_tp_project_gather_b300", "csrc", "*"))):
+    for name in KERNEL_SOURCES:
+        f = os.path.join(ROOT, "backprojection_tp_project_gather_b300", "csrc", name)
         with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
