@@ -52,7 +52,6 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kGroup = 4;        // 32-pose chunks per batch of a work unit
 constexpr int kUnitPoses = 32 * kGroup;
 constexpr int kUnitHits = 64;    // reaching poses per work unit (load-balance target)
-constexpr int kQueueStride = 21; // floats per queued scatter sample (odd: no bank conflicts)
 constexpr float kMargin = 0.01f; // enumeration margin in voxel units
 
 // Brick + halo in shared memory.  Linear: row-major with pitches 20 x 20.
@@ -821,107 +820,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // (ownership, stencil weights, conj(phase) * y), queue the owned samples in
 // shared memory and then spread them cooperatively over the taps.
 
-// Linear: a block shares one accumulator for brick + halo; the warps work on
-// different poses of the unit and add with shared-memory atomics, the 32
-// lanes taking the 8 taps of each of four samples per round.
-struct Queue {
-    float w[32][kQueueStride];   // per sample: wx*wy products (16), wz (4); odd stride
-    float4 rec[32];              // per sample: conj(phase) * y (re, im), omega, first tap
-};
-
-template <bool WEIGHTS>
-__global__ void __launch_bounds__(kThreads, 2) k_brick_scatter_linear(Params q, int nb, Scratch sc,
-                                                                     const float2 *__restrict__ img,
-                                                                     const float *__restrict__ omega,
-                                                                     float2 *__restrict__ dst,
-                                                                     float *__restrict__ wdst) {
-    using H = Halo<false>;
-    constexpr int NACC = WEIGHTS ? 3 : 2;
-    extern __shared__ float s_dyn[];
-    __shared__ UnitTable s_tab;
-    float *s_re = s_dyn, *s_im = s_dyn + H::ELEMS, *s_w = s_dyn + 2 * H::ELEMS;
-    Queue &Q = reinterpret_cast<Queue *>(s_dyn + NACC * H::ELEMS)[threadIdx.x >> 5];
-    const int lane = threadIdx.x & 31;
-    const int txy = (lane & 1) + 4 * ((lane >> 1) & 1), tz = (lane >> 2) & 1, tsub = lane >> 3;
-    const int toff = (txy & 3) + H::PX * (txy >> 2) + H::PX * H::PY * tz;
-    const int half = q.M >> 1;
-    const int v = blockIdx.z, nbr = nb * nb * nb;
-    float2 *Vd = dst + (size_t)v * q.src_stride;
-    float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
-    int4 rec;
-    while (next_unit(sc, 2, v, nbr, s_tab, rec)) {
-        const BrickBox bx = brick_box(rec.x, nb);
-        for (int e = threadIdx.x; e < NACC * H::ELEMS; e += kThreads) s_dyn[e] = 0.f;
-        __syncthreads();
-        for (int c0 = rec.y; c0 < rec.z;) {
-            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
-            for (int k; (k = next_pose(s_tab)) >= 0;) {
-                const PoseGeo &g = s_tab.pose[k];
-                const size_t ib = (size_t)g.bp * q.plane;
-                const float sx = g.sx, sy = g.sy;
-                for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                    int l[3];
-                    float w[3][4], d[3][4];
-                    const bool own = active && own_sample<false, false>(g, bx, qx, qy, l, w, d);
-                    const unsigned mask = __ballot_sync(0xffffffffu, own);
-                    if (own) {
-                        const int slot = __popc(mask & ((1u << lane) - 1u));
-                        const int iy = qy < 0 ? qy + q.N : qy;
-                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
-                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, sx, sy, q.fN, q.invN), cv);
-                        float *wq = Q.w[slot];
-#pragma unroll
-                        for (int jy = 0; jy < 2; ++jy)
-#pragma unroll
-                            for (int jx = 0; jx < 2; ++jx) wq[jx + 4 * jy] = w[0][jx] * w[1][jy];
-                        wq[16] = w[2][0];
-                        wq[17] = w[2][1];
-                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
-                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
-                                                  __int_as_float((l[2] * H::PY + l[1]) * H::PX + l[0]));
-                    }
-                    __syncwarp();
-                    const int nq = __popc(mask);
-                    for (int s0 = 0; s0 < nq; s0 += 4) {
-                        const int sq = s0 + tsub;
-                        if (sq < nq) {
-                            const float wt = Q.w[sq][txy] * Q.w[sq][16 + tz];
-                            const float4 r4 = Q.rec[sq];
-                            const int idx = __float_as_int(r4.w) + toff;
-                            atomicAdd(s_re + idx, wt * r4.x);
-                            atomicAdd(s_im + idx, wt * r4.y);
-                            if (WEIGHTS) atomicAdd(s_w + idx, wt * r4.z);
-                        }
-                    }
-                    __syncwarp();
-                });
-            }
-            __syncthreads();
-        }
-        // Fold brick + halo into the stored half-spectrum.
-        const int x0 = bx.o[0], y0 = bx.o[1], z0 = bx.o[2];
-        for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
-            const int lx = e % H::S, ly = (e / H::S) % H::S, lz = e / (H::S * H::S);
-            const int k = (lz * H::PY + ly) * H::PX + lx;
-            const float re = s_re[k], im = s_im[k];
-            const float wv = WEIGHTS ? s_w[k] : 0.f;
-            if (re == 0.f && im == 0.f && wv == 0.f) continue;
-            int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
-            const bool cj = nx < 0;
-            if (cj) {
-                nx = -nx;
-                ny = -ny;
-                nz = -nz;
-            }
-            if (!stored(nx, ny, nz, half)) continue;
-            const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
-            if (re != 0.f || im != 0.f) atomicAdd(Vd + idx, make_float2(re, cj ? -im : im));
-            if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
-        }
-        __syncthreads();
-    }
-}
-
 // Cubic: every warp owns a private accumulator for one octant (8^3) of a
 // brick plus the stencil's halo, so the spreading needs no atomics.  A warp
 // takes (work unit, octant) items from the global counter on its own, runs
@@ -1097,6 +995,154 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
     }
 }
 
+// Linear: the same warp-private octant tiles, here 8^3 plus the one-voxel
+// halo of the taps x0, x0 + 1, stored as 9 x 10 x 10 complex words (x and y
+// pitches 10: the 8 taps of one sample fall into 8 distinct bank pairs).  A
+// round spreads four queued samples at once, the lanes of group g = lane / 8
+// taking the 8 taps of sample r + R g (R = rounds of the queue).  Samples R
+// slots apart rarely share a voxel; a round in which two of them do (found by
+// a warp match on the target words) is spread one sample at a time, so the
+// plain read-add-write never races.
+constexpr int kLS = kOct + 1;               // octant + linear halo
+constexpr int kLPX = 10, kLPY = 10;         // x and y pitches of the tile
+constexpr int kLElems = kLS * kLPY * kLPX;  // complex words of the tile
+constexpr int kLQW = 7;                     // floats per queued weight row (odd)
+
+struct LinQueue {
+    float w[32][kLQW];   // per sample: wx (2), wy (2), wz (2)
+    float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
+};
+
+template <bool WEIGHTS>
+struct LinLayout {
+    static constexpr int WARPS = 4;
+    static constexpr size_t TILE = sizeof(float2) * kLElems;
+    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * kLElems : 0;
+    static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(LinQueue);
+    static_assert(TILE % 16 == 0 && WTILE % 16 == 0 && sizeof(LinQueue) % 16 == 0,
+                  "16-byte aligned sections");
+};
+
+template <bool WEIGHTS>
+__global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 6)
+    k_brick_scatter_linear(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
+                           const float *__restrict__ omega, float2 *__restrict__ dst,
+                           float *__restrict__ wdst) {
+    using LL = LinLayout<WEIGHTS>;
+    extern __shared__ float4 s_lin[];
+    const int lane = threadIdx.x & 31;
+    char *mine = reinterpret_cast<char *>(s_lin) + (threadIdx.x >> 5) * LL::WARP_BYTES;
+    float2 *acc = reinterpret_cast<float2 *>(mine);
+    float *wacc = reinterpret_cast<float *>(mine + LL::TILE);
+    LinQueue &Q = *reinterpret_cast<LinQueue *>(mine + LL::TILE + LL::WTILE);
+    const int grp = lane >> 3, jx = lane & 1, jy = (lane >> 1) & 1, jz = (lane >> 2) & 1;
+    const int toff = jx + kLPX * (jy + kLPY * jz);
+    const int half = q.M >> 1;
+    const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
+    const int items = 8 * (int)__ldg(sc.counters + 3 * nvol + v);
+    const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
+    float2 *Vd = dst + (size_t)v * q.src_stride;
+    float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
+    for (int e = lane; e < kLElems; e += 32) {
+        acc[e] = make_float2(0.f, 0.f);
+        if (WEIGHTS) wacc[e] = 0.f;
+    }
+    __syncwarp();
+    for (;;) {
+        int item = 0;
+        if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= items) break;
+        const int4 rec = __ldg(units + (item >> 3));
+        const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
+        const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
+        bool touched = false;
+        for (int c = rec.y; c < rec.z; ++c) {
+            for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
+                const PoseGeo g = load_geo(sc.geo + pose_id(q, v, c * 32 + __ffs(m) - 1));
+                if (!pose_reaches(g, ob)) continue;
+                touched = true;
+                const size_t ib = (size_t)g.bp * q.plane;
+                for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
+                    int l[3];
+                    float w[3][4], d[3][4];
+                    const bool own = active && own_sample<false, false, kOct>(g, ob, qx, qy, l, w, d);
+                    const unsigned mask = __ballot_sync(0xffffffffu, own);
+                    if (own) {
+                        const int slot = __popc(mask & ((1u << lane) - 1u));
+                        const int iy = qy < 0 ? qy + q.N : qy;
+                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
+                        float *wq = Q.w[slot];
+                        wq[0] = w[0][0];
+                        wq[1] = w[0][1];
+                        wq[2] = w[1][0];
+                        wq[3] = w[1][1];
+                        wq[4] = w[2][0];
+                        wq[5] = w[2][1];
+                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
+                                                  __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
+                    }
+                    __syncwarp();
+                    const int nq = __popc(mask);
+                    const int R = (nq + 3) >> 2;
+                    for (int r = 0; r < R; ++r) {
+                        const int sq = r + R * grp;
+                        const bool act = sq < nq;
+                        float wt = 0.f;
+                        float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
+                        int idx = -1 - lane;   // unique for idle lanes
+                        if (act) {
+                            wt = Q.w[sq][jx] * Q.w[sq][2 + jy] * Q.w[sq][4 + jz];
+                            cur = Q.rec[sq];
+                            idx = __float_as_int(cur.w) + toff;
+                        }
+                        const unsigned same = __match_any_sync(0xffffffffu, idx);
+                        const bool clash = __any_sync(0xffffffffu, __popc(same) > 1);
+                        for (int k = 0; k < 4; ++k) {
+                            if (act && (!clash || grp == k)) {
+                                float2 a = acc[idx];
+                                a.x = fmaf(wt, cur.x, a.x);
+                                a.y = fmaf(wt, cur.y, a.y);
+                                acc[idx] = a;
+                                if (WEIGHTS) wacc[idx] = fmaf(wt, cur.z, wacc[idx]);
+                            }
+                            __syncwarp();
+                            if (!clash) break;
+                        }
+                    }
+                    __syncwarp();
+                });
+            }
+        }
+        if (!touched) continue;
+        // Fold the tile into the stored half-spectrum and clear it.
+        const int x0 = ob.o[0], y0 = ob.o[1], z0 = ob.o[2];
+        for (int e = lane; e < kLS * kLS * kLS; e += 32) {
+            const int lx = e % kLS, ly = (e / kLS) % kLS, lz = e / (kLS * kLS);
+            const int k = (lz * kLPY + ly) * kLPX + lx;
+            const float2 cv = acc[k];
+            const float wv = WEIGHTS ? wacc[k] : 0.f;
+            if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
+            acc[k] = make_float2(0.f, 0.f);
+            if (WEIGHTS) wacc[k] = 0.f;
+            int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
+            const bool cj = nx < 0;
+            if (cj) {
+                nx = -nx;
+                ny = -ny;
+                nz = -nz;
+            }
+            if (!stored(nx, ny, nz, half)) continue;
+            const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
+            if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, cj ? -cv.y : cv.y));
+            if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
+        }
+        __syncwarp();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Launch geometry and scratch layout.
 int bricks_per_axis(int M, bool cubic) {
@@ -1200,6 +1246,19 @@ dim3 main_grid(const Params &q, const void *kern, size_t smem) {
     return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
 }
 
+// Blocks of a kernel whose warps take work items on their own (the octant
+// scatters): every resident block, shared out over the volumes.
+dim3 warp_grid(const Params &q, const void *kern, int threads, size_t smem) {
+    int dev = 0, sms = 148, per_sm = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const long long per = ((long long)sms * per_sm + q.Bsrc - 1) / q.Bsrc;
+    return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
+}
+
 template <bool CUBIC, bool SAVE>
 cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, BinMode mode,
                       cudaStream_t st) {
@@ -1232,15 +1291,17 @@ cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gs
 template <bool WEIGHTS>
 cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
                              float *wdst, void *ws, BinMode mode, cudaStream_t st) {
+    using LL = LinLayout<WEIGHTS>;
     const Layout L = layout(q, false);
     const Scratch sc = scratch_in(ws, L);
-    const size_t smem = sizeof(float) * Halo<false>::ELEMS * (WEIGHTS ? 3 : 2) + sizeof(Queue) * kWarps;
+    const int threads = 32 * LL::WARPS;
+    const size_t smem = LL::WARP_BYTES * LL::WARPS;
     auto kern = k_brick_scatter_linear<WEIGHTS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
-    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, img, omega,
-                                                                       dst, wdst);
+    kern<<<warp_grid(q, (const void *)kern, threads, smem), threads, smem, st>>>(q, L.nb, sc, img,
+                                                                               omega, dst, wdst);
     return cudaGetLastError();
 }
 
@@ -1256,15 +1317,8 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
-    int dev = 0, sms = 148, per_sm = 1;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    const long long per = ((long long)sms * per_sm + q.Bsrc - 1) / q.Bsrc;
-    kern<<<dim3((unsigned)per, 1, (unsigned)q.Bsrc), threads, smem, st>>>(q, L.nb, sc, img, omega,
-                                                                        dst, wdst);
+    kern<<<warp_grid(q, (const void *)kern, threads, smem), threads, smem, st>>>(q, L.nb, sc, img,
+                                                                               omega, dst, wdst);
     return cudaGetLastError();
 }
 
