@@ -835,10 +835,15 @@ constexpr int kOct = kBS / 2;              // octant edge
 constexpr int kOS = kOct + 3;              // octant + cubic halo (taps x0 - 1 .. x0 + 2)
 constexpr int kOPX = 12;                   // x pitch of the tile (complex words)
 constexpr int kOElems = kOS * kOS * kOPX;  // complex words of the tile
-constexpr int kOQW = 13;                   // floats per queued weight row (odd: no bank conflicts)
+// The real weight tile is addressed with 32-bit words by the whole warp at
+// once: with pitches 12 x 12 the second half-warp's taps (jz + 1, 144 words
+// on, 16 banks away) land in the 16 banks the first half-warp leaves free.
+constexpr int kOWPY = 12;                    // y pitch of the weight tile
+constexpr int kOWElems = kOS * kOWPY * kOPX; // words of the weight tile
+constexpr int kOQW = 13;                     // floats per queued weight row (odd: no bank conflicts)
 
 struct OctQueue {
-    float w[32][kOQW];   // per sample: wx (4), wy (4), wz (4)
+    float w[32][kOQW];   // per sample: wx (4), wy (4), wz (4), first weight-tile tap
     float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
 };
 
@@ -846,7 +851,7 @@ template <bool WEIGHTS>
 struct OctLayout {
     static constexpr int WARPS = WEIGHTS ? 2 : 4;   // warps per block (blocks only share an SM)
     static constexpr size_t TILE = sizeof(float2) * kOElems;
-    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * kOElems : 0;
+    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * kOWElems : 0;
     static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(OctQueue);
     static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned queue");
 };
@@ -877,17 +882,18 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
     OctQueue &Q = *reinterpret_cast<OctQueue *>(mine + OL::TILE + OL::WTILE);
     const int jx = lane & 3, jy = (lane >> 2) & 3, tz = lane >> 4;
     const int toff = jx + kOPX * (jy + kOS * tz);
-    constexpr int ZSTEP = 2 * kOPX * kOS;   // tile offset of taps jz + 2
+    const int toff_w = jx + kOPX * (jy + kOWPY * tz);
+    constexpr int ZSTEP = 2 * kOPX * kOS;      // tile offset of taps jz + 2
+    constexpr int ZSTEP_W = 2 * kOPX * kOWPY;  // the same in the weight tile
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
     const int items = 8 * (int)__ldg(sc.counters + 3 * nvol + v);
     const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
-    for (int e = lane; e < kOElems; e += 32) {
-        acc[e] = make_float2(0.f, 0.f);
-        if (WEIGHTS) wacc[e] = 0.f;
-    }
+    for (int e = lane; e < kOElems; e += 32) acc[e] = make_float2(0.f, 0.f);
+    if (WEIGHTS)
+        for (int e = lane; e < kOWElems; e += 32) wacc[e] = 0.f;
     __syncwarp();
     for (;;) {
         int item = 0;
@@ -921,6 +927,7 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                             wq[4 + j] = w[1][j];
                             wq[8 + j] = w[2][j];
                         }
+                        if (WEIGHTS) wq[12] = __int_as_float((l[2] * kOWPY + l[1]) * kOPX + l[0]);
                         const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * kOS + l[1]) * kOPX + l[0]));
@@ -930,23 +937,27 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                     // The next sample's queue entries are read before this
                     // sample's tile words, hiding their latency.
                     float wx = 0.f, wy = 0.f, wz0 = 0.f, wz1 = 0.f;
+                    int wb = 0;
                     float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (nq > 0) {
                         wx = Q.w[0][jx];
                         wy = Q.w[0][4 + jy];
                         wz0 = Q.w[0][8 + tz];
                         wz1 = Q.w[0][10 + tz];
+                        if (WEIGHTS) wb = __float_as_int(Q.w[0][12]);
                         r4 = Q.rec[0];
                     }
                     for (int sq = 0; sq < nq; ++sq) {
                         const float wxy = wx * wy;
                         const float wt0 = wxy * wz0, wt1 = wxy * wz1;
                         const float4 cur = r4;
+                        const int widx = wb + toff_w;
                         if (sq + 1 < nq) {
                             wx = Q.w[sq + 1][jx];
                             wy = Q.w[sq + 1][4 + jy];
                             wz0 = Q.w[sq + 1][8 + tz];
                             wz1 = Q.w[sq + 1][10 + tz];
+                            if (WEIGHTS) wb = __float_as_int(Q.w[sq + 1][12]);
                             r4 = Q.rec[sq + 1];
                         }
                         const int idx = __float_as_int(cur.w) + toff;
@@ -958,8 +969,8 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                         acc[idx] = a0;
                         acc[idx + ZSTEP] = a1;
                         if (WEIGHTS) {
-                            wacc[idx] = fmaf(wt0, cur.z, wacc[idx]);
-                            wacc[idx + ZSTEP] = fmaf(wt1, cur.z, wacc[idx + ZSTEP]);
+                            wacc[widx] = fmaf(wt0, cur.z, wacc[widx]);
+                            wacc[widx + ZSTEP_W] = fmaf(wt1, cur.z, wacc[widx + ZSTEP_W]);
                         }
                         // The lanes' words of a sample are distinct, but the
                         // next sample's taps may reuse another lane's words.
@@ -974,11 +985,12 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
         for (int e = lane; e < kOS * kOS * kOS; e += 32) {
             const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
             const int k = (lz * kOS + ly) * kOPX + lx;
+            const int kw = (lz * kOWPY + ly) * kOPX + lx;
             const float2 cv = acc[k];
-            const float wv = WEIGHTS ? wacc[k] : 0.f;
+            const float wv = WEIGHTS ? wacc[kw] : 0.f;
             if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
             acc[k] = make_float2(0.f, 0.f);
-            if (WEIGHTS) wacc[k] = 0.f;
+            if (WEIGHTS) wacc[kw] = 0.f;
             int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
             const bool cj = nx < 0;
             if (cj) {
