@@ -46,20 +46,33 @@ __global__ void __launch_bounds__(kSavedThreads) k_pose_grad_saved(Params q,
         if (rr < 0) continue;
         const int xcut = min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
-        for (int kx = lane; kx <= xcut; kx += 32) {
-            const size_t e = r0 + kx;
-            const float2 gv = __ldg(g + e), yv = __ldg(y + e);
-            const float skx = q.s * (float)kx, sky = q.s * (float)ky;
+        // Four pixels per lane per pass: all their loads are issued before
+        // any of them is used, to keep enough bytes in flight.
+        for (int x0 = 0; x0 <= xcut; x0 += 4 * 32) {
+            float2 gv[4], yv[4], dv[4][3];
 #pragma unroll
-            for (int a = 0; a < 3; ++a) {
-                const float2 da = __ldg(D + 3 * e + a);
-                const float dl = gv.x * da.x + gv.y * da.y;   // Re(conj(g) D_a)
-                acc[a] = fmaf(skx, dl, acc[a]);
-                acc[3 + a] = fmaf(sky, dl, acc[3 + a]);
+            for (int u = 0; u < 4; ++u) {
+                const int kx = x0 + u * 32 + lane;
+                const size_t e = r0 + min(kx, xcut);
+                gv[u] = kx <= xcut ? __ldg(g + e) : make_float2(0.f, 0.f);
+                yv[u] = __ldg(y + e);
+#pragma unroll
+                for (int a = 0; a < 3; ++a) dv[u][a] = __ldg(D + 3 * e + a);
             }
-            const float qv = tau * (gv.x * yv.y - gv.y * yv.x);   // (2 pi / N) Im(conj(g) y)
-            acc[6] = fmaf((float)kx, qv, acc[6]);
-            acc[7] = fmaf((float)ky, qv, acc[7]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int kx = x0 + u * 32 + lane;   // gv is 0 beyond xcut
+                const float skx = q.s * (float)kx, sky = q.s * (float)ky;
+#pragma unroll
+                for (int a = 0; a < 3; ++a) {
+                    const float dl = gv[u].x * dv[u][a].x + gv[u].y * dv[u][a].y;   // Re(conj(g) D_a)
+                    acc[a] = fmaf(skx, dl, acc[a]);
+                    acc[3 + a] = fmaf(sky, dl, acc[3 + a]);
+                }
+                const float qv = tau * (gv[u].x * yv[u].y - gv[u].y * yv[u].x);   // (2 pi / N) Im(conj(g) y)
+                acc[6] = fmaf((float)kx, qv, acc[6]);
+                acc[7] = fmaf((float)ky, qv, acc[7]);
+            }
         }
     }
 #pragma unroll
