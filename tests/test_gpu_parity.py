@@ -271,3 +271,52 @@ def test_cfg5_box256_full_step_sampled(tp):
     rv12, _, _ = oracle.project_backward(3, g[:, sub], vol, R[:, sub], shift=t[:, sub],
                                          need_rot=False, need_shift=False, **kw)
     assert rel(host(gv12), rv12) <= ATOMIC_TOL
+
+
+# ---------------------------------------------------------------------------
+# Large sizes: a box-512 spectrum (67 M complex words) and a 100,000-pose list
+# exercise the 64-bit offsets and the chunk / mask / work-unit indexing at
+# sizes far beyond the configs; both are compared on samples.
+def test_box512_forward_and_backward_sampled(tp):
+    rng = np.random.default_rng(512)
+    M = N = 512
+    vol = crandn(rng, (1, M, M, M // 2 + 1))
+    R = synth.random_rotations(3, rng).reshape(1, 3, 3, 3)
+    t = rng.uniform(-20, 20, (1, 3, 2)).astype(np.float32)
+    g = crandn(rng, (1, 3, N, N // 2 + 1))
+    kw = dict(interp="cubic", oversampling=1.0, radius=-1.0)
+    dv = dev(vol)
+    out = host(tp.tp_project_3d_2d(dv, dev(R), dev(t), **kw))
+    assert rel(out, oracle.project(3, vol, R, shift=t, **kw)) <= FWD_TOL
+    gv, gr, gt = tp.tp_project_3d_2d_backward(dev(g), dv, dev(R), dev(t), **kw)
+    rv, rr, rt = oracle.project_backward(3, g, vol, R, shift=t, **kw)
+    assert rel(host(gr), rr) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+    # the volume gradient on a sample of voxels across the whole spectrum
+    gvh = host(gv)
+    idx = tuple(rng.integers(0, n, 20000) for n in vol.shape)
+    assert rel(gvh[idx], rv[idx]) <= ATOMIC_TOL
+    assert rel(gvh, rv) <= ATOMIC_TOL
+
+
+def test_hundred_thousand_poses_sampled(tp):
+    rng = np.random.default_rng(100000)
+    M = N = 16
+    P = 100_000
+    vol = crandn(rng, (1, M, M, M // 2 + 1))
+    R = synth.random_rotations(P, rng).reshape(1, P, 3, 3)
+    g = crandn(rng, (1, P, N, N // 2 + 1))
+    kw = dict(interp="linear", oversampling=1.0, radius=-1.0)
+    dv, dR = dev(vol), dev(R)
+    out, dout = tp.tp_project_3d_2d_save(dv, dR, None, **kw)
+    pick = np.concatenate([np.arange(0, P, 9973), [P - 1]])
+    ref = oracle.project(3, vol, R[:, pick], **kw)
+    assert rel(host(out)[:, pick], ref) <= FWD_TOL
+    gr, _ = tp.tp_project_3d_2d_backward_saved(dev(g), out, dout, dR, None, **kw)
+    _, rr, _ = oracle.project_backward(3, g[:, pick], vol, R[:, pick], need_src=False, **kw)
+    assert rel(host(gr)[:, pick], rr) <= ATOMIC_TOL
+    # all 100,000 images scattered into one spectrum: the adjoint identity
+    gv, _, _ = tp.tp_project_3d_2d_backward(dev(g), dv, dR, want_rot=False, want_shift=False, **kw)
+    lhs = np.vdot(g.astype(np.complex128), host(out).astype(np.complex128)).real
+    rhs = np.vdot(host(gv).astype(np.complex128), vol.astype(np.complex128)).real
+    assert abs(lhs - rhs) <= 1e-4 * abs(lhs)
