@@ -161,6 +161,32 @@ def test_non_orthogonal_matrix_and_large_shift(tp):
         assert rel(out, oracle.project(3, V, R, shift=t, interp=interp)) <= FWD_TOL
 
 
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_degenerate_poses(tp, interp):
+    """Matrices whose sample set collapses or leaves the volume: the zero
+    matrix (every pixel reads the DC voxel), parallel rows (a line), a zero
+    second row, and a rotation scaled by 3 (most samples beyond the stored
+    range, which reads zero)."""
+    rng = np.random.default_rng(26)
+    M = N = 20
+    V = crandn(rng, (1, M, M, M // 2 + 1))
+    a = synth.random_rotations(1, rng)[0]
+    R = np.stack([np.zeros((3, 3), np.float32),
+                  np.stack([a[0], 0.7 * a[0], a[2]]),
+                  np.stack([a[0], np.zeros(3, np.float32), a[2]]),
+                  3.0 * synth.random_rotations(1, rng)[0]]).astype(np.float32)[None]
+    t = rng.uniform(-4, 4, (1, 4, 2)).astype(np.float32)
+    g = crandn(rng, (1, 4, N, N // 2 + 1))
+    kw = dict(interp=interp)
+    out = host(tp.tp_project_3d_2d(dev(V), dev(R), dev(t), **kw))
+    assert rel(out, oracle.project(3, V, R, shift=t, **kw)) <= FWD_TOL
+    gv, gr, gt = tp.tp_project_3d_2d_backward(dev(g), dev(V), dev(R), dev(t), **kw)
+    rv, rr, rt = oracle.project_backward(3, g, V, R, shift=t, **kw)
+    assert rel(host(gv), rv) <= ATOMIC_TOL
+    assert rel(host(gr), rr) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+
+
 def test_minimum_box(tp):
     rng = np.random.default_rng(25)
     V = crandn(rng, (1, 2, 2, 2))
