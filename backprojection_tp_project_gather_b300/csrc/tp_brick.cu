@@ -51,7 +51,7 @@ constexpr int kWarps = 8;        // warps per block
 constexpr int kThreads = 32 * kWarps;
 constexpr int kGroup = 4;        // 32-pose chunks per batch of a work unit
 constexpr int kUnitPoses = 32 * kGroup;
-constexpr int kUnitHits = 64;    // reaching poses per work unit (load-balance target)
+constexpr int kUnitHits = 128;   // reaching poses per work unit (load-balance target)
 constexpr float kMargin = 0.01f; // enumeration margin in voxel units
 
 // Brick + halo in shared memory.  Linear: row-major with pitches 20 x 20.
