@@ -52,8 +52,9 @@ def parse_args():
                     help="poses of the workload one CPU-baseline oracle step processes")
     ap.add_argument("--cpu-min-seconds", type=float, default=10.0,
                     help="the CPU-baseline leg repeats oracle steps until this much time has passed")
-    ap.add_argument("--ref-poses", type=int, default=1,
-                    help="poses per step of the reference (oracle) arm")
+    ap.add_argument("--ref-poses", type=int, default=8,
+                    help="poses per step of the reference (oracle) arm (each step also pays for "
+                         "the float64 volume gradient of the whole 256^3 spectrum)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--poses", type=int, default=None,
