@@ -579,10 +579,11 @@ def run_ours(args):
                     "copies": "every step: volume, targets, poses up; volume, rotation and shift "
                               "gradients down; pipelined with the neighbouring steps' compute "
                               "on two copy streams"},
-            # per step: forward (pose geometry, brick masks, unit plan, zero fill, gather
-            # with saved derivatives), the saved-path pose gradient (one streaming
-            # kernel) and the volume-gradient call (geometry, masks, plan, scatter)
-            "gpu_launches": 10 * args.steps,
+            # per step: forward (pose geometry, brick masks, unit plan, gather with
+            # saved derivatives and the zero fill as its prologue), the saved-path
+            # pose gradient (one streaming kernel) and the volume-gradient call
+            # (geometry, masks, plan, scatter); plus two 4-byte memsets
+            "gpu_launches": 9 * args.steps,
             "clocks": clocks.record(),
             "cpu_baseline": cpu_line,
         }
