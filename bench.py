@@ -60,13 +60,18 @@ def parse_args():
     ap.add_argument("--poses", type=int, default=None,
                     help="pose count (default: the workload's 512); smaller runs are for profiling")
     ap.add_argument("--workload", default="fwdbwd",
-                    choices=["fwdbwd", "backproject", "backproject-backward", "oversampling"],
-                    help="fwdbwd: the differentiable step (the headline, default); backproject: "
+                    choices=["fwdbwd", "project", "rot2d", "backproject", "backproject-backward",
+                             "oversampling"],
+                    help="fwdbwd: the differentiable step (the headline, default); project: box-128 "
+                         "cubic forward of 4096 poses (--oversampling 1 or 2); rot2d: 2D rotate + "
+                         "shift of 1024 images at 128, forward and backward; backproject: "
                          "2048 images into a 256^3 data + weight spectrum; backproject-backward: "
                          "the gradients of that backprojection; oversampling: cubic at s = 1 "
                          "against linear at s = 2 with the padding FFT, box 128, 4096 poses")
     ap.add_argument("--interp", default="cubic", choices=["linear", "cubic"],
-                    help="interpolation of the backproject workloads")
+                    help="interpolation of the project and backproject workloads")
+    ap.add_argument("--oversampling", type=int, default=1, choices=[1, 2],
+                    help="oversampling of the project workload (2: the 256^3 padded spectrum)")
     ap.add_argument("--ncu-summary", metavar="RAW_CSV", default=None,
                     help="write profiles/ncu_traffic.json from `ncu -i REP --page raw --csv` output")
     return ap.parse_args()
@@ -628,7 +633,79 @@ def run_workload(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "impl": "ours", "workload": args.workload}
 
-    if args.workload in ("backproject", "backproject-backward"):
+    if args.workload == "project":
+        s = args.oversampling
+        w = synth.workload(3, oversampling=s)
+        N, P = w["box"], w["P"]
+        samples = P * N * (N // 2 + 1)
+        vol = torch.from_numpy(w["vol"]).to(dev)
+        rot = torch.from_numpy(w["rot"]).to(dev)
+        out = torch.empty((1, P, N, N // 2 + 1), dtype=torch.complex64, device=dev)
+        kw = dict(N=N, interp=args.interp, oversampling=float(s), radius=w["radius"])
+        ws = torch.empty(tp.tp_workspace_bytes(1, 1, P, vol.shape[1], args.interp),
+                         dtype=torch.uint8, device=dev)
+        rots = [rot, rot + 1e-4]          # new poses every step: the binning re-runs
+
+        def step(i):
+            tp.tp_project_3d_2d(vol, rots[i & 1], out=out, workspace=ws, **kw)
+        ms, clocks = _timed(step, args.steps, args.warmup, stream, flush)
+        t = float(ms.mean())
+        nbytes = samples * 8 + vol.numel() * 8
+        line.update(metric="projected Fourier samples/sec (Gsamples/s)", unit="Gsamples/s",
+                    value=samples / (t * 1e-3) / 1e9, ms_per_step=t, clocks=clocks,
+                    config={"workload": f"project-box{N}-{P}poses-{args.interp}-s{s}", "box": N,
+                            "volume_box": int(vol.shape[1]), "poses": P, "interp": args.interp,
+                            "oversampling": s, "radius": w["radius"],
+                            "l2_cache": "flushed between steps (256 MB write)"},
+                    roofline={"bound": "hbm", "achieved": nbytes / (t * 1e-3) / 1e9, "peak": peak,
+                              "peak_source": peak_src, "unit": "GB/s",
+                              "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
+                              "algorithmic_bytes_per_step": nbytes,
+                              "timed": "whole call (binning + kernels)"})
+    elif args.workload == "rot2d":
+        w = synth.workload(2)
+        N, n = w["box"], w["img"].shape[0]
+        samples = n * N * (N // 2 + 1)
+        img = torch.from_numpy(w["img"]).to(dev)
+        rot = torch.from_numpy(w["rot"]).to(dev)
+        shift = torch.from_numpy(w["shift"]).to(dev)
+        g = torch.from_numpy(w["grad"]).to(dev)
+        out = torch.empty((n, 1, N, N // 2 + 1), dtype=torch.complex64, device=dev)
+        gi, gr, gs = torch.zeros_like(img), torch.zeros_like(rot), torch.zeros_like(shift)
+        kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        seg = []
+
+        def step(i):
+            k = i - args.warmup
+            if k >= 0:
+                ev[k][0].record(stream)
+            tp.tp_project_2d_2d(img, rot, shift, out=out, **kw)
+            if k >= 0:
+                ev[k][1].record(stream)
+            gi.zero_()
+            gr.zero_()
+            gs.zero_()
+            tp.tp_project_2d_2d_backward(g, img, rot, shift, grad_img=gi, grad_rot=gr,
+                                         grad_shift=gs, **kw)
+        ms, clocks = _timed(step, args.steps, args.warmup, stream, flush)
+        fwd = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        t = float(ms.mean())
+        img_bytes = samples * 8
+        nbytes = 2 * img_bytes + 2 * img_bytes + 2 * img_bytes   # fwd; bwd: g + image, grad RMW
+        line.update(metric="Fourier samples/sec (Gsamples/s) of the 2D rotate + shift, fwd + bwd",
+                    unit="Gsamples/s", value=samples / (t * 1e-3) / 1e9, ms_per_step=t,
+                    clocks=clocks, breakdown_ms={"forward": fwd, "backward": t - fwd},
+                    config={"workload": f"rot2d-{n}img-box{N}-{w['interp']}", "images": n,
+                            "box": N, "interp": w["interp"], "radius": w["radius"],
+                            "shift_px": 5.0, "l2_cache": "flushed between steps (256 MB write)"},
+                    roofline={"bound": "hbm", "achieved": nbytes / (t * 1e-3) / 1e9, "peak": peak,
+                              "peak_source": peak_src, "unit": "GB/s",
+                              "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
+                              "algorithmic_bytes_per_step": nbytes,
+                              "timed": "forward + backward calls"})
+    elif args.workload in ("backproject", "backproject-backward"):
         w = synth.workload(4)
         n, N = w["P"], w["box"]
         samples = n * N * (N // 2 + 1)
