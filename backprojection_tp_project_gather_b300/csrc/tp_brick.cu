@@ -86,6 +86,15 @@ struct PoseGeo {
 };
 constexpr int kGeoWords = sizeof(PoseGeo) / 4;
 
+// What the brick-mask pass needs of a pose, with the plane's extents over a
+// brick precomputed: the brick half-size is kBS/2 plus the margin on every
+// axis, so |n|.h and |v|.h are per-pose constants.
+struct ReachGeo {
+    float4 n;   // plane normal, then |n| . h
+    float4 v;   // qx-direction v, then |v| . h
+    float4 r;   // reach^2, degenerate (1 / 0), unused, unused
+};
+
 // Scratch layout inside the caller's workspace.
 // Identity of a binning: the sizes it was computed for.  Together with the
 // pose geometry it determines the masks and work units completely.
@@ -99,6 +108,7 @@ struct Scratch {
     unsigned *changed;    // set by k_pose_geometry when key or geometry differ
     unsigned *counters;   // [4][Bsrc]: work counters of the three main kernels, unit counts
     PoseGeo *geo;         // B*P poses
+    ReachGeo *reach;      // B*P poses, for the brick-mask pass
     unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
     int *hits;            // [Bsrc][bricks] reaching poses per brick
     int4 *units;          // [Bsrc][bricks * chunks] work units (brick, first chunk, end chunk)
@@ -299,6 +309,16 @@ __global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratc
     const int b = id / q.P, pi = id - b * q.P;
     PoseGeo g;
     pose_geo(q, b, pi, g);
+    {
+        const float h = 0.5f * (float)kBS + kMargin;
+        ReachGeo rg;
+        rg.n = make_float4(g.n[0], g.n[1], g.n[2],
+                           h * (fabsf(g.n[0]) + fabsf(g.n[1]) + fabsf(g.n[2])));
+        rg.v = make_float4(g.v[0], g.v[1], g.v[2],
+                           h * (fabsf(g.v[0]) + fabsf(g.v[1]) + fabsf(g.v[2])));
+        rg.r = make_float4(g.reach * g.reach, g.degenerate ? 1.f : 0.f, 0.f, 0.f);
+        sc.reach[id] = rg;
+    }
     const int *now = reinterpret_cast<const int *>(&g);
     int *held = reinterpret_cast<int *>(sc.geo + id);
     bool same = true;
@@ -320,37 +340,52 @@ __device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
 }
 
 // Bit l of mask (volume, brick, chunk) = pose 32*chunk + l of the volume's
-// list can reach the brick; the brick's count grows by the number of set
-// bits.  A warp keeps one chunk's 32 poses in registers and sweeps a range
-// of kMaskBricks bricks.
-constexpr int kMaskBricks = 8;
-
+// list can reach the brick (the test of pose_reaches, with the per-pose
+// constants of ReachGeo); the brick's count grows by the number of set bits.
+// A lane owns one brick and runs through the chunk's 32 poses, whose
+// records every lane of the warp reads at once.
 __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
     if (*sc.changed == 0u) return;
     const int nbr = nb * nb * nb;
     const int nchunks = sc.nchunks;
-    const int ranges = (nbr + kMaskBricks - 1) / kMaskBricks;
-    const long long total = (long long)q.Bsrc * nchunks * ranges;
+    const int groups = (nbr + 31) / 32;
+    const long long total = (long long)q.Bsrc * nchunks * groups;
     const int Pv = poses_of_volume(q);
     const int lane = threadIdx.x & 31;
+    const float h = 0.5f * (float)kBS + kMargin;
     for (long long w = ((long long)blockIdx.x * 256 + threadIdx.x) >> 5; w < total;
          w += ((long long)gridDim.x * 256) >> 5) {
-        const int rg = (int)(w % ranges);
-        const long long r = w / ranges;
+        const int grp = (int)(w % groups);
+        const long long r = w / groups;
         const int c = (int)(r % nchunks), v = (int)(r / nchunks);
-        const int i = c * 32 + lane;
-        const bool valid = i < Pv;
-        PoseGeo g;
-        if (valid) g = load_geo(sc.geo + pose_id(q, v, i));
-        const int j1 = min(nbr, (rg + 1) * kMaskBricks);
-        for (int j = rg * kMaskBricks; j < j1; ++j) {
-            const bool hit = valid && pose_reaches(g, brick_box(j, nb));
-            const unsigned m = __ballot_sync(0xffffffffu, hit);
-            if (lane == 0) {
-                const size_t vj = (size_t)v * nbr + j;
-                sc.masks[vj * nchunks + c] = m;
-                if (m) atomicAdd(sc.hits + vj, __popc(m));
+        const int j = grp * 32 + lane;
+        const BrickBox bx = brick_box(min(j, nbr - 1), nb);
+        float cen[3], e2 = 0.f;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            cen[d] = 0.5f * (bx.lo[d] + bx.hi[d]);
+            const float e = fmaxf(fabsf(cen[d]) - h, 0.f);
+            e2 += e * e;
+        }
+        const int np = min(32, Pv - c * 32);
+        unsigned m = 0u;
+        for (int k = 0; k < np; ++k) {
+            const ReachGeo *rg = sc.reach + pose_id(q, v, c * 32 + k);
+            const float4 rr = __ldg(&rg->r);
+            if (e2 > rr.x) continue;
+            bool hit = rr.y != 0.f;   // degenerate poses reach every brick within reach
+            if (!hit) {
+                const float4 nn = __ldg(&rg->n), vv = __ldg(&rg->v);
+                const float cn = nn.x * cen[0] + nn.y * cen[1] + nn.z * cen[2];
+                const float cv = vv.x * cen[0] + vv.y * cen[1] + vv.z * cen[2];
+                hit = fabsf(cn) <= nn.w * 1.0001f + 1e-6f && cv + vv.w >= -0.01f;
             }
+            m |= (hit ? 1u : 0u) << k;
+        }
+        if (j < nbr) {
+            const size_t vj = (size_t)v * nbr + j;
+            sc.masks[vj * nchunks + c] = m;
+            if (m) atomicAdd(sc.hits + vj, __popc(m));
         }
     }
 }
@@ -1165,7 +1200,7 @@ int bricks_per_axis(int M, bool cubic) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t counters, geo, masks, hits, units, total;
+    size_t counters, geo, reach, masks, hits, units, total;
     int nb, nchunks;
 };
 
@@ -1177,7 +1212,8 @@ Layout layout(const Params &q, bool cubic) {
     L.nchunks = (int)((Pv + 31) / 32);
     L.counters = 256;                                         // key and flag first
     L.geo = L.counters + align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);
-    L.masks = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
+    L.reach = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
+    L.masks = L.reach + align256(sizeof(ReachGeo) * (size_t)q.B * q.P);
     L.hits = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.units = L.hits + align256(sizeof(int) * (size_t)q.Bsrc * nbr);
     L.total = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
@@ -1191,6 +1227,7 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.changed = sc.key + kKeyWords;
     sc.counters = reinterpret_cast<unsigned *>(base + L.counters);
     sc.geo = reinterpret_cast<PoseGeo *>(base + L.geo);
+    sc.reach = reinterpret_cast<ReachGeo *>(base + L.reach);
     sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
     sc.hits = reinterpret_cast<int *>(base + L.hits);
     sc.units = reinterpret_cast<int4 *>(base + L.units);
@@ -1233,7 +1270,7 @@ cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_
     cudaError_t e = cudaMemsetAsync(sc.changed, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
     k_pose_geometry<<<pb, 256, 0, st>>>(q, nbr, sc, bin_key(q, L));
-    const long long warps = (long long)q.Bsrc * L.nchunks * ((nbr + kMaskBricks - 1) / kMaskBricks);
+    const long long warps = (long long)q.Bsrc * L.nchunks * ((nbr + 31) / 32);
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 32) blocks = 65535LL * 32;
     k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, sc);
