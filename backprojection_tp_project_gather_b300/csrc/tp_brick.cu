@@ -12,24 +12,26 @@
 //
 //  - gather (forward, pose gradients): a block stages brick+halo of F in
 //    shared memory, then every owned sample reads its 8 or 64 taps from
-//    shared memory with one branch-free code path;
-//  - scatter (backprojection, spectrum gradient): a block accumulates its
-//    samples' contributions into brick+halo accumulators in shared memory
-//    and adds them to the stored half-spectrum once per work unit (Friedel
-//    positions conjugated at -n), with vector atomics because halos of
-//    neighbouring bricks and other work units overlap.
+//    shared memory with one branch-free code path (for cubic in a tiled
+//    layout and a per-lane tap order free of bank conflicts);
+//  - scatter (backprojection, spectrum gradient): every warp owns a private
+//    tile for one octant of a brick plus the stencil halo, spreads its
+//    samples into it with plain read-add-write, and adds the tile to the
+//    stored half-spectrum once per work item (Friedel positions conjugated
+//    at -n), with vector atomics because halos of neighbouring octants and
+//    other work items overlap.
 //
 // Binning.  Three small passes precede every operator: one thread per pose
-// computes the pose's geometry once (into the caller's workspace); one warp
-// per (brick, 32-pose chunk) marks with a ballot which poses can reach the
-// brick (the plane spanned by a = s R[0], b = s R[1] must meet it, the
-// half-plane qx >= 0 must touch it and it must lie within the pose's reach)
-// and counts them per brick; one block per volume then turns the counts
-// into a compact list of work units -- a brick and a range of chunks holding
-// about kUnitHits reaching poses, so busy bricks near the origin are split
-// and empty bricks vanish.  Persistent blocks take units from a global
-// counter in brick order (busiest first), stage the brick once per unit and
-// walk its poses in batches of up to 128.  For one (pose, brick) pair the
+// computes the pose's geometry (into the caller's workspace, where a later
+// call on the same poses finds and keeps it); a lane per brick marks which
+// of a 32-pose chunk's poses can reach the brick (the plane spanned by
+// a = s R[0], b = s R[1] must meet it, the half-plane qx >= 0 must touch it
+// and it must lie within the pose's reach) and counts them per brick; one
+// block per volume then turns the counts into a compact list of work units
+// -- a brick and a range of chunks holding about kUnitHits reaching poses,
+// so busy bricks near the origin are split and empty bricks vanish.  The
+// main kernels take units (or, in the scatters, unit octants) from a global
+// counter in brick order, busiest first.  For one (pose, box) pair the
 // owned pixels form a convex polygon in k-space: its rows come from the
 // pseudo-inverse of [a b] and each row's qx interval from the three slab
 // constraints; the enumeration is a small superset and the exact floor(p)
