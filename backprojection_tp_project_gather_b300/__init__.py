@@ -20,12 +20,16 @@ import torch
 
 __all__ = [
     "TPError", "lib", "tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
-    "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_last_error", "tp_version",
-    "tp_workspace_bytes", "tp_project_3d_2d_noalloc", "LINEAR", "CUBIC",
+    "tp_project_3d_2d_save", "tp_project_3d_2d_backward_saved", "tp_backproject_2d_3d_backward",
+    "tp_backproject_backward_scratch_bytes", "tp_project_2d_2d", "tp_project_2d_2d_backward",
+    "tp_last_error", "tp_version", "tp_workspace_bytes", "tp_project_3d_2d_noalloc",
+    "tp_debug_bounds_word", "tp_debug_bounds_selftest", "LINEAR", "CUBIC",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtp_b300.so")
+# TP_B300_LIB=debug selects the bounds-checking build (libtp_b300_debug.so).
+LIB_PATH = os.path.join(_HERE, "libtp_b300_debug.so" if os.environ.get("TP_B300_LIB") == "debug"
+                        else "libtp_b300.so")
 LINEAR, CUBIC = 0, 1
 
 if not os.path.exists(LIB_PATH):
@@ -63,7 +67,10 @@ _SIGS = {
     "tp_backproject_backward_scratch_bytes": [_I, _I, _I, _I, _I, _I],
 }
 _SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, TPOptions]
+_SIGS["tp_debug_bounds_word"] = [_I]
+_SIGS["tp_debug_bounds_selftest"] = [_I, ctypes.c_void_p]
 _RESTYPES = {"tp_workspace_bytes": ctypes.c_size_t, "tp_last_error": ctypes.c_char_p,
+             "tp_debug_bounds_word": ctypes.c_uint,
              "tp_backproject_backward_scratch_bytes": ctypes.c_size_t,
              "tp_version": ctypes.c_char_p}
 _bound = {}
@@ -93,6 +100,16 @@ def tp_last_error() -> str:
 
 def tp_version() -> str:
     return _fn("tp_version")().decode()
+
+
+def tp_debug_bounds_word(reset: bool = False) -> int:
+    """Failed index-check bits of the debug build (0 in the normal build); see tp.h."""
+    return int(_fn("tp_debug_bounds_word")(1 if reset else 0))
+
+
+def tp_debug_bounds_selftest(bit: int, stream=None) -> None:
+    """Debug build: set bit `bit` of the check word through a failing check."""
+    _call("tp_debug_bounds_selftest", int(bit), _stream(stream))
 
 
 def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic"):

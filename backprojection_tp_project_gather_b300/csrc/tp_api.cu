@@ -15,6 +15,23 @@ namespace {
 
 thread_local char g_err[512] = "";
 
+#ifdef TP_DEBUG_BOUNDS
+// The bounds-check word of the debug build (see TP_CHECK), one per device.
+__device__ unsigned g_dbg_word;
+
+unsigned *dbg_word() {
+    void *p = nullptr;
+    return cudaGetSymbolAddress(&p, g_dbg_word) == cudaSuccess ? static_cast<unsigned *>(p)
+                                                                : nullptr;
+}
+
+// A check that fails by construction and guards no access: it only sets
+// bit `bit` of the word, so the reporting path can be tested on its own.
+__global__ void k_check_selftest(unsigned *dbg, int bit) { (void)TP_CHECK(dbg, bit < 0, bit); }
+#else
+unsigned *dbg_word() { return nullptr; }
+#endif
+
 tp_status fail(tp_status st, const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -92,6 +109,7 @@ tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const
     q.fN = (float)N;
     q.invN = 1.0f / (float)N;
     q.r2max = r2 > 2e9 ? 2000000000 : (int)r2;
+    q.dbg = dbg_word();
     g.dim = dim;
     g.cubic = o.interp == TP_CUBIC;
     return TP_OK;
@@ -254,6 +272,7 @@ tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *ou
     const double r = (opts.radius < 0.0f) ? 0.5 * N : (double)opts.radius;
     const double r2 = std::floor(r * r);
     q.r2max = r2 > 2e9 ? 2000000000 : (int)r2;
+    q.dbg = dbg_word();
     return launched(tp::launch_pose_grad_saved(q, reinterpret_cast<const float2 *>(grad_out),
                                                reinterpret_cast<const float2 *>(out),
                                                reinterpret_cast<const float2 *>(dout), grad_rot,
@@ -399,6 +418,36 @@ tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float 
         if (e != cudaSuccess) return launched(e, "backprojection gradient (weights)");
     }
     return ok();
+}
+
+unsigned tp_debug_bounds_word(int reset) {
+#ifdef TP_DEBUG_BOUNDS
+    unsigned w = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ~0u;
+    if (cudaMemcpyFromSymbol(&w, g_dbg_word, sizeof w) != cudaSuccess) return ~0u;
+    if (reset) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_dbg_word, &zero, sizeof zero) != cudaSuccess) return ~0u;
+    }
+    return w;
+#else
+    (void)reset;
+    return 0u;
+#endif
+}
+
+tp_status tp_debug_bounds_selftest(int bit, void *stream) {
+#ifdef TP_DEBUG_BOUNDS
+    if (bit < 0 || bit > 31) return fail(TP_ERR_SHAPE, "bit must be in [0, 31] (got %d)", bit);
+    unsigned *w = dbg_word();
+    if (!w) return fail(TP_ERR_CUDA, "no bounds-check word on this device");
+    k_check_selftest<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(w, bit);
+    return launched(cudaGetLastError(), "bounds-check self-test");
+#else
+    (void)bit;
+    (void)stream;
+    return fail(TP_ERR_UNSUPPORTED, "not a bounds-checking build (TP_DEBUG_BOUNDS)");
+#endif
 }
 
 const char *tp_last_error(void) { return g_err; }

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kThreads) k_weight_grads(Params q, const float
         const int rr = q.r2max - ky * ky;
         const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        if (!TP_CHECK(q.dbg, r0 + half < (size_t)q.B * q.P * q.plane, 10)) continue;
         if (grad_weights)
             for (int kx = lane; kx <= half; kx += 32) grad_weights[r0 + kx] = __ldg(&y[r0 + kx].x);
         if (!grad_rot) continue;
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) k_weight_grads(Params q, const float
     for (int w = 0; w < kWarps; ++w) t += part[w][lane];
     const int b = bp / q.P, pi = bp - b * q.P;
     const int ridx = ((q.Bp == 1) ? 0 : b) * q.P + pi;
-    if (t != 0.f) atomicAdd(grad_rot + (size_t)ridx * 9 + lane, t);
+    if (t != 0.f && TP_CHECK(q.dbg, ridx < q.Bp * q.P, 9)) atomicAdd(grad_rot + (size_t)ridx * 9 + lane, t);
 }
 
 }  // namespace

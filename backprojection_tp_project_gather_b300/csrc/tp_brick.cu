@@ -372,7 +372,9 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch s
         const int np = min(32, Pv - c * 32);
         unsigned m = 0u;
         for (int k = 0; k < np; ++k) {
-            const ReachGeo *rg = sc.reach + pose_id(q, v, c * 32 + k);
+            const int pid = pose_id(q, v, c * 32 + k);
+            if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
+            const ReachGeo *rg = sc.reach + pid;
             const float4 rr = __ldg(&rg->r);
             if (e2 > rr.x) continue;
             bool hit = rr.y != 0.f;   // degenerate poses reach every brick within reach
@@ -386,6 +388,7 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch s
         }
         if (j < nbr) {
             const size_t vj = (size_t)v * nbr + j;
+            if (!TP_CHECK(q.dbg, vj < (size_t)q.Bsrc * nbr && c < nchunks, 8)) continue;
             sc.masks[vj * nchunks + c] = m;
             if (m) atomicAdd(sc.hits + vj, __popc(m));
         }
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch s
 // in brick order (a block-wide exclusive scan gives each brick its slots).
 constexpr int kPlanThreads = 1024;
 
-__global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc) {
+__global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc, unsigned *dbg) {
     if (*sc.changed == 0u) return;
     __shared__ int warp_sum[kPlanThreads / 32];
     const int v = blockIdx.x;
@@ -438,8 +441,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc
         const int h = hits[j];
         if (!h) continue;
         const int n = min(nch, (h + kUnitHits - 1) / kUnitHits);
-        for (int i = 0; i < n; ++i)
-            out[at++] = make_int4(j, (int)((long long)nch * i / n), (int)((long long)nch * (i + 1) / n), 0);
+        for (int i = 0; i < n; ++i, ++at)
+            if (TP_CHECK(dbg, at < nbr * nch, 8))
+                out[at] = make_int4(j, (int)((long long)nch * i / n), (int)((long long)nch * (i + 1) / n), 0);
     }
 }
 
@@ -460,16 +464,18 @@ struct UnitTable {
 
 // Take the next unit of volume v from the global counter (block-wide).
 // Returns false when the volume's units are exhausted.
-__device__ __forceinline__ bool next_unit(const Scratch &sc, int slot, int v, int nbr,
-                                          UnitTable &t, int4 &rec) {
+__device__ __forceinline__ bool next_unit(const Params &q, const Scratch &sc, int slot, int v,
+                                          int nbr, UnitTable &t, int4 &rec) {
     const int nvol = gridDim.z;
     if (threadIdx.x == 0) t.unit = (int)atomicAdd(sc.counters + slot * nvol + v, 1u);
     __syncthreads();
     const int u = t.unit;
     __syncthreads();   // everyone has read t.unit before the next request
     if (u >= (int)__ldg(sc.counters + 3 * nvol + v)) return false;
+    if (!TP_CHECK(q.dbg, u >= 0 && u < nbr * sc.nchunks, 8)) return false;
     rec = __ldg(sc.units + (size_t)v * nbr * sc.nchunks + u);
-    return true;
+    return TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
+                               rec.z <= sc.nchunks, 8);
 }
 
 // Load the reaching poses of the unit's chunks, from chunk c on, into the
@@ -505,7 +511,9 @@ __device__ __forceinline__ int load_batch(const Params &q, const Scratch &sc, in
         const unsigned m = t.mask[i];
         if ((m >> lane) & 1u) {
             const int at = t.base[i] + __popc(m & ((1u << lane) - 1u));
-            const int *src = reinterpret_cast<const int *>(sc.geo + pose_id(q, v, (c + i) * 32 + lane));
+            const int pid = pose_id(q, v, (c + i) * 32 + lane);
+            if (!TP_CHECK(q.dbg, at < kUnitPoses && pid >= 0 && pid < q.B * q.P, 8)) continue;
+            const int *src = reinterpret_cast<const int *>(sc.geo + pid);
             int *dst = reinterpret_cast<int *>(&t.pose[at]);
             for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
         }
@@ -532,7 +540,7 @@ __device__ __forceinline__ bool stored(int x, int y, int z, int half) {
 // side (n_x < 0) are conjugated in a second pass.
 template <bool CUBIC>
 __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X, const BrickBox &bx,
-                                      float2 *s) {
+                                      float2 *s, unsigned *dbg) {
     using H = Halo<CUBIC>;
     const int half = M >> 1;
     const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
@@ -547,7 +555,10 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
         }
         const bool ok = stored(nx, ny, nz, half);
         const float2 *src = ok ? V + ((size_t)wrap_row(nz, M) * M + wrap_row(ny, M)) * X + nx : V;
-        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + H::index(lx, ly, lz));
+        const int at = H::index(lx, ly, lz);
+        if (!TP_CHECK(dbg, (size_t)(src - V) < (size_t)M * M * X, 0)) continue;
+        if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
+        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + at);
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src),
                      "r"(ok ? 8 : 0)
                      : "memory");
@@ -560,7 +571,9 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
         for (int e = threadIdx.x; e < nneg * H::S * H::S; e += kThreads) {
             const int lx = e % nneg, r = e / nneg;
             const int ly = r % H::S, lz = r / H::S;
-            float2 *p = s + H::index(lx, ly, lz);
+            const int at = H::index(lx, ly, lz);
+            if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
+            float2 *p = s + at;
             p->y = -p->y;
         }
     }
@@ -585,7 +598,7 @@ __device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) 
 
 template <bool CUBIC, bool DERIV>
 __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float (*w)[4],
-                                            float (*d)[4], float2 &S, float2 *dS) {
+                                            float (*d)[4], float2 &S, float2 *dS, unsigned *dbg) {
     using H = Halo<CUBIC>;
     constexpr int T = Stencil<CUBIC>::TAPS;
     S = make_float2(0.f, 0.f);
@@ -619,6 +632,8 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
                 float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
                 for (int sx = 0; sx < 4; ++sx) {
+                    const long long at = (row - s) + ox[sx];
+                    if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 2)) continue;
                     const float2 val = row[ox[sx]];
                     cfma(wx[sx], val, r0);
                     if (DERIV) cfma(dx[sx], val, r1);
@@ -648,6 +663,8 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
             float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
             for (int jx = 0; jx < T; ++jx) {
+                const long long at = (row - s) + jx;
+                if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 2)) continue;
                 const float2 val = row[jx];
                 cfma(w[0][jx], val, r0);
                 if (DERIV) cfma(d[0][jx], val, r1);
@@ -699,12 +716,14 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const PoseG
     const int lane = threadIdx.x & 31;
     const int half = q.N >> 1;
     const float2 zero = make_float2(0.f, 0.f);
+    const size_t nout = (size_t)q.B * q.P * q.plane;
     for (long long row = warp; row < rows; row += nwarps) {
         const int bp = (int)(row / q.N), iy = (int)(row - (long long)bp * q.N);
         const int ky = row_freq(iy, q.N);
         const int rr = q.r2max - ky * ky;
         const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        if (!TP_CHECK(q.dbg, r0 + half < nout, 3)) continue;
         for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
         if (dout)
             for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
@@ -746,9 +765,9 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
                  ((long long)(blockIdx.z * gridDim.x + blockIdx.x) * kThreads + threadIdx.x) >> 5,
                  (long long)gridDim.x * gridDim.z * kWarps);
     int4 rec;
-    while (next_unit(sc, 0, v, nbr, s_tab, rec)) {
+    while (next_unit(q, sc, 0, v, nbr, s_tab, rec)) {
         const BrickBox bx = brick_box(rec.x, nb);
-        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol, q.dbg);
         for (int c0 = rec.y; c0 < rec.z;) {
             c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
             for (int k; (k = next_pose(s_tab)) >= 0;) {
@@ -760,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
                     float w[3][4], d[3][4];
                     if (!active || !own_sample<CUBIC, SAVE>(g, bx, qx, qy, l, w, d)) return;
                     float2 S, dS[3];
-                    gather_smem<CUBIC, SAVE>(s_vol, l, w, d, S, dS);
+                    gather_smem<CUBIC, SAVE>(s_vol, l, w, d, S, dS, q.dbg);
                     const int iy = qy < 0 ? qy + q.N : qy;
                     const size_t e = ob + (size_t)iy * q.Xo + qx;
                     if (q.shift) {
@@ -770,6 +789,8 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
 #pragma unroll
                             for (int a = 0; a < 3; ++a) dS[a] = cmul(ph, dS[a]);
                     }
+                    if (!TP_CHECK(q.dbg, e < (size_t)q.B * q.P * q.plane && qx >= 0 && qx < q.Xo, 3))
+                        return;
                     out[e] = S;
                     if (SAVE)
 #pragma unroll
@@ -793,9 +814,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
     __shared__ UnitTable s_tab;
     const int v = blockIdx.z, nbr = nb * nb * nb;
     int4 rec;
-    while (next_unit(sc, 1, v, nbr, s_tab, rec)) {
+    while (next_unit(q, sc, 1, v, nbr, s_tab, rec)) {
         const BrickBox bx = brick_box(rec.x, nb);
-        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol);
+        stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol, q.dbg);
         for (int c0 = rec.y; c0 < rec.z;) {
             c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
             for (int k; (k = next_pose(s_tab)) >= 0;) {
@@ -810,8 +831,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
                     float w[3][4], d[3][4];
                     if (!active || !own_sample<CUBIC, true>(g, bx, qx, qy, l, w, d)) return;
                     float2 S, dS[3];
-                    gather_smem<CUBIC, true>(s_vol, l, w, d, S, dS);
+                    gather_smem<CUBIC, true>(s_vol, l, w, d, S, dS, q.dbg);
                     const int iy = qy < 0 ? qy + q.N : qy;
+                    if (!TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo &&
+                                             g.bp < q.B * q.P, 7))
+                        return;
                     const float2 gv = __ldg(gp + iy * q.Xo + qx);
                     float2 ph = make_float2(1.f, 0.f);
                     if (q.shift) ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
@@ -834,7 +858,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
                     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
                     acc[i] = t;
                 }
-                if ((threadIdx.x & 31) == 0) {
+                if ((threadIdx.x & 31) == 0 &&
+                    TP_CHECK(q.dbg, g.ridx >= 0 && g.ridx < q.Bp * q.P && g.sidx >= 0 &&
+                                        g.sidx < q.Bs * q.P, 9)) {
                     if (grad_rot)
 #pragma unroll
                         for (int i = 0; i < 6; ++i)
@@ -937,13 +963,19 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= items) break;
+        if (!TP_CHECK(q.dbg, (item >> 3) < nbr * sc.nchunks, 8)) break;
         const int4 rec = __ldg(units + (item >> 3));
+        if (!TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
+                                 rec.z <= sc.nchunks, 8))
+            break;
         const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
         const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
         bool touched = false;
         for (int c = rec.y; c < rec.z; ++c) {
             for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
-                const PoseGeo g = load_geo(sc.geo + pose_id(q, v, c * 32 + __ffs(m) - 1));
+                const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
+                if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
+                const PoseGeo g = load_geo(sc.geo + pid);
                 if (!pose_reaches(g, ob)) continue;
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
@@ -955,7 +987,9 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                     if (own) {
                         const int slot = __popc(mask & ((1u << lane) - 1u));
                         const int iy = qy < 0 ? qy + q.N : qy;
-                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                        const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo &&
+                                                            g.bp < q.B * q.P, 7);
+                        float2 cv = in ? __ldg(img + ib + iy * q.Xo + qx) : make_float2(0.f, 0.f);
                         if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
                         float *wq = Q.w[slot];
 #pragma unroll
@@ -965,7 +999,7 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                             wq[8 + j] = w[2][j];
                         }
                         if (WEIGHTS) wq[12] = __int_as_float((l[2] * kOWPY + l[1]) * kOPX + l[0]);
-                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * kOS + l[1]) * kOPX + l[0]));
                     }
@@ -998,14 +1032,16 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                             r4 = Q.rec[sq + 1];
                         }
                         const int idx = __float_as_int(cur.w) + toff;
-                        float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
-                        a0.x = fmaf(wt0, cur.x, a0.x);
-                        a0.y = fmaf(wt0, cur.y, a0.y);
-                        a1.x = fmaf(wt1, cur.x, a1.x);
-                        a1.y = fmaf(wt1, cur.y, a1.y);
-                        acc[idx] = a0;
-                        acc[idx + ZSTEP] = a1;
-                        if (WEIGHTS) {
+                        if (TP_CHECK(q.dbg, idx >= 0 && idx + ZSTEP < kOElems, 4)) {
+                            float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
+                            a0.x = fmaf(wt0, cur.x, a0.x);
+                            a0.y = fmaf(wt0, cur.y, a0.y);
+                            a1.x = fmaf(wt1, cur.x, a1.x);
+                            a1.y = fmaf(wt1, cur.y, a1.y);
+                            acc[idx] = a0;
+                            acc[idx + ZSTEP] = a1;
+                        }
+                        if (WEIGHTS && TP_CHECK(q.dbg, widx >= 0 && widx + ZSTEP_W < kOWElems, 5)) {
                             wacc[widx] = fmaf(wt0, cur.z, wacc[widx]);
                             wacc[widx + ZSTEP_W] = fmaf(wt1, cur.z, wacc[widx + ZSTEP_W]);
                         }
@@ -1037,6 +1073,7 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
             }
             if (!stored(nx, ny, nz, half)) continue;
             const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
+            if (!TP_CHECK(q.dbg, idx < (size_t)q.M * q.M * q.Xs, 6)) continue;
             if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, cj ? -cv.y : cv.y));
             if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
         }
@@ -1102,13 +1139,19 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= items) break;
+        if (!TP_CHECK(q.dbg, (item >> 3) < nbr * sc.nchunks, 8)) break;
         const int4 rec = __ldg(units + (item >> 3));
+        if (!TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
+                                 rec.z <= sc.nchunks, 8))
+            break;
         const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
         const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
         bool touched = false;
         for (int c = rec.y; c < rec.z; ++c) {
             for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
-                const PoseGeo g = load_geo(sc.geo + pose_id(q, v, c * 32 + __ffs(m) - 1));
+                const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
+                if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
+                const PoseGeo g = load_geo(sc.geo + pid);
                 if (!pose_reaches(g, ob)) continue;
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
@@ -1120,7 +1163,9 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                     if (own) {
                         const int slot = __popc(mask & ((1u << lane) - 1u));
                         const int iy = qy < 0 ? qy + q.N : qy;
-                        float2 cv = __ldg(img + ib + iy * q.Xo + qx);
+                        const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo &&
+                                                            g.bp < q.B * q.P, 7);
+                        float2 cv = in ? __ldg(img + ib + iy * q.Xo + qx) : make_float2(0.f, 0.f);
                         if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
                         float *wq = Q.w[slot];
                         wq[0] = w[0][0];
@@ -1129,7 +1174,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         wq[3] = w[1][1];
                         wq[4] = w[2][0];
                         wq[5] = w[2][1];
-                        const float om = (WEIGHTS && omega) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
                     }
@@ -1150,7 +1195,8 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         const unsigned same = __match_any_sync(0xffffffffu, idx);
                         const bool clash = __any_sync(0xffffffffu, __popc(same) > 1);
                         for (int k = 0; k < 4; ++k) {
-                            if (act && (!clash || grp == k)) {
+                            if (act && (!clash || grp == k) &&
+                                TP_CHECK(q.dbg, idx >= 0 && idx < kLElems, 4)) {
                                 float2 a = acc[idx];
                                 a.x = fmaf(wt, cur.x, a.x);
                                 a.y = fmaf(wt, cur.y, a.y);
@@ -1185,6 +1231,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
             }
             if (!stored(nx, ny, nz, half)) continue;
             const size_t idx = ((size_t)wrap_row(nz, q.M) * q.M + wrap_row(ny, q.M)) * q.Xs + nx;
+            if (!TP_CHECK(q.dbg, idx < (size_t)q.M * q.M * q.Xs, 6)) continue;
             if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, cj ? -cv.y : cv.y));
             if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
         }
@@ -1276,7 +1323,7 @@ cudaError_t bin(const Params &q, const Layout &L, const Scratch &sc, cudaStream_
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 32) blocks = 65535LL * 32;
     k_brick_masks<<<(unsigned)blocks, 256, 0, st>>>(q, L.nb, sc);
-    k_plan_units<<<q.Bsrc, kPlanThreads, 0, st>>>(nbr, sc);
+    k_plan_units<<<q.Bsrc, kPlanThreads, 0, st>>>(nbr, sc, q.dbg);
     return cudaGetLastError();
 }
 

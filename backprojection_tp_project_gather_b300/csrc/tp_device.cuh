@@ -37,7 +37,29 @@ struct Params {
     float fN;              // N as a float
     float invN;            // 1 / N
     int r2max;             // pixels with kx^2 + ky^2 > r2max are outside the radius
+    unsigned *dbg;         // bounds-check word of a TP_DEBUG_BOUNDS build, else null
 };
+
+// Bounds checks of the debug build (nvcc -DTP_DEBUG_BOUNDS): TP_CHECK(dbg,
+// cond, bit) is cond, and when cond is false it also sets bit `bit` of the
+// word *dbg, so that the access it guards is skipped and the host can read
+// which kind of index went out of range (tp_debug_bounds_word).  In the
+// normal build it is the constant true and cond is not evaluated (only named
+// in a sizeof, so that the variables it alone uses stay referenced).  Bits:
+// 0 source spectrum read (staging or direct gather), 1 staging destination,
+// 2 staged gather taps, 3 output rows,
+// 4 scatter tile, 5 weight tile, 6 fold target, 7 image read, 8 workspace
+// lists (units, masks, poses), 9 rotation / shift gradient rows, 10 saved
+// derivative or weight-gradient rows.
+#ifdef TP_DEBUG_BOUNDS
+__device__ __forceinline__ bool flag_bound(unsigned *dbg, int bit) {
+    if (dbg) atomicOr(dbg, 1u << bit);
+    return false;
+}
+#define TP_CHECK(dbg, cond, bit) ((cond) || ::tp::flag_bound((dbg), (bit)))
+#else
+#define TP_CHECK(dbg, cond, bit) (sizeof(cond) > 0)
+#endif
 
 // ---------------------------------------------------------------------------
 // Stencils [it §2 "Interpolazione"; ko §2 "보간법"; ar §2].

@@ -32,7 +32,8 @@ struct Gather {
     // w/d are the per-axis weights in ascending storage order.
     __device__ __forceinline__ static void run_fast(const float2 *__restrict__ src, int M, int X,
                                                     const int *base, float (*w)[4], float (*d)[4],
-                                                    float2 &S, float2 *dS) {
+                                                    float2 &S, float2 *dS, unsigned *dbg) {
+        const long long nsrc = (long long)(D == 3 ? M : 1) * M * X;
         if constexpr (D == 3) {
 #pragma unroll
             for (int jz = 0; jz < T; ++jz) {
@@ -45,6 +46,8 @@ struct Gather {
                     float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
                     for (int jx = 0; jx < T; ++jx) {
+                        const long long at = (row - src) + jx;
+                        if (!TP_CHECK(dbg, at >= 0 && at < nsrc, 0)) continue;
                         const float2 v = __ldg(row + jx);
                         cfma(w[0][jx], v, r0);
                         if (DERIV) cfma(d[0][jx], v, r1);
@@ -70,6 +73,8 @@ struct Gather {
                 float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
                 for (int jx = 0; jx < T; ++jx) {
+                    const long long at = (row - src) + jx;
+                    if (!TP_CHECK(dbg, at >= 0 && at < nsrc, 0)) continue;
                     const float2 v = __ldg(row + jx);
                     cfma(w[0][jx], v, r0);
                     if (DERIV) cfma(d[0][jx], v, r1);
@@ -86,7 +91,7 @@ struct Gather {
     // General path: per-tap Friedel reflection and range checks.
     __device__ __forceinline__ static void run_general(const float2 *__restrict__ src, int M, int X,
                                                        const int *x0, float (*w)[4], float (*d)[4],
-                                                       float2 &S, float2 *dS) {
+                                                       float2 &S, float2 *dS, unsigned *dbg) {
         const int half = M >> 1;
         const int TZ = (D == 3) ? T : 1;
         for (int jz = 0; jz < TZ; ++jz) {
@@ -105,6 +110,7 @@ struct Gather {
                     if (nx > half || !row_ok(ny, half) || (D == 3 && !row_ok(nz, half))) continue;
                     size_t e = (size_t)wrap_row(ny, M) * X + nx;
                     if (D == 3) e += (size_t)wrap_row(nz, M) * M * X;
+                    if (!TP_CHECK(dbg, e < (size_t)(D == 3 ? M : 1) * M * X, 0)) continue;
                     float2 v = __ldg(src + e);
                     if (cj) v.y = -v.y;
                     const float wz = (D == 3) ? w[2][jz] : 1.0f;
@@ -122,7 +128,8 @@ struct Gather {
 
     // Interpolated value at p (and its gradient when DERIV).
     __device__ __forceinline__ static void sample(const float2 *__restrict__ src, int M, int X,
-                                                  const float *p, float2 &S, float2 *dS) {
+                                                  const float *p, float2 &S, float2 *dS,
+                                                  unsigned *dbg) {
         const int half = M >> 1;
         int x0[D];
         float w[D][4], d[D][4];
@@ -151,7 +158,7 @@ struct Gather {
             int base[D];
 #pragma unroll
             for (int a = 0; a < D; ++a) base[a] = x0[a] - St::LO;
-            run_fast(src, M, X, base, w, d, S, dS);
+            run_fast(src, M, X, base, w, d, S, dS, dbg);
         } else if (friedel) {
             // Tap n = x0 - LO + j reads conj(V[-n]); in storage order the
             // reflected taps run from -(x0 + HI) upwards with weights reversed.
@@ -166,13 +173,13 @@ struct Gather {
                     if (DERIV) dr[a][j] = d[a][T - 1 - j];
                 }
             }
-            run_fast(src, M, X, base, wr, dr, S, dS);
+            run_fast(src, M, X, base, wr, dr, S, dS, dbg);
             S.y = -S.y;
             if (DERIV)
 #pragma unroll
                 for (int a = 0; a < D; ++a) dS[a].y = -dS[a].y;
         } else {
-            run_general(src, M, X, x0, w, d, S, dS);
+            run_general(src, M, X, x0, w, d, S, dS, dbg);
         }
     }
 };
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) k_project(Params q, float2 *__restri
     for (int j = 0; j < D; ++j) p[j] = fmaf(ps.a[j], (float)kx, ps.b[j] * (float)ky);
     const float2 *src = q.src + (q.Bsrc == 1 ? 0 : (size_t)b * q.src_stride);
     float2 S;
-    Gather<D, CUBIC, false>::sample(src, q.M, q.Xs, p, S, nullptr);
+    Gather<D, CUBIC, false>::sample(src, q.M, q.Xs, p, S, nullptr, q.dbg);
     if (q.shift) S = cmul(shift_phase(kx, ky, ps.sx, ps.sy, q.fN, q.invN), S);
     *o = S;
 }
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) k_pose_grad(Params q, const float2 *
             for (int j = 0; j < D; ++j) p[j] = fmaf(ps.a[j], (float)kx, ps.b[j] * (float)ky);
             const float2 *src = q.src + (q.Bsrc == 1 ? 0 : (size_t)b * q.src_stride);
             float2 S, dS[D];
-            Gather<D, CUBIC, true>::sample(src, q.M, q.Xs, p, S, dS);
+            Gather<D, CUBIC, true>::sample(src, q.M, q.Xs, p, S, dS, q.dbg);
             const float2 g = __ldg(g_out + (size_t)bp * q.plane + rem);
             float2 ph = make_float2(1.f, 0.f);
             if (q.shift) ph = shift_phase(kx, ky, ps.sx, ps.sy, q.fN, q.invN);
@@ -268,6 +275,7 @@ __global__ void __launch_bounds__(kThreads) k_pose_grad(Params q, const float2 *
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) v += red[w][threadIdx.x];
         const int i = threadIdx.x;
+        if (!TP_CHECK(q.dbg, ps.ridx < q.Bp * q.P && ps.sidx < q.Bs * q.P, 9)) return;
         if (i < NR) {
             if (grad_rot) atomicAdd(grad_rot + (size_t)ps.ridx * D * D + i, v);
         } else if (grad_shift) {

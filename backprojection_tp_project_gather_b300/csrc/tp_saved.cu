@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kSavedThreads) k_pose_grad_saved(Params q,
         if (rr < 0) continue;
         const int xcut = min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
+        if (!TP_CHECK(q.dbg, r0 + half < (size_t)q.B * q.P * q.plane, 10)) continue;
         // Four pixels per lane per pass: all their loads are issued before
         // any of them is used, to keep enough bytes in flight.
         for (int x0 = 0; x0 <= xcut; x0 += 4 * 32) {
@@ -90,10 +91,12 @@ __global__ void __launch_bounds__(kSavedThreads) k_pose_grad_saved(Params q,
     const int b = bp / q.P, pi = bp - b * q.P;
     if (lane < 6 && grad_rot) {
         const int ridx = ((q.Bp == 1) ? 0 : b) * q.P + pi;
-        if (t != 0.f) atomicAdd(grad_rot + (size_t)ridx * 9 + lane, t);
+        if (t != 0.f && TP_CHECK(q.dbg, ridx < q.Bp * q.P, 9))
+            atomicAdd(grad_rot + (size_t)ridx * 9 + lane, t);
     } else if (lane >= 6 && lane < 8 && grad_shift) {
         const int sidx = ((q.Bs == 1) ? 0 : b) * q.P + pi;
-        if (t != 0.f) atomicAdd(grad_shift + 2 * (size_t)sidx + (lane - 6), t);
+        if (t != 0.f && TP_CHECK(q.dbg, sidx < q.Bs * q.P, 9))
+            atomicAdd(grad_shift + 2 * (size_t)sidx + (lane - 6), t);
     }
 }
 

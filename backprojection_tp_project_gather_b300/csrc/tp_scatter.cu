@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads) k_scatter(Params q, const float2 *__
                     e += (size_t)wrap_row(nz, M) * M * X;
                     wt *= w[2][jz];
                 }
+                if (!TP_CHECK(q.dbg, e < (size_t)(D == 3 ? M : 1) * M * X, 6)) continue;
                 atomicAdd(V + e, make_float2(wt * c.x, cj ? -wt * c.y : wt * c.y));
                 if (W) atomicAdd(W + e, wt * om);
             }

@@ -274,6 +274,29 @@ tp_status tp_project_3d_2d_noalloc(const float *vol, int Bv, int Nv,
                                    const float *shift, int Bs,
                                    int N, tp_options opts, float *out, void *stream);
 
+/*
+ * Bounds checks of a debug build of this library (compiled with
+ * -DTP_DEBUG_BOUNDS, libtp_b300_debug.so): waits for the current device and
+ * returns the bits of the index checks that have failed since the last reset
+ * (0 = none; a failed check skips its access).  reset != 0 clears the word.
+ * The normal build checks nothing and returns 0; ~0u reports a CUDA error.
+ * Bits: 0 source spectrum read, 1 staged-brick write, 2 staged tap read,
+ * 3 output image row, 4 scatter accumulator tile, 5 weight accumulator
+ * tile, 6 spectrum fold / scatter target, 7 image read, 8 workspace lists
+ * (work units, pose masks, pose records), 9 rotation / shift gradient row,
+ * 10 saved-derivative or weight-gradient row.
+ */
+unsigned tp_debug_bounds_word(int reset);
+
+/*
+ * Debug build only: enqueue on `stream` one check that fails by
+ * construction and guards no memory access, so that bit `bit` (0..31) of
+ * the word above is set.  Tests the reporting path itself.  Returns
+ * TP_ERR_SHAPE for a bit outside 0..31 and TP_ERR_UNSUPPORTED in the
+ * normal build (nothing is launched).
+ */
+tp_status tp_debug_bounds_selftest(int bit, void *stream);
+
 /* Message for the calling thread's most recent failure ("" if none). */
 const char *tp_last_error(void);
 

@@ -47,6 +47,19 @@ def test_library_exports_every_declared_symbol(tp):
     assert re.fullmatch(r"\d+\.\d+\.\d+", tp.tp_version())
 
 
+def test_bounds_checking_build_exports_the_same_symbols(tp):
+    """libtp_b300_debug.so (-DTP_DEBUG_BOUNDS) is a drop-in for the normal
+    library; the normal build reports no failed index checks."""
+    from backprojection_tp_project_gather_b300 import build
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for name in declared_symbols():
+        assert hasattr(dbg, name), name
+    assert tp.tp_debug_bounds_word() == 0
+    assert tp.tp_debug_bounds_word(reset=True) == 0
+    # The self-test exists only in the debug build; nothing is launched here.
+    assert tp._fn("tp_debug_bounds_selftest")(3, None) == TP_ERR_UNSUPPORTED
+
+
 # Fake, well-aligned device addresses: validation rejects each call first.
 A = 0x10000
 MIS = 0x10004      # 4-byte aligned, not 8-byte aligned (bad for complex64)
