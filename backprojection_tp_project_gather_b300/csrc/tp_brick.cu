@@ -903,11 +903,15 @@ constexpr int kOElems = kOS * kOS * kOPX;  // complex words of the tile
 // on, 16 banks away) land in the 16 banks the first half-warp leaves free.
 constexpr int kOWPY = 12;                    // y pitch of the weight tile
 constexpr int kOWElems = kOS * kOWPY * kOPX; // words of the weight tile
-constexpr int kOQW = 13;                     // floats per queued weight row (odd: no bank conflicts)
+constexpr int kOQW = 9;                      // floats per queued weight row (odd: no bank conflicts)
 
+// Queued samples of a warp.  A lane of half-warp h reads its z weights
+// (wz[h], wz[h + 2]) with one 64-bit load from wz[], hence their order there.
 struct OctQueue {
-    float w[32][kOQW];   // per sample: wx (4), wy (4), wz (4), first weight-tile tap
-    float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
+    float w[32][kOQW];   // per sample: wx (4), wy (4), unused
+    float4 wz[32];       // per sample: wz0, wz2, wz1, wz3
+    float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap (| z << 16
+                         // with weights)
 };
 
 template <bool WEIGHTS>
@@ -996,42 +1000,42 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                         for (int j = 0; j < 4; ++j) {
                             wq[j] = w[0][j];
                             wq[4 + j] = w[1][j];
-                            wq[8 + j] = w[2][j];
                         }
-                        if (WEIGHTS) wq[12] = __int_as_float((l[2] * kOWPY + l[1]) * kOPX + l[0]);
+                        Q.wz[slot] = make_float4(w[2][0], w[2][2], w[2][1], w[2][3]);
                         const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
+                        // The weight tile's first tap differs from the complex
+                        // tile's by kOPX (kOWPY - kOS) z: the z travels along.
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
-                                                  __int_as_float((l[2] * kOS + l[1]) * kOPX + l[0]));
+                                                  __int_as_float(((l[2] * kOS + l[1]) * kOPX + l[0]) |
+                                                                 (WEIGHTS ? l[2] << 16 : 0)));
                     }
                     __syncwarp();
                     const int nq = __popc(mask);
                     // The next sample's queue entries are read before this
                     // sample's tile words, hiding their latency.
-                    float wx = 0.f, wy = 0.f, wz0 = 0.f, wz1 = 0.f;
-                    int wb = 0;
+                    float wx = 0.f, wy = 0.f;
+                    float2 wz = make_float2(0.f, 0.f);
                     float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (nq > 0) {
                         wx = Q.w[0][jx];
                         wy = Q.w[0][4 + jy];
-                        wz0 = Q.w[0][8 + tz];
-                        wz1 = Q.w[0][10 + tz];
-                        if (WEIGHTS) wb = __float_as_int(Q.w[0][12]);
+                        wz = reinterpret_cast<const float2 *>(&Q.wz[0])[tz];
                         r4 = Q.rec[0];
                     }
                     for (int sq = 0; sq < nq; ++sq) {
                         const float wxy = wx * wy;
-                        const float wt0 = wxy * wz0, wt1 = wxy * wz1;
+                        const float wt0 = wxy * wz.x, wt1 = wxy * wz.y;
                         const float4 cur = r4;
-                        const int widx = wb + toff_w;
                         if (sq + 1 < nq) {
                             wx = Q.w[sq + 1][jx];
                             wy = Q.w[sq + 1][4 + jy];
-                            wz0 = Q.w[sq + 1][8 + tz];
-                            wz1 = Q.w[sq + 1][10 + tz];
-                            if (WEIGHTS) wb = __float_as_int(Q.w[sq + 1][12]);
+                            wz = reinterpret_cast<const float2 *>(&Q.wz[sq + 1])[tz];
                             r4 = Q.rec[sq + 1];
                         }
-                        const int idx = __float_as_int(cur.w) + toff;
+                        const int packed = __float_as_int(cur.w);
+                        const int base = WEIGHTS ? packed & 0xffff : packed;
+                        const int idx = base + toff;
+                        const int widx = base + kOPX * (kOWPY - kOS) * (packed >> 16) + toff_w;
                         if (TP_CHECK(q.dbg, idx >= 0 && idx + ZSTEP < kOElems, 4)) {
                             float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
                             a0.x = fmaf(wt0, cur.x, a0.x);
@@ -1092,10 +1096,10 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
 constexpr int kLS = kOct + 1;               // octant + linear halo
 constexpr int kLPX = 10, kLPY = 10;         // x and y pitches of the tile
 constexpr int kLElems = kLS * kLPY * kLPX;  // complex words of the tile
-constexpr int kLQW = 7;                     // floats per queued weight row (odd)
+constexpr int kLQW = 9;                     // floats per queued weight row (odd)
 
 struct LinQueue {
-    float w[32][kLQW];   // per sample: wx (2), wy (2), wz (2)
+    float w[32][kLQW];   // per sample: the 8 tap weights wx wy wz (x fastest), unused
     float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
 };
 
@@ -1168,12 +1172,8 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         float2 cv = in ? __ldg(img + ib + iy * q.Xo + qx) : make_float2(0.f, 0.f);
                         if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
                         float *wq = Q.w[slot];
-                        wq[0] = w[0][0];
-                        wq[1] = w[0][1];
-                        wq[2] = w[1][0];
-                        wq[3] = w[1][1];
-                        wq[4] = w[2][0];
-                        wq[5] = w[2][1];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) wq[t] = w[0][t & 1] * w[1][(t >> 1) & 1] * w[2][t >> 2];
                         const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
@@ -1188,7 +1188,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
                         int idx = -1 - lane;   // unique for idle lanes
                         if (act) {
-                            wt = Q.w[sq][jx] * Q.w[sq][2 + jy] * Q.w[sq][4 + jz];
+                            wt = Q.w[sq][lane & 7];
                             cur = Q.rec[sq];
                             idx = __float_as_int(cur.w) + toff;
                         }
