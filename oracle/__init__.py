@@ -209,3 +209,43 @@ def backproject_backward(dim, grad_data, img, rot, shift=None, grad_weight=None,
                                       shift=None, need_src=False, need_shift=False, **kw)
         grad_rot = grad_rot + gr_w
     return grad_img, grad_weights, grad_rot, grad_shift
+
+
+def hermitian_x0(spec, dim, weight=None):
+    """Symmetrised zero-frequency axis of accumulated half-spectra.
+
+    The pages' backward pass accumulates the contributions that land on the
+    kx = 0 axis symmetrically, so that the pair (0, k), (0, -k) -- one
+    Fourier coefficient of a real object and its conjugate -- is not counted
+    twice with different values ("torch-projectors", [ar §2] Friedel
+    symmetry, backward pass; [de §2 "Friedel-Symmetrie"]).  The pages give no
+    formula; the reading taken here is the Hermitian part of the stored
+    kx = 0 plane (3D) or column (2D):
+
+        V'(0, k) = (V(0, k) + conj(V(0, -k))) / 2,    W'(0, k) = (W(0, k) + W(0, -k)) / 2,
+
+    with -k taken modulo the box in every stored axis (rfftn row order), so
+    self-conjugate points keep their real part.  Every other coefficient is
+    unchanged.  spec is (B, M, M, M/2+1) for dim 3 or (B, M, M/2+1) for dim
+    2, weight (real, same shape) or None.  Returns new arrays (spec', weight').
+    """
+    spec = np.array(spec, dtype=np.complex128)
+    out_w = None if weight is None else np.array(weight, dtype=np.float64)
+    M = spec.shape[1]
+    neg = (-np.arange(M)) % M          # row of -k for the row of k
+    if dim == 3:
+        plane = spec[:, :, :, 0].copy()                      # (B, z, y)
+        mirror = plane[:, neg][:, :, neg]                    # V(0, -z, -y)
+        spec[:, :, :, 0] = 0.5 * (plane + np.conj(mirror))
+        if out_w is not None:
+            wp = out_w[:, :, :, 0].copy()
+            out_w[:, :, :, 0] = 0.5 * (wp + wp[:, neg][:, :, neg])
+    elif dim == 2:
+        col = spec[:, :, 0].copy()                           # (B, y)
+        spec[:, :, 0] = 0.5 * (col + np.conj(col[:, neg]))
+        if out_w is not None:
+            wc = out_w[:, :, 0].copy()
+            out_w[:, :, 0] = 0.5 * (wc + wc[:, neg])
+    else:
+        raise ValueError("dim must be 2 or 3")
+    return spec, out_w

@@ -5,11 +5,16 @@ in a temporary directory) and runs the pin suite against it in a child
 process; every mutant must make the pins fail.  This shows that the pins
 constrain the oracle rather than restate it.
 """
+import inspect
 import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
+
+import hermitian_pins
+import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "tp_oracle.c")
@@ -53,3 +58,32 @@ def test_pins_reject_mutant(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins accepted mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# Planted mistakes in the symmetrised zero-frequency axis (a Python function
+# of the oracle): each copy must fail at least one of its pins.
+HERMITIAN_MUTANTS = {
+    "mirror-without-modulo": ("neg = (-np.arange(M)) % M", "neg = np.arange(M)[::-1]"),
+    "no-conj": ("0.5 * (plane + np.conj(mirror))", "0.5 * (plane + mirror)"),
+    "no-half": ("0.5 * (plane + np.conj(mirror))", "(plane + np.conj(mirror))"),
+    "2d-no-conj": ("0.5 * (col + np.conj(col[:, neg]))", "0.5 * (col + col[:, neg])"),
+    "mirror-one-axis": ("mirror = plane[:, neg][:, :, neg]", "mirror = plane[:, neg]"),
+    "weight-not-mirrored": ("0.5 * (wp + wp[:, neg][:, :, neg])", "0.5 * (wp + wp)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HERMITIAN_MUTANTS))
+def test_hermitian_pins_reject_mutant(name):
+    old, new = HERMITIAN_MUTANTS[name]
+    src = inspect.getsource(oracle.hermitian_x0)
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    mutant = ns["hermitian_x0"]
+    failed = 0
+    for check in hermitian_pins.ALL:
+        try:
+            check(mutant)
+        except AssertionError:
+            failed += 1
+    assert failed > 0, f"pins accepted mutant {name}"

@@ -493,3 +493,34 @@ def test_backprojection_gradients_finite_differences(interp, with_weights):
         # The weight spectrum with unit image weights still depends on the poses.
         gy1, gw1, gR1, _ = oracle.backproject_backward(3, G, y, R, shift=t, grad_weight=GW, **kw)
         assert gw1.shape == y.shape
+
+
+# --------------------------------------------------------------------------
+# P17: the symmetrised zero-frequency axis (the optional backward-pass
+# treatment of [ar §2] / [de §2 "Friedel-Symmetrie"]): fixed on spectra of
+# real data, closed forms for a lone coefficient, an orthogonal projector.
+import hermitian_pins  # noqa: E402
+
+
+@pytest.mark.parametrize("check", hermitian_pins.ALL, ids=lambda f: f.__name__)
+def test_hermitian_x0(check):
+    check(oracle.hermitian_x0)
+
+
+def test_hermitian_x0_keeps_the_adjoint_identity_for_real_objects():
+    """With the axis symmetrised after the backprojection B, Re<F V, y> =
+    Re<V, H(B y)> still holds for every spectrum V of a real object (H
+    fixes V and is self-adjoint), but not for a general V."""
+    rng = np.random.default_rng(172)
+    M = N = 12
+    R = synth.random_rotations(3, rng).astype(np.float64)[None]
+    t = rng.uniform(-2, 2, (1, 3, 2))
+    y = hermitian_pins.crandn(rng, (1, 3, N, N // 2 + 1))
+    kw = dict(interp="cubic", radius=-1.0)
+    Hb, _ = oracle.hermitian_x0(oracle.backproject(3, y, R, shift=t, M=M, **kw)[0], 3)
+    V = np.fft.rfftn(rng.standard_normal((M, M, M)))[None]
+    lhs = np.vdot(y, oracle.project(3, V, R, shift=t, N=N, **kw)).real
+    assert abs(lhs - np.vdot(Hb, V).real) <= 1e-10 * abs(lhs)
+    G = hermitian_pins.crandn(rng, V.shape)
+    lhs = np.vdot(y, oracle.project(3, G, R, shift=t, N=N, **kw)).real
+    assert abs(lhs - np.vdot(Hb, G).real) > 1e-6 * abs(lhs)
