@@ -23,7 +23,8 @@ __all__ = [
     "tp_project_3d_2d_save", "tp_project_3d_2d_backward_saved", "tp_backproject_2d_3d_backward",
     "tp_backproject_backward_scratch_bytes", "tp_project_2d_2d", "tp_project_2d_2d_backward",
     "tp_last_error", "tp_version", "tp_workspace_bytes", "tp_project_3d_2d_noalloc",
-    "tp_debug_bounds_word", "tp_debug_bounds_selftest", "LINEAR", "CUBIC",
+    "tp_debug_bounds_word", "tp_debug_bounds_selftest", "tp_hermitian_x0", "LINEAR", "CUBIC",
+    "FLAG_HERMITIAN_X0",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtp_b300_debug.so" if os.environ.get("TP_B300_LIB") == "debug"
                         else "libtp_b300.so")
 LINEAR, CUBIC = 0, 1
+FLAG_HERMITIAN_X0 = 1   # TP_FLAG_HERMITIAN_X0: symmetrised kx = 0 axis of accumulated spectra
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -68,6 +70,7 @@ _SIGS = {
 }
 _SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, TPOptions]
 _SIGS["tp_debug_bounds_word"] = [_I]
+_SIGS["tp_hermitian_x0"] = [_P, _P, _I, _I, _I, ctypes.c_void_p]
 _SIGS["tp_debug_bounds_selftest"] = [_I, ctypes.c_void_p]
 _RESTYPES = {"tp_workspace_bytes": ctypes.c_size_t, "tp_last_error": ctypes.c_char_p,
              "tp_debug_bounds_word": ctypes.c_uint,
@@ -128,10 +131,11 @@ def _workspace(ws, Bv, B, P, Nv, interp, device):
     return ws, nbytes
 
 
-def _opts(interp, oversampling, radius):
+def _opts(interp, oversampling, radius, hermitian_x0=False):
     if isinstance(interp, str):
         interp = {"linear": LINEAR, "cubic": CUBIC}[interp]
-    return TPOptions(int(interp), float(oversampling), float(radius), 0)
+    return TPOptions(int(interp), float(oversampling), float(radius),
+                     FLAG_HERMITIAN_X0 if hermitian_x0 else 0)
 
 
 def _ptr(t):
@@ -200,7 +204,8 @@ def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, s
 
 
 def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius, grad_src,
-              grad_rot, grad_shift, want_src, want_rot, want_shift, stream, workspace=None):
+              grad_rot, grad_shift, want_src, want_rot, want_shift, stream, workspace=None,
+              hermitian_x0=False):
     _need(grad_out, "grad_out", torch.complex64, 4)
     _need(src, "source", torch.complex64, dim + 1)
     Bsrc, M = src.shape[0], src.shape[1]
@@ -225,7 +230,8 @@ def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius
         if shift is None or grad_shift.shape != shift.shape:
             raise ValueError("grad_shift must have shift's shape")
     args = [_ptr(grad_out), _ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
-            _opts(interp, oversampling, radius), _ptr(grad_src), _ptr(grad_rot), _ptr(grad_shift)]
+            _opts(interp, oversampling, radius, hermitian_x0), _ptr(grad_src), _ptr(grad_rot),
+            _ptr(grad_shift)]
     if dim == 3:
         B = grad_out.shape[0]
         ws, nbytes = _workspace(workspace, Bsrc, B, P, M, interp, grad_out.device)
@@ -334,27 +340,33 @@ def tp_project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampli
 def tp_project_3d_2d_backward(grad_out, vol, rot, shift=None, *, interp="cubic",
                               oversampling=1.0, radius=-1.0, grad_vol=None, grad_rot=None,
                               grad_shift=None, want_vol=True, want_rot=True, want_shift=True,
-                              workspace=None, stream=None):
-    """(grad_vol, grad_rot, grad_shift), accumulated into the given tensors; see tp.h."""
+                              workspace=None, stream=None, hermitian_x0=False):
+    """(grad_vol, grad_rot, grad_shift), accumulated into the given tensors; see tp.h.
+
+    hermitian_x0: symmetrise the kx = 0 plane of grad_vol (TP_FLAG_HERMITIAN_X0)."""
     return _backward("tp_project_3d_2d_backward", 3, grad_out, vol, rot, shift, interp,
                      oversampling, radius, grad_vol, grad_rot, grad_shift, want_vol, want_rot,
-                     want_shift, stream, workspace)
+                     want_shift, stream, workspace, hermitian_x0)
 
 
 def tp_project_2d_2d_backward(grad_out, img, rot, shift=None, *, interp="cubic",
                               oversampling=1.0, radius=-1.0, grad_img=None, grad_rot=None,
                               grad_shift=None, want_img=True, want_rot=True, want_shift=True,
-                              stream=None):
-    """(grad_img, grad_rot, grad_shift), accumulated into the given tensors; see tp.h."""
+                              stream=None, hermitian_x0=False):
+    """(grad_img, grad_rot, grad_shift), accumulated into the given tensors; see tp.h.
+
+    hermitian_x0: symmetrise the kx = 0 column of grad_img (TP_FLAG_HERMITIAN_X0)."""
     return _backward("tp_project_2d_2d_backward", 2, grad_out, img, rot, shift, interp,
                      oversampling, radius, grad_img, grad_rot, grad_shift, want_img, want_rot,
-                     want_shift, stream)
+                     want_shift, stream, None, hermitian_x0)
 
 
 def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, interp="cubic",
                          oversampling=1.0, radius=-1.0, data_vol=None, weight_vol=None,
-                         want_weights=True, workspace=None, stream=None):
-    """Scatter proj (B, P, N, N/2+1) into (data_vol, weight_vol) of box Nv (+=); see tp.h."""
+                         want_weights=True, workspace=None, stream=None, hermitian_x0=False):
+    """Scatter proj (B, P, N, N/2+1) into (data_vol, weight_vol) of box Nv (+=); see tp.h.
+
+    hermitian_x0: symmetrise the kx = 0 planes afterwards (TP_FLAG_HERMITIAN_X0)."""
     _need(proj, "proj", torch.complex64, 4)
     B, P, N = proj.shape[0], proj.shape[1], proj.shape[2]
     Bp, Pr, Bs = _poses(rot, shift, 3)
@@ -379,9 +391,31 @@ def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, 
             raise ValueError(f"weight_vol must be {shape}")
     ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, proj.device)
     _call("tp_backproject_2d_3d", _ptr(proj), _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift),
-          Bs, Bv, Nv, _opts(interp, oversampling, radius), _ptr(data_vol), _ptr(weight_vol),
+          Bs, Bv, Nv, _opts(interp, oversampling, radius, hermitian_x0), _ptr(data_vol),
+          _ptr(weight_vol),
           _ptr(ws), nbytes, _stream(stream))
     return data_vol, weight_vol
+
+
+def tp_hermitian_x0(spec=None, weight=None, *, dim=3, stream=None):
+    """Symmetrise the kx = 0 plane (dim 3) or column (dim 2) in place; see tp.h.
+
+    spec: complex64 (B, N, N, N/2+1) or (B, N, N/2+1); weight: float32 of the
+    same shape; either may be None.  Returns (spec, weight)."""
+    ref = spec if spec is not None else weight
+    if ref is None:
+        raise ValueError("spec or weight is required")
+    if dim not in (2, 3):
+        raise ValueError("dim must be 2 or 3")
+    if spec is not None:
+        _need(spec, "spec", torch.complex64, dim + 1)
+    if weight is not None:
+        _need(weight, "weight", torch.float32, dim + 1)
+        if spec is not None and weight.shape != spec.shape:
+            raise ValueError("weight must have spec's shape")
+    _call("tp_hermitian_x0", _ptr(spec), _ptr(weight), ref.shape[0], ref.shape[1], dim,
+          _stream(stream))
+    return spec, weight
 
 
 def tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, with_weight_grad=True):

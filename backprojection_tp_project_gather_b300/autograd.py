@@ -13,6 +13,10 @@ route tensors and gradients.  Complex gradients follow PyTorch's convention
 The 3D forward saves D = phase * dS/dp when rot or shift need gradients, so
 that their backward is a streaming pass (tp_project_3d_2d_backward_saved);
 the volume gradient is the brick scatter of the upstream gradient.
+
+hermitian_x0=True symmetrises the kx = 0 axis of the volume (image)
+gradient (TP_FLAG_HERMITIAN_X0): the gradient with respect to a spectrum
+constrained to be that of a real object.  The forward is unchanged.
 """
 from __future__ import annotations
 
@@ -25,7 +29,7 @@ from . import (tp_project_2d_2d, tp_project_2d_2d_backward, tp_project_3d_2d,
 
 class _Project3D(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, vol, rot, shift, N, interp, oversampling, radius):
+    def forward(ctx, vol, rot, shift, N, interp, oversampling, radius, hermitian_x0):
         kw = dict(N=N, interp=interp, oversampling=oversampling, radius=radius)
         need_pose = rot.requires_grad or (shift is not None and shift.requires_grad)
         # One workspace per call: the backward finds the forward's binning in it.
@@ -38,6 +42,7 @@ class _Project3D(torch.autograd.Function):
             out, dout = tp_project_3d_2d(vol, rot, shift, workspace=ws, **kw), None
         ctx.save_for_backward(vol, rot, shift, out, dout, ws)
         ctx.opts = dict(interp=interp, oversampling=oversampling, radius=radius)
+        ctx.hermitian_x0 = hermitian_x0
         return out
 
     @staticmethod
@@ -54,17 +59,19 @@ class _Project3D(torch.autograd.Function):
         if want_vol:
             # The workspace still holds the forward's binning of these poses.
             gv, _, _ = tp_project_3d_2d_backward(grad_out, vol, rot, shift, want_rot=False,
-                                                 want_shift=False, workspace=ws, **ctx.opts)
-        return gv, gr, gs, None, None, None, None
+                                                 want_shift=False, workspace=ws,
+                                                 hermitian_x0=ctx.hermitian_x0, **ctx.opts)
+        return gv, gr, gs, None, None, None, None, None
 
 
 class _Project2D(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, img, rot, shift, N, interp, oversampling, radius):
+    def forward(ctx, img, rot, shift, N, interp, oversampling, radius, hermitian_x0):
         out = tp_project_2d_2d(img, rot, shift, N=N, interp=interp, oversampling=oversampling,
                                radius=radius)
         ctx.save_for_backward(img, rot, shift)
-        ctx.opts = dict(interp=interp, oversampling=oversampling, radius=radius)
+        ctx.opts = dict(interp=interp, oversampling=oversampling, radius=radius,
+                        hermitian_x0=hermitian_x0)
         return out
 
     @staticmethod
@@ -76,16 +83,16 @@ class _Project2D(torch.autograd.Function):
                                                want_shift=want_shift and shift is not None,
                                                **ctx.opts)
         return (gi if want_img else None, gr if want_rot else None,
-                gs if want_shift else None, None, None, None, None)
+                gs if want_shift else None, None, None, None, None, None)
 
 
 def project_3d_2d(vol, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
-                  radius=-1.0):
+                  radius=-1.0, hermitian_x0=False):
     """Differentiable central slices (B, P, N, N/2+1) of vol (Bv, Nv, Nv, Nv/2+1)."""
-    return _Project3D.apply(vol, rot, shift, N, interp, oversampling, radius)
+    return _Project3D.apply(vol, rot, shift, N, interp, oversampling, radius, hermitian_x0)
 
 
 def project_2d_2d(img, rot, shift=None, *, N=None, interp="cubic", oversampling=1.0,
-                  radius=-1.0):
+                  radius=-1.0, hermitian_x0=False):
     """Differentiable rotated / shifted copies (B, P, N, N/2+1) of img (Bi, Ni, Ni/2+1)."""
-    return _Project2D.apply(img, rot, shift, N, interp, oversampling, radius)
+    return _Project2D.apply(img, rot, shift, N, interp, oversampling, radius, hermitian_x0)

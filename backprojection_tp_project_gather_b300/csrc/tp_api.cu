@@ -54,9 +54,15 @@ struct Geometry {
     bool cubic = false;
 };
 
+// allowed: the tp_options.flags bits the calling operator accepts.
 tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const float *shift,
-                int Bs, int N, const tp_options &o, int Bout, Geometry &g) {
-    if (o.flags != 0) return fail(TP_ERR_UNSUPPORTED, "tp_options.flags must be 0 (got %u)", o.flags);
+                int Bs, int N, const tp_options &o, int Bout, Geometry &g, unsigned allowed = 0u) {
+    if (o.flags & ~allowed)
+        return fail(TP_ERR_UNSUPPORTED, "tp_options.flags 0x%x not supported by this operator%s",
+                    o.flags & ~allowed,
+                    (o.flags & TP_FLAG_HERMITIAN_X0)
+                        ? " (TP_FLAG_HERMITIAN_X0 applies to accumulated spectra only)"
+                        : "");
     if (o.interp != TP_LINEAR && o.interp != TP_CUBIC)
         return fail(TP_ERR_UNSUPPORTED, "interp must be TP_LINEAR or TP_CUBIC (got %d)", o.interp);
     if (!(o.oversampling > 0.0f) || !std::isfinite(o.oversampling))
@@ -164,7 +170,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
                    tp_options opts, float *grad_src, float *grad_rot, float *grad_shift, void *ws,
                    size_t ws_bytes, void *stream) {
     Geometry g;
-    tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g);
+    tp_status st = setup(dim, Bsrc, M, rot, Bp, P, shift, Bs, N, opts, 1, g, TP_FLAG_HERMITIAN_X0);
     if (st != TP_OK) return st;
     if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
     if (!grad_out || !rot) return fail(TP_ERR_NULL, "grad_out and rotation pointers are required");
@@ -198,6 +204,10 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
                                                        mode, s)
                             : tp::launch_scatter(dim, g.cubic, g.q, go, nullptr, gs, nullptr, s);
         if (e != cudaSuccess) return launched(e, "spectrum gradient");
+        if (opts.flags & TP_FLAG_HERMITIAN_X0) {
+            e = tp::launch_hermitian_x0(gs, nullptr, Bsrc, M, dim, s, g.q.dbg);
+            if (e != cudaSuccess) return launched(e, "zero-axis symmetrisation");
+        }
     }
     return ok();
 }
@@ -308,7 +318,7 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
                                int Nv, tp_options opts, float *data_vol, float *weight_vol,
                                void *workspace, size_t workspace_bytes, void *stream) {
     Geometry g;
-    tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
+    tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g, TP_FLAG_HERMITIAN_X0);
     if (st != TP_OK) return st;
     if (g.q.B != B)
         return fail(TP_ERR_SHAPE, "operand batches (%d) exceed the image batch B = %d", g.q.B, B);
@@ -321,12 +331,13 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
     if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
         return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
     if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
-    return launched(tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
-                                             weights, reinterpret_cast<float2 *>(data_vol),
-                                             weight_vol, workspace,
-                                             tp::kBinNew,
-                                             static_cast<cudaStream_t>(stream)),
-                    "backproject");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float2 *dv = reinterpret_cast<float2 *>(data_vol);
+    cudaError_t e = tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
+                                             weights, dv, weight_vol, workspace, tp::kBinNew, s);
+    if (e == cudaSuccess && (opts.flags & TP_FLAG_HERMITIAN_X0))
+        e = tp::launch_hermitian_x0(dv, weight_vol, Bv, Nv, 3, s, g.q.dbg);
+    return launched(e, "backproject");
 }
 
 size_t tp_backproject_backward_scratch_bytes(int Bv, int B, int P, int N, int Nv,
@@ -349,6 +360,10 @@ tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float 
                                         float *grad_weights, float *grad_rot, float *grad_shift,
                                         void *scratch, size_t scratch_bytes, void *workspace,
                                         size_t workspace_bytes, void *stream) {
+    if (opts.flags & TP_FLAG_HERMITIAN_X0)
+        return fail(TP_ERR_UNSUPPORTED,
+                    "TP_FLAG_HERMITIAN_X0: the gradients of a symmetrised backprojection are those of "
+                    "the plain one at symmetrised upstream gradients (apply tp_hermitian_x0 to them)");
     Geometry g;
     tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, B, g);
     if (st != TP_OK) return st;
@@ -418,6 +433,20 @@ tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float 
         if (e != cudaSuccess) return launched(e, "backprojection gradient (weights)");
     }
     return ok();
+}
+
+tp_status tp_hermitian_x0(float *spec, float *weight, int B, int N, int dim, void *stream) {
+    if (dim != 2 && dim != 3) return fail(TP_ERR_UNSUPPORTED, "dim must be 2 or 3 (got %d)", dim);
+    if (B < 0 || N < 2 || (N & 1) || N > 4096)
+        return fail(TP_ERR_SHAPE, "box must be even, 2..4096 and B >= 0 (got N %d, B %d)", N, B);
+    if (B == 0) return ok();
+    if (!spec && !weight) return fail(TP_ERR_NULL, "spec or weight is required");
+    tp_status st;
+    if (spec && (st = check_complex(spec, "spec")) != TP_OK) return st;
+    if (weight && !aligned(weight, 4)) return fail(TP_ERR_ALIGN, "weight must be 4-byte aligned");
+    return launched(tp::launch_hermitian_x0(reinterpret_cast<float2 *>(spec), weight, B, N, dim,
+                                            static_cast<cudaStream_t>(stream), dbg_word()),
+                    "zero-axis symmetrisation");
 }
 
 unsigned tp_debug_bounds_word(int reset) {

@@ -52,4 +52,9 @@ cudaError_t launch_weight_grads(const Params &q, const float *omega, const float
                                 const float2 *D, float *grad_weights, float *grad_rot,
                                 cudaStream_t st);
 
+// The symmetrised kx = 0 plane (dim 3) or column (dim 2) of B stored
+// half-spectra of box M, complex V and / or real W (tp_hermitian.cu), in place.
+cudaError_t launch_hermitian_x0(float2 *V, float *W, int B, int M, int dim, cudaStream_t st,
+                                unsigned *dbg);
+
 }  // namespace tp

@@ -92,12 +92,39 @@ typedef enum {
 
 enum { TP_LINEAR = 0, TP_CUBIC = 1 };
 
+/*
+ * Option flags (tp_options.flags).
+ *
+ * TP_FLAG_HERMITIAN_X0: symmetrise the zero-frequency axis of an accumulated
+ * spectrum.  The pages' backward pass accumulates the contributions on the
+ * kx = 0 axis symmetrically, so that a Fourier coefficient of a real object
+ * and its conjugate partner are not counted twice with different values
+ * ([ar §2] Friedel symmetry, backward pass; [de §2 "Friedel-Symmetrie"]).
+ * They give no formula; this library takes the Hermitian part of the stored
+ * kx = 0 plane (3D) or column (2D) after the accumulation:
+ *   V(0, k) <- (V(0, k) + conj(V(0, -k))) / 2,  W(0, k) <- (W(0, k) + W(0, -k)) / 2
+ * with -k taken modulo the box in every stored axis (self-conjugate points
+ * keep their real part); every other coefficient is unchanged.  The whole
+ * plane is symmetrised, including what the output held before the call.
+ * Accepted by tp_backproject_2d_3d (data and weight spectra),
+ * tp_project_3d_2d_backward (grad_vol) and tp_project_2d_2d_backward
+ * (grad_img); other outputs of those calls are unaffected.  Without it
+ * (the default) the backward operators are the exact real adjoint of the
+ * forward on any input; with it they are the adjoint of the forward
+ * restricted to spectra of real objects (Hermitian on kx = 0), which the
+ * symmetrisation leaves unchanged.  The forward operators and
+ * tp_project_3d_2d_backward_saved reject it (TP_ERR_UNSUPPORTED), as does
+ * tp_backproject_2d_3d_backward: the gradients of a symmetrised
+ * backprojection are the plain ones at symmetrised upstream gradients
+ * (tp_hermitian_x0 applied to them; the symmetrisation is self-adjoint).
+ */
+#define TP_FLAG_HERMITIAN_X0 1u
 
 typedef struct {
     int interp;         /* TP_LINEAR or TP_CUBIC */
     float oversampling; /* s > 0: sample position p = s * R^T k */
     float radius;       /* cutoff in output-pixel frequency units; < 0 means N/2 */
-    unsigned flags;     /* reserved, must be 0 */
+    unsigned flags;     /* TP_FLAG_* bits where the operator accepts them, else 0 */
 } tp_options;
 
 /*
@@ -122,7 +149,8 @@ tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv,
  *   grad_vol    (Bv, Nv, Nv, Nv/2+1) complex, += adjoint applied to grad_out
  *   grad_rot    (Bp, P, 3, 3) float, += dL/dR (row 3 is always 0: k_z = 0)
  *   grad_shift  (Bs, P, 2) float, += dL/dshift; requires shift != NULL
- * Any of the three may be NULL.
+ * Any of the three may be NULL.  opts.flags may hold TP_FLAG_HERMITIAN_X0
+ * (applied to grad_vol after the accumulation).
  */
 tp_status tp_project_3d_2d_backward(const float *grad_out, const float *vol, int Bv, int Nv,
                                     const float *rot, int Bp, int P,
@@ -177,6 +205,8 @@ tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *ou
  * A direct tap adds w * conj(phase) * proj to data_vol[n]; a Friedel tap adds
  * the conjugate of that to data_vol[-n]; weight_vol gets w * weight at the
  * same location.  Bv is 1 (all batch elements add into one volume) or B.
+ * opts.flags may hold TP_FLAG_HERMITIAN_X0 (applied to both spectra after
+ * the accumulation).
  */
 tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, int P, int N,
                                const float *rot, int Bp, const float *shift, int Bs,
@@ -206,7 +236,7 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
  * other arguments are those of tp_backproject_2d_3d.  scratch: at least
  * tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, weight terms?) bytes
  * of device memory, 16-byte aligned, owned by the caller; workspace as for
- * the other 3D calls.
+ * the other 3D calls.  opts.flags must be 0 (see TP_FLAG_HERMITIAN_X0).
  */
 tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float *grad_weight_vol,
                                         const float *proj, const float *weights, int B, int P,
@@ -240,12 +270,25 @@ tp_status tp_project_2d_2d(const float *img, int Bi, int Ni,
  *   grad_img    (Bi, Ni, Ni/2+1) complex, +=
  *   grad_rot    (Bp, P, 2, 2) float, +=
  *   grad_shift  (Bs, P, 2) float, +=; requires shift != NULL
+ * opts.flags may hold TP_FLAG_HERMITIAN_X0 (applied to grad_img after the
+ * accumulation).
  */
 tp_status tp_project_2d_2d_backward(const float *grad_out, const float *img, int Bi, int Ni,
                                     const float *rot, int Bp, int P,
                                     const float *shift, int Bs, int N, tp_options opts,
                                     float *grad_img, float *grad_rot, float *grad_shift,
                                     void *stream);
+
+/*
+ * The symmetrisation of TP_FLAG_HERMITIAN_X0 on its own, in place, enqueued
+ * on `stream`: the kx = 0 plane (dim 3: spec (B, N, N, N/2+1)) or column
+ * (dim 2: spec (B, N, N/2+1)) of a complex spectrum and / or of a real
+ * weight spectrum of the same shape.  Either pointer may be NULL, not both;
+ * spec must be 8-byte aligned.  B == 0 does nothing.  Errors:
+ * TP_ERR_UNSUPPORTED for dim other than 2 or 3, TP_ERR_SHAPE for an odd box
+ * or one outside 2..4096, TP_ERR_NULL, TP_ERR_ALIGN.
+ */
+tp_status tp_hermitian_x0(float *spec, float *weight, int B, int N, int dim, void *stream);
 
 /*
  * Bytes of workspace the 3D entry points need for a volume batch Bv, batch

@@ -215,3 +215,52 @@ def test_binding_rejects_cpu_tensors(tp):
     rot = torch.eye(3).reshape(1, 1, 3, 3)
     with pytest.raises(ValueError, match="CUDA"):
         tp.tp_project_3d_2d(vol, rot)
+
+
+TP_FLAG_HERMITIAN_X0 = 1
+
+
+def test_hermitian_flag_acceptance(tp):
+    """TP_FLAG_HERMITIAN_X0 is accepted where a spectrum is accumulated and
+    refused by the forward calls, the saved-path backward and the
+    backprojection's backward; other bits are refused everywhere.  Every
+    call here stops at validation or has P == 0."""
+    assert tp.FLAG_HERMITIAN_X0 == TP_FLAG_HERMITIAN_X0
+    text = open(HEADER).read()
+    assert re.search(r"#define\s+TP_FLAG_HERMITIAN_X0\s+1u", text)
+    h = opts(tp, flags=TP_FLAG_HERMITIAN_X0)
+    assert proj3(tp, o=h) == TP_ERR_UNSUPPORTED
+    assert "TP_FLAG_HERMITIAN_X0" in tp.tp_last_error()
+    assert tp._fn("tp_project_2d_2d")(A, 1, 16, A, 1, 4, None, 1, 16, h, A, None) == TP_ERR_UNSUPPORTED
+    # accepted: the 3D and 2D backward (P == 0: nothing launched) and the backprojection
+    assert tp._fn("tp_project_3d_2d_backward")(A, A, 1, 16, A, 1, 0, None, 1, 16, h, A, A, None,
+                                               WS, WSB, None) == TP_OK
+    assert tp._fn("tp_project_2d_2d_backward")(A, A, 1, 16, A, 1, 0, None, 1, 16, h, A, A, None,
+                                               None) == TP_OK
+    assert tp._fn("tp_backproject_2d_3d")(A, None, 1, 0, 16, A, 1, None, 1, 1, 16, h, A, A, WS,
+                                          WSB, None) == TP_OK
+    # a validation error still wins over the accepted flag
+    assert tp._fn("tp_project_3d_2d_backward")(None, A, 1, 16, A, 1, 4, None, 1, 16, h, A, A,
+                                               None, WS, WSB, None) == TP_ERR_NULL
+    # refused
+    bad = opts(tp, flags=TP_FLAG_HERMITIAN_X0 | 2)
+    assert tp._fn("tp_project_3d_2d_backward")(A, A, 1, 16, A, 1, 0, None, 1, 16, bad, A, A, None,
+                                               WS, WSB, None) == TP_ERR_UNSUPPORTED
+    assert tp._fn("tp_project_3d_2d_backward_saved")(A, A, A, 1, 4, 16, 1, 1, h, A, None,
+                                                     None) == TP_ERR_UNSUPPORTED
+    assert tp._fn("tp_backproject_2d_3d_backward")(A, None, A, None, 2, 4, 16, A, 1, None, 1, 1,
+                                                   16, h, A, None, A, None, 0x40000, WSB, WS,
+                                                   WSB, None) == TP_ERR_UNSUPPORTED
+    assert "tp_hermitian_x0" in tp.tp_last_error()
+
+
+def test_hermitian_x0_validation(tp):
+    f = tp._fn("tp_hermitian_x0")
+    assert f(A, None, 1, 16, 4, None) == TP_ERR_UNSUPPORTED     # dim
+    assert f(A, None, 1, 15, 3, None) == TP_ERR_SHAPE           # odd box
+    assert f(A, None, 1, 8192, 3, None) == TP_ERR_SHAPE
+    assert f(A, None, -1, 16, 3, None) == TP_ERR_SHAPE
+    assert f(None, None, 1, 16, 3, None) == TP_ERR_NULL
+    assert f(MIS, None, 1, 16, 3, None) == TP_ERR_ALIGN
+    assert f(None, A + 2, 1, 16, 2, None) == TP_ERR_ALIGN
+    assert f(A, A, 0, 16, 3, None) == TP_OK                     # B == 0: nothing to do
