@@ -1038,10 +1038,9 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                         const int widx = base + kOPX * (kOWPY - kOS) * (packed >> 16) + toff_w;
                         if (TP_CHECK(q.dbg, idx >= 0 && idx + ZSTEP < kOElems, 4)) {
                             float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
-                            a0.x = fmaf(wt0, cur.x, a0.x);
-                            a0.y = fmaf(wt0, cur.y, a0.y);
-                            a1.x = fmaf(wt1, cur.x, a1.x);
-                            a1.y = fmaf(wt1, cur.y, a1.y);
+                            const float2 cv = make_float2(cur.x, cur.y);
+                            cfma(wt0, cv, a0);
+                            cfma(wt1, cv, a1);
                             acc[idx] = a0;
                             acc[idx + ZSTEP] = a1;
                         }
@@ -1198,8 +1197,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                             if (act && (!clash || grp == k) &&
                                 TP_CHECK(q.dbg, idx >= 0 && idx < kLElems, 4)) {
                                 float2 a = acc[idx];
-                                a.x = fmaf(wt, cur.x, a.x);
-                                a.y = fmaf(wt, cur.y, a.y);
+                                cfma(wt, make_float2(cur.x, cur.y), a);
                                 acc[idx] = a;
                                 if (WEIGHTS) wacc[idx] = fmaf(wt, cur.z, wacc[idx]);
                             }

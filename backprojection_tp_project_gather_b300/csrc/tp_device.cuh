@@ -161,9 +161,10 @@ __device__ __forceinline__ float2 cmul_conj_a(float2 a, float2 b) {  // conj(a) 
     return make_float2(a.x * b.x + a.y * b.y, a.x * b.y - a.y * b.x);
 }
 
+// acc += w v for a real weight and a complex value: one packed two-lane FMA
+// (both lanes fused, so the result equals two fmaf calls bit for bit).
 __device__ __forceinline__ void cfma(float w, float2 v, float2 &acc) {
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
+    acc = __ffma2_rn(make_float2(w, w), v, acc);
 }
 
 // Per-pose geometry, loaded once per thread block.
