@@ -622,19 +622,24 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
             ox[i] = (x >> 2) * 16 + (x & 3);
             oy[i] = (y >> 2) * (16 * H::PX / 4) + 4 * (y & 3);
         }
+        // The 16 (x, y) tap offsets are formed once; the four z layers add
+        // constants to them.
         const float2 *base = s + l[2] * (H::PX * H::PY);
+        int oxy[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) oxy[i] = oy[i >> 2] + ox[i & 3];
 #pragma unroll
         for (int jz = 0; jz < 4; ++jz) {
             float2 ay = make_float2(0.f, 0.f), ayx = ay, ayy = ay;
 #pragma unroll
             for (int sy = 0; sy < 4; ++sy) {
-                const float2 *row = base + jz * (H::PX * H::PY) + oy[sy];
                 float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
                 for (int sx = 0; sx < 4; ++sx) {
-                    const long long at = (row - s) + ox[sx];
+                    const int off = oxy[4 * sy + sx] + jz * (H::PX * H::PY);
+                    const long long at = (base - s) + off;
                     if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 2)) continue;
-                    const float2 val = row[ox[sx]];
+                    const float2 val = base[off];
                     cfma(wx[sx], val, r0);
                     if (DERIV) cfma(dx[sx], val, r1);
                 }
