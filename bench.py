@@ -121,10 +121,36 @@ def cpu_baseline(P, min_seconds):
         dt += time.perf_counter() - t0
         reps += 1
     samples = reps * P * w["box"] * (w["box"] // 2 + 1)
-    return {"value": samples / dt / 1e9, "unit": UNIT, "cores": oracle.num_threads(),
+    cores = oracle.num_threads()
+    # The same step on one thread, over a smaller leading subset of poses.
+    P1 = max(1, P // 32)
+    w1 = oracle_sample_workload(P1)
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle_step(w1, P1)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": samples / dt / 1e9, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} x {P} of the 512 poses of the box-256 step (fwd + L2 grad + bwd), "
-                      f"float64, {dt:.1f} s"}
+                      f"float64, {dt:.1f} s",
+            "single_thread": {"value": P1 * w1["box"] * (w1["box"] // 2 + 1) / dt1 / 1e9,
+                              "sample": f"{P1} poses, {dt1:.1f} s"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model():
+    """The host CPU's model name, from /proc/cpuinfo when there is one."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def run_reference(args):

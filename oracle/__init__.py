@@ -53,12 +53,19 @@ def _load():
             for f in (lib.oracle_project, lib.oracle_backproject, lib.oracle_project_backward):
                 f.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [i]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads for the oracle's later calls (for single-thread timing)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _c(a, dtype):

@@ -489,3 +489,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads for the oracle's later calls (n >= 1; the single-thread CPU figure). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
