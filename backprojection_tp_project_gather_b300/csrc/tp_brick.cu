@@ -536,45 +536,65 @@ __device__ __forceinline__ bool stored(int x, int y, int z, int half) {
 
 // Stage brick + halo of the virtual spectrum into shared memory.  Every
 // element is one 8-byte cp.async (zero-filled outside the stored range), so
-// all copies of the block are in flight at once; elements on the Friedel
-// side (n_x < 0) are conjugated in a second pass.
+// all copies of the block are in flight at once.  A thread keeps the same
+// (x, y) positions of the S x S layer in every z layer: whether its column
+// lies on the Friedel side (n_x < 0, read from -n), its source column and
+// its y row are fixed per brick, and each layer only adds the z row.  The
+// thread then conjugates its own Friedel-side elements once its copies have
+// landed.  Offsets within one stored spectrum fit 32 bits (the entry points
+// refuse larger spectra).
 template <bool CUBIC>
 __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X, const BrickBox &bx,
                                       float2 *s, unsigned *dbg) {
     using H = Halo<CUBIC>;
+    constexpr int L = H::S * H::S;                      // elements of one z layer
+    constexpr int SLOTS = (L + kThreads - 1) / kThreads;
     const int half = M >> 1;
     const int x0 = bx.o[0] - Stencil<CUBIC>::LO, y0 = bx.o[1] - Stencil<CUBIC>::LO,
               z0 = bx.o[2] - Stencil<CUBIC>::LO;
-    for (int e = threadIdx.x; e < H::S * H::S * H::S; e += kThreads) {
-        const int lx = e % H::S, ly = (e / H::S) % H::S, lz = e / (H::S * H::S);
-        int nx = x0 + lx, ny = y0 + ly, nz = z0 + lz;
-        if (nx < 0) {
-            nx = -nx;
-            ny = -ny;
-            nz = -nz;
+    const int MX = M * X;
+    const unsigned sbase = (unsigned)__cvta_generic_to_shared(s);
+    int at_xy[SLOTS], yoff[SLOTS];
+    bool live[SLOTS], cj[SLOTS], okxy[SLOTS];
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        const int j = threadIdx.x + k * kThreads;
+        live[k] = j < L;
+        const int lx = j % H::S, ly = j / H::S;
+        const int nx = x0 + lx, ny = y0 + ly;
+        cj[k] = nx < 0;
+        const int col = cj[k] ? -nx : nx, ys = cj[k] ? -ny : ny;
+        okxy[k] = live[k] && col <= half && row_ok(ys, half);
+        yoff[k] = wrap_row(ys, M) * X + col;
+        at_xy[k] = H::index(lx, ly, 0);
+    }
+    for (int lz = 0; lz < H::S; ++lz) {
+        const int nz = z0 + lz;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            if (!live[k]) continue;
+            const int zs = cj[k] ? -nz : nz;
+            const bool ok = okxy[k] && row_ok(zs, half);
+            const int off = ok ? wrap_row(zs, M) * MX + yoff[k] : 0;
+            const int at = at_xy[k] + lz * (H::PX * H::PY);
+            if (!TP_CHECK(dbg, off >= 0 && off < M * MX, 0)) continue;
+            if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(sbase + 8u * at),
+                         "l"(V + off), "r"(ok ? 8 : 0)
+                         : "memory");
         }
-        const bool ok = stored(nx, ny, nz, half);
-        const float2 *src = ok ? V + ((size_t)wrap_row(nz, M) * M + wrap_row(ny, M)) * X + nx : V;
-        const int at = H::index(lx, ly, lz);
-        if (!TP_CHECK(dbg, (size_t)(src - V) < (size_t)M * M * X, 0)) continue;
-        if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
-        const unsigned dst = (unsigned)__cvta_generic_to_shared(s + at);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src),
-                     "r"(ok ? 8 : 0)
-                     : "memory");
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    if (x0 < 0) {
-        __syncthreads();
-        const int nneg = min(-x0, H::S);   // staged columns lx < -x0 hold n_x < 0
-        for (int e = threadIdx.x; e < nneg * H::S * H::S; e += kThreads) {
-            const int lx = e % nneg, r = e / nneg;
-            const int ly = r % H::S, lz = r / H::S;
-            const int at = H::index(lx, ly, lz);
+    // The Friedel side holds conj(V[-n]): negate the imaginary parts this
+    // thread copied (zero-filled ones included, as the sign of zero is moot).
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        if (!live[k] || !cj[k]) continue;
+        for (int lz = 0; lz < H::S; ++lz) {
+            const int at = at_xy[k] + lz * (H::PX * H::PY);
             if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
-            float2 *p = s + at;
-            p->y = -p->y;
+            s[at].y = -s[at].y;
         }
     }
 }

@@ -61,13 +61,15 @@ def parse_args():
                     help="pose count (default: the workload's 512); smaller runs are for profiling")
     ap.add_argument("--workload", default="fwdbwd",
                     choices=["fwdbwd", "project", "rot2d", "backproject", "backproject-backward",
-                             "oversampling"],
+                             "oversampling", "hostlink"],
                     help="fwdbwd: the differentiable step (the headline, default); project: box-128 "
                          "cubic forward of 4096 poses (--oversampling 1 or 2); rot2d: 2D rotate + "
                          "shift of 1024 images at 128, forward and backward; backproject: "
                          "2048 images into a 256^3 data + weight spectrum; backproject-backward: "
                          "the gradients of that backprojection; oversampling: cubic at s = 1 "
-                         "against linear at s = 2 with the padding FFT, box 128, 4096 poses")
+                         "against linear at s = 2 with the padding FFT, box 128, 4096 poses; "
+                         "hostlink: pinned host <-> device copy bandwidth, the bound of the "
+                         "end-to-end figure")
     ap.add_argument("--interp", default="cubic", choices=["linear", "cubic"],
                     help="interpolation of the project and backproject workloads")
     ap.add_argument("--oversampling", type=int, default=1, choices=[1, 2],
@@ -786,6 +788,46 @@ def run_workload(args):
                               "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
                               "algorithmic_bytes_per_step": nbytes,
                               "timed": "whole call (binning + kernels)"})
+    elif args.workload == "hostlink":
+        # The copies of the end-to-end step (203 MB up, 68 MB down) at the
+        # link's own rates: one direction at a time, then both at once on two
+        # streams, as the pipelined step issues them.
+        up_b, down_b = 202921984, 67655680
+        h_up = torch.empty(up_b, dtype=torch.uint8).pin_memory()
+        d_up = torch.empty(up_b, dtype=torch.uint8, device=dev)
+        h_dn = torch.empty(down_b, dtype=torch.uint8).pin_memory()
+        d_dn = torch.empty(down_b, dtype=torch.uint8, device=dev)
+        s_up, s_dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+        def h2d(i):
+            d_up.copy_(h_up, non_blocking=True)
+
+        def d2h(i):
+            h_dn.copy_(d_dn, non_blocking=True)
+
+        def both(i):
+            cur = torch.cuda.current_stream()
+            s_up.wait_stream(cur)
+            s_dn.wait_stream(cur)
+            with torch.cuda.stream(s_up):
+                d_up.copy_(h_up, non_blocking=True)
+            with torch.cuda.stream(s_dn):
+                h_dn.copy_(d_dn, non_blocking=True)
+            cur.wait_stream(s_up)
+            cur.wait_stream(s_dn)
+        res = {}
+        for name, fn, nbytes in (("h2d", h2d, up_b), ("d2h", d2h, down_b),
+                                 ("both", both, up_b + down_b)):
+            ms, clocks = _timed(fn, args.steps, args.warmup, stream, flush)
+            t = float(ms.mean())
+            res[name] = {"ms": t, "GB_s": nbytes / (t * 1e-3) / 1e9}
+        fwd_bwd_samples = 512 * 256 * 129
+        line.update(metric="pinned host <-> device copy time of one end-to-end step's bytes",
+                    unit="ms", value=res["both"]["ms"], higher_is_better=False,
+                    ms_per_step=res["both"]["ms"], results=res, clocks=clocks,
+                    config={"workload": "hostlink-203MB-up-68MB-down",
+                            "e2e_bound_gsamples_s": fwd_bwd_samples / (res["both"]["ms"] * 1e-3)
+                            / 1e9})
     elif args.workload == "oversampling":
         c = synth.CONFIGS[3]
         M, P = c["box"], c["poses"]
