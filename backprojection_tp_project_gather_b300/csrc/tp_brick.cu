@@ -1114,16 +1114,17 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
 // pitches 10: the 8 taps of one sample fall into 8 distinct bank pairs).  A
 // round spreads four queued samples at once, the lanes of group g = lane / 8
 // taking the 8 taps of sample r + R g (R = rounds of the queue).  Samples R
-// slots apart rarely share a voxel; a round in which two of them do (found by
-// a warp match on the target words) is spread one sample at a time, so the
-// plain read-add-write never races.
+// slots apart rarely share a voxel; a round in which two of them do (their
+// octant coordinates, exchanged by shuffles, differ by less than 2 on every
+// axis) is spread one sample at a time, so the plain read-add-write never
+// races.
 constexpr int kLS = kOct + 1;               // octant + linear halo
 constexpr int kLPX = 10, kLPY = 10;         // x and y pitches of the tile
 constexpr int kLElems = kLS * kLPY * kLPX;  // complex words of the tile
 constexpr int kLQW = 9;                     // floats per queued weight row (odd)
 
 struct LinQueue {
-    float w[32][kLQW];   // per sample: the 8 tap weights wx wy wz (x fastest), unused
+    float w[32][kLQW];   // per sample: the 8 tap weights wx wy wz (x fastest), tile x | y << 8 | z << 16
     float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap
 };
 
@@ -1198,6 +1199,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         float *wq = Q.w[slot];
 #pragma unroll
                         for (int t = 0; t < 8; ++t) wq[t] = w[0][t & 1] * w[1][(t >> 1) & 1] * w[2][t >> 2];
+                        wq[8] = __int_as_float(l[0] | (l[1] << 8) | (l[2] << 16));
                         const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
                         Q.rec[slot] = make_float4(cv.x, cv.y, om,
                                                   __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
@@ -1210,14 +1212,14 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                         const bool act = sq < nq;
                         float wt = 0.f;
                         float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
-                        int idx = -1 - lane;   // unique for idle lanes
+                        int idx = 0, at = kFarAway;
                         if (act) {
                             wt = Q.w[sq][lane & 7];
+                            at = __float_as_int(Q.w[sq][8]);
                             cur = Q.rec[sq];
                             idx = __float_as_int(cur.w) + toff;
                         }
-                        const unsigned same = __match_any_sync(0xffffffffu, idx);
-                        const bool clash = __any_sync(0xffffffffu, __popc(same) > 1);
+                        const bool clash = stencils_meet<4, 3>(at, 8, 2);
                         for (int k = 0; k < 4; ++k) {
                             if (act && (!clash || grp == k) &&
                                 TP_CHECK(q.dbg, idx >= 0 && idx < kLElems, 4)) {

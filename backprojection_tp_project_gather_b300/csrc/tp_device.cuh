@@ -167,6 +167,32 @@ __device__ __forceinline__ void cfma(float w, float2 v, float2 &acc) {
     acc = __ffma2_rn(make_float2(w, w), v, acc);
 }
 
+// Do any two of the G samples of a spreading round share a tile word?  Lane
+// group g (lanes g * lanes .. g * lanes + lanes - 1) holds its sample's tile
+// coordinates packed one per byte (x | y << 8 | z << 16), or kFarAway when
+// it has no sample; two stencils of `taps` taps per axis meet iff the
+// coordinates differ by less than `taps` on every axis.  The groups'
+// coordinates are exchanged with shuffles, which cost far less than a warp
+// match on the tap words.  Call with the whole warp.
+constexpr int kFarAway = 0x00404040;
+
+template <int G, int AXES>
+__device__ __forceinline__ bool stencils_meet(int mine, int lanes, int taps) {
+    bool meet = false;
+#pragma unroll
+    for (int k = 1; k < G; ++k) {
+        const int other = __shfl_xor_sync(0xffffffffu, mine, k * lanes);
+        bool all = mine != kFarAway;
+#pragma unroll
+        for (int a = 0; a < AXES; ++a) {
+            const int d = ((mine >> (8 * a)) & 0xff) - ((other >> (8 * a)) & 0xff);
+            all = all && d < taps && d > -taps;
+        }
+        meet = meet || all;
+    }
+    return __any_sync(0xffffffffu, meet);
+}
+
 // Per-pose geometry, loaded once per thread block.
 template <int D>
 struct Pose {
