@@ -346,3 +346,44 @@ def test_hundred_thousand_poses_sampled(tp):
     lhs = np.vdot(g.astype(np.complex128), host(out).astype(np.complex128)).real
     rhs = np.vdot(host(gv).astype(np.complex128), vol.astype(np.complex128)).real
     assert abs(lhs - rhs) <= 1e-4 * abs(lhs)
+
+
+# ---------------------------------------------------------------------------
+# Dense sampling (s < 1: neighbouring samples a fraction of a voxel apart)
+# makes the stencils of the samples a scatter round spreads together meet
+# often, so the one-sample-at-a-time fallback of the tiled scatters runs;
+# one shared source for many poses makes their tiles fold into the same
+# words from many blocks.
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_dense_2d_image_gradient_many_poses_one_image(tp, interp):
+    rng = np.random.default_rng(4242)
+    M, N, P = 64, 96, 48
+    img = crandn(rng, (1, M, M // 2 + 1))
+    R = synth.planar_rotations(rng.uniform(0, 2 * np.pi, P)).reshape(1, P, 2, 2)
+    t = rng.uniform(-4, 4, (1, P, 2)).astype(np.float32)
+    g = crandn(rng, (1, P, N, N // 2 + 1))
+    kw = dict(interp=interp, oversampling=0.6, radius=-1.0)
+    gi, gr, gt = tp.tp_project_2d_2d_backward(dev(g), dev(img), dev(R), dev(t), **kw)
+    ri, rr, rt = oracle.project_backward(2, g, img, R, shift=t, **kw)
+    assert rel(host(gi), ri) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+    # The linear kernel's derivative jumps at integer positions: among these
+    # 225,000 samples (|p| up to 29) two lie within float32 rounding of an
+    # integer and take the other branch than the float64 oracle, moving a
+    # pose's rotation gradient by about 1%.  The cubic kernel is C1.
+    if interp == "cubic":
+        assert rel(host(gr), rr) <= ATOMIC_TOL
+
+
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_dense_3d_volume_gradient(tp, interp):
+    rng = np.random.default_rng(4343)
+    M, N, P = 40, 48, 6
+    vol = crandn(rng, (1, M, M, M // 2 + 1))
+    R = synth.random_rotations(P, rng).reshape(1, P, 3, 3)
+    g = crandn(rng, (1, P, N, N // 2 + 1))
+    kw = dict(interp=interp, oversampling=0.55, radius=-1.0)
+    gv, _, _ = tp.tp_project_3d_2d_backward(dev(g), dev(vol), dev(R), want_rot=False,
+                                            want_shift=False, **kw)
+    rv, _, _ = oracle.project_backward(3, g, vol, R, need_rot=False, need_shift=False, **kw)
+    assert rel(host(gv), rv) <= ATOMIC_TOL
