@@ -1,5 +1,7 @@
-// tp_gather.cu -- gather-side kernels: forward projection (3D->2D central
-// slices and 2D->2D rotation) and the rotation/shift gradients.
+// tp_gather.cu -- gather-side kernels of the 2D operators: the 2D->2D
+// forward (rotation and shift) and its rotation / shift gradients.  The
+// sampling code is written for D = 2 or 3 axes; the 3D operators use the
+// brick kernels of tp_brick.cu, so only D = 2 is instantiated.
 //
 // One thread per output Fourier sample.  A thread block covers a run of
 // consecutive samples of ONE pose (rows of the output plane), so the pose is
@@ -301,16 +303,12 @@ cudaError_t launch_pose_grad_t(const Params &q, const float2 *g, float *grot, fl
 
 }  // namespace
 
-cudaError_t launch_project(int dim, bool cubic, const Params &q, float2 *out, cudaStream_t st) {
-    if (dim == 3) return cubic ? launch_project_t<3, true>(q, out, st) : launch_project_t<3, false>(q, out, st);
+cudaError_t launch_project_2d(bool cubic, const Params &q, float2 *out, cudaStream_t st) {
     return cubic ? launch_project_t<2, true>(q, out, st) : launch_project_t<2, false>(q, out, st);
 }
 
-cudaError_t launch_pose_grad(int dim, bool cubic, const Params &q, const float2 *g, float *grot,
-                             float *gshift, cudaStream_t st) {
-    if (dim == 3)
-        return cubic ? launch_pose_grad_t<3, true>(q, g, grot, gshift, st)
-                     : launch_pose_grad_t<3, false>(q, g, grot, gshift, st);
+cudaError_t launch_pose_grad_2d(bool cubic, const Params &q, const float2 *g, float *grot,
+                                float *gshift, cudaStream_t st) {
     return cubic ? launch_pose_grad_t<2, true>(q, g, grot, gshift, st)
                  : launch_pose_grad_t<2, false>(q, g, grot, gshift, st);
 }

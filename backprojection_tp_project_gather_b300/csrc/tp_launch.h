@@ -7,18 +7,20 @@
 
 namespace tp {
 
-// Forward projection into out (overwritten).  dim = 2 or 3.
-cudaError_t launch_project(int dim, bool cubic, const Params &q, float2 *out, cudaStream_t st);
+// 2D operators (the 3D ones are the brick kernels below).
+// Forward 2D -> 2D projection into out (overwritten) (tp_gather.cu).
+cudaError_t launch_project_2d(bool cubic, const Params &q, float2 *out, cudaStream_t st);
 
-// dL/dR (rows 0 and 1) and dL/dshift, accumulated with atomics.
-cudaError_t launch_pose_grad(int dim, bool cubic, const Params &q, const float2 *grad_out,
-                             float *grad_rot, float *grad_shift, cudaStream_t st);
+// dL/dR (rows 0 and 1) and dL/dshift of the 2D forward, accumulated with
+// atomics (tp_gather.cu).
+cudaError_t launch_pose_grad_2d(bool cubic, const Params &q, const float2 *grad_out,
+                                float *grad_rot, float *grad_shift, cudaStream_t st);
 
-// Adjoint scatter of img (same layout as a forward output) into dst (+=),
-// and of w * omega into wdst (+=) when wdst is not null.  q.src / q.Bsrc
-// describe the DESTINATION spectrum here (its batch and box).
-cudaError_t launch_scatter(int dim, bool cubic, const Params &q, const float2 *img,
-                           const float *omega, float2 *dst, float *wdst, cudaStream_t st);
+// Adjoint scatter of img (same layout as a forward output) into the 2D
+// spectrum dst (+=) (tp_scatter.cu).  q.src / q.Bsrc describe the
+// DESTINATION spectrum here (its batch and box).
+cudaError_t launch_scatter_2d(bool cubic, const Params &q, const float2 *img, float2 *dst,
+                              cudaStream_t st);
 
 // 3D brick-binned kernels (tp_brick.cu): forward, pose gradients and
 // scatter.  ws is the caller's workspace of brick_workspace_bytes() bytes.
