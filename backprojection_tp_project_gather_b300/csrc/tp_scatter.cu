@@ -29,10 +29,10 @@ namespace {
 // [a b], each row's qx interval from the two slab constraints, a warp
 // prefix sum packing the candidates into 32-lane rounds), queues the owned
 // ones and spreads them into a private tile with plain read-add-write: tap
-// lanes (jx, jy), several samples per round, one at a time in a round where
-// two of them share a word (found by a warp match).  The tile
-// is then added to the stored half-spectrum with one vector atomic per
-// touched word (Friedel positions conjugated at -n).
+// lanes (jx, jy); linear spreads several samples per round, one at a time
+// in a round where two of their stencils meet (stencils_meet).  The tile is
+// then added to the stored half-spectrum with one vector atomic per touched
+// word (Friedel positions conjugated at -n).
 constexpr int kTile = 16;
 constexpr int kTileWarps = 4;
 constexpr float kTileMargin = 0.01f;
