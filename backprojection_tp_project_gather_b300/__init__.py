@@ -4,7 +4,9 @@ Argument marshalling only: every function checks tensor types, derives the
 sizes the C ABI asks for, allocates outputs with PyTorch when the caller
 passes none, and calls the ``tp_*`` entry point of the same name on the
 current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there
-is no CPU path, and importing this package fails if the library is missing.
+is no CPU path, and every call raises ImportError while the library file is
+missing (the package itself imports without it, so that its build module can
+run on a fresh checkout).
 
 Layouts follow ``include/tp.h``: spectra are complex64 half-spectra in
 ``torch.fft.rfftn`` order, rotations float32 ``(Bp, P, d, d)``, shifts float32
@@ -34,10 +36,6 @@ LIB_PATH = os.path.join(_HERE, "libtp_b300_debug.so" if os.environ.get("TP_B300_
 LINEAR, CUBIC = 0, 1
 FLAG_HERMITIAN_X0 = 1   # TP_FLAG_HERMITIAN_X0: symmetrised kx = 0 axis of accumulated spectra
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(
-        f"{LIB_PATH} is missing: build it with "
-        "`python -m backprojection_tp_project_gather_b300.build` (nvcc, sm_103a)")
 
 
 class TPOptions(ctypes.Structure):
@@ -51,7 +49,23 @@ class TPError(RuntimeError):
         self.status = status
 
 
-_lib = ctypes.CDLL(LIB_PATH)
+_lib = None
+
+
+def _library() -> ctypes.CDLL:
+    """Load the library on first use.  The package itself imports without
+    it, so that its build module can run on a fresh checkout; every call
+    into the library fails loudly while the file is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m backprojection_tp_project_gather_b300.build` (nvcc, sm_103a)")
+        _lib = ctypes.CDLL(LIB_PATH)
+    return _lib
+
+
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
     "tp_project_3d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _Z, _P],
@@ -84,7 +98,7 @@ def _fn(name):
     rebuild can run while an older library is on disk)."""
     f = _bound.get(name)
     if f is None:
-        f = getattr(_lib, name)
+        f = getattr(_library(), name)
         if name in _SIGS:
             f.argtypes = _SIGS[name]
         f.restype = _RESTYPES.get(name, ctypes.c_int)
@@ -94,7 +108,7 @@ def _fn(name):
 
 def lib() -> ctypes.CDLL:
     """The loaded ctypes handle of libtp_b300.so."""
-    return _lib
+    return _library()
 
 
 def tp_last_error() -> str:

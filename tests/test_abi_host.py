@@ -264,3 +264,29 @@ def test_hermitian_x0_validation(tp):
     assert f(MIS, None, 1, 16, 3, None) == TP_ERR_ALIGN
     assert f(None, A + 2, 1, 16, 2, None) == TP_ERR_ALIGN
     assert f(A, A, 0, 16, 3, None) == TP_OK                     # B == 0: nothing to do
+
+
+def test_package_imports_without_the_library_and_calls_fail_loudly(tmp_path):
+    """On a fresh checkout the library file does not exist yet: the package
+    (and its build module) must import, so that the build can run, while
+    every call into the library raises ImportError."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "backprojection_tp_project_gather_b300")
+    dst = tmp_path / "backprojection_tp_project_gather_b300"
+    dst.mkdir()
+    for name in os.listdir(src):
+        if name.endswith(".py"):
+            shutil.copy(os.path.join(src, name), dst / name)
+    code = ("import backprojection_tp_project_gather_b300 as tp\n"
+            "import backprojection_tp_project_gather_b300.build as b\n"
+            "assert b.LIB.endswith('libtp_b300.so')\n"
+            "try:\n"
+            "    tp.tp_version()\n"
+            "except ImportError as e:\n"
+            "    assert 'is missing' in str(e)\n"
+            "    print('loud')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True,
+                       env=dict(os.environ, PYTHONPATH=str(tmp_path)), timeout=300)
+    assert r.returncode == 0 and "loud" in r.stdout, r.stdout + r.stderr
