@@ -41,6 +41,8 @@
 // Library for PyTorch", 3D->2D projection and 2D->3D backprojection
 // [it §2 "Operazioni Supportate"; de §2 "Unterstützte Operationen"] with the
 // weight spectrum [de §2 "Dual-Volumen-Ansatz"].
+#include <cstddef>
+
 #include "tp_device.cuh"
 #include "tp_launch.h"
 
@@ -87,6 +89,11 @@ struct PoseGeo {
     int degenerate;     // a and b (nearly) parallel: no pseudo-inverse
 };
 constexpr int kGeoWords = sizeof(PoseGeo) / 4;
+// In the workspace a pose's geometry is a record of kGeoVec 16-byte words
+// (the PoseGeo words, then zeros), so one warp-uniform record load is
+// kGeoVec 128-bit loads.
+constexpr int kGeoVec = (kGeoWords + 3) / 4;
+constexpr int kGeoReach = offsetof(PoseGeo, reach) / 4;   // word of reach in the record
 
 // What the brick-mask pass needs of a pose, with the plane's extents over a
 // brick precomputed: the brick half-size is kBS/2 plus the margin on every
@@ -109,7 +116,7 @@ struct Scratch {
     unsigned *key;        // BinKey of the binning held in the workspace
     unsigned *changed;    // set by k_pose_geometry when key or geometry differ
     unsigned *counters;   // [4][Bsrc]: work counters of the three main kernels, unit counts
-    PoseGeo *geo;         // B*P poses
+    int4 *geo;            // B*P pose records of kGeoVec words
     ReachGeo *reach;      // B*P poses, for the brick-mask pass
     unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
     int *hits;            // [Bsrc][bricks] reaching poses per brick
@@ -321,24 +328,47 @@ __global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratc
         rg.r = make_float4(g.reach * g.reach, g.degenerate ? 1.f : 0.f, 0.f, 0.f);
         sc.reach[id] = rg;
     }
-    const int *now = reinterpret_cast<const int *>(&g);
-    int *held = reinterpret_cast<int *>(sc.geo + id);
+    int now[4 * kGeoVec];
+    const int *gw = reinterpret_cast<const int *>(&g);
+#pragma unroll
+    for (int k = 0; k < 4 * kGeoVec; ++k) now[k] = k < kGeoWords ? gw[k] : 0;
+    int4 *rec = sc.geo + (size_t)kGeoVec * id;
     bool same = true;
 #pragma unroll
-    for (int k = 0; k < kGeoWords; ++k) same = same && held[k] == now[k];
+    for (int j = 0; j < kGeoVec; ++j) {
+        const int4 h = rec[j];
+        same = same && h.x == now[4 * j] && h.y == now[4 * j + 1] && h.z == now[4 * j + 2] &&
+               h.w == now[4 * j + 3];
+    }
     if (!same) {
-        sc.geo[id] = g;
+#pragma unroll
+        for (int j = 0; j < kGeoVec; ++j)
+            rec[j] = make_int4(now[4 * j], now[4 * j + 1], now[4 * j + 2], now[4 * j + 3]);
         atomicOr(sc.changed, 1u);
     }
 }
 
-__device__ __forceinline__ PoseGeo load_geo(const PoseGeo *p) {
+// Pose pid's record (kGeoVec 128-bit loads) as a PoseGeo.
+__device__ __forceinline__ PoseGeo load_geo(const int4 *geo, int pid) {
+    const int4 *rec = geo + (size_t)kGeoVec * pid;
+    int w[4 * kGeoVec];
+#pragma unroll
+    for (int j = 0; j < kGeoVec; ++j) {
+        const int4 v = __ldg(rec + j);
+        w[4 * j] = v.x;
+        w[4 * j + 1] = v.y;
+        w[4 * j + 2] = v.z;
+        w[4 * j + 3] = v.w;
+    }
     PoseGeo g;
-    const int *src = reinterpret_cast<const int *>(p);
     int *dst = reinterpret_cast<int *>(&g);
 #pragma unroll
-    for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+    for (int k = 0; k < kGeoWords; ++k) dst[k] = w[k];
     return g;
+}
+
+__device__ __forceinline__ float geo_reach(const int4 *geo, int pid) {
+    return __ldg(reinterpret_cast<const float *>(geo + (size_t)kGeoVec * pid) + kGeoReach);
 }
 
 // Bit l of mask (volume, brick, chunk) = pose 32*chunk + l of the volume's
@@ -513,9 +543,11 @@ __device__ __forceinline__ int load_batch(const Params &q, const Scratch &sc, in
             const int at = t.base[i] + __popc(m & ((1u << lane) - 1u));
             const int pid = pose_id(q, v, (c + i) * 32 + lane);
             if (!TP_CHECK(q.dbg, at < kUnitPoses && pid >= 0 && pid < q.B * q.P, 8)) continue;
-            const int *src = reinterpret_cast<const int *>(sc.geo + pid);
+            const PoseGeo g = load_geo(sc.geo, pid);
+            const int *src = reinterpret_cast<const int *>(&g);
             int *dst = reinterpret_cast<int *>(&t.pose[at]);
-            for (int k = 0; k < kGeoWords; ++k) dst[k] = __ldg(src + k);
+#pragma unroll
+            for (int k = 0; k < kGeoWords; ++k) dst[k] = src[k];
         }
     }
     __syncthreads();
@@ -734,7 +766,7 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
 // outside it (all their taps lie outside the stored range).  dout, when
 // given, receives the matching zeros (three complex values per pixel).  The
 // rows are shared out over the nwarps warps of the grid.
-__device__ __forceinline__ void zero_unowned(const Params &q, int G, const PoseGeo *__restrict__ geo,
+__device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 *__restrict__ geo,
                                              float2 *__restrict__ out, float2 *__restrict__ dout,
                                              long long warp, long long nwarps) {
     const long long rows = (long long)q.B * q.P * q.N;
@@ -752,8 +784,8 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const PoseG
         for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
         if (dout)
             for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
-        if (xcut >= 0 && __ldg(&geo[bp].reach) >= (float)G - 0.5f) {
-            const PoseGeo g = load_geo(geo + bp);
+        if (xcut >= 0 && geo_reach(geo, bp) >= (float)G - 0.5f) {
+            const PoseGeo g = load_geo(geo, bp);
             for (int x = lane; x <= xcut; x += 32) {
                 bool outside = false;
 #pragma unroll
@@ -1004,7 +1036,7 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
             for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
                 const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
                 if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
-                const PoseGeo g = load_geo(sc.geo + pid);
+                const PoseGeo g = load_geo(sc.geo, pid);
                 if (!pose_reaches(g, ob)) continue;
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
@@ -1180,7 +1212,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
             for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
                 const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
                 if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
-                const PoseGeo g = load_geo(sc.geo + pid);
+                const PoseGeo g = load_geo(sc.geo, pid);
                 if (!pose_reaches(g, ob)) continue;
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
@@ -1286,7 +1318,7 @@ Layout layout(const Params &q, bool cubic) {
     L.nchunks = (int)((Pv + 31) / 32);
     L.counters = 256;                                         // key and flag first
     L.geo = L.counters + align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);
-    L.reach = L.geo + align256(sizeof(PoseGeo) * (size_t)q.B * q.P);
+    L.reach = L.geo + align256(sizeof(int4) * kGeoVec * (size_t)q.B * q.P);
     L.masks = L.reach + align256(sizeof(ReachGeo) * (size_t)q.B * q.P);
     L.hits = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.units = L.hits + align256(sizeof(int) * (size_t)q.Bsrc * nbr);
@@ -1300,7 +1332,7 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.key = reinterpret_cast<unsigned *>(base);
     sc.changed = sc.key + kKeyWords;
     sc.counters = reinterpret_cast<unsigned *>(base + L.counters);
-    sc.geo = reinterpret_cast<PoseGeo *>(base + L.geo);
+    sc.geo = reinterpret_cast<int4 *>(base + L.geo);
     sc.reach = reinterpret_cast<ReachGeo *>(base + L.reach);
     sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
     sc.hits = reinterpret_cast<int *>(base + L.hits);
