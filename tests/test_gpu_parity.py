@@ -355,6 +355,34 @@ def test_hundred_thousand_poses_sampled(tp):
 # one shared source for many poses makes their tiles fold into the same
 # words from many blocks.
 @pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_degenerate_2d_matrices(tp, interp):
+    """2D matrices without an inverse, for which the tiled image gradient
+    enumerates every row: the zero matrix, parallel rows, a zero second and
+    a zero first row, plus a rotation scaled by 3 (most samples outside the
+    stored range)."""
+    rng = np.random.default_rng(27)
+    M = N = 24
+    img = crandn(rng, (2, M, M // 2 + 1))
+    c, s_ = np.cos(0.7), np.sin(0.7)
+    R = np.array([[[0, 0], [0, 0]],
+                  [[c, s_], [0.7 * c, 0.7 * s_]],
+                  [[c, s_], [0, 0]],
+                  [[0, 0], [-s_, c]],
+                  [[3 * c, 3 * s_], [-3 * s_, 3 * c]]], np.float32)
+    R = np.stack([R, R[::-1]])                      # (2, 5, 2, 2): both images, other order
+    t = rng.uniform(-4, 4, (2, 5, 2)).astype(np.float32)
+    g = crandn(rng, (2, 5, N, N // 2 + 1))
+    kw = dict(interp=interp)
+    out = host(tp.tp_project_2d_2d(dev(img), dev(R), dev(t), **kw))
+    assert rel(out, oracle.project(2, img, R, shift=t, **kw)) <= FWD_TOL
+    gi, gr, gt = tp.tp_project_2d_2d_backward(dev(g), dev(img), dev(R), dev(t), **kw)
+    ri, rr, rt = oracle.project_backward(2, g, img, R, shift=t, **kw)
+    assert rel(host(gi), ri) <= ATOMIC_TOL
+    assert rel(host(gr), rr) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+
+
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
 def test_dense_2d_image_gradient_many_poses_one_image(tp, interp):
     rng = np.random.default_rng(4242)
     M, N, P = 64, 96, 48
