@@ -138,7 +138,11 @@ def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic"):
 def _workspace(ws, Bv, B, P, Nv, interp, device):
     need = tp_workspace_bytes(Bv, B, P, Nv, interp)
     if ws is None:
+        # A block fresh from the caching allocator may hold an old workspace
+        # of the same shape; clearing its first 256 bytes (the key of the
+        # binning kept there) makes the library recompute the binning.
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+        ws[:256].zero_()
     if ws.device.type != "cuda" or not ws.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
     nbytes = ws.numel() * ws.element_size()

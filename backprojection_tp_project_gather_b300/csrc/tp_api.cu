@@ -32,13 +32,7 @@ __global__ void k_check_selftest(unsigned *dbg, int bit) { (void)TP_CHECK(dbg, b
 unsigned *dbg_word() { return nullptr; }
 #endif
 
-tp_status fail(tp_status st, const char *fmt, ...) {
-    va_list ap;
-    va_start(ap, fmt);
-    vsnprintf(g_err, sizeof g_err, fmt, ap);
-    va_end(ap);
-    return st;
-}
+using tp::fail;
 
 tp_status ok() {
     g_err[0] = '\0';
@@ -213,6 +207,18 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
 }
 
 }  // namespace
+
+namespace tp {
+
+tp_status fail(tp_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+}  // namespace tp
 
 extern "C" {
 

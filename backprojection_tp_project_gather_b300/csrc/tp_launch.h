@@ -3,9 +3,14 @@
 
 #include <cuda_runtime.h>
 
+#include "../../include/tp.h"
 #include "tp_device.cuh"
 
 namespace tp {
+
+// Record the calling thread's failure message (read back by tp_last_error)
+// and return st; every entry point reports its failures through this.
+tp_status fail(tp_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 
 // 2D operators (the 3D ones are the brick kernels below).
 // Forward 2D -> 2D projection into out (overwritten) (tp_gather.cu).

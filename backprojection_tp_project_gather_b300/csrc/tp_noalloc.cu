@@ -18,13 +18,16 @@
 //    scratch and must be serialised by the caller;
 //  - the first call on each device looks the array's address up (set-up
 //    below), which can load the module; make that first call before any
-//    stream capture.
+//    stream capture;
+//  - the address is kept for the life of the process, so after a
+//    cudaDeviceReset() of a device this entry point must not be called on
+//    that device again.
 #include <cuda_runtime.h>
 
-#include <cstdio>
 #include <mutex>
 
 #include "../../include/tp.h"
+#include "tp_launch.h"
 
 namespace {
 
@@ -71,20 +74,16 @@ tp_status tp_project_3d_2d_noalloc(const float *vol, int Bv, int Nv, const float
     int B = Bv > Bp ? Bv : Bp;
     if (shift && Bs > B) B = Bs;
     const size_t need = tp_workspace_bytes(Bv, B, P, Nv, opts);
-    if (need > kMaxScratch) {
-        fprintf(stderr,
-                "tp_project_3d_2d_noalloc: this problem needs %zu bytes of scratch, the fixed "
-                "array holds %zu; use tp_project_3d_2d with a workspace\n",
-                need, kMaxScratch);
-        return TP_ERR_SHAPE;
-    }
+    if (need > kMaxScratch)
+        return tp::fail(TP_ERR_SHAPE,
+                        "tp_project_3d_2d_noalloc: this problem needs %zu bytes of scratch, the "
+                        "fixed array holds %zu; use tp_project_3d_2d with a workspace",
+                        need, kMaxScratch);
     void *scratch = nullptr;
     const cudaError_t e = scratch_address(&scratch);
-    if (e != cudaSuccess) {
-        fprintf(stderr, "tp_project_3d_2d_noalloc: scratch set-up failed: %s\n",
-                cudaGetErrorString(e));
-        return TP_ERR_CUDA;
-    }
+    if (e != cudaSuccess)
+        return tp::fail(TP_ERR_CUDA, "tp_project_3d_2d_noalloc: scratch set-up failed: %s",
+                        cudaGetErrorString(e));
     // Same validation, kernels and error reporting as tp_project_3d_2d.
     return tp_project_3d_2d(vol, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, out, scratch,
                             kMaxScratch, stream);

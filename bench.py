@@ -415,7 +415,7 @@ def run_ours(args):
     grad_rot = torch.zeros_like(rot)
     grad_shift = torch.zeros_like(shift)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    ws = torch.empty(tp.tp_workspace_bytes(1, 1, P, N, w["interp"]), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(tp.tp_workspace_bytes(1, 1, P, N, w["interp"]), dtype=torch.uint8, device=dev)
     kw["workspace"] = ws
     stream = torch.cuda.current_stream()
 
@@ -670,7 +670,7 @@ def run_workload(args):
         rot = torch.from_numpy(w["rot"]).to(dev)
         out = torch.empty((1, P, N, N // 2 + 1), dtype=torch.complex64, device=dev)
         kw = dict(N=N, interp=args.interp, oversampling=float(s), radius=w["radius"])
-        ws = torch.empty(tp.tp_workspace_bytes(1, 1, P, vol.shape[1], args.interp),
+        ws = torch.zeros(tp.tp_workspace_bytes(1, 1, P, vol.shape[1], args.interp),
                          dtype=torch.uint8, device=dev)
         rots = [rot, rot + 1e-4]          # new poses every step: the binning re-runs
 
@@ -741,7 +741,7 @@ def run_workload(args):
         rot = torch.from_numpy(w["rot"]).to(dev)
         kw = dict(interp=args.interp, oversampling=1.0, radius=w["radius"])
         shape = (1, N, N, N // 2 + 1)
-        ws = torch.empty(tp.tp_workspace_bytes(1, 1, n, N, args.interp), dtype=torch.uint8,
+        ws = torch.zeros(tp.tp_workspace_bytes(1, 1, n, N, args.interp), dtype=torch.uint8,
                          device=dev)
         vol_bytes = 8 * N * N * (N // 2 + 1)
         cfg = {"workload": f"backproject-box{N}-{n}img-{args.interp}", "box": N, "images": n,
@@ -837,8 +837,8 @@ def run_workload(args):
         rot = torch.from_numpy(synth.random_rotations(P, r_rot)[None]).to(dev)
         radius = c["radius"]
         out = torch.empty((1, P, M, M // 2 + 1), dtype=torch.complex64, device=dev)
-        ws1 = torch.empty(tp.tp_workspace_bytes(1, 1, P, M, "cubic"), dtype=torch.uint8, device=dev)
-        ws2 = torch.empty(tp.tp_workspace_bytes(1, 1, P, 2 * M, "linear"), dtype=torch.uint8,
+        ws1 = torch.zeros(tp.tp_workspace_bytes(1, 1, P, M, "cubic"), dtype=torch.uint8, device=dev)
+        ws2 = torch.zeros(tp.tp_workspace_bytes(1, 1, P, 2 * M, "linear"), dtype=torch.uint8,
                           device=dev)
         big = torch.zeros((2 * M,) * 3, dtype=torch.float32, device=dev)
         o = M // 2

@@ -58,12 +58,16 @@
  * Workspace.  The 3D entry points bin poses against bricks of the volume in
  * a scratch area the caller provides: `workspace` must point to at least
  * tp_workspace_bytes(...) bytes of device memory, 16-byte aligned, owned by
- * the caller.  Its contents need no initialisation.  A call that finds in it
- * the binning of identical poses and sizes (compared on the device, bit for
- * bit: for example the backward call after the forward call of one step)
- * keeps the brick masks and work units instead of recomputing them; any
- * difference, or a fresh workspace, recomputes them.  It must not be used by
- * two calls that can run at the same time (one workspace per stream).
+ * the caller.  A call that finds in it the binning of identical poses and
+ * sizes (its key and the pose records compared on the device, bit for bit:
+ * for example the backward call after the forward call of one step) keeps
+ * the brick masks and work units stored there instead of recomputing them;
+ * any difference recomputes them.  So the first 256 bytes of a workspace
+ * that is new to the library, or whose memory served anything else since
+ * its last call, must be zero (the rest needs no initialisation): memory
+ * recycled by an allocator can hold the key and poses of an old workspace
+ * but other data in its masks.  It must not be used by two calls that can
+ * run at the same time (one workspace per stream).
  *
  * Errors.  Each call returns a tp_status.  Argument errors are detected
  * before anything is enqueued; TP_ERR_CUDA reports a launch failure.  No
@@ -306,11 +310,13 @@ size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts);
  * those of tp_project_3d_2d.  The scratch lives in a fixed 16 MiB array in
  * the library's device memory, reserved on every GPU that loads the
  * library until the process exits; problems needing more scratch than that
- * (tp_workspace_bytes) fail with TP_ERR_SHAPE and a message on stderr.
+ * (tp_workspace_bytes) fail with TP_ERR_SHAPE (tp_last_error says why).
  * All calls share the array: calls that can overlap on the GPU race and
  * must be serialised by the caller.  The first call on each device looks
  * the array up (and may load the module); make it before any stream
- * capture.  No memory is allocated.
+ * capture.  The address found then is kept for the life of the process:
+ * after cudaDeviceReset() of a device, do not call this entry point on that
+ * device again.  No memory is allocated.
  */
 tp_status tp_project_3d_2d_noalloc(const float *vol, int Bv, int Nv,
                                    const float *rot, int Bp, int P,

@@ -46,7 +46,7 @@ def test_step_in_a_cuda_graph(tp):
     D = torch.empty(tuple(target.shape) + (3,), dtype=torch.complex64, device=dev)
     g = torch.empty_like(target)
     gv, gr, gs = torch.zeros_like(vol), torch.zeros_like(rot), torch.zeros_like(shift)
-    ws = torch.empty(tp.tp_workspace_bytes(1, 1, P, M, "cubic"), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(tp.tp_workspace_bytes(1, 1, P, M, "cubic"), dtype=torch.uint8, device=dev)
 
     def step():
         tp.tp_project_3d_2d_save(vol, rot, shift, out=y, dout=D, workspace=ws, **kw)

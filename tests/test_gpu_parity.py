@@ -252,6 +252,73 @@ def test_cfg4_backprojection_subset(tp, interp):
     assert rel(host(wt), rw) <= ATOMIC_TOL
 
 
+def _central(a, half):
+    """The entries of a (…, M, M, M/2+1) spectrum with |n_y|, |n_z| < half and n_x < half:
+    the bricks every pose reaches, whose work is split over the most work units."""
+    M = a.shape[-2]
+    rows = np.r_[0:half, M - half + 1:M]
+    return a[..., rows[:, None, None], rows[None, :, None], np.arange(half)[None, None, :]]
+
+
+def assert_elementwise(got, ref, tol, what):
+    """Whole-tensor relative L2 within tol, the central region on its own within tol, and
+    no single element off by more than tol times the largest reference magnitude."""
+    assert rel(got, ref) <= tol, f"{what}: rel L2 {rel(got, ref):.3e}"
+    cg, cr = _central(got, 24), _central(ref, 24)
+    assert rel(cg, cr) <= tol, f"{what}: central rel L2 {rel(cg, cr):.3e}"
+    worst = np.abs(np.asarray(got, np.complex128) - ref).max()
+    assert worst <= tol * np.abs(ref).max(), f"{what}: max error {worst:.3e}"
+
+
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_cfg4_backprojection_full_elementwise(tp, interp):
+    """All 2048 images into one 256^3 spectrum, data and weights, element by element.  The
+    central bricks are reached by nearly every image, so their work is split over many
+    work units whose tiles fold into the same words from different blocks."""
+    w = synth.workload(4)
+    kw = dict(interp=interp, oversampling=1.0, radius=w["radius"])
+    d, wt = tp.tp_backproject_2d_3d(dev(w["proj"]), dev(w["rot"]), **kw)
+    rd, rw = oracle.backproject(3, w["proj"], w["rot"], **kw)
+    assert_elementwise(host(d), rd, ATOMIC_TOL, "data spectrum")
+    assert_elementwise(host(wt), rw, ATOMIC_TOL, "weight spectrum")
+
+
+def test_cfg5_grad_vol_full_elementwise(tp):
+    """The volume gradient of the whole 512-pose box-256 step, element by element."""
+    w = synth.workload(5)
+    kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
+    vol, R, t, g = w["vol"], w["rot"], w["shift"], w["grad"]
+    gv, _, _ = tp.tp_project_3d_2d_backward(dev(g), dev(vol), dev(R), dev(t), want_rot=False,
+                                            want_shift=False, **kw)
+    rv, _, _ = oracle.project_backward(3, g, vol, R, shift=t, need_rot=False, need_shift=False,
+                                       **kw)
+    assert_elementwise(host(gv), rv, ATOMIC_TOL, "grad_vol")
+
+
+def test_outer_shell_golden(tp):
+    """Taps on and beyond the outermost stored shell against hand-worked values (forward), and
+    the scatter's deposits there through the adjoint identity with the same values."""
+    import outer_shell
+    for name, dim, M, V, R, want in outer_shell.cases():
+        Vd, Rd = dev(V.astype(np.complex64)), dev(R.astype(np.float32))
+        fwd = tp.tp_project_3d_2d if dim == 3 else tp.tp_project_2d_2d
+        out = host(fwd(Vd, Rd, N=8, interp="cubic", radius=-1.0))
+        got = complex(out[(0, 0) + outer_shell.PIXEL])
+        assert abs(got - want) <= 1e-6 * abs(want), f"{name}: {got} != {want}"
+        # Backprojecting y = 1 and y = i at that pixel gives P^T y; <V, P^T y> = <P V, y>.
+        for yv, part in ((1.0, want.real), (1j, want.imag)):
+            y = np.zeros((1, 1, 8, 5), np.complex64)
+            y[(0, 0) + outer_shell.PIXEL] = yv
+            if dim == 3:
+                bp, _ = tp.tp_backproject_2d_3d(dev(y), Rd, Nv=M, interp="cubic", radius=-1.0,
+                                                want_weights=False)
+            else:
+                bp, _, _ = tp.tp_project_2d_2d_backward(dev(y), Vd, Rd, interp="cubic",
+                                                        radius=-1.0, want_rot=False)
+            ip = np.vdot(V.astype(np.complex128), host(bp).astype(np.complex128)).real
+            assert abs(ip - part) <= 1e-6 * abs(want), f"{name}: adjoint {ip} != {part}"
+
+
 @pytest.mark.parametrize("interp", ["linear", "cubic"])
 def test_cfg4_backprojection_full_adjoint_identity(tp, interp):
     """At full size (2048 images) the scatter is the exact adjoint of the gather."""

@@ -40,6 +40,20 @@ MUTANTS = {
                          "if (kx * kx + ky * ky >= r * r)\n                    continue;\n                double p[3];\n                sample_position(R, dim, s, kx, ky, p);\n                cplx S"),
     "weight-ignores-omega": ("W[e] += wt * omega;", "W[e] += wt;"),
     "grad-rot-no-scale": ("gR[i * dim + j] += s * k[i] * d.re;", "gR[i * dim + j] += k[i] * d.re;"),
+    # The outermost shell: -M/2 is a stored row, +M/2 and columns beyond M/2 are not, and
+    # the Friedel reflection comes before the range test.
+    "nyquist-row-accepted": ("if (f < -M / 2 || f > M / 2 - 1)", "if (f < -M / 2 || f > M / 2)"),
+    "nyquist-row-rejected": ("if (f < -M / 2 || f > M / 2 - 1)", "if (f <= -M / 2 || f > M / 2 - 1)"),
+    "periodic-rows": ("    if (f < -M / 2 || f > M / 2 - 1)\n        return -1;\n    return (f < 0) ? f + M : f;",
+                      "    return ((f % M) + M) % M;"),
+    "nyquist-column-rejected": ("if (m[0] > s.M / 2)\n        return -1;",
+                                "if (m[0] >= s.M / 2)\n        return -1;"),
+    "periodic-columns": ("if (m[0] > s.M / 2)\n        return -1;",
+                         "if (m[0] > s.M / 2) {\n        m[0] = s.M - m[0];\n        m[1] = -m[1];\n"
+                         "        m[2] = -m[2];\n        *conj = !*conj;\n    }"),
+    "range-test-before-reflection": ("    *conj = 0;\n    if (m[0] < 0) {",
+                                     "    *conj = 0;\n    if (row_of(m[1], s.M) < 0 || (s.dim == 3 && row_of(m[2], s.M) < 0))\n"
+                                     "        return -1;\n    if (m[0] < 0) {"),
 }
 
 

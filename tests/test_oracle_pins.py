@@ -107,6 +107,42 @@ def test_quarter_turn_is_not_its_transpose():
     assert np.abs(bad[mask] - ref[mask]).max() > 1e-2 * np.abs(ref).max()
 
 
+def test_2d_quarter_turns_match_rot90():
+    """2D rotation convention: the forward by a quarter turn R equals the rfft2 of the image
+    turned by np.rot90 about the grid origin, and its transpose (the inverse turn) does not."""
+    rng = np.random.default_rng(31)
+    M = 16
+    e = np.fft.ifftshift(rng.standard_normal((M, M)))      # object centre at index 0
+    V = np.fft.rfft2(e)[None]
+    # np.rot90 turns the array about the centre of its corner pixels; rolling one row puts
+    # the turn's fixed point back on index 0: new[y][x] = old[x][-y], i.e. d'(x, y) =
+    # d(-y, x) = d(R^T (x, y)) with R = [[0, 1], [-1, 0]].
+    Q = np.array([[0.0, 1.0], [-1.0, 0.0]])
+    mask = in_radius(M, M / 2 - 1)                          # keeps the Nyquist shell out
+    turned = e
+    R = np.eye(2)
+    for quarter in range(1, 4):
+        turned = np.roll(np.rot90(turned), 1, axis=0)
+        R = R @ Q
+        ref = np.fft.rfft2(turned)
+        for interp in ("linear", "cubic"):
+            out = oracle.project(2, V, R[None, None], interp=interp, radius=M / 2 - 1)[0, 0]
+            np.testing.assert_allclose(out[mask], ref[mask], rtol=0, atol=1e-10 * np.abs(ref).max())
+        if quarter != 2:                                    # a half turn is its own transpose
+            bad = oracle.project(2, V, R.T[None, None], interp="cubic", radius=M / 2 - 1)[0, 0]
+            assert np.abs(bad[mask] - ref[mask]).max() > 1e-2 * np.abs(ref).max()
+
+
+def test_outer_shell_golden_values():
+    """Taps on and beyond the outermost stored shell, against hand-worked values: -M/2 is
+    stored, +M/2 and x > M/2 read zero, Friedel taps reflect before the range test."""
+    import outer_shell
+    for name, dim, M, V, R, want in outer_shell.cases():
+        out = oracle.project(dim, V, R, N=8, interp="cubic", radius=-1.0)
+        got = out[(0, 0) + outer_shell.PIXEL]
+        assert abs(got - want) <= 1e-15, f"{name}: {got} != {want}"
+
+
 # P3: kernels reproduce polynomials; Catmull-Rom midpoint weights are textbook.
 def _poly(c, x, y, z, cubic):
     v = c[0] + c[1] * x + c[2] * y + c[3] * z + c[5] * y * z + c[6] * x * y * z

@@ -58,11 +58,14 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(tp):
 
 
 def test_noalloc_refuses_problems_beyond_its_array(tp):
-    # 200000 poses against a 256^3 volume need far more than the fixed array;
-    # the call is refused before any pointer is used.
-    fake = 0x10000
+    # 200000 poses against a 256^3 volume need far more than the fixed array.
+    # The array pointers are NULL: the size check refuses the call first, and
+    # were it ever to let the call through, the NULL check behind it would
+    # refuse it too (a different status), so nothing is launched either way.
     o = tp.TPOptions(1, 1.0, -1.0, 0)
-    st = tp._fn("tp_project_3d_2d_noalloc")(fake, 1, 256, fake, 1, 200000, None, 1, 256, o, fake,
+    st = tp._fn("tp_project_3d_2d_noalloc")(None, 1, 256, None, 1, 200000, None, 1, 256, o, None,
                                              None)
     assert st == 2   # TP_ERR_SHAPE
+    msg = tp.tp_last_error()
+    assert "tp_project_3d_2d_noalloc" in msg and "bytes of scratch" in msg, msg
     assert tp.tp_workspace_bytes(1, 1, 200000, 256, "cubic") > 16 << 20
