@@ -57,6 +57,9 @@ def parse_args():
                          "the float64 volume gradient of the whole 256^3 spectrum)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary figures of the headline line (2D step, box-256 "
+                         "backprojection)")
     ap.add_argument("--poses", type=int, default=None,
                     help="pose count (default: the workload's 512); smaller runs are for profiling")
     ap.add_argument("--workload", default="fwdbwd",
@@ -561,6 +564,27 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = whole_job_rate(world, samples, args.e2e_steps, e2e_ms)
 
+    # Secondary figures, timed the same way in the same run (rank 0, one GPU):
+    # the 2D rotate + shift step and the 2048-image box-256 backprojection.
+    secondary = None
+    if rank == 0 and not args.no_secondary:
+        secondary = {}
+        r = rot2d_setup(tp, dev, stream, 20, 3)
+        ms, _ = _timed(r["step"], 20, 3, stream, flush)
+        secondary["rot2d_fwdbwd"] = {"workload": r["config"]["workload"],
+                                     "ms": float(ms.mean()), "forward_ms": r["forward_ms"](),
+                                     "gsamples_s": r["samples"] / (float(ms.mean()) * 1e-3) / 1e9}
+        del r
+        for interp in ("cubic", "linear"):
+            r = backproject_setup(tp, dev, interp)
+            ms, _ = _timed(r["step"], 5, 2, stream, flush)
+            secondary[f"backproject_{interp}"] = {
+                "workload": r["config"]["workload"], "ms": float(ms.mean()),
+                "gsamples_s": r["samples"] / (float(ms.mean()) * 1e-3) / 1e9,
+                "timed": "whole call (binning + kernels), data + weight spectra"}
+            del r
+        torch.cuda.empty_cache()
+
     if rank == 0:
         names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_saved (side stream)",
                  "volume_grad_scatter"]
@@ -592,6 +616,14 @@ def run_ours(args):
                                           ("mem_sol_pct", "l1_pct", "l2_pct", "dram_pct")}
                                       for k in kern if k in prof},
                        "source": "profiles/ncu_traffic.json (ncu --set full, same sources)"}
+        # The scatter's own bound is the shared-memory pipe: every in-radius
+        # sample reads and writes its 64 tile words (8 B each) once; the pipe
+        # moves 128 B per clock per SM.
+        clk = clocks.record()
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        smem_bytes = n_in * 64 * 8 * 2
+        smem_peak = sms * 128 * clk.get("sm_mhz", 2032.0) * 1e6 / 1e9
+        smem_achieved = smem_bytes / (mean_seg[3] * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -602,7 +634,16 @@ def run_ours(args):
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": nbytes},
+            "roofline_shared": {"bound": "shared", "kernel": "volume_grad_scatter",
+                                "achieved": smem_achieved, "peak": smem_peak, "unit": "GB/s",
+                                "frac": smem_achieved / smem_peak,
+                                "peak_source": f"{sms} SMs x 128 B/clk x median sampled SM clock "
+                                               f"({clk.get('sm_mhz')} MHz)",
+                                "algorithmic_bytes_per_launch": smem_bytes,
+                                "per_unit": "64 taps x (8 B read + 8 B written) per in-radius "
+                                            "sample"},
             "ncu_memory_sol": sol,
+            "secondary": secondary,
             "breakdown_ms": {n: float(mean_seg[i]) for i, n in enumerate(names)},
             "fwd_gsamples_s": samples / (mean_seg[0] * 1e-3) / 1e9,
             "bwd_gsamples_s": samples / ((float(step_ms.mean()) - mean_seg[0]) * 1e-3) / 1e9,
@@ -617,7 +658,7 @@ def run_ours(args):
             # pose gradient (one streaming kernel) and the volume-gradient call
             # (geometry, masks, plan, scatter); plus two 4-byte memsets
             "gpu_launches": 9 * args.steps,
-            "clocks": clocks.record(),
+            "clocks": clk,
             "cpu_baseline": cpu_line,
         }
         print(json.dumps(line), flush=True)
@@ -628,7 +669,100 @@ def run_ours(args):
 
 # ---------------------------------------------------------------------------
 # Further workloads (one GPU; not the headline line): each prints one JSON
-# line with CUDA-event timing of its step, inputs resident, L2 flushed.
+# line with CUDA-event timing of its step, inputs resident, L2 flushed.  The
+# 2D step and the box-256 backprojection are also timed in the headline run,
+# as its "secondary" figures.
+def rot2d_setup(tp, dev, stream, steps, warmup):
+    """The 2D rotate + shift step of 1024 images at box 128 (forward, then the image,
+    rotation and shift gradients); forward_ms() gives the forward's mean time."""
+    import torch
+    w = synth.workload(2)
+    N, n = w["box"], w["img"].shape[0]
+    img = torch.from_numpy(w["img"]).to(dev)
+    rot = torch.from_numpy(w["rot"]).to(dev)
+    shift = torch.from_numpy(w["shift"]).to(dev)
+    g = torch.from_numpy(w["grad"]).to(dev)
+    out = torch.empty((n, 1, N, N // 2 + 1), dtype=torch.complex64, device=dev)
+    gi, gr, gs = torch.zeros_like(img), torch.zeros_like(rot), torch.zeros_like(shift)
+    kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+
+    def step(i):
+        k = i - warmup
+        if 0 <= k < steps:
+            ev[k][0].record(stream)
+        tp.tp_project_2d_2d(img, rot, shift, out=out, **kw)
+        if 0 <= k < steps:
+            ev[k][1].record(stream)
+        gi.zero_()
+        gr.zero_()
+        gs.zero_()
+        tp.tp_project_2d_2d_backward(g, img, rot, shift, grad_img=gi, grad_rot=gr,
+                                     grad_shift=gs, **kw)
+
+    samples = n * N * (N // 2 + 1)
+    img_bytes = samples * 8
+    return {"step": step, "samples": samples,
+            "forward_ms": lambda: float(np.mean([a.elapsed_time(b) for a, b in ev])),
+            # forward: image read, output written; backward: g and the image read,
+            # the image gradient read and written
+            "bytes": 2 * img_bytes + 2 * img_bytes + 2 * img_bytes,
+            "config": {"workload": f"rot2d-{n}img-box{N}-{w['interp']}", "images": n, "box": N,
+                       "interp": w["interp"], "radius": w["radius"], "shift_px": 5.0,
+                       "l2_cache": "flushed between steps (256 MB write)"}}
+
+
+def backproject_setup(tp, dev, interp, backward=False, images=None):
+    """2048 noise images (box 256) backprojected into a data and a weight spectrum, or
+    (backward) the gradients of that backprojection."""
+    import torch
+    w = synth.workload(4, poses=images)
+    n, N = w["P"], w["box"]
+    samples = n * N * (N // 2 + 1)
+    proj = torch.from_numpy(w["proj"]).to(dev)
+    rot = torch.from_numpy(w["rot"]).to(dev)
+    kw = dict(interp=interp, oversampling=1.0, radius=w["radius"])
+    shape = (1, N, N, N // 2 + 1)
+    ws = torch.zeros(tp.tp_workspace_bytes(1, 1, n, N, interp), dtype=torch.uint8, device=dev)
+    vol_bytes = 8 * N * N * (N // 2 + 1)
+    cfg = {"workload": f"backproject-box{N}-{n}img-{interp}", "box": N, "images": n,
+           "interp": interp, "radius": w["radius"], "weights": "1 (default)",
+           "l2_cache": "flushed between steps (256 MB write)"}
+    if not backward:
+        data = torch.zeros(shape, dtype=torch.complex64, device=dev)
+        wvol = torch.zeros(shape, dtype=torch.float32, device=dev)
+
+        def step(i):
+            tp.tp_backproject_2d_3d(proj, rot, data_vol=data, weight_vol=wvol, workspace=ws, **kw)
+        nbytes = samples * 8 + 2 * vol_bytes + 2 * vol_bytes // 2
+        metric = "backprojected Fourier samples/sec (Gsamples/s), data + weight spectra"
+    else:
+        rng = synth.streams(7004, 1)[0]
+        G = torch.from_numpy(synth.complex_normal(shape, rng)).to(dev)
+        GW = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(dev)
+        gp = torch.empty_like(proj)
+        gw = torch.empty(proj.shape, dtype=torch.float32, device=dev)
+        gr = torch.zeros_like(rot)
+        sc = torch.empty(tp.tp_backproject_backward_scratch_bytes(1, 1, n, N, N, True),
+                         dtype=torch.uint8, device=dev)
+
+        def step(i):
+            gr.zero_()
+            tp.tp_backproject_2d_3d_backward(G, proj, rot, grad_weight_vol=GW, grad_proj=gp,
+                                             grad_weights=gw, grad_rot=gr, scratch=sc,
+                                             workspace=ws, **kw)
+        # data: spectrum read, y and D written (32 B), images read with y and
+        # D (40 B); weights: spectrum read and converted, y_W and D_W written,
+        # read back with grad_weights written (4 B).
+        nbytes = (vol_bytes + samples * 32 + samples * 40
+                  + vol_bytes // 2 + vol_bytes + samples * 32 + samples * 36)
+        metric = ("Fourier samples/sec (Gsamples/s) of the backprojection's gradients "
+                  "(images, image weights, rotations)")
+        cfg["upstream"] = "random data (complex) and weight (real) spectrum gradients"
+    return {"step": step, "samples": samples, "bytes": nbytes, "metric": metric, "config": cfg}
+
+
 def _timed(step, steps, warmup, stream, flush):
     import torch
     for i in range(warmup):
@@ -691,98 +825,28 @@ def run_workload(args):
                               "algorithmic_bytes_per_step": nbytes,
                               "timed": "whole call (binning + kernels)"})
     elif args.workload == "rot2d":
-        w = synth.workload(2)
-        N, n = w["box"], w["img"].shape[0]
-        samples = n * N * (N // 2 + 1)
-        img = torch.from_numpy(w["img"]).to(dev)
-        rot = torch.from_numpy(w["rot"]).to(dev)
-        shift = torch.from_numpy(w["shift"]).to(dev)
-        g = torch.from_numpy(w["grad"]).to(dev)
-        out = torch.empty((n, 1, N, N // 2 + 1), dtype=torch.complex64, device=dev)
-        gi, gr, gs = torch.zeros_like(img), torch.zeros_like(rot), torch.zeros_like(shift)
-        kw = dict(interp=w["interp"], oversampling=1.0, radius=w["radius"])
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        seg = []
-
-        def step(i):
-            k = i - args.warmup
-            if k >= 0:
-                ev[k][0].record(stream)
-            tp.tp_project_2d_2d(img, rot, shift, out=out, **kw)
-            if k >= 0:
-                ev[k][1].record(stream)
-            gi.zero_()
-            gr.zero_()
-            gs.zero_()
-            tp.tp_project_2d_2d_backward(g, img, rot, shift, grad_img=gi, grad_rot=gr,
-                                         grad_shift=gs, **kw)
-        ms, clocks = _timed(step, args.steps, args.warmup, stream, flush)
-        fwd = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        r = rot2d_setup(tp, dev, stream, args.steps, args.warmup)
+        ms, clocks = _timed(r["step"], args.steps, args.warmup, stream, flush)
+        fwd = r["forward_ms"]()
         t = float(ms.mean())
-        img_bytes = samples * 8
-        nbytes = 2 * img_bytes + 2 * img_bytes + 2 * img_bytes   # fwd; bwd: g + image, grad RMW
+        nbytes = r["bytes"]
         line.update(metric="Fourier samples/sec (Gsamples/s) of the 2D rotate + shift, fwd + bwd",
-                    unit="Gsamples/s", value=samples / (t * 1e-3) / 1e9, ms_per_step=t,
+                    unit="Gsamples/s", value=r["samples"] / (t * 1e-3) / 1e9, ms_per_step=t,
                     clocks=clocks, breakdown_ms={"forward": fwd, "backward": t - fwd},
-                    config={"workload": f"rot2d-{n}img-box{N}-{w['interp']}", "images": n,
-                            "box": N, "interp": w["interp"], "radius": w["radius"],
-                            "shift_px": 5.0, "l2_cache": "flushed between steps (256 MB write)"},
+                    config=r["config"],
                     roofline={"bound": "hbm", "achieved": nbytes / (t * 1e-3) / 1e9, "peak": peak,
                               "peak_source": peak_src, "unit": "GB/s",
                               "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
                               "algorithmic_bytes_per_step": nbytes,
                               "timed": "forward + backward calls"})
     elif args.workload in ("backproject", "backproject-backward"):
-        w = synth.workload(4)
-        n, N = w["P"], w["box"]
-        samples = n * N * (N // 2 + 1)
-        proj = torch.from_numpy(w["proj"]).to(dev)
-        rot = torch.from_numpy(w["rot"]).to(dev)
-        kw = dict(interp=args.interp, oversampling=1.0, radius=w["radius"])
-        shape = (1, N, N, N // 2 + 1)
-        ws = torch.zeros(tp.tp_workspace_bytes(1, 1, n, N, args.interp), dtype=torch.uint8,
-                         device=dev)
-        vol_bytes = 8 * N * N * (N // 2 + 1)
-        cfg = {"workload": f"backproject-box{N}-{n}img-{args.interp}", "box": N, "images": n,
-               "interp": args.interp, "radius": w["radius"], "weights": "1 (default)",
-               "l2_cache": "flushed between steps (256 MB write)"}
-        if args.workload == "backproject":
-            data = torch.zeros(shape, dtype=torch.complex64, device=dev)
-            wvol = torch.zeros(shape, dtype=torch.float32, device=dev)
-
-            def step(i):
-                tp.tp_backproject_2d_3d(proj, rot, data_vol=data, weight_vol=wvol, workspace=ws,
-                                        **kw)
-            nbytes = samples * 8 + 2 * vol_bytes + 2 * vol_bytes // 2
-            metric = "backprojected Fourier samples/sec (Gsamples/s), data + weight spectra"
-        else:
-            rng = synth.streams(7004, 1)[0]
-            G = torch.from_numpy(synth.complex_normal(shape, rng)).to(dev)
-            GW = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(dev)
-            gp = torch.empty_like(proj)
-            gw = torch.empty(proj.shape, dtype=torch.float32, device=dev)
-            gr = torch.zeros_like(rot)
-            sc = torch.empty(tp.tp_backproject_backward_scratch_bytes(1, 1, n, N, N, True),
-                             dtype=torch.uint8, device=dev)
-
-            def step(i):
-                gr.zero_()
-                tp.tp_backproject_2d_3d_backward(G, proj, rot, grad_weight_vol=GW, grad_proj=gp,
-                                                 grad_weights=gw, grad_rot=gr, scratch=sc,
-                                                 workspace=ws, **kw)
-            # data: spectrum read, y and D written (32 B), images read with y and
-            # D (40 B); weights: spectrum read and converted, y_W and D_W written,
-            # read back with grad_weights written (4 B).
-            nbytes = (vol_bytes + samples * 32 + samples * 40
-                      + vol_bytes // 2 + vol_bytes + samples * 32 + samples * 36)
-            metric = ("Fourier samples/sec (Gsamples/s) of the backprojection's gradients "
-                      "(images, image weights, rotations)")
-            cfg["upstream"] = "random data (complex) and weight (real) spectrum gradients"
-        ms, clocks = _timed(step, args.steps, args.warmup, stream, flush)
+        r = backproject_setup(tp, dev, args.interp, args.workload == "backproject-backward",
+                              args.poses)
+        ms, clocks = _timed(r["step"], args.steps, args.warmup, stream, flush)
         t = float(ms.mean())
-        line.update(metric=metric, unit="Gsamples/s", value=samples / (t * 1e-3) / 1e9,
-                    ms_per_step=t, config=cfg, clocks=clocks,
+        nbytes = r["bytes"]
+        line.update(metric=r["metric"], unit="Gsamples/s", value=r["samples"] / (t * 1e-3) / 1e9,
+                    ms_per_step=t, config=r["config"], clocks=clocks,
                     roofline={"bound": "hbm", "achieved": nbytes / (t * 1e-3) / 1e9, "peak": peak,
                               "peak_source": peak_src, "unit": "GB/s",
                               "frac": nbytes / (t * 1e-3) / 1e9 / peak, "traffic": None,
