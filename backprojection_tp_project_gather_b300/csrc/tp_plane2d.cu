@@ -1,0 +1,597 @@
+// tp_plane2d.cu -- the 2D -> 2D forward projection and its rotation / shift
+// gradients with the whole source plane staged in shared memory.
+//
+// A 2D half-spectrum of box M (M x (M/2+1) complex) is small enough that a
+// thread block can hold its Friedel-completed "virtual" plane -- F(n) = V[n]
+// for n_x >= 0, conj(V[-n]) for n_x < 0, zero outside the stored range
+// [ar §2 "التمرير الأمامي"; ko §2 "Friedel 대칭성 처리"] -- over every
+// position a stencil can reach while touching the stored range.  Every
+// sample then reads its taps from shared memory on one branch-free path.
+//
+//  - Layout.  The plane covers n in [X0, X0 + W)^2 with X0 = -(M/2 + 4) and W
+//    the next multiple of 4 of M + 8, so a stencil (taps floor(p) - LO ..
+//    floor(p) + HI) that leaves the region lies wholly outside the stored
+//    range and reads zero.  It is cut into 4 x 4 tiles of 16 complex words
+//    (one 128-byte row of banks): element (x, y) sits in bank pair
+//    (x mod 4) + 4 (y mod 4).  For cubic, lane L visits its 16 taps in its own
+//    order -- at step (sx, sy) the tap in bank pair ((sx + L) mod 4) +
+//    4 ((sy + L / 4) mod 4) -- so the 16 lanes of a half-warp never share a
+//    bank pair and every 64-bit load takes the minimum two wavefronts.
+//  - Staging.  A block copies the raw stored image into a second shared
+//    buffer with 16-byte (else 8-byte) cp.async, then unpacks it into the
+//    tiled virtual plane, conjugating the Friedel side.  The copy of the
+//    block's NEXT source image is issued before the current one is used, so
+//    it lands while the block computes.
+//  - Work.  The poses of each source image are cut into items; a persistent
+//    block takes a contiguous range of items (consecutive items mostly share
+//    their source, which then stays staged).  Threads take output pixels in
+//    row order (coalesced reads of the upstream gradient and writes of the
+//    output); pixels outside the radius are written as zeros by the forward.
+//
+// The forward gives out = phase * S(p); with GRAD the same gather also forms
+// the derivative weights and reduces, per pose, dL/dR[i][a] = s k_i dL/dp_a and
+// dL/dshift_a (the analytic gradients of [de §3 item 4; ar §2]) over the block,
+// adding them to grad_rot / grad_shift with one atomic per entry.
+//
+// Method: "torch-projectors: A High-Performance Differentiable Projection
+// Library for PyTorch", 2D -> 2D forward and its gradients [it §2 "Operazioni
+// Supportate"; de §2 "Unterstützte Operationen" items 1 and 4].
+#include <cstdint>
+
+#include "tp_device.cuh"
+#include "tp_launch.h"
+
+namespace tp {
+
+namespace {
+
+constexpr int kPlaneThreads = 512;
+constexpr int kPlaneWarps = kPlaneThreads / 32;
+
+// Geometry of the staged virtual plane of a box-M source.
+struct PlaneGeo {
+    int M, half, Xs;   // source box, M/2, M/2 + 1
+    int X0;            // virtual coordinate of local index 0 (both axes)
+    int W;             // local extent (both axes), a multiple of 4
+    int TW;            // tiles per row (W / 4)
+    int raw_words;     // complex words of one stored source image (M * Xs)
+};
+
+__host__ __device__ inline PlaneGeo plane_geo(int M) {
+    PlaneGeo g;
+    g.M = M;
+    g.half = M / 2;
+    g.Xs = M / 2 + 1;
+    g.X0 = -(M / 2 + 4);
+    g.W = ((M + 8) + 3) & ~3;
+    g.TW = g.W / 4;
+    g.raw_words = M * g.Xs;
+    return g;
+}
+
+__host__ __device__ inline size_t plane_smem_bytes(int M) {
+    const PlaneGeo g = plane_geo(M);
+    return sizeof(float2) * ((size_t)g.W * g.W + (size_t)g.raw_words);
+}
+
+// Tiled index of local element (lx, ly).
+__device__ __forceinline__ int tidx(const PlaneGeo &g, int lx, int ly) {
+    return ((ly >> 2) * g.TW + (lx >> 2)) * 16 + (lx & 3) + 4 * (ly & 3);
+}
+
+// Issue the copy of one stored source image (raw_words complex words at src)
+// into the raw buffer; the caller commits the group.
+__device__ __forceinline__ void issue_raw_copy(const float2 *src, int words, float2 *raw,
+                                               bool vec16) {
+    const unsigned sbase = (unsigned)__cvta_generic_to_shared(raw);
+    if (vec16) {
+        // words is even (M even), so the image is a whole number of 16-byte chunks.
+        const int chunks = words >> 1;
+        for (int c = threadIdx.x; c < chunks; c += kPlaneThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16u * c),
+                         "l"(src + 2 * c)
+                         : "memory");
+    } else {
+        for (int c = threadIdx.x; c < words; c += kPlaneThreads)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(sbase + 8u * c),
+                         "l"(src + c)
+                         : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// Fill the tiled virtual plane from the raw stored image: direct side
+// n_x >= 0 reads V[n], Friedel side conj(V[-n]); zero outside the stored
+// range.  Threads walk the plane in tiled order, so their writes are
+// consecutive words.
+__device__ __forceinline__ void unpack_plane(const PlaneGeo &g, const float2 *raw, float2 *plane,
+                                             unsigned *dbg) {
+    const int total = g.W * g.W;
+    for (int j = threadIdx.x; j < total; j += kPlaneThreads) {
+        const int tile = j >> 4, r = j & 15;
+        const int ty = tile / g.TW, tx = tile - ty * g.TW;
+        const int vx = g.X0 + 4 * tx + (r & 3), vy = g.X0 + 4 * ty + (r >> 2);
+        const bool cj = vx < 0;
+        const int mx = cj ? -vx : vx, my = cj ? -vy : vy;
+        float2 v = make_float2(0.f, 0.f);
+        if (mx <= g.half && row_ok(my, g.half)) {
+            const int at = wrap_row(my, g.M) * g.Xs + mx;
+            if (TP_CHECK(dbg, at >= 0 && at < g.raw_words, 0)) {
+                v = raw[at];
+                if (cj) v.y = -v.y;
+            }
+        }
+        plane[j] = v;
+    }
+}
+
+// r[i] = v[(i + c) mod 4] with static register indexes (two selects per
+// entry): the per-lane rotation of a cubic stencil's separable weights.
+__device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) {
+    float t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = (c & 1) ? v[(i + 1) & 3] : v[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = (c & 2) ? t[(i + 2) & 3] : t[i];
+}
+
+// Weighted sum over the stencil of the sample at local tap origin (lx, ly)
+// (the local coordinates of tap floor(p) - LO), with derivative weights when
+// DERIV.  Cubic visits the taps in the lane-rotated order described above.
+template <bool CUBIC, bool DERIV>
+__device__ __forceinline__ void gather_plane(const PlaneGeo &g, const float2 *plane, int lx, int ly,
+                                             const float (&w)[2][4], const float (&d)[2][4],
+                                             float2 &S, float2 (&dS)[2], unsigned *dbg) {
+    S = make_float2(0.f, 0.f);
+    dS[0] = dS[1] = S;
+    const int total = g.W * g.W;
+    if constexpr (CUBIC) {
+        const int lane = threadIdx.x & 31;
+        const int cx = (lane - lx) & 3, cy = ((lane >> 2) - ly) & 3;
+        float wx[4], wy[4], dx[4], dy[4];
+        rot4(w[0], cx, wx);   // the separable weights follow the tap order
+        rot4(w[1], cy, wy);
+        if (DERIV) {
+            rot4(d[0], cx, dx);
+            rot4(d[1], cy, dy);
+        }
+#pragma unroll
+        for (int sy = 0; sy < 4; ++sy) {
+            const int y = ly + ((sy + cy) & 3);
+            const int rowb = (y >> 2) * (16 * g.TW) + 4 * (y & 3);
+            float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+#pragma unroll
+            for (int sx = 0; sx < 4; ++sx) {
+                const int x = lx + ((sx + cx) & 3);
+                const int at = rowb + (x >> 2) * 16 + (x & 3);
+                if (!TP_CHECK(dbg, at >= 0 && at < total, 2)) continue;
+                const float2 v = plane[at];
+                cfma(wx[sx], v, r0);
+                if (DERIV) cfma(dx[sx], v, r1);
+            }
+            cfma(wy[sy], r0, S);
+            if (DERIV) {
+                cfma(wy[sy], r1, dS[0]);
+                cfma(dy[sy], r0, dS[1]);
+            }
+        }
+    } else {
+#pragma unroll
+    for (int jy = 0; jy < 2; ++jy) {
+        float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+#pragma unroll
+        for (int jx = 0; jx < 2; ++jx) {
+            const int at = tidx(g, lx + jx, ly + jy);
+            if (!TP_CHECK(dbg, at >= 0 && at < total, 2)) continue;
+            const float2 v = plane[at];
+            cfma(w[0][jx], v, r0);
+            if (DERIV) cfma(d[0][jx], v, r1);
+        }
+        cfma(w[1][jy], r0, S);
+        if (DERIV) {
+            cfma(w[1][jy], r1, dS[0]);
+            cfma(d[1][jy], r0, dS[1]);
+        }
+    }
+    }
+}
+
+// Work items: item i covers source v = i / per_src and the poses
+// [c * chunk, min((c + 1) * chunk, pps)) of that source's pose list, c = i % per_src.
+struct Items {
+    int per_src;   // items per source image
+    int chunk;     // poses per item
+    int pps;       // poses per source: B * P when the source is shared, else P
+    int count;     // Bsrc * per_src
+};
+
+// Output-image index of pose j of source v's pose list.
+__device__ __forceinline__ int image_of(const Params &q, int v, int j) {
+    return (q.Bsrc == 1) ? j : v * q.P + j;
+}
+
+template <bool CUBIC, bool GRAD>
+__global__ void __launch_bounds__(kPlaneThreads, 1)
+    k_plane2d(Params q, Items it, bool vec16, float2 *__restrict__ out,
+              const float2 *__restrict__ g_out, float *__restrict__ grad_rot,
+              float *__restrict__ grad_shift) {
+    using St = Stencil<CUBIC>;
+    extern __shared__ float4 s_plane4[];
+    __shared__ float s_red[kPlaneWarps][6];
+    const PlaneGeo g = plane_geo(q.M);
+    float2 *plane = reinterpret_cast<float2 *>(s_plane4);
+    float2 *raw = plane + (size_t)g.W * g.W;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int first = (int)((long long)it.count * blockIdx.x / gridDim.x);
+    const int last = (int)((long long)it.count * (blockIdx.x + 1) / gridDim.x);
+    if (first >= last) return;
+    const int span = St::LO + St::HI + 1;   // stencil width
+    const int npix = q.N * q.Xo;
+    const int half_n = q.N >> 1;
+    int staged = -1;   // source held in the plane
+    issue_raw_copy(q.src + (size_t)(first / it.per_src) * q.src_stride, g.raw_words, raw, vec16);
+    for (int i = first; i < last; ++i) {
+        const int v = i / it.per_src;
+        if (v != staged) {
+            asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+            __syncthreads();   // raw landed for every thread; the plane is free
+            unpack_plane(g, raw, plane, q.dbg);
+            staged = v;
+            __syncthreads();   // plane complete; raw free again
+            // Prefetch the next different source while this one is used.
+            for (int k = i + 1; k < last; ++k)
+                if (k / it.per_src != v) {
+                    issue_raw_copy(q.src + (size_t)(k / it.per_src) * q.src_stride, g.raw_words,
+                                   raw, vec16);
+                    break;
+                }
+        }
+        const int c = i - v * it.per_src;
+        const int j1 = min((c + 1) * it.chunk, it.pps);
+        for (int j = c * it.chunk; j < j1; ++j) {
+            const int bp = image_of(q, v, j);
+            const int b = bp / q.P, pi = bp - b * q.P;
+            const Pose<2> ps = load_pose<2>(q, b, pi);
+            float acc[6];
+#pragma unroll
+            for (int k = 0; k < 6; ++k) acc[k] = 0.f;
+            const size_t ob = (size_t)bp * q.plane;
+            for (int e = threadIdx.x; e < npix; e += kPlaneThreads) {
+                const int iy = e / q.Xo, kx = e - iy * q.Xo;
+                const int ky = iy < half_n ? iy : iy - q.N;
+                const bool inside = kx * kx + ky * ky <= q.r2max;
+                if (!GRAD && !inside) {
+                    out[ob + e] = make_float2(0.f, 0.f);
+                    continue;
+                }
+                if (GRAD && !inside) continue;
+                float w[2][4], d[2][4], t;
+                const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)ky);
+                const float py = fmaf(ps.a[1], (float)kx, ps.b[1] * (float)ky);
+                const int lx = split_coord(px, t) - St::LO - g.X0;
+                St::weights(t, w[0]);
+                if (GRAD) St::derivs(t, d[0]);
+                const int ly = split_coord(py, t) - St::LO - g.X0;
+                St::weights(t, w[1]);
+                if (GRAD) St::derivs(t, d[1]);
+                float2 S = make_float2(0.f, 0.f), dS[2] = {S, S};
+                // A stencil leaving the region lies wholly outside the stored range.
+                if ((unsigned)lx <= (unsigned)(g.W - span) && (unsigned)ly <= (unsigned)(g.W - span))
+                    gather_plane<CUBIC, GRAD>(g, plane, lx, ly, w, d, S, dS, q.dbg);
+                float2 ph = make_float2(1.f, 0.f);
+                if (q.shift) ph = shift_phase(kx, ky, ps.sx, ps.sy, q.fN, q.invN);
+                if (!GRAD) {
+                    out[ob + e] = cmul(ph, S);
+                } else {
+                    const float2 gv = __ldg(g_out + ob + e);
+                    const float2 gq = cmul_conj_a(ph, gv);   // conj(phase) * g
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) {
+                        const float dl = gq.x * dS[a].x + gq.y * dS[a].y;   // dL/dp_a
+                        acc[a] = fmaf(q.s * (float)kx, dl, acc[a]);
+                        acc[2 + a] = fmaf(q.s * (float)ky, dl, acc[2 + a]);
+                    }
+                    const float2 y = cmul(ph, S);
+                    const float qv = 6.283185307179586f * q.invN * (gv.x * y.y - gv.y * y.x);
+                    acc[4] = fmaf((float)kx, qv, acc[4]);
+                    acc[5] = fmaf((float)ky, qv, acc[5]);
+                }
+            }
+            if (GRAD) {
+#pragma unroll
+                for (int k = 0; k < 6; ++k) {
+                    float x = acc[k];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                    if (lane == 0) s_red[warp][k] = x;
+                }
+                __syncthreads();
+                if (threadIdx.x < 6) {
+                    float x = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < kPlaneWarps; ++w2) x += s_red[w2][threadIdx.x];
+                    const int k = threadIdx.x;
+                    if (TP_CHECK(q.dbg, ps.ridx < q.Bp * q.P && ps.sidx < q.Bs * q.P, 9)) {
+                        if (k < 4) {
+                            if (grad_rot && x != 0.f) atomicAdd(grad_rot + (size_t)ps.ridx * 4 + k, x);
+                        } else if (grad_shift && x != 0.f) {
+                            atomicAdd(grad_shift + 2 * (size_t)ps.sidx + (k - 4), x);
+                        }
+                    }
+                }
+                __syncthreads();   // s_red is reused by the next pose
+            }
+        }
+    }
+    // Leave no copy in flight (a prefetch is only issued for an item that follows).
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Image gradient (the real adjoint of the forward applied to an upstream
+// gradient): the staged plane is the accumulator.  Warp w owns the tile rows
+// [w TW / 16, (w + 1) TW / 16) of it and no other warp writes there, so the
+// spreading needs no atomics.  For every pose of an item a warp enumerates
+// the pixels whose stencil rows meet its band (rows of the output image, each
+// with its qx interval from the slab of p_y, packed into 32-lane rounds by a
+// warp prefix sum), sets up one sample per lane and spreads the taps that lie
+// in its band, lanes 0-15 and then lanes 16-31: with the lane-rotated tap
+// order the 16 lanes of a pass touch 16 different bank pairs, hence 16
+// different words, so the plain read-add-write never races.  After the item
+// the block folds the plane into the stored half-spectrum -- G[m] = A[m] +
+// conj(A[-m]) for m_x > 0 (the Friedel taps' share), A[m] for m_x = 0 -- and
+// adds it to the gradient: plainly when the block owns every pose of that
+// source image, else with vector atomics.
+template <bool CUBIC>
+__global__ void __launch_bounds__(kPlaneThreads, 1)
+    k_plane2d_scatter(Params q, Items it, bool exclusive, const float2 *__restrict__ g_in,
+                      float2 *__restrict__ dst) {
+    using St = Stencil<CUBIC>;
+    extern __shared__ float4 s_plane4[];
+    const PlaneGeo g = plane_geo(q.M);
+    float2 *plane = reinterpret_cast<float2 *>(s_plane4);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int first = (int)((long long)it.count * blockIdx.x / gridDim.x);
+    const int last = (int)((long long)it.count * (blockIdx.x + 1) / gridDim.x);
+    const int span = St::LO + St::HI + 1;
+    const int total = g.W * g.W;
+    // This warp's band of plane rows (local coordinates) and the sample rows
+    // floor(p_y) whose stencils reach into it.
+    const int ylo = 4 * (warp * g.TW / kPlaneWarps), yhi = 4 * ((warp + 1) * g.TW / kPlaneWarps);
+    const float pylo = (float)(ylo - (span - 1) + St::LO + g.X0);   // floor(p_y) >= this
+    const float pyhi = (float)(yhi + St::LO + g.X0);                // p_y < this
+    const int half_n = q.N >> 1;
+    const int rmax = (int)floorf(sqrtf((float)q.r2max));
+    for (int i = first; i < last; ++i) {
+        const int v = i / it.per_src;
+        for (int j = threadIdx.x; j < total; j += kPlaneThreads) plane[j] = make_float2(0.f, 0.f);
+        __syncthreads();
+        const int c = i - v * it.per_src;
+        const int j1 = min((c + 1) * it.chunk, it.pps);
+        for (int j = c * it.chunk; j < j1; ++j) {
+            const int bp = image_of(q, v, j);
+            const int b = bp / q.P, pi = bp - b * q.P;
+            const Pose<2> ps = load_pose<2>(q, b, pi);
+            const float a1 = ps.a[1], b1 = ps.b[1];   // p_y = a1 kx + b1 ky
+            const float ia1 = fabsf(a1) > 1e-6f ? 1.0f / a1 : 0.f;
+            const float2 *gim = g_in + (size_t)bp * q.plane;
+            const int qy0 = max(-half_n, -rmax), qy1 = min(half_n - 1, rmax);
+            for (int base = qy0; base <= qy1; base += 32) {
+                const int ky = base + lane;
+                int xs = 0, cnt = 0;
+                if (ky <= qy1) {
+                    const int rr = q.r2max - ky * ky;
+                    float xl = 0.f, xh = (float)min(half_n, (int)floorf(sqrtf((float)max(rr, 0))));
+                    bool empty = rr < 0;
+                    const float by = (float)ky * b1;
+                    if (ia1 != 0.f) {
+                        const float t1 = (pylo - 0.01f - by) * ia1, t2 = (pyhi + 0.01f - by) * ia1;
+                        xl = fmaxf(xl, fminf(t1, t2));
+                        xh = fminf(xh, fmaxf(t1, t2));
+                    } else if (by < pylo - 0.01f || by > pyhi + 0.01f) {
+                        empty = true;
+                    }
+                    if (!empty && xl <= xh) {
+                        xs = (int)ceilf(xl);
+                        cnt = max(0, (int)floorf(xh) - xs + 1);
+                    }
+                }
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                const int ntot = __shfl_sync(0xffffffffu, incl, 31);
+                const int excl = incl - cnt;
+                for (int i0 = 0; i0 < ntot; i0 += 32) {
+                    const int k = i0 + lane;
+                    int r = 0;
+#pragma unroll
+                    for (int step = 16; step > 0; step >>= 1) {
+                        const int x = __shfl_sync(0xffffffffu, incl, r + step - 1);
+                        if (x <= k) r += step;
+                    }
+                    r = min(r, 31);
+                    const int kx = __shfl_sync(0xffffffffu, xs, r) + (k - __shfl_sync(0xffffffffu, excl, r));
+                    const int kyr = base + r;
+                    // One sample per lane: its stencil, the tap origin and the value.
+                    bool live = k < ntot;
+                    float w[2][4];
+                    int lx = 0, ly = 0;
+                    float2 cv = make_float2(0.f, 0.f);
+                    if (live) {
+                        float t;
+                        const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)kyr);
+                        const float py = fmaf(a1, (float)kx, b1 * (float)kyr);
+                        lx = split_coord(px, t) - St::LO - g.X0;
+                        St::weights(t, w[0]);
+                        ly = split_coord(py, t) - St::LO - g.X0;
+                        St::weights(t, w[1]);
+                        // in the region, and some stencil row in this band
+                        live = (unsigned)lx <= (unsigned)(g.W - span) &&
+                               (unsigned)ly <= (unsigned)(g.W - span) && ly + span > ylo && ly < yhi;
+                        if (live) {
+                            const int iy = kyr < 0 ? kyr + q.N : kyr;
+                            if (TP_CHECK(q.dbg, iy >= 0 && iy < q.N && kx >= 0 && kx < q.Xo, 7)) {
+                                cv = __ldg(gim + iy * q.Xo + kx);
+                                if (q.shift)
+                                    cv = cmul_conj_a(shift_phase(kx, kyr, ps.sx, ps.sy, q.fN, q.invN), cv);
+                            }
+                        }
+                    }
+                    for (int pass = 0; pass < 2; ++pass) {
+                        if (live && (lane >> 4) == pass) {
+                            if constexpr (CUBIC) {
+                                const int cx = (lane - lx) & 3, cy = ((lane >> 2) - ly) & 3;
+                                float wx[4], wy[4];
+                                rot4(w[0], cx, wx);
+                                rot4(w[1], cy, wy);
+#pragma unroll
+                                for (int sy = 0; sy < 4; ++sy) {
+                                    const int y = ly + ((sy + cy) & 3);
+                                    if (y < ylo || y >= yhi) continue;
+                                    const int rowb = (y >> 2) * (16 * g.TW) + 4 * (y & 3);
+                                    const float2 cy2 = make_float2(wy[sy] * cv.x, wy[sy] * cv.y);
+#pragma unroll
+                                    for (int sx = 0; sx < 4; ++sx) {
+                                        const int x = lx + ((sx + cx) & 3);
+                                        const int at = rowb + (x >> 2) * 16 + (x & 3);
+                                        if (!TP_CHECK(q.dbg, at >= 0 && at < total, 4)) continue;
+                                        float2 a = plane[at];
+                                        cfma(wx[sx], cy2, a);
+                                        plane[at] = a;
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int jy = 0; jy < 2; ++jy) {
+                                    const int y = ly + jy;
+                                    if (y < ylo || y >= yhi) continue;
+                                    const float2 cy2 = make_float2(w[1][jy] * cv.x, w[1][jy] * cv.y);
+#pragma unroll
+                                    for (int jx = 0; jx < 2; ++jx) {
+                                        const int at = tidx(g, lx + jx, y);
+                                        if (!TP_CHECK(q.dbg, at >= 0 && at < total, 4)) continue;
+                                        float2 a = plane[at];
+                                        cfma(w[0][jx], cy2, a);
+                                        plane[at] = a;
+                                    }
+                                }
+                            }
+                        }
+                        __syncwarp();
+                    }
+                }
+            }
+        }
+        __syncthreads();   // every band spread
+        // Fold into the stored half-spectrum of source v.
+        float2 *V = dst + (size_t)v * q.src_stride;
+        for (int e = threadIdx.x; e < g.raw_words; e += kPlaneThreads) {
+            const int row = e / g.Xs, mx = e - row * g.Xs;
+            const int my = row < g.half ? row : row - g.M;
+            const int lxm = mx - g.X0, lym = my - g.X0;
+            float2 val = plane[tidx(g, lxm, lym)];
+            if (mx > 0) {
+                const float2 f = plane[tidx(g, -mx - g.X0, -my - g.X0)];
+                val.x += f.x;
+                val.y -= f.y;
+            }
+            if (val.x == 0.f && val.y == 0.f) continue;
+            if (!TP_CHECK(q.dbg, e < g.raw_words, 6)) continue;
+            if (exclusive) {
+                float2 o = V[e];
+                o.x += val.x;
+                o.y += val.y;
+                V[e] = o;
+            } else {
+                atomicAdd(V + e, val);
+            }
+        }
+        __syncthreads();   // the plane is zeroed again for the next item
+    }
+}
+
+int sm_count() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+Items make_items(const Params &q, int blocks_target) {
+    Items it;
+    it.pps = (q.Bsrc == 1) ? q.B * q.P : q.P;
+    // About two items per block, never an item smaller than one pose.
+    const long long want = 2LL * blocks_target;
+    const long long per_src = (want + q.Bsrc - 1) / q.Bsrc;
+    it.chunk = (int)((it.pps + per_src - 1) / per_src);
+    if (it.chunk < 1) it.chunk = 1;
+    it.per_src = (it.pps + it.chunk - 1) / it.chunk;
+    it.count = q.Bsrc * it.per_src;
+    return it;
+}
+
+template <bool CUBIC, bool GRAD>
+cudaError_t plane_launch(const Params &q, float2 *out, const float2 *g, float *grot, float *gshift,
+                         cudaStream_t st) {
+    if ((long long)q.B * q.P == 0) return cudaSuccess;
+    const size_t smem = plane_smem_bytes(q.M);
+    auto kern = k_plane2d<CUBIC, GRAD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    const Items it = make_items(q, sms);
+    const int blocks = it.count < sms ? it.count : sms;
+    const bool vec16 = (reinterpret_cast<uintptr_t>(q.src) & 15) == 0 && (q.src_stride & 1) == 0;
+    kern<<<blocks, kPlaneThreads, smem, st>>>(q, it, vec16, out, g, grot, gshift);
+    return cudaGetLastError();
+}
+
+template <bool CUBIC>
+cudaError_t plane_scatter_launch(const Params &q, const float2 *img, float2 *dst, cudaStream_t st) {
+    if ((long long)q.B * q.P == 0) return cudaSuccess;
+    const PlaneGeo g = plane_geo(q.M);
+    const size_t smem = sizeof(float2) * (size_t)g.W * g.W;
+    auto kern = k_plane2d_scatter<CUBIC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    const Items it = make_items(q, sms);
+    const int blocks = it.count < sms ? it.count : sms;
+    // A block owns a source's gradient when that source's poses form one item.
+    kern<<<blocks, kPlaneThreads, smem, st>>>(q, it, it.per_src == 1, img, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool plane2d_fits(int M) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return false;
+    // The static reduction array and a margin for the runtime's own use.
+    return plane_smem_bytes(M) + 1024 <= (size_t)optin;
+}
+
+cudaError_t launch_plane2d_project(bool cubic, const Params &q, float2 *out, cudaStream_t st) {
+    return cubic ? plane_launch<true, false>(q, out, nullptr, nullptr, nullptr, st)
+                 : plane_launch<false, false>(q, out, nullptr, nullptr, nullptr, st);
+}
+
+cudaError_t launch_plane2d_scatter(bool cubic, const Params &q, const float2 *img, float2 *dst,
+                                   cudaStream_t st) {
+    return cubic ? plane_scatter_launch<true>(q, img, dst, st)
+                 : plane_scatter_launch<false>(q, img, dst, st);
+}
+
+cudaError_t launch_plane2d_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
+                                     float *grad_rot, float *grad_shift, cudaStream_t st) {
+    if (!grad_rot && !grad_shift) return cudaSuccess;
+    return cubic ? plane_launch<true, true>(q, nullptr, grad_out, grad_rot, grad_shift, st)
+                 : plane_launch<false, true>(q, nullptr, grad_out, grad_rot, grad_shift, st);
+}
+
+}  // namespace tp

@@ -482,3 +482,73 @@ def test_dense_3d_volume_gradient(tp, interp):
                                             want_shift=False, **kw)
     rv, _, _ = oracle.project_backward(3, g, vol, R, need_rot=False, need_shift=False, **kw)
     assert rel(host(gv), rv) <= ATOMIC_TOL
+
+
+# ---------------------------------------------------------------------------
+# The 2D operators stage the whole Friedel-completed source plane in shared
+# memory when it fits (sources up to box 132 on a 227 KB block) and fall back to the
+# per-sample kernels above that.  These cases cover both sides of the limit,
+# a source pointer that is only 8-byte aligned (the staging copies 8 bytes at
+# a time then), a shared source whose many poses are cut into work items,
+# and several poses per source image.
+@pytest.mark.parametrize("M,N,s", [(128, 64, 0.5), (130, 130, 1.0), (132, 96, 0.7),
+                                   (134, 134, 1.0), (256, 64, 0.25)])
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_2d_staged_plane_limits(tp, M, N, s, interp):
+    rng = np.random.default_rng(M + N)
+    B, P = 2, 3
+    img = crandn(rng, (B, M, M // 2 + 1))
+    R = synth.planar_rotations(rng.uniform(0, 2 * np.pi, B * P)).reshape(B, P, 2, 2)
+    t = rng.uniform(-8, 8, (B, P, 2)).astype(np.float32)
+    g = crandn(rng, (B, P, N, N // 2 + 1))
+    kw = dict(interp=interp, oversampling=s, radius=-1.0)
+    out = host(tp.tp_project_2d_2d(dev(img), dev(R), dev(t), N=N, **kw))
+    assert rel(out, oracle.project(2, img, R, shift=t, N=N, **kw)) <= FWD_TOL
+    gi, gr, gt = tp.tp_project_2d_2d_backward(dev(g), dev(img), dev(R), dev(t), **kw)
+    ri, rr, rt = oracle.project_backward(2, g, img, R, shift=t, **kw)
+    assert rel(host(gi), ri) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+    if interp == "cubic":   # see test_dense_2d_image_gradient_many_poses_one_image
+        assert rel(host(gr), rr) <= ATOMIC_TOL
+
+
+@pytest.mark.parametrize("interp", ["linear", "cubic"])
+def test_2d_source_only_8_byte_aligned(tp, interp):
+    rng = np.random.default_rng(77)
+    M, P = 40, 5
+    img = crandn(rng, (1, M, M // 2 + 1))
+    buf = torch.zeros(img.size + 1, dtype=torch.complex64, device="cuda")
+    src = buf[1:].view(img.shape)                    # starts 8 bytes past a 16-byte boundary
+    src.copy_(dev(img))
+    assert src.data_ptr() % 16 == 8
+    R = synth.planar_rotations(rng.uniform(0, 2 * np.pi, P)).reshape(1, P, 2, 2)
+    t = rng.uniform(-3, 3, (1, P, 2)).astype(np.float32)
+    g = crandn(rng, (1, P, M, M // 2 + 1))
+    kw = dict(interp=interp, radius=-1.0)
+    out = host(tp.tp_project_2d_2d(src, dev(R), dev(t), **kw))
+    assert rel(out, oracle.project(2, img, R, shift=t, **kw)) <= FWD_TOL
+    _, gr, gt = tp.tp_project_2d_2d_backward(dev(g), src, dev(R), dev(t), want_img=False, **kw)
+    _, rr, rt = oracle.project_backward(2, g, img, R, shift=t, need_src=False, **kw)
+    assert rel(host(gt), rt) <= ATOMIC_TOL
+    if interp == "cubic":
+        assert rel(host(gr), rr) <= ATOMIC_TOL
+
+
+@pytest.mark.parametrize("Bi,B,P", [(1, 3, 700), (3, 3, 150)])
+def test_2d_many_poses_per_source(tp, Bi, B, P):
+    """A shared source for 2100 poses (cut into many work items over all blocks)
+    and three sources with 150 poses each (several items per source)."""
+    rng = np.random.default_rng(Bi * 1000 + P)
+    M = N = 32
+    img = crandn(rng, (Bi, M, M // 2 + 1))
+    R = synth.planar_rotations(rng.uniform(0, 2 * np.pi, B * P)).reshape(B, P, 2, 2)
+    t = rng.uniform(-3, 3, (B, P, 2)).astype(np.float32)
+    g = crandn(rng, (B, P, N, N // 2 + 1))
+    kw = dict(interp="cubic", radius=-1.0)
+    out = host(tp.tp_project_2d_2d(dev(img), dev(R), dev(t), **kw))
+    assert rel(out, oracle.project(2, img, R, shift=t, **kw)) <= FWD_TOL
+    gi, gr, gt = tp.tp_project_2d_2d_backward(dev(g), dev(img), dev(R), dev(t), **kw)
+    ri, rr, rt = oracle.project_backward(2, g, img, R, shift=t, **kw)
+    assert rel(host(gi), ri) <= ATOMIC_TOL
+    assert rel(host(gr), rr) <= ATOMIC_TOL
+    assert rel(host(gt), rt) <= ATOMIC_TOL
