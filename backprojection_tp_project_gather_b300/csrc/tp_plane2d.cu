@@ -335,9 +335,11 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
 // the pixels whose stencil rows meet its band (rows of the output image, each
 // with its qx interval from the slab of p_y, packed into 32-lane rounds by a
 // warp prefix sum), sets up one sample per lane and spreads the taps that lie
-// in its band, lanes 0-15 and then lanes 16-31: with the lane-rotated tap
-// order the 16 lanes of a pass touch 16 different bank pairs, hence 16
-// different words, so the plain read-add-write never races.  After the item
+// in its band.  Cubic spreads with lanes 0-15 and then lanes 16-31: with the
+// lane-rotated tap order the 16 lanes of a pass touch 16 different bank
+// pairs, hence 16 different words, so the plain read-add-write never races.
+// Linear (four taps, which no lane order keeps apart) adds with shared-memory
+// atomics instead.  After the item
 // the block folds the plane into the stored half-spectrum -- G[m] = A[m] +
 // conj(A[-m]) for m_x > 0 (the Friedel taps' share), A[m] for m_x = 0 -- and
 // adds it to the gradient: plainly when the block owns every pose of that
@@ -440,8 +442,11 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
                             }
                         }
                     }
-                    for (int pass = 0; pass < 2; ++pass) {
-                        if (live && (lane >> 4) == pass) {
+                    // Cubic: two passes of 16 lanes (distinct words, plain adds);
+                    // linear: one pass with shared-memory atomics (its four taps
+                    // cannot be ordered so that lanes never meet).
+                    for (int pass = 0; pass < (CUBIC ? 2 : 1); ++pass) {
+                        if (live && (!CUBIC || (lane >> 4) == pass)) {
                             if constexpr (CUBIC) {
                                 const int cx = (lane - lx) & 3, cy = ((lane >> 2) - ly) & 3;
                                 float wx[4], wy[4];
@@ -473,9 +478,8 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
                                     for (int jx = 0; jx < 2; ++jx) {
                                         const int at = tidx(g, lx + jx, y);
                                         if (!TP_CHECK(q.dbg, at >= 0 && at < total, 4)) continue;
-                                        float2 a = plane[at];
-                                        cfma(w[0][jx], cy2, a);
-                                        plane[at] = a;
+                                        atomicAdd(&plane[at].x, w[0][jx] * cy2.x);
+                                        atomicAdd(&plane[at].y, w[0][jx] * cy2.y);
                                     }
                                 }
                             }
