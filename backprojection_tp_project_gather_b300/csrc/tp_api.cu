@@ -155,7 +155,7 @@ tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, 
     float2 *o = reinterpret_cast<float2 *>(out);
     return launched(dim == 3 ? tp::launch_brick_project(g.cubic, g.q, o, reinterpret_cast<float2 *>(dout),
                                                         ws, tp::kBinNew, s)
-                             : tp::plane2d_fits(M) ? tp::launch_plane2d_project(g.cubic, g.q, o, s)
+                             : tp::plane2d_fits(M, N) ? tp::launch_plane2d_project(g.cubic, g.q, o, s)
                                                    : tp::launch_project_2d(g.cubic, g.q, o, s),
                     "project");
 }
@@ -186,7 +186,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
         cudaError_t e = dim == 3
                             ? tp::launch_brick_pose_grad(g.cubic, g.q, go, grad_rot, grad_shift, ws,
                                                          mode, s)
-                            : tp::plane2d_fits(M)
+                            : tp::plane2d_fits(M, N)
                                 ? tp::launch_plane2d_pose_grad(g.cubic, g.q, go, grad_rot, grad_shift, s)
                                 : tp::launch_pose_grad_2d(g.cubic, g.q, go, grad_rot, grad_shift, s);
         if (e != cudaSuccess) return launched(e, "pose gradient");
@@ -199,8 +199,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
         cudaError_t e = dim == 3
                             ? tp::launch_brick_scatter(g.cubic, g.q, go, nullptr, gs, nullptr, ws,
                                                        mode, s)
-                            : tp::plane2d_fits(M) ? tp::launch_plane2d_scatter(g.cubic, g.q, go, gs, s)
-                                                  : tp::launch_scatter_2d(g.cubic, g.q, go, gs, s);
+                            : tp::launch_scatter_2d(g.cubic, g.q, go, gs, s);
         if (e != cudaSuccess) return launched(e, "spectrum gradient");
         if (opts.flags & TP_FLAG_HERMITIAN_X0) {
             e = tp::launch_hermitian_x0(gs, nullptr, Bsrc, M, dim, s, g.q.dbg);

@@ -22,16 +22,13 @@ cudaError_t launch_pose_grad_2d(bool cubic, const Params &q, const float2 *grad_
                                 float *grad_rot, float *grad_shift, cudaStream_t st);
 
 // The same two operators with the whole Friedel-completed source plane staged
-// in shared memory (tp_plane2d.cu), for source boxes whose plane fits a
-// block's shared memory (plane2d_fits).
-bool plane2d_fits(int M);
+// in shared memory (tp_plane2d.cu), for source box M and output box N whose
+// plane (and phase tables) fit a block's shared memory (plane2d_fits).
+bool plane2d_fits(int M, int N);
 cudaError_t launch_plane2d_project(bool cubic, const Params &q, float2 *out, cudaStream_t st);
 cudaError_t launch_plane2d_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
                                      float *grad_rot, float *grad_shift, cudaStream_t st);
-// Image gradient on the staged-plane layout (q.src / q.Bsrc describe the
-// destination spectrum, as for launch_scatter_2d).
-cudaError_t launch_plane2d_scatter(bool cubic, const Params &q, const float2 *img, float2 *dst,
-                                   cudaStream_t st);
+
 
 // Adjoint scatter of img (same layout as a forward output) into the 2D
 // spectrum dst (+=) (tp_scatter.cu).  q.src / q.Bsrc describe the

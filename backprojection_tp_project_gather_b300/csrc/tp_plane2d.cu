@@ -27,11 +27,19 @@
 //    their source, which then stays staged).  Threads take output pixels in
 //    row order (coalesced reads of the upstream gradient and writes of the
 //    output); pixels outside the radius are written as zeros by the forward.
+//  - Phase.  The shift phase is separable, exp(-2 pi i (kx sx + ky sy) / N) =
+//    exp(-2 pi i kx sx / N) exp(-2 pi i ky sy / N): per pose the block
+//    tabulates both factors in shared memory (N/2 + 1 and N values, each from
+//    the exactly period-reduced cycle count), and a pixel multiplies two
+//    table entries instead of evaluating a sine and a cosine.
 //
 // The forward gives out = phase * S(p); with GRAD the same gather also forms
 // the derivative weights and reduces, per pose, dL/dR[i][a] = s k_i dL/dp_a and
 // dL/dshift_a (the analytic gradients of [de §3 item 4; ar §2]) over the block,
-// adding them to grad_rot / grad_shift with one atomic per entry.
+// adding them to grad_rot / grad_shift with one atomic per entry.  (The
+// image gradient stays on the tiled scatter of tp_scatter.cu: accumulating
+// into a shared plane measured slower there, with warps that own bands of
+// rows stalled on the busiest band and with shared-memory atomics.)
 //
 // Method: "torch-projectors: A High-Performance Differentiable Projection
 // Library for PyTorch", 2D -> 2D forward and its gradients [it §2 "Operazioni
@@ -69,9 +77,18 @@ __host__ __device__ inline PlaneGeo plane_geo(int M) {
     return g;
 }
 
-__host__ __device__ inline size_t plane_smem_bytes(int M) {
+// Complex words of the phase tables of one pose (N/2 + 1 column and N row
+// factors), rounded up to an even count so that what follows stays 16-byte
+// aligned.
+__host__ __device__ inline int table_words(int N) { return (N + N / 2 + 1 + 1) & ~1; }
+
+// Shared memory of a launch: the plane, the phase tables and, for the
+// gathers, the raw buffer of the next source image (16-byte aligned: W^2 and
+// the table words are even).
+__host__ __device__ inline size_t plane_smem_bytes(int M, int N, bool raw) {
     const PlaneGeo g = plane_geo(M);
-    return sizeof(float2) * ((size_t)g.W * g.W + (size_t)g.raw_words);
+    return sizeof(float2) * ((size_t)g.W * g.W + (size_t)table_words(N) +
+                             (raw ? (size_t)g.raw_words : 0));
 }
 
 // Tiled index of local element (lx, ly).
@@ -79,8 +96,34 @@ __device__ __forceinline__ int tidx(const PlaneGeo &g, int lx, int ly) {
     return ((ly >> 2) * g.TW + (lx >> 2)) * 16 + (lx & 3) + 4 * (ly & 3);
 }
 
+// Quotient and remainder of e by d (e < 2^24, inv = 1/d rounded) without an
+// integer division: the float quotient is off by at most one.
+__device__ __forceinline__ int divmod(int e, int d, float inv, int &rem) {
+    int quo = (int)((float)e * inv);
+    int r = e - quo * d;
+    if (r < 0) {
+        --quo;
+        r += d;
+    } else if (r >= d) {
+        ++quo;
+        r -= d;
+    }
+    rem = r;
+    return quo;
+}
+
+// r[i] = v[(i + c) mod 4] with static register indexes (two selects per
+// entry): the per-lane rotation of a cubic stencil's separable weights.
+__device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) {
+    float t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = (c & 1) ? v[(i + 1) & 3] : v[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = (c & 2) ? t[(i + 2) & 3] : t[i];
+}
+
 // Issue the copy of one stored source image (raw_words complex words at src)
-// into the raw buffer; the caller commits the group.
+// into the raw buffer and commit it as one group.
 __device__ __forceinline__ void issue_raw_copy(const float2 *src, int words, float2 *raw,
                                                bool vec16) {
     const unsigned sbase = (unsigned)__cvta_generic_to_shared(raw);
@@ -102,14 +145,16 @@ __device__ __forceinline__ void issue_raw_copy(const float2 *src, int words, flo
 
 // Fill the tiled virtual plane from the raw stored image: direct side
 // n_x >= 0 reads V[n], Friedel side conj(V[-n]); zero outside the stored
-// range.  Threads walk the plane in tiled order, so their writes are
+// range.  Half-warps take whole 4 x 4 tiles, so their writes are 16
 // consecutive words.
 __device__ __forceinline__ void unpack_plane(const PlaneGeo &g, const float2 *raw, float2 *plane,
                                              unsigned *dbg) {
-    const int total = g.W * g.W;
-    for (int j = threadIdx.x; j < total; j += kPlaneThreads) {
-        const int tile = j >> 4, r = j & 15;
-        const int ty = tile / g.TW, tx = tile - ty * g.TW;
+    const int ntiles = g.TW * g.TW;
+    const float inv = 1.0f / (float)g.TW;
+    for (int t = threadIdx.x >> 4; t < ntiles; t += kPlaneThreads >> 4) {
+        int tx;
+        const int ty = divmod(t, g.TW, inv, tx);
+        const int r = threadIdx.x & 15;
         const int vx = g.X0 + 4 * tx + (r & 3), vy = g.X0 + 4 * ty + (r >> 2);
         const bool cj = vx < 0;
         const int mx = cj ? -vx : vx, my = cj ? -vy : vy;
@@ -121,25 +166,51 @@ __device__ __forceinline__ void unpack_plane(const PlaneGeo &g, const float2 *ra
                 if (cj) v.y = -v.y;
             }
         }
-        plane[j] = v;
+        plane[16 * t + r] = v;
     }
 }
 
-// r[i] = v[(i + c) mod 4] with static register indexes (two selects per
-// entry): the per-lane rotation of a cubic stencil's separable weights.
-__device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) {
-    float t[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) t[i] = (c & 1) ? v[(i + 1) & 3] : v[i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = (c & 2) ? t[(i + 2) & 3] : t[i];
+// The two factors of the shift phase of one pose: phx[kx] = exp(-2 pi i kx sx / N)
+// for kx = 0 .. N/2 and phy[iy] = exp(-2 pi i ky(iy) sy / N) for iy = 0 .. N-1,
+// each from the exactly period-reduced cycle count (frac_cycles).
+__device__ __forceinline__ void phase_tables(const Params &q, float sx, float sy, float2 *phx,
+                                             float2 *phy) {
+    for (int i = threadIdx.x; i < q.N + q.Xo; i += kPlaneThreads) {
+        const bool col = i < q.Xo;
+        const int k = col ? i : row_freq(i - q.Xo, q.N);
+        float sn, cs;
+        sincospif(-2.0f * frac_cycles(k, col ? sx : sy, q.fN, q.invN), &sn, &cs);
+        (col ? phx[i] : phy[i - q.Xo]) = make_float2(cs, sn);
+    }
 }
 
 // Weighted sum over the stencil of the sample at local tap origin (lx, ly)
 // (the local coordinates of tap floor(p) - LO), with derivative weights when
 // DERIV.  Cubic visits the taps in the lane-rotated order described above.
+//
+// At step sx a lane reads the tap whose x is (sx + lane) mod 4 (its
+// residue rho); within [lx, lx + 3] that is x = 4 ((lx + 3 - rho) >> 2) + rho,
+// so the tiled x offset is 16 ((lx + 3 - rho) >> 2) + rho, and likewise in y
+// with the residue (sy + lane / 4) mod 4.  The residues are the lane's own
+// and are passed in precomputed.
+struct LaneRes {
+    int rx[4], ry[4];   // tap residues of the steps
+};
+
+__device__ __forceinline__ LaneRes lane_residues() {
+    LaneRes r;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.rx[i] = (i + lane) & 3;
+        r.ry[i] = (i + (lane >> 2)) & 3;
+    }
+    return r;
+}
+
 template <bool CUBIC, bool DERIV>
-__device__ __forceinline__ void gather_plane(const PlaneGeo &g, const float2 *plane, int lx, int ly,
+__device__ __forceinline__ void gather_plane(const PlaneGeo &g, const LaneRes &res,
+                                             const float2 *plane, int lx, int ly,
                                              const float (&w)[2][4], const float (&d)[2][4],
                                              float2 &S, float2 (&dS)[2], unsigned *dbg) {
     S = make_float2(0.f, 0.f);
@@ -155,15 +226,18 @@ __device__ __forceinline__ void gather_plane(const PlaneGeo &g, const float2 *pl
             rot4(d[0], cx, dx);
             rot4(d[1], cy, dy);
         }
+        int ox[4], oy[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ox[i] = ((lx + 3 - res.rx[i]) >> 2) * 16 + res.rx[i];
+            oy[i] = ((ly + 3 - res.ry[i]) >> 2) * (16 * g.TW) + 4 * res.ry[i];
+        }
 #pragma unroll
         for (int sy = 0; sy < 4; ++sy) {
-            const int y = ly + ((sy + cy) & 3);
-            const int rowb = (y >> 2) * (16 * g.TW) + 4 * (y & 3);
             float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
             for (int sx = 0; sx < 4; ++sx) {
-                const int x = lx + ((sx + cx) & 3);
-                const int at = rowb + (x >> 2) * 16 + (x & 3);
+                const int at = oy[sy] + ox[sx];
                 if (!TP_CHECK(dbg, at >= 0 && at < total, 2)) continue;
                 const float2 v = plane[at];
                 cfma(wx[sx], v, r0);
@@ -177,22 +251,22 @@ __device__ __forceinline__ void gather_plane(const PlaneGeo &g, const float2 *pl
         }
     } else {
 #pragma unroll
-    for (int jy = 0; jy < 2; ++jy) {
-        float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+        for (int jy = 0; jy < 2; ++jy) {
+            float2 r0 = make_float2(0.f, 0.f), r1 = r0;
 #pragma unroll
-        for (int jx = 0; jx < 2; ++jx) {
-            const int at = tidx(g, lx + jx, ly + jy);
-            if (!TP_CHECK(dbg, at >= 0 && at < total, 2)) continue;
-            const float2 v = plane[at];
-            cfma(w[0][jx], v, r0);
-            if (DERIV) cfma(d[0][jx], v, r1);
+            for (int jx = 0; jx < 2; ++jx) {
+                const int at = tidx(g, lx + jx, ly + jy);
+                if (!TP_CHECK(dbg, at >= 0 && at < total, 2)) continue;
+                const float2 v = plane[at];
+                cfma(w[0][jx], v, r0);
+                if (DERIV) cfma(d[0][jx], v, r1);
+            }
+            cfma(w[1][jy], r0, S);
+            if (DERIV) {
+                cfma(w[1][jy], r1, dS[0]);
+                cfma(d[1][jy], r0, dS[1]);
+            }
         }
-        cfma(w[1][jy], r0, S);
-        if (DERIV) {
-            cfma(w[1][jy], r1, dS[0]);
-            cfma(d[1][jy], r0, dS[1]);
-        }
-    }
     }
 }
 
@@ -210,24 +284,49 @@ __device__ __forceinline__ int image_of(const Params &q, int v, int j) {
     return (q.Bsrc == 1) ? j : v * q.P + j;
 }
 
+// Stencil of the pixel (kx, ky) of pose ps: local tap origin and weights.
+// Returns false when the stencil leaves the staged region, i.e. lies wholly
+// outside the stored range.
+template <bool CUBIC, bool DERIV>
+__device__ __forceinline__ bool stencil_at(const PlaneGeo &g, const Pose<2> &ps, int kx, int ky,
+                                           int &lx, int &ly, float (&w)[2][4], float (&d)[2][4]) {
+    using St = Stencil<CUBIC>;
+    float t;
+    const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)ky);
+    const float py = fmaf(ps.a[1], (float)kx, ps.b[1] * (float)ky);
+    lx = split_coord(px, t) - St::LO - g.X0;
+    St::weights(t, w[0]);
+    if (DERIV) St::derivs(t, d[0]);
+    ly = split_coord(py, t) - St::LO - g.X0;
+    St::weights(t, w[1]);
+    if (DERIV) St::derivs(t, d[1]);
+    const unsigned lim = (unsigned)(g.W - (St::LO + St::HI + 1));
+    return (unsigned)lx <= lim && (unsigned)ly <= lim;
+}
+
 template <bool CUBIC, bool GRAD>
 __global__ void __launch_bounds__(kPlaneThreads, 1)
     k_plane2d(Params q, Items it, bool vec16, float2 *__restrict__ out,
               const float2 *__restrict__ g_out, float *__restrict__ grad_rot,
               float *__restrict__ grad_shift) {
-    using St = Stencil<CUBIC>;
     extern __shared__ float4 s_plane4[];
     __shared__ float s_red[kPlaneWarps][6];
     const PlaneGeo g = plane_geo(q.M);
     float2 *plane = reinterpret_cast<float2 *>(s_plane4);
-    float2 *raw = plane + (size_t)g.W * g.W;
+    float2 *phx = plane + (size_t)g.W * g.W;
+    float2 *phy = phx + q.Xo;
+    float2 *raw = phx + table_words(q.N);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int first = (int)((long long)it.count * blockIdx.x / gridDim.x);
     const int last = (int)((long long)it.count * (blockIdx.x + 1) / gridDim.x);
     if (first >= last) return;
-    const int span = St::LO + St::HI + 1;   // stencil width
     const int npix = q.N * q.Xo;
-    const int half_n = q.N >> 1;
+    const LaneRes res = lane_residues();
+    // Pixel e = threadIdx.x + k * kPlaneThreads as (row, column), advanced
+    // without a division: the stride is dq rows and dr columns.
+    int iy0, kx0;
+    iy0 = divmod(threadIdx.x, q.Xo, 1.0f / (float)q.Xo, kx0);
+    const int dq = kPlaneThreads / q.Xo, dr = kPlaneThreads - dq * q.Xo;
     int staged = -1;   // source held in the plane
     issue_raw_copy(q.src + (size_t)(first / it.per_src) * q.src_stride, g.raw_words, raw, vec16);
     for (int i = first; i < last; ++i) {
@@ -252,48 +351,50 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
             const int bp = image_of(q, v, j);
             const int b = bp / q.P, pi = bp - b * q.P;
             const Pose<2> ps = load_pose<2>(q, b, pi);
+            if (q.shift) {
+                __syncthreads();   // the previous pose's tables are no longer read
+                phase_tables(q, ps.sx, ps.sy, phx, phy);
+                __syncthreads();
+            }
             float acc[6];
 #pragma unroll
             for (int k = 0; k < 6; ++k) acc[k] = 0.f;
             const size_t ob = (size_t)bp * q.plane;
+            int iy = iy0, kx = kx0;
             for (int e = threadIdx.x; e < npix; e += kPlaneThreads) {
-                const int iy = e / q.Xo, kx = e - iy * q.Xo;
-                const int ky = iy < half_n ? iy : iy - q.N;
-                const bool inside = kx * kx + ky * ky <= q.r2max;
-                if (!GRAD && !inside) {
-                    out[ob + e] = make_float2(0.f, 0.f);
+                const int ry = iy, rx = kx;
+                kx += dr;
+                iy += dq;
+                if (kx >= q.Xo) {
+                    kx -= q.Xo;
+                    ++iy;
+                }
+                const int ky = row_freq(ry, q.N);
+                if (rx * rx + ky * ky > q.r2max) {
+                    if (!GRAD) out[ob + e] = make_float2(0.f, 0.f);
                     continue;
                 }
-                if (GRAD && !inside) continue;
-                float w[2][4], d[2][4], t;
-                const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)ky);
-                const float py = fmaf(ps.a[1], (float)kx, ps.b[1] * (float)ky);
-                const int lx = split_coord(px, t) - St::LO - g.X0;
-                St::weights(t, w[0]);
-                if (GRAD) St::derivs(t, d[0]);
-                const int ly = split_coord(py, t) - St::LO - g.X0;
-                St::weights(t, w[1]);
-                if (GRAD) St::derivs(t, d[1]);
+                float2 gv = make_float2(0.f, 0.f);
+                if (GRAD) gv = __ldg(g_out + ob + e);   // in flight during the gather
+                float w[2][4], d[2][4];
+                int lx, ly;
                 float2 S = make_float2(0.f, 0.f), dS[2] = {S, S};
-                // A stencil leaving the region lies wholly outside the stored range.
-                if ((unsigned)lx <= (unsigned)(g.W - span) && (unsigned)ly <= (unsigned)(g.W - span))
-                    gather_plane<CUBIC, GRAD>(g, plane, lx, ly, w, d, S, dS, q.dbg);
-                float2 ph = make_float2(1.f, 0.f);
-                if (q.shift) ph = shift_phase(kx, ky, ps.sx, ps.sy, q.fN, q.invN);
+                if (stencil_at<CUBIC, GRAD>(g, ps, rx, ky, lx, ly, w, d))
+                    gather_plane<CUBIC, GRAD>(g, res, plane, lx, ly, w, d, S, dS, q.dbg);
+                const float2 ph = q.shift ? cmul(phx[rx], phy[ry]) : make_float2(1.f, 0.f);
                 if (!GRAD) {
                     out[ob + e] = cmul(ph, S);
                 } else {
-                    const float2 gv = __ldg(g_out + ob + e);
                     const float2 gq = cmul_conj_a(ph, gv);   // conj(phase) * g
 #pragma unroll
                     for (int a = 0; a < 2; ++a) {
                         const float dl = gq.x * dS[a].x + gq.y * dS[a].y;   // dL/dp_a
-                        acc[a] = fmaf(q.s * (float)kx, dl, acc[a]);
+                        acc[a] = fmaf(q.s * (float)rx, dl, acc[a]);
                         acc[2 + a] = fmaf(q.s * (float)ky, dl, acc[2 + a]);
                     }
                     const float2 y = cmul(ph, S);
                     const float qv = 6.283185307179586f * q.invN * (gv.x * y.y - gv.y * y.x);
-                    acc[4] = fmaf((float)kx, qv, acc[4]);
+                    acc[4] = fmaf((float)rx, qv, acc[4]);
                     acc[5] = fmaf((float)ky, qv, acc[5]);
                 }
             }
@@ -327,196 +428,6 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Image gradient (the real adjoint of the forward applied to an upstream
-// gradient): the staged plane is the accumulator.  Warp w owns the tile rows
-// [w TW / 16, (w + 1) TW / 16) of it and no other warp writes there, so the
-// spreading needs no atomics.  For every pose of an item a warp enumerates
-// the pixels whose stencil rows meet its band (rows of the output image, each
-// with its qx interval from the slab of p_y, packed into 32-lane rounds by a
-// warp prefix sum), sets up one sample per lane and spreads the taps that lie
-// in its band.  Cubic spreads with lanes 0-15 and then lanes 16-31: with the
-// lane-rotated tap order the 16 lanes of a pass touch 16 different bank
-// pairs, hence 16 different words, so the plain read-add-write never races.
-// Linear (four taps, which no lane order keeps apart) adds with shared-memory
-// atomics instead.  After the item
-// the block folds the plane into the stored half-spectrum -- G[m] = A[m] +
-// conj(A[-m]) for m_x > 0 (the Friedel taps' share), A[m] for m_x = 0 -- and
-// adds it to the gradient: plainly when the block owns every pose of that
-// source image, else with vector atomics.
-template <bool CUBIC>
-__global__ void __launch_bounds__(kPlaneThreads, 1)
-    k_plane2d_scatter(Params q, Items it, bool exclusive, const float2 *__restrict__ g_in,
-                      float2 *__restrict__ dst) {
-    using St = Stencil<CUBIC>;
-    extern __shared__ float4 s_plane4[];
-    const PlaneGeo g = plane_geo(q.M);
-    float2 *plane = reinterpret_cast<float2 *>(s_plane4);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int first = (int)((long long)it.count * blockIdx.x / gridDim.x);
-    const int last = (int)((long long)it.count * (blockIdx.x + 1) / gridDim.x);
-    const int span = St::LO + St::HI + 1;
-    const int total = g.W * g.W;
-    // This warp's band of plane rows (local coordinates) and the sample rows
-    // floor(p_y) whose stencils reach into it.
-    const int ylo = 4 * (warp * g.TW / kPlaneWarps), yhi = 4 * ((warp + 1) * g.TW / kPlaneWarps);
-    const float pylo = (float)(ylo - (span - 1) + St::LO + g.X0);   // floor(p_y) >= this
-    const float pyhi = (float)(yhi + St::LO + g.X0);                // p_y < this
-    const int half_n = q.N >> 1;
-    const int rmax = (int)floorf(sqrtf((float)q.r2max));
-    for (int i = first; i < last; ++i) {
-        const int v = i / it.per_src;
-        for (int j = threadIdx.x; j < total; j += kPlaneThreads) plane[j] = make_float2(0.f, 0.f);
-        __syncthreads();
-        const int c = i - v * it.per_src;
-        const int j1 = min((c + 1) * it.chunk, it.pps);
-        for (int j = c * it.chunk; j < j1; ++j) {
-            const int bp = image_of(q, v, j);
-            const int b = bp / q.P, pi = bp - b * q.P;
-            const Pose<2> ps = load_pose<2>(q, b, pi);
-            const float a1 = ps.a[1], b1 = ps.b[1];   // p_y = a1 kx + b1 ky
-            const float ia1 = fabsf(a1) > 1e-6f ? 1.0f / a1 : 0.f;
-            const float2 *gim = g_in + (size_t)bp * q.plane;
-            const int qy0 = max(-half_n, -rmax), qy1 = min(half_n - 1, rmax);
-            for (int base = qy0; base <= qy1; base += 32) {
-                const int ky = base + lane;
-                int xs = 0, cnt = 0;
-                if (ky <= qy1) {
-                    const int rr = q.r2max - ky * ky;
-                    float xl = 0.f, xh = (float)min(half_n, (int)floorf(sqrtf((float)max(rr, 0))));
-                    bool empty = rr < 0;
-                    const float by = (float)ky * b1;
-                    if (ia1 != 0.f) {
-                        const float t1 = (pylo - 0.01f - by) * ia1, t2 = (pyhi + 0.01f - by) * ia1;
-                        xl = fmaxf(xl, fminf(t1, t2));
-                        xh = fminf(xh, fmaxf(t1, t2));
-                    } else if (by < pylo - 0.01f || by > pyhi + 0.01f) {
-                        empty = true;
-                    }
-                    if (!empty && xl <= xh) {
-                        xs = (int)ceilf(xl);
-                        cnt = max(0, (int)floorf(xh) - xs + 1);
-                    }
-                }
-                int incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int x = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += x;
-                }
-                const int ntot = __shfl_sync(0xffffffffu, incl, 31);
-                const int excl = incl - cnt;
-                for (int i0 = 0; i0 < ntot; i0 += 32) {
-                    const int k = i0 + lane;
-                    int r = 0;
-#pragma unroll
-                    for (int step = 16; step > 0; step >>= 1) {
-                        const int x = __shfl_sync(0xffffffffu, incl, r + step - 1);
-                        if (x <= k) r += step;
-                    }
-                    r = min(r, 31);
-                    const int kx = __shfl_sync(0xffffffffu, xs, r) + (k - __shfl_sync(0xffffffffu, excl, r));
-                    const int kyr = base + r;
-                    // One sample per lane: its stencil, the tap origin and the value.
-                    bool live = k < ntot;
-                    float w[2][4];
-                    int lx = 0, ly = 0;
-                    float2 cv = make_float2(0.f, 0.f);
-                    if (live) {
-                        float t;
-                        const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)kyr);
-                        const float py = fmaf(a1, (float)kx, b1 * (float)kyr);
-                        lx = split_coord(px, t) - St::LO - g.X0;
-                        St::weights(t, w[0]);
-                        ly = split_coord(py, t) - St::LO - g.X0;
-                        St::weights(t, w[1]);
-                        // in the region, and some stencil row in this band
-                        live = (unsigned)lx <= (unsigned)(g.W - span) &&
-                               (unsigned)ly <= (unsigned)(g.W - span) && ly + span > ylo && ly < yhi;
-                        if (live) {
-                            const int iy = kyr < 0 ? kyr + q.N : kyr;
-                            if (TP_CHECK(q.dbg, iy >= 0 && iy < q.N && kx >= 0 && kx < q.Xo, 7)) {
-                                cv = __ldg(gim + iy * q.Xo + kx);
-                                if (q.shift)
-                                    cv = cmul_conj_a(shift_phase(kx, kyr, ps.sx, ps.sy, q.fN, q.invN), cv);
-                            }
-                        }
-                    }
-                    // Cubic: two passes of 16 lanes (distinct words, plain adds);
-                    // linear: one pass with shared-memory atomics (its four taps
-                    // cannot be ordered so that lanes never meet).
-                    for (int pass = 0; pass < (CUBIC ? 2 : 1); ++pass) {
-                        if (live && (!CUBIC || (lane >> 4) == pass)) {
-                            if constexpr (CUBIC) {
-                                const int cx = (lane - lx) & 3, cy = ((lane >> 2) - ly) & 3;
-                                float wx[4], wy[4];
-                                rot4(w[0], cx, wx);
-                                rot4(w[1], cy, wy);
-#pragma unroll
-                                for (int sy = 0; sy < 4; ++sy) {
-                                    const int y = ly + ((sy + cy) & 3);
-                                    if (y < ylo || y >= yhi) continue;
-                                    const int rowb = (y >> 2) * (16 * g.TW) + 4 * (y & 3);
-                                    const float2 cy2 = make_float2(wy[sy] * cv.x, wy[sy] * cv.y);
-#pragma unroll
-                                    for (int sx = 0; sx < 4; ++sx) {
-                                        const int x = lx + ((sx + cx) & 3);
-                                        const int at = rowb + (x >> 2) * 16 + (x & 3);
-                                        if (!TP_CHECK(q.dbg, at >= 0 && at < total, 4)) continue;
-                                        float2 a = plane[at];
-                                        cfma(wx[sx], cy2, a);
-                                        plane[at] = a;
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int jy = 0; jy < 2; ++jy) {
-                                    const int y = ly + jy;
-                                    if (y < ylo || y >= yhi) continue;
-                                    const float2 cy2 = make_float2(w[1][jy] * cv.x, w[1][jy] * cv.y);
-#pragma unroll
-                                    for (int jx = 0; jx < 2; ++jx) {
-                                        const int at = tidx(g, lx + jx, y);
-                                        if (!TP_CHECK(q.dbg, at >= 0 && at < total, 4)) continue;
-                                        atomicAdd(&plane[at].x, w[0][jx] * cy2.x);
-                                        atomicAdd(&plane[at].y, w[0][jx] * cy2.y);
-                                    }
-                                }
-                            }
-                        }
-                        __syncwarp();
-                    }
-                }
-            }
-        }
-        __syncthreads();   // every band spread
-        // Fold into the stored half-spectrum of source v.
-        float2 *V = dst + (size_t)v * q.src_stride;
-        for (int e = threadIdx.x; e < g.raw_words; e += kPlaneThreads) {
-            const int row = e / g.Xs, mx = e - row * g.Xs;
-            const int my = row < g.half ? row : row - g.M;
-            const int lxm = mx - g.X0, lym = my - g.X0;
-            float2 val = plane[tidx(g, lxm, lym)];
-            if (mx > 0) {
-                const float2 f = plane[tidx(g, -mx - g.X0, -my - g.X0)];
-                val.x += f.x;
-                val.y -= f.y;
-            }
-            if (val.x == 0.f && val.y == 0.f) continue;
-            if (!TP_CHECK(q.dbg, e < g.raw_words, 6)) continue;
-            if (exclusive) {
-                float2 o = V[e];
-                o.x += val.x;
-                o.y += val.y;
-                V[e] = o;
-            } else {
-                atomicAdd(V + e, val);
-            }
-        }
-        __syncthreads();   // the plane is zeroed again for the next item
-    }
-}
-
 int sm_count() {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -541,7 +452,7 @@ template <bool CUBIC, bool GRAD>
 cudaError_t plane_launch(const Params &q, float2 *out, const float2 *g, float *grot, float *gshift,
                          cudaStream_t st) {
     if ((long long)q.B * q.P == 0) return cudaSuccess;
-    const size_t smem = plane_smem_bytes(q.M);
+    const size_t smem = plane_smem_bytes(q.M, q.N, true);
     auto kern = k_plane2d<CUBIC, GRAD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -553,42 +464,20 @@ cudaError_t plane_launch(const Params &q, float2 *out, const float2 *g, float *g
     return cudaGetLastError();
 }
 
-template <bool CUBIC>
-cudaError_t plane_scatter_launch(const Params &q, const float2 *img, float2 *dst, cudaStream_t st) {
-    if ((long long)q.B * q.P == 0) return cudaSuccess;
-    const PlaneGeo g = plane_geo(q.M);
-    const size_t smem = sizeof(float2) * (size_t)g.W * g.W;
-    auto kern = k_plane2d_scatter<CUBIC>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int sms = sm_count();
-    const Items it = make_items(q, sms);
-    const int blocks = it.count < sms ? it.count : sms;
-    // A block owns a source's gradient when that source's poses form one item.
-    kern<<<blocks, kPlaneThreads, smem, st>>>(q, it, it.per_src == 1, img, dst);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
-bool plane2d_fits(int M) {
+bool plane2d_fits(int M, int N) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return false;
     // The static reduction array and a margin for the runtime's own use.
-    return plane_smem_bytes(M) + 1024 <= (size_t)optin;
+    return plane_smem_bytes(M, N, true) + 1024 <= (size_t)optin;
 }
 
 cudaError_t launch_plane2d_project(bool cubic, const Params &q, float2 *out, cudaStream_t st) {
     return cubic ? plane_launch<true, false>(q, out, nullptr, nullptr, nullptr, st)
                  : plane_launch<false, false>(q, out, nullptr, nullptr, nullptr, st);
-}
-
-cudaError_t launch_plane2d_scatter(bool cubic, const Params &q, const float2 *img, float2 *dst,
-                                   cudaStream_t st) {
-    return cubic ? plane_scatter_launch<true>(q, img, dst, st)
-                 : plane_scatter_launch<false>(q, img, dst, st);
 }
 
 cudaError_t launch_plane2d_pose_grad(bool cubic, const Params &q, const float2 *grad_out,

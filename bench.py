@@ -77,8 +77,10 @@ def parse_args():
                     help="interpolation of the project and backproject workloads")
     ap.add_argument("--oversampling", type=int, default=1, choices=[1, 2],
                     help="oversampling of the project workload (2: the 256^3 padded spectrum)")
-    ap.add_argument("--ncu-summary", metavar="RAW_CSV", default=None,
-                    help="write profiles/ncu_traffic.json from `ncu -i REP --page raw --csv` output")
+    ap.add_argument("--ncu-summary", metavar="RAW_CSV", nargs="+", default=None,
+                    help="write profiles/ncu_traffic.json from `ncu -i REP --page raw --csv` "
+                         "exports (one capture per kernel; the first launch of each kernel in "
+                         "the order given is kept)")
     return ap.parse_args()
 
 
@@ -290,33 +292,40 @@ UNIT_SCALE = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "M
               "%": 1, "register/thread": 1, "": 1}
 
 
-def ncu_summary(csv_path, out_path):
-    """Write profiles/ncu_traffic.json from `ncu -i <rep> --page raw --csv` output.
+def ncu_summary(csv_paths, out_path):
+    """Write profiles/ncu_traffic.json from `ncu -i <rep> --page raw --csv` exports.
 
     One entry per bench segment with the captured launch's DRAM bytes, duration
     and throughput percentages, tagged with the hash of the kernel sources so
-    that a stale summary is never reported against changed kernels."""
+    that a stale summary is never reported against changed kernels.  Each
+    export may hold one kernel (one capture per kernel) or several; the first
+    launch of each kernel is kept."""
     import csv
-    rows = list(csv.reader(open(csv_path)))
-    hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
-    names, units = rows[hdr], rows[hdr + 1]
-    col = {n: i for i, n in enumerate(names)}
+    if isinstance(csv_paths, str):
+        csv_paths = [csv_paths]
     kernels = {}
-    for r in rows[hdr + 2:]:
-        if len(r) != len(names):
-            continue
-        kname = r[col["Kernel Name"]]
-        seg = next((s for s, k in NCU_KERNELS.items() if k + "<" in kname or k + "(" in kname), None)
-        if seg is None or seg in kernels:
-            continue
-        d = {"kernel": kname.split("(")[0]}
-        for m, key in NCU_METRICS.items():
-            if m in col and r[col[m]] not in ("", "n/a"):
-                d[key] = float(r[col[m]].replace(",", "")) * UNIT_SCALE.get(units[col[m]], 1)
-        if "dram_read_bytes" in d and "dram_write_bytes" in d:
-            d["dram_bytes_per_launch"] = d["dram_read_bytes"] + d["dram_write_bytes"]
-        kernels[seg] = d
-    out = {"source_sha": kernel_source_sha(), "from": os.path.basename(csv_path), "kernels": kernels}
+    for csv_path in csv_paths:
+        rows = list(csv.reader(open(csv_path)))
+        hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+        names, units = rows[hdr], rows[hdr + 1]
+        col = {n: i for i, n in enumerate(names)}
+        for r in rows[hdr + 2:]:
+            if len(r) != len(names):
+                continue
+            kname = r[col["Kernel Name"]]
+            seg = next((s for s, k in NCU_KERNELS.items() if k + "<" in kname or k + "(" in kname),
+                       None)
+            if seg is None or seg in kernels:
+                continue
+            d = {"kernel": kname.split("(")[0]}
+            for m, key in NCU_METRICS.items():
+                if m in col and r[col[m]] not in ("", "n/a"):
+                    d[key] = float(r[col[m]].replace(",", "")) * UNIT_SCALE.get(units[col[m]], 1)
+            if "dram_read_bytes" in d and "dram_write_bytes" in d:
+                d["dram_bytes_per_launch"] = d["dram_read_bytes"] + d["dram_write_bytes"]
+            kernels[seg] = d
+    out = {"source_sha": kernel_source_sha(),
+           "from": [os.path.basename(p) for p in csv_paths], "kernels": kernels}
     with open(out_path, "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")
@@ -928,9 +937,9 @@ def run_workload(args):
             ms, clocks = _timed(fn, args.steps, args.warmup, stream, flush)
             res[name] = {"ms": float(ms.mean())}
         # Accuracy against the exact transform of the density at the sample
-        # positions p = R^T k (box-M units), on the first 4 poses: separable
-        # sums over x, y, z as batched complex products.
-        Q = 4
+        # positions p = R^T k (box-M units), on the first Q poses: separable
+        # sums over x, y, z as batched complex products in float64.
+        Q = 16
         ky = torch.fft.fftfreq(M, 1.0 / M, device=dev, dtype=torch.float64)
         kx = torch.arange(M // 2 + 1, device=dev, dtype=torch.float64)
         KY, KX = torch.meshgrid(ky, kx, indexing="ij")
@@ -952,12 +961,39 @@ def run_workload(args):
                 t2 = torch.einsum("szy,sy->sz", t1, ey[sl])
                 vals[sl] = torch.einsum("sz,sz->s", t2, ez[sl])
             exact[q] = vals.reshape(M, M // 2 + 1) * inside
+        # Fourier shells of 1 pixel (|k| rounded) and real-space rings of 2 pixels
+        # about the image centre.
+        shell = torch.round(torch.sqrt(KX * KX + KY * KY)).long()
+        nshell = int(radius) + 1
+        cc = torch.arange(M, device=dev, dtype=torch.float64) - M // 2
+        ring = (torch.sqrt(cc[:, None] ** 2 + cc[None, :] ** 2) / 2).long()
+        nring = M // 4 + 1                                  # out to half the box
+        ex_img = torch.fft.fftshift(torch.fft.irfft2(exact, s=(M, M)), dim=(-2, -1))
+        ex_pow = torch.zeros(nring, dtype=torch.float64, device=dev).index_add_(
+            0, ring.flatten().clamp(max=nring - 1).repeat(Q), (ex_img ** 2).flatten())
         for name, fn in (("cubic_s1", cubic1), ("linear_s2", linear2), ("cubic_s2", cubic2)):
             fn(0)
             torch.cuda.synchronize()
             got = out[0, :Q].to(torch.complex128) * inside
             res[name]["rel_l2_vs_exact"] = float(torch.linalg.vector_norm(got - exact)
                                                  / torch.linalg.vector_norm(exact))
+            # Relative error per shell, over the Q poses.
+            e2 = torch.zeros(nshell, dtype=torch.float64, device=dev).index_add_(
+                0, shell[inside].repeat(Q), (torch.abs(got - exact)[:, inside] ** 2).flatten())
+            n2 = torch.zeros(nshell, dtype=torch.float64, device=dev).index_add_(
+                0, shell[inside].repeat(Q), (torch.abs(exact)[:, inside] ** 2).flatten())
+            curve = torch.sqrt(e2 / n2.clamp(min=1e-300)).cpu().numpy()
+            res[name]["shell_rel_error"] = [round(float(c), 6) for c in curve]
+            over = np.nonzero(curve > 0.1)[0]
+            res[name]["first_shell_over_10pct"] = int(over[0]) if len(over) else None
+            # Real-space intensity relative to the exact projection, ring by ring:
+            # sum(img * exact) / sum(exact^2) (1 = no falloff).
+            img = torch.fft.fftshift(torch.fft.irfft2(got, s=(M, M)), dim=(-2, -1))
+            cross = torch.zeros(nring, dtype=torch.float64, device=dev).index_add_(
+                0, ring.flatten().clamp(max=nring - 1).repeat(Q), (img * ex_img).flatten())
+            res[name]["realspace_gain_per_2px_ring"] = [
+                round(float(a / b), 5) if b > 1e-6 * float(ex_pow.max()) else None
+                for a, b in zip(cross.cpu().numpy(), ex_pow.cpu().numpy())]
         samples = P * M * (M // 2 + 1)
         line.update(metric="box-128 forward incl. rfftn (and the 2x padding for s = 2): ms per "
                            "4096 poses and rel. L2 error vs the exact transform",
@@ -965,6 +1001,9 @@ def run_workload(args):
                     ms_per_step=res["cubic_s1"]["ms"], results=res, clocks=clocks,
                     config={"workload": "oversampling-study-box128-4096poses",
                             "radius": radius, "exact_subset": f"first {Q} poses, in-radius pixels",
+                            "shells": "1-pixel |k| shells (rounded), rel. error over the subset",
+                            "realspace": "irfft2 of each projection vs the exact one, fftshifted, "
+                                         "2-pixel rings about the centre out to half the box",
                             "samples_per_step": samples,
                             "fft": "torch.fft.rfftn (cuFFT) inside the timed region"})
     print(json.dumps(line), flush=True)

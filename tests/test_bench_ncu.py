@@ -34,6 +34,21 @@ def _raw_csv(path):
         w.writerows(rows)
 
 
+def test_summary_merges_one_capture_per_kernel(tmp_path):
+    """Exports of separate single-kernel captures merge into one summary."""
+    a, b = tmp_path / "a.csv", tmp_path / "b.csv"
+    _raw_csv(a)
+    rows = list(csv.reader(open(a)))
+    with open(b, "w", newline="") as f:
+        w = csv.writer(f)
+        w.writerows(rows[:2])
+        w.writerow(["0", "k_pose_grad_saved(tp::Params)", "560", "3", "100", "73", "40"])
+    d = bench.ncu_summary([str(a), str(b)], str(tmp_path / "out.json"))
+    assert set(d["kernels"]) == {"project_3d_2d", "volume_grad_scatter", "pose_grad_saved"}
+    assert d["kernels"]["pose_grad_saved"]["dram_read_bytes"] == 560e6
+    assert d["from"] == ["a.csv", "b.csv"]
+
+
 def test_summary_scales_units_and_keeps_the_first_launch(tmp_path):
     src = tmp_path / "raw.csv"
     out = tmp_path / "ncu_traffic.json"
