@@ -567,8 +567,9 @@ __device__ __forceinline__ bool stored(int x, int y, int z, int half) {
 }
 
 // Stage brick + halo of the virtual spectrum into shared memory.  Every
-// element is one 8-byte cp.async (zero-filled outside the stored range), so
-// all copies of the block are in flight at once.  A thread keeps the same
+// element is one 8-byte cp.async (zero-filled outside the stored range, with
+// an L2 evict-last hint), so all copies of the block are in flight at once.
+// A thread keeps the same
 // (x, y) positions of the S x S layer in every z layer: whether its column
 // lies on the Friedel side (n_x < 0, read from -n), its source column and
 // its y row are fixed per brick, and each layer only adds the z row.  The
@@ -586,6 +587,10 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
               z0 = bx.o[2] - Stencil<CUBIC>::LO;
     const int MX = M * X;
     const unsigned sbase = (unsigned)__cvta_generic_to_shared(s);
+    // The spectrum is read by many bricks' stagings; ask L2 to keep it over
+    // the output images, which stream past it (written evict-first).
+    unsigned long long keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(keep));
     int at_xy[SLOTS], yoff[SLOTS];
     bool live[SLOTS], cj[SLOTS], okxy[SLOTS];
 #pragma unroll
@@ -611,8 +616,9 @@ __device__ __forceinline__ void stage(const float2 *__restrict__ V, int M, int X
             const int at = at_xy[k] + lz * (H::PX * H::PY);
             if (!TP_CHECK(dbg, off >= 0 && off < M * MX, 0)) continue;
             if (!TP_CHECK(dbg, at >= 0 && at < H::ELEMS, 1)) continue;
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(sbase + 8u * at),
-                         "l"(V + off), "r"(ok ? 8 : 0)
+            asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2, %3;\n" ::"r"(
+                             sbase + 8u * at),
+                         "l"(V + off), "r"(ok ? 8 : 0), "l"(keep)
                          : "memory");
         }
     }
@@ -742,7 +748,8 @@ __device__ __forceinline__ void gather_smem(const float2 *s, const int *l, float
 }
 
 // Owned-sample set-up: position, ownership and stencil of pixel (qx, qy).
-template <bool CUBIC, bool DERIV, int SIZE = kBS>
+// The box is SIZE voxels wide in x and y and SIZEZ in z.
+template <bool CUBIC, bool DERIV, int SIZE = kBS, int SIZEZ = SIZE>
 __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx, int qx, int qy,
                                            int *l, float (*w)[4], float (*d)[4]) {
     bool own = true;
@@ -752,7 +759,7 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
         float t;
         const int x0 = split_coord(p, t);
         l[a] = x0 - bx.o[a];
-        own = own && (unsigned)l[a] < (unsigned)SIZE;
+        own = own && (unsigned)l[a] < (unsigned)(a == 2 ? SIZEZ : SIZE);
         Stencil<CUBIC>::weights(t, w[a]);
         if (DERIV) Stencil<CUBIC>::derivs(t, d[a]);
     }
@@ -781,9 +788,10 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 
         const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
         if (!TP_CHECK(q.dbg, r0 + half < nout, 3)) continue;
-        for (int x = xcut + 1 + lane; x <= half; x += 32) out[r0 + x] = zero;
+        for (int x = xcut + 1 + lane; x <= half; x += 32) __stcs(out + r0 + x, zero);
         if (dout)
-            for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32) dout[3 * r0 + k] = zero;
+            for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32)
+                __stcs(dout + 3 * r0 + k, zero);
         if (xcut >= 0 && geo_reach(geo, bp) >= (float)G - 0.5f) {
             const PoseGeo g = load_geo(geo, bp);
             for (int x = lane; x <= xcut; x += 32) {
@@ -795,10 +803,10 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 
                     outside = outside || x0 < -G || x0 >= G;
                 }
                 if (outside) {
-                    out[r0 + x] = zero;
+                    __stcs(out + r0 + x, zero);
                     if (dout)
 #pragma unroll
-                        for (int a = 0; a < 3; ++a) dout[3 * (r0 + x) + a] = zero;
+                        for (int a = 0; a < 3; ++a) __stcs(dout + 3 * (r0 + x) + a, zero);
                 }
             }
         }
@@ -848,10 +856,10 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
                     }
                     if (!TP_CHECK(q.dbg, e < (size_t)q.B * q.P * q.plane && qx >= 0 && qx < q.Xo, 3))
                         return;
-                    out[e] = S;
+                    __stcs(out + e, S);
                     if (SAVE)
 #pragma unroll
-                        for (int a = 0; a < 3; ++a) dout[3 * e + a] = dS[a];
+                        for (int a = 0; a < 3; ++a) __stcs(dout + 3 * e + a, dS[a]);
                 });
             }
             __syncthreads();
@@ -954,12 +962,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 constexpr int kOct = kBS / 2;              // octant edge
 constexpr int kOS = kOct + 3;              // octant + cubic halo (taps x0 - 1 .. x0 + 2)
 constexpr int kOPX = 12;                   // x pitch of the tile (complex words)
-constexpr int kOElems = kOS * kOS * kOPX;  // complex words of the tile
 // The real weight tile is addressed with 32-bit words by the whole warp at
 // once: with pitches 12 x 12 the second half-warp's taps (jz + 1, 144 words
 // on, 16 banks away) land in the 16 banks the first half-warp leaves free.
 constexpr int kOWPY = 12;                    // y pitch of the weight tile
-constexpr int kOWElems = kOS * kOWPY * kOPX; // words of the weight tile
 constexpr int kOQW = 9;                      // floats per queued weight row (odd: no bank conflicts)
 
 // Queued samples of a warp.  A lane of half-warp h reads its z weights
@@ -971,29 +977,41 @@ struct OctQueue {
                          // with weights)
 };
 
+// A work item is one part of a unit's brick: an octant (8^3), or, with the
+// weight spectrum, half of one in z (8 x 8 x 4), so that the two tiles and
+// the queue of a warp fit 16 warps into an SM's shared memory.
 template <bool WEIGHTS>
 struct OctLayout {
     static constexpr int WARPS = WEIGHTS ? 2 : 4;   // warps per block (blocks only share an SM)
-    static constexpr size_t TILE = sizeof(float2) * kOElems;
-    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * kOWElems : 0;
+    static constexpr int OZ = WEIGHTS ? kOct / 2 : kOct;   // z extent of an item's box
+    static constexpr int PARTS = 4 * (kBS / OZ);     // items per work unit
+    static constexpr int SZ = OZ + 3;                // z layers of the tiles
+    static constexpr int ELEMS = kOS * kOPX * SZ;    // complex words of the tile
+    static constexpr int WELEMS = kOWPY * kOPX * SZ; // words of the weight tile
+    static constexpr size_t TILE = sizeof(float2) * ELEMS;
+    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * WELEMS : 0;
     static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(OctQueue);
     static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned queue");
 };
 
-__device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct) {
+// Box of part `oct` of a brick: x and y halves from bits 0 and 1, the z
+// slice of depth oz from the bits above.
+__device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct, int oz = kOct) {
     BrickBox ob;
+    const int off[3] = {kOct * (oct & 1), kOct * ((oct >> 1) & 1), oz * (oct >> 2)};
+    const int ext[3] = {kOct, kOct, oz};
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-        ob.o[d] = bx.o[d] + kOct * ((oct >> d) & 1);
+        ob.o[d] = bx.o[d] + off[d];
         ob.lo[d] = (float)ob.o[d] - kMargin;
-        ob.hi[d] = (float)(ob.o[d] + kOct) + kMargin;
+        ob.hi[d] = (float)(ob.o[d] + ext[d]) + kMargin;
     }
     return ob;
 }
 
 
 template <bool WEIGHTS>
-__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 4)
+__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 8 : 4)
     k_brick_scatter_cubic(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
                           const float *__restrict__ omega, float2 *__restrict__ dst,
                           float *__restrict__ wdst) {
@@ -1011,7 +1029,8 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
     constexpr int ZSTEP_W = 2 * kOPX * kOWPY;  // the same in the weight tile
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int items = 8 * (int)__ldg(sc.counters + 3 * nvol + v);
+    constexpr int kOElems = OL::ELEMS, kOWElems = OL::WELEMS;
+    const int items = OL::PARTS * (int)__ldg(sc.counters + 3 * nvol + v);
     const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
@@ -1024,12 +1043,13 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= items) break;
-        if (!TP_CHECK(q.dbg, (item >> 3) < nbr * sc.nchunks, 8)) break;
-        const int4 rec = __ldg(units + (item >> 3));
+        const int ui = item / OL::PARTS, part = item - ui * OL::PARTS;
+        if (!TP_CHECK(q.dbg, ui < nbr * sc.nchunks, 8)) break;
+        const int4 rec = __ldg(units + ui);
         if (!TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
                                  rec.z <= sc.nchunks, 8))
             break;
-        const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
+        const BrickBox ob = octant_box(brick_box(rec.x, nb), part, OL::OZ);
         const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
         bool touched = false;
         for (int c = rec.y; c < rec.z; ++c) {
@@ -1043,7 +1063,8 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
                 for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
                     int l[3];
                     float w[3][4], d[3][4];
-                    const bool own = active && own_sample<true, false, kOct>(g, ob, qx, qy, l, w, d);
+                    const bool own =
+                        active && own_sample<true, false, kOct, OL::OZ>(g, ob, qx, qy, l, w, d);
                     const unsigned mask = __ballot_sync(0xffffffffu, own);
                     if (own) {
                         const int slot = __popc(mask & ((1u << lane) - 1u));
@@ -1115,7 +1136,7 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 5 : 
         if (!touched) continue;
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0] - 1, y0 = ob.o[1] - 1, z0 = ob.o[2] - 1;
-        for (int e = lane; e < kOS * kOS * kOS; e += 32) {
+        for (int e = lane; e < kOS * kOS * OL::SZ; e += 32) {
             const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
             const int k = (lz * kOS + ly) * kOPX + lx;
             const int kw = (lz * kOWPY + ly) * kOPX + lx;
