@@ -48,6 +48,7 @@
 
 #include "tp_device.cuh"
 #include "tp_launch.h"
+#include "tp_tiles.cuh"
 
 namespace tp {
 
@@ -110,16 +111,6 @@ __device__ __forceinline__ int divmod(int e, int d, float inv, int &rem) {
     }
     rem = r;
     return quo;
-}
-
-// r[i] = v[(i + c) mod 4] with static register indexes (two selects per
-// entry): the per-lane rotation of a cubic stencil's separable weights.
-__device__ __forceinline__ void rot4(const float (&v)[4], int c, float (&r)[4]) {
-    float t[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) t[i] = (c & 1) ? v[(i + 1) & 3] : v[i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = (c & 2) ? t[(i + 2) & 3] : t[i];
 }
 
 // Issue the copy of one stored source image (raw_words complex words at src)

@@ -11,6 +11,7 @@
 // [it §4 "Backward Pass"], which the tiles below avoid.
 #include "tp_device.cuh"
 #include "tp_launch.h"
+#include "tp_tiles.cuh"
 
 namespace tp {
 
@@ -27,33 +28,44 @@ namespace {
 // from a counter in shared memory.  A warp enumerates the image's pixels
 // whose sample position falls in its tile (rows from the inverse of
 // [a b], each row's qx interval from the two slab constraints, a warp
-// prefix sum packing the candidates into 32-lane rounds), queues the owned
-// ones and spreads them into a private tile with plain read-add-write: tap
-// lanes (jx, jy); linear spreads several samples per round, one at a time
-// in a round where two of their stencils meet (stencils_meet).  The tile is
-// then added to the stored half-spectrum with one vector atomic per touched
-// word (Friedel positions conjugated at -n).
+// prefix sum packing the candidates into 32-lane rounds) and spreads the
+// owned ones into a private tile with plain read-add-write.  Cubic: each lane
+// spreads its own sample's 16 taps in a lane-rotated order that keeps the 16
+// lanes of a pass on 16 different words (lanes 0-15, then 16-31), with no
+// queue.  Linear: owned samples are queued and tap lanes (jx, jy) spread
+// several samples per round, one at a time in a round where two of their
+// stencils meet (stencils_meet).  The tile is then added to the stored
+// half-spectrum with one vector atomic per touched word (Friedel positions
+// conjugated at -n).
 constexpr int kTile = 16;
 constexpr int kTileWarps = 4;
 constexpr float kTileMargin = 0.01f;
 
+// The warp's tile.  Cubic: 20 x 20 words in 4 x 4 tiles of 16 complex words,
+// so word (x, y) sits in bank pair (x mod 4) + 4 (y mod 4).  Linear: row-major
+// 17 x 18 (x pitch 18).
 template <bool CUBIC>
 struct Tile2 {
     using St = Stencil<CUBIC>;
     static constexpr int S = kTile + St::LO + St::HI;  // staged edge (19 or 17)
-    static constexpr int PX = CUBIC ? 20 : 18;          // x pitch: a half-warp's 4 x 4 taps hit 16 bank pairs
-    static constexpr int ELEMS = S * PX;
-    static constexpr int LANES = St::TAPS * St::TAPS;   // lanes per sample
-    // Samples spread per round.  Cubic spreads one (16 lanes): neighbouring
-    // queue slots lie a pixel or a row apart, their 4 x 4 stencils nearly
-    // always meet, and pairing slots further apart measured slower.  Linear
-    // spreads eight, drawn R slots apart, whose 2 x 2 stencils rarely meet;
-    // a round in which two of them do is spread one sample at a time.
-    static constexpr int SPS = CUBIC ? 1 : 32 / LANES;
+    static constexpr int PX = CUBIC ? 20 : 18;          // x extent (pitch)
+    static constexpr int ELEMS = (CUBIC ? 20 : S) * PX;
+    static constexpr int LANES = St::TAPS * St::TAPS;   // lanes per linear sample
+    // Linear spreads eight samples per round, drawn R slots apart, whose 2 x 2
+    // stencils rarely meet; a round in which two of them do is spread one
+    // sample at a time.
+    static constexpr int SPS = 32 / LANES;
     static constexpr size_t TILE_BYTES = sizeof(float2) * ELEMS;
+    static constexpr size_t QUEUE_BYTES = CUBIC ? 0 : sizeof(float) * 32 * 9 + sizeof(float4) * 32;
+    static constexpr size_t WARP_BYTES = TILE_BYTES + QUEUE_BYTES;
     static_assert(TILE_BYTES % 16 == 0, "16-byte aligned queue");
+    __device__ __forceinline__ static int index(int x, int y) {
+        if (CUBIC) return ((y >> 2) * (PX / 4) + (x >> 2)) * 16 + (x & 3) + 4 * (y & 3);
+        return y * PX + x;
+    }
 };
 
+// Linear: queued samples of a warp.
 struct Queue2 {
     float w[32][9];   // per sample: wx (4), wy (4), unused
     float4 rec[32];   // per sample: conj(phase) * g (re, im), tile x | y << 8, first tap
@@ -68,11 +80,18 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
     extern __shared__ float4 s_t2[];
     __shared__ int s_next;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    char *mine = reinterpret_cast<char *>(s_t2) + warp * (T::TILE_BYTES + sizeof(Queue2));
+    char *mine = reinterpret_cast<char *>(s_t2) + warp * T::WARP_BYTES;
     float2 *acc = reinterpret_cast<float2 *>(mine);
-    Queue2 &Q = *reinterpret_cast<Queue2 *>(mine + T::TILE_BYTES);
+    Queue2 &Q = *reinterpret_cast<Queue2 *>(mine + T::TILE_BYTES);   // linear only
     const int grp = lane / T::LANES, jx = lane % St::TAPS, jy = (lane / St::TAPS) % St::TAPS;
     const int toff = jx + T::PX * jy;
+    // Cubic: this lane's tap residues per step (see the spreading below).
+    int rx[4], ry[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        rx[i] = (i + lane) & 3;
+        ry[i] = (i + (lane >> 2)) & 3;
+    }
 
     const int bp = blockIdx.x;
     const int b = bp / q.P, pi = bp - b * q.P;
@@ -187,6 +206,54 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                     own = (unsigned)l0 < (unsigned)kTile && (unsigned)l1 < (unsigned)kTile;
                 }
                 const unsigned mask = __ballot_sync(0xffffffffu, own);
+                if constexpr (CUBIC) {
+                    // Each lane spreads its own sample's 16 taps, lanes 0-15 and
+                    // then lanes 16-31.  At step (sx, sy) lane L takes the tap
+                    // whose x is (sx + L) mod 4 and y (sy + L / 4) mod 4: the 16
+                    // lanes of a pass touch 16 different bank pairs, hence 16
+                    // different words, so the plain read-add-write never races;
+                    // the warp synchronises between steps because the stencils of
+                    // different lanes' samples meet at different steps.
+                    touched = touched || mask != 0u;
+                    if (mask == 0u) continue;
+                    float2 cy[4];
+                    int tox[4], toy[4];
+                    float wx[4];
+                    if (own) {
+                        const int iy = qyr < 0 ? qyr + q.N : qyr;
+                        const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo, 7);
+                        float2 cv = in ? __ldg(gimg + iy * q.Xo + qx) : make_float2(0.f, 0.f);
+                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qyr, sx, sy, q.fN, q.invN), cv);
+                        float wy[4];
+                        rot4(w[0], (lane - l0) & 3, wx);
+                        rot4(w[1], ((lane >> 2) - l1) & 3, wy);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // the tap of residue r within [l, l + 3] is 4 ((l + 3 - r) >> 2) + r
+                            tox[i] = ((l0 + 3 - rx[i]) >> 2) * 16 + rx[i];
+                            toy[i] = ((l1 + 3 - ry[i]) >> 2) * (16 * (T::PX / 4)) + 4 * ry[i];
+                            cy[i] = make_float2(wy[i] * cv.x, wy[i] * cv.y);
+                        }
+                    }
+                    for (int pass = 0; pass < 2; ++pass) {
+                        if (((mask >> (16 * pass)) & 0xffffu) == 0u) continue;   // warp-uniform
+                        const bool now = own && (lane >> 4) == pass;
+#pragma unroll
+                        for (int sy2 = 0; sy2 < 4; ++sy2) {
+#pragma unroll
+                            for (int sx2 = 0; sx2 < 4; ++sx2) {
+                                const int at = toy[sy2] + tox[sx2];
+                                if (now && TP_CHECK(q.dbg, at >= 0 && at < T::ELEMS, 4)) {
+                                    float2 a = acc[at];
+                                    cfma(wx[sx2], cy[sy2], a);
+                                    acc[at] = a;
+                                }
+                                __syncwarp();
+                            }
+                        }
+                    }
+                    continue;
+                }
                 if (own) {
                     const int slot = __popc(mask & ((1u << lane) - 1u));
                     const int iy = qyr < 0 ? qyr + q.N : qyr;
@@ -240,7 +307,7 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
         const int x0 = ox - St::LO, y0 = oy - St::LO;
         for (int e = lane; e < T::S * T::S; e += 32) {
             const int lx = e % T::S, ly = e / T::S;
-            const int k = ly * T::PX + lx;
+            const int k = T::index(lx, ly);
             const float2 cv = acc[k];
             if (cv.x == 0.f && cv.y == 0.f) continue;
             acc[k] = make_float2(0.f, 0.f);
@@ -264,7 +331,7 @@ cudaError_t launch_scatter2d_tiles(const Params &q, const float2 *img, float2 *d
     using T = Tile2<CUBIC>;
     const long long images = (long long)q.B * q.P;
     if (images == 0) return cudaSuccess;
-    const size_t smem = kTileWarps * (T::TILE_BYTES + sizeof(Queue2));
+    const size_t smem = kTileWarps * T::WARP_BYTES;
     auto kern = k_scatter2d_tiles<CUBIC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
