@@ -23,6 +23,7 @@ import torch
 __all__ = [
     "TPError", "lib", "tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
     "tp_project_3d_2d_save", "tp_project_3d_2d_backward_saved", "tp_backproject_2d_3d_backward",
+    "tp_project_3d_2d_l2",
     "tp_backproject_backward_scratch_bytes", "tp_project_2d_2d", "tp_project_2d_2d_backward",
     "tp_last_error", "tp_version", "tp_workspace_bytes", "tp_project_3d_2d_noalloc",
     "tp_debug_bounds_word", "tp_debug_bounds_selftest", "tp_hermitian_x0", "LINEAR", "CUBIC",
@@ -72,6 +73,8 @@ _SIGS = {
     "tp_project_2d_2d": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
     "tp_project_3d_2d_noalloc": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P],
     "tp_project_3d_2d_save": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _Z, _P],
+    "tp_project_3d_2d_l2": [_P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P, _P, _P, _P,
+                            _Z, _P],
     "tp_project_3d_2d_backward": [_P, _P, _I, _I, _P, _I, _I, _P, _I, _I, TPOptions, _P, _P, _P,
                                   _P, _Z, _P],
     "tp_project_3d_2d_backward_saved": [_P, _P, _P, _I, _I, _I, _I, _I, TPOptions, _P, _P, _P],
@@ -291,6 +294,48 @@ def tp_project_3d_2d_save(vol, rot, shift=None, *, N=None, interp="cubic", overs
           _opts(interp, oversampling, radius), _ptr(out), _ptr(dout), _ptr(ws), nbytes,
           _stream(stream))
     return out, dout
+
+
+def tp_project_3d_2d_l2(vol, rot, shift, target, *, N=None, interp="cubic", oversampling=1.0,
+                        radius=-1.0, out=None, grad_out=None, grad_rot=None, grad_shift=None,
+                        want_rot=True, want_shift=True, workspace=None, stream=None):
+    """The forward fused with L = sum |out - target|^2; returns (out, grad_out,
+    grad_rot, grad_shift) with grad_out = 2 (out - target) written and the
+    rotation / shift gradients accumulated (None where not requested); see tp.h."""
+    _need(vol, "vol", torch.complex64, 4)
+    Bv, Nv = vol.shape[0], vol.shape[1]
+    Bp, P, Bs = _poses(rot, shift, 3)
+    N = Nv if N is None else int(N)
+    B = _batch(Bv, Bp, Bs)
+    shape = (B, P, N, N // 2 + 1)
+    _need(target, "target", torch.complex64, 4)
+    if tuple(target.shape) != shape:
+        raise ValueError(f"target must be {shape}")
+    if out is None:
+        out = torch.empty(shape, dtype=torch.complex64, device=vol.device)
+    if grad_out is None:
+        grad_out = torch.empty(shape, dtype=torch.complex64, device=vol.device)
+    for t, name in ((out, "out"), (grad_out, "grad_out")):
+        _need(t, name, torch.complex64, 4)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {shape}")
+    if want_rot and grad_rot is None:
+        grad_rot = torch.zeros_like(rot)
+    if want_shift and shift is not None and grad_shift is None:
+        grad_shift = torch.zeros_like(shift)
+    if grad_rot is not None:
+        _need(grad_rot, "grad_rot", torch.float32, 4)
+        if grad_rot.shape != rot.shape:
+            raise ValueError("grad_rot must have rot's shape")
+    if grad_shift is not None:
+        _need(grad_shift, "grad_shift", torch.float32, 3)
+        if shift is None or grad_shift.shape != shift.shape:
+            raise ValueError("grad_shift must have shift's shape")
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, vol.device)
+    _call("tp_project_3d_2d_l2", _ptr(vol), Bv, Nv, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
+          _opts(interp, oversampling, radius), _ptr(target), _ptr(out), _ptr(grad_out),
+          _ptr(grad_rot), _ptr(grad_shift), _ptr(ws), nbytes, _stream(stream))
+    return out, grad_out, grad_rot, grad_shift
 
 
 def tp_project_3d_2d_backward_saved(grad_out, out, dout, rot, shift=None, *, interp="cubic",

@@ -251,6 +251,32 @@ tp_status tp_project_3d_2d_save(const float *vol, int Bv, int Nv, const float *r
                    workspace_bytes, stream);
 }
 
+tp_status tp_project_3d_2d_l2(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
+                              const float *shift, int Bs, int N, tp_options opts,
+                              const float *target, float *out, float *grad_out, float *grad_rot,
+                              float *grad_shift, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    Geometry g;
+    tp_status st = setup(3, Bv, Nv, rot, Bp, P, shift, Bs, N, opts, 1, g);
+    if (st != TP_OK) return st;
+    if (P == 0) return ok();  // zero-size tensors may carry NULL pointers
+    if (!vol || !rot || !target || !out || !grad_out)
+        return fail(TP_ERR_NULL, "vol, rotation, target, out and grad_out pointers are required");
+    if (grad_shift && !shift) return fail(TP_ERR_NULL, "grad_shift requested without a shift tensor");
+    if ((st = check_complex(vol, "vol")) != TP_OK || (st = check_complex(target, "target")) != TP_OK ||
+        (st = check_complex(out, "out")) != TP_OK || (st = check_complex(grad_out, "grad_out")) != TP_OK)
+        return st;
+    if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
+        return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
+    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    g.q.src = reinterpret_cast<const float2 *>(vol);
+    return launched(tp::launch_brick_project_l2(g.cubic, g.q, reinterpret_cast<const float2 *>(target),
+                                                reinterpret_cast<float2 *>(out),
+                                                reinterpret_cast<float2 *>(grad_out), grad_rot,
+                                                grad_shift, workspace, static_cast<cudaStream_t>(stream)),
+                    "project with L2 term");
+}
+
 tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *out,
                                           const float *dout, int B, int P, int N, int Bp, int Bs,
                                           tp_options opts, float *grad_rot, float *grad_shift,

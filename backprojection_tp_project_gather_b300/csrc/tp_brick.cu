@@ -767,15 +767,26 @@ __device__ __forceinline__ bool own_sample(const PoseGeo &g, const BrickBox &bx,
 }
 
 // ---------------------------------------------------------------------------
+// The fused L2 data term of the forward (tp_project_3d_2d_l2): the target
+// images, the residual gradient written beside the output, and the rotation
+// and shift gradients it accumulates.
+struct L2Args {
+    const float2 *target;   // (B, P, N, N/2+1)
+    float2 *gout;           // g = 2 (out - target), same shape
+    float *grad_rot;        // (Bp, P, 3, 3) +=, or null
+    float *grad_shift;      // (Bs, P, 2) +=, or null
+};
+
 // Zeros for the pixels no brick owns: outside the radius (a warp writes the
 // tail of an output row beyond the radius), and, for poses whose reach
 // exceeds the brick grid of half-width G, in-radius pixels with floor(p)
 // outside it (all their taps lie outside the stored range).  dout, when
-// given, receives the matching zeros (three complex values per pixel).  The
-// rows are shared out over the nwarps warps of the grid.
+// given, receives the matching zeros (three complex values per pixel), and
+// with an L2 term gout receives -2 target there.  The rows are shared out
+// over the nwarps warps of the grid.
 __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 *__restrict__ geo,
                                              float2 *__restrict__ out, float2 *__restrict__ dout,
-                                             long long warp, long long nwarps) {
+                                             const L2Args *l2, long long warp, long long nwarps) {
     const long long rows = (long long)q.B * q.P * q.N;
     const int lane = threadIdx.x & 31;
     const int half = q.N >> 1;
@@ -788,7 +799,13 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 
         const int xcut = rr < 0 ? -1 : min(half, (int)floorf(sqrtf((float)rr)));
         const size_t r0 = (size_t)bp * q.plane + (size_t)iy * q.Xo;
         if (!TP_CHECK(q.dbg, r0 + half < nout, 3)) continue;
-        for (int x = xcut + 1 + lane; x <= half; x += 32) __stcs(out + r0 + x, zero);
+        for (int x = xcut + 1 + lane; x <= half; x += 32) {
+            __stcs(out + r0 + x, zero);
+            if (l2) {
+                const float2 t = __ldcs(l2->target + r0 + x);
+                __stcs(l2->gout + r0 + x, make_float2(-2.f * t.x, -2.f * t.y));
+            }
+        }
         if (dout)
             for (int k = 3 * (xcut + 1) + lane; k < 3 * (half + 1); k += 32)
                 __stcs(dout + 3 * r0 + k, zero);
@@ -804,6 +821,10 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 
                 }
                 if (outside) {
                     __stcs(out + r0 + x, zero);
+                    if (l2) {
+                        const float2 t = __ldcs(l2->target + r0 + x);
+                        __stcs(l2->gout + r0 + x, make_float2(-2.f * t.x, -2.f * t.y));
+                    }
                     if (dout)
 #pragma unroll
                         for (int a = 0; a < 3; ++a) __stcs(dout + 3 * (r0 + x) + a, zero);
@@ -814,19 +835,29 @@ __device__ __forceinline__ void zero_unowned(const Params &q, int G, const int4 
 }
 
 // ---------------------------------------------------------------------------
-// Forward projection.  With SAVE the stencil's derivative weights are
-// gathered too and D_a = phase * dS/dp_a (the derivative of the output with
-// respect to the sample position) is written next to the output, three
-// complex values per pixel.
-template <bool CUBIC, bool SAVE>
-__global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params q, int nb, Scratch sc,
-                                                                         float2 *__restrict__ out,
-                                                                         float2 *__restrict__ dout) {
+// Forward projection, in one of three modes.  kPlain writes the output.
+// kSave also gathers the stencil's derivative weights and writes
+// D_a = phase * dS/dp_a (the derivative of the output with respect to the
+// sample position) next to the output, three complex values per pixel.
+// kL2 fuses an L2 data term L = sum |out - target|^2: it writes the output
+// and the residual gradient g = 2 (out - target), and from the same
+// derivative gather reduces, per warp and (pose, brick), the rotation and
+// shift gradients of L (the sums of the recomputing backward) into
+// grad_rot / grad_shift with one atomic per entry.
+enum ProjectMode { kPlain = 0, kSave = 1, kL2 = 2 };
+
+template <bool CUBIC, int MODE>
+__global__ void __launch_bounds__(kThreads, MODE == kPlain ? 3 : 2)
+    k_brick_project(Params q, int nb, Scratch sc, float2 *__restrict__ out,
+                    float2 *__restrict__ dout, L2Args l2) {
+    constexpr bool SAVE = MODE == kSave;
+    constexpr bool L2 = MODE == kL2;
+    constexpr bool DERIV = MODE != kPlain;
     extern __shared__ float2 s_vol[];
     __shared__ UnitTable s_tab;
     const int v = blockIdx.z, nbr = nb * nb * nb;
     // The zeros go out first: plain stores that overlap the gathers below.
-    zero_unowned(q, (nb / 2) * kBS, sc.geo, out, dout,
+    zero_unowned(q, (nb / 2) * kBS, sc.geo, out, dout, L2 ? &l2 : nullptr,
                  ((long long)(blockIdx.z * gridDim.x + blockIdx.x) * kThreads + threadIdx.x) >> 5,
                  (long long)gridDim.x * gridDim.z * kWarps);
     int4 rec;
@@ -839,28 +870,73 @@ __global__ void __launch_bounds__(kThreads, SAVE ? 2 : 3) k_brick_project(Params
                 const PoseGeo &g = s_tab.pose[k];
                 const size_t ob = (size_t)g.bp * q.plane;
                 const float sx = g.sx, sy = g.sy;
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                 for_pixels_in_box(g, bx, q.N, q.r2max, [&](int qx, int qy, bool active) {
                     int l[3];
                     float w[3][4], d[3][4];
-                    if (!active || !own_sample<CUBIC, SAVE>(g, bx, qx, qy, l, w, d)) return;
-                    float2 S, dS[3];
-                    gather_smem<CUBIC, SAVE>(s_vol, l, w, d, S, dS, q.dbg);
+                    if (!active || !own_sample<CUBIC, DERIV>(g, bx, qx, qy, l, w, d)) return;
                     const int iy = qy < 0 ? qy + q.N : qy;
                     const size_t e = ob + (size_t)iy * q.Xo + qx;
+                    if (!TP_CHECK(q.dbg, e < (size_t)q.B * q.P * q.plane && qx >= 0 && qx < q.Xo, 3))
+                        return;
+                    float2 t = make_float2(0.f, 0.f);
+                    if (L2) t = __ldcs(l2.target + e);   // in flight during the gather
+                    float2 S, dS[3];
+                    gather_smem<CUBIC, DERIV>(s_vol, l, w, d, S, dS, q.dbg);
+                    float2 ph = make_float2(1.f, 0.f);
                     if (q.shift) {
-                        const float2 ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
+                        ph = shift_phase(qx, qy, sx, sy, q.fN, q.invN);
                         S = cmul(ph, S);
                         if (SAVE)
 #pragma unroll
                             for (int a = 0; a < 3; ++a) dS[a] = cmul(ph, dS[a]);
                     }
-                    if (!TP_CHECK(q.dbg, e < (size_t)q.B * q.P * q.plane && qx >= 0 && qx < q.Xo, 3))
-                        return;
                     __stcs(out + e, S);
                     if (SAVE)
 #pragma unroll
                         for (int a = 0; a < 3; ++a) __stcs(dout + 3 * e + a, dS[a]);
+                    if (L2) {
+                        const float2 gv = make_float2(2.f * (S.x - t.x), 2.f * (S.y - t.y));
+                        __stcs(l2.gout + e, gv);
+                        // dL/dp_a = Re(conj(g) phase dS_a) with dS unphased here.
+                        const float2 gq = cmul_conj_a(ph, gv);
+#pragma unroll
+                        for (int a = 0; a < 3; ++a) {
+                            const float dl = gq.x * dS[a].x + gq.y * dS[a].y;
+                            acc[a] = fmaf(q.s * (float)qx, dl, acc[a]);
+                            acc[3 + a] = fmaf(q.s * (float)qy, dl, acc[3 + a]);
+                        }
+                        // Im(conj(g) y) = -2 Im(conj(t) y) exactly for g = 2 (y - t):
+                        // the |y|^2 terms cancel, so form it from t and y alone
+                        // (from g it would lose the digits where |y| >> |t|).
+                        const float qv = -12.566370614359172f * q.invN * (t.x * S.y - t.y * S.x);
+                        acc[6] = fmaf((float)qx, qv, acc[6]);
+                        acc[7] = fmaf((float)qy, qv, acc[7]);
+                    }
                 });
+                if (L2) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float t = acc[i];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                        acc[i] = t;
+                    }
+                    if ((threadIdx.x & 31) == 0 &&
+                        TP_CHECK(q.dbg, g.ridx >= 0 && g.ridx < q.Bp * q.P && g.sidx >= 0 &&
+                                            g.sidx < q.Bs * q.P, 9)) {
+                        if (l2.grad_rot)
+#pragma unroll
+                            for (int i = 0; i < 6; ++i)
+                                if (acc[i] != 0.f) atomicAdd(l2.grad_rot + (size_t)g.ridx * 9 + i, acc[i]);
+                        if (l2.grad_shift) {
+                            if (acc[6] != 0.f) atomicAdd(l2.grad_shift + 2 * (size_t)g.sidx, acc[6]);
+                            if (acc[7] != 0.f) atomicAdd(l2.grad_shift + 2 * (size_t)g.sidx + 1, acc[7]);
+                        }
+                    }
+                }
             }
             __syncthreads();
         }
@@ -1435,17 +1511,17 @@ dim3 warp_grid(const Params &q, const void *kern, int threads, size_t smem) {
     return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
 }
 
-template <bool CUBIC, bool SAVE>
-cudaError_t project_t(const Params &q, float2 *out, float2 *dout, void *ws, BinMode mode,
-                      cudaStream_t st) {
+template <bool CUBIC, int MODE>
+cudaError_t project_t(const Params &q, float2 *out, float2 *dout, const L2Args &l2, void *ws,
+                      BinMode mode, cudaStream_t st) {
     const Layout L = layout(q, CUBIC);
     const Scratch sc = scratch_in(ws, L);
     const size_t smem = sizeof(float2) * Halo<CUBIC>::ELEMS;
-    auto kern = k_brick_project<CUBIC, SAVE>;
+    auto kern = k_brick_project<CUBIC, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = prepare(q, L, sc, 0, mode, st)) != cudaSuccess) return e;
-    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out, dout);
+    kern<<<main_grid(q, (const void *)kern, smem), kThreads, smem, st>>>(q, L.nb, sc, out, dout, l2);
     return cudaGetLastError();
 }
 
@@ -1504,11 +1580,20 @@ size_t brick_workspace_bytes(const Params &q, bool cubic) { return layout(q, cub
 
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  BinMode mode, cudaStream_t st) {
+    const L2Args none{};
     if (dout)
-        return cubic ? project_t<true, true>(q, out, dout, ws, mode, st)
-                     : project_t<false, true>(q, out, dout, ws, mode, st);
-    return cubic ? project_t<true, false>(q, out, nullptr, ws, mode, st)
-                 : project_t<false, false>(q, out, nullptr, ws, mode, st);
+        return cubic ? project_t<true, kSave>(q, out, dout, none, ws, mode, st)
+                     : project_t<false, kSave>(q, out, dout, none, ws, mode, st);
+    return cubic ? project_t<true, kPlain>(q, out, nullptr, none, ws, mode, st)
+                 : project_t<false, kPlain>(q, out, nullptr, none, ws, mode, st);
+}
+
+cudaError_t launch_brick_project_l2(bool cubic, const Params &q, const float2 *target, float2 *out,
+                                    float2 *grad_out, float *grad_rot, float *grad_shift, void *ws,
+                                    cudaStream_t st) {
+    const L2Args l2{target, grad_out, grad_rot, grad_shift};
+    return cubic ? project_t<true, kL2>(q, out, nullptr, l2, ws, kBinNew, st)
+                 : project_t<false, kL2>(q, out, nullptr, l2, ws, kBinNew, st);
 }
 
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *g, float *grot,

@@ -47,6 +47,12 @@ enum BinMode { kBinNew = 0, kBinSameCall = 1 };
 size_t brick_workspace_bytes(const Params &q, bool cubic);
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  BinMode mode, cudaStream_t st);
+// The forward fused with an L2 data term (always bins its poses): writes out
+// and grad_out = 2 (out - target), and accumulates the rotation and shift
+// gradients of sum |out - target|^2 (either may be null).
+cudaError_t launch_brick_project_l2(bool cubic, const Params &q, const float2 *target, float2 *out,
+                                    float2 *grad_out, float *grad_rot, float *grad_shift, void *ws,
+                                    cudaStream_t st);
 cudaError_t launch_brick_pose_grad(bool cubic, const Params &q, const float2 *grad_out,
                                    float *grad_rot, float *grad_shift, void *ws, BinMode mode,
                                    cudaStream_t st);

@@ -4,10 +4,10 @@
 One step is the whole hot path over one batch: forward 3D->2D projection of a
 256^3 spectrum for 512 poses with shifts (cubic, radius 128), the L2-loss
 gradient g = 2 (y - target) against seeded noisy targets (SNR 0.1), and the
-backward pass producing dL/dR, dL/dshift and dL/dvolume.  The forward saves
-D = phase * dS/dp per pixel, so the rotation and shift gradients are a
-streaming reduction over (g, y, D); the volume gradient is the brick scatter
-of g.  The metric is
+backward pass producing dL/dR, dL/dshift and dL/dvolume.  The forward carries
+the L2 data term (tp_project_3d_2d_l2): it writes y and g and reduces the
+rotation and shift gradients from its own gather of the stencil derivatives;
+the volume gradient is the brick scatter of g.  The metric is
 Fourier samples per second (one sample = one stored output RFFT pixel) over
 forward + backward, in Gsamples/s.
 
@@ -260,10 +260,10 @@ def measured_peak_hbm():
         return 6400.0, "fallback"
 
 
-# The sources of the step's kernels (k_brick_project, k_pose_grad_saved,
-# k_brick_scatter_cubic and the binning passes): a committed ncu summary is
-# reported only while these files are unchanged.
-KERNEL_SOURCES = ("tp_brick.cu", "tp_saved.cu", "tp_device.cuh")
+# The sources of the step's kernels (k_brick_project, k_brick_scatter_cubic
+# and the binning passes): a committed ncu summary is reported only while
+# these files are unchanged.
+KERNEL_SOURCES = ("tp_brick.cu", "tp_device.cuh")
 
 
 def kernel_source_sha():
@@ -276,9 +276,8 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-# The three kernels that do the work of a step, by the bench's segment names.
-NCU_KERNELS = {"project_3d_2d": "k_brick_project", "pose_grad_saved": "k_pose_grad_saved",
-               "volume_grad_scatter": "k_brick_scatter_cubic"}
+# The two kernels that do the work of a step, by the bench's segment names.
+NCU_KERNELS = {"project_3d_2d": "k_brick_project", "volume_grad_scatter": "k_brick_scatter_cubic"}
 NCU_METRICS = {"dram__bytes_read.sum": "dram_read_bytes", "dram__bytes_write.sum": "dram_write_bytes",
                "gpu__time_duration.sum": "duration_ns",
                "gpu__compute_memory_throughput.avg.pct_of_peak_sustained_elapsed": "mem_sol_pct",
@@ -416,12 +415,10 @@ def run_ours(args):
                             + np.arange(N // 2 + 1)[None, :] ** 2 <= w["radius"] ** 2).to(dev)
     n_in = float(mask.sum())
     sig_pow = (clean.abs() ** 2 * mask).sum((2, 3), keepdim=True) / n_in
-    target = clean + noise * torch.sqrt(10.0 * sig_pow) * mask
-    m2t = (-2.0 * target).contiguous()
+    target = (clean + noise * torch.sqrt(10.0 * sig_pow) * mask).contiguous()
     del clean, noise
 
     y = torch.empty_like(target)
-    D = torch.empty(tuple(target.shape) + (3,), dtype=torch.complex64, device=dev)
     g = torch.empty_like(target)
     grad_vol = torch.zeros_like(vol)
     grad_rot = torch.zeros_like(rot)
@@ -431,16 +428,11 @@ def run_ours(args):
     kw["workspace"] = ws
     stream = torch.cuda.current_stream()
 
-    kw_saved = {k: kw[k] for k in ("interp", "oversampling", "radius")}
-    # The rotation / shift gradients (HBM-bound) run on a side stream beside
-    # the volume gradient (bound by shared memory); both only read g.
-    side = torch.cuda.Stream(device=dev)
-    g_ready, pose_done = torch.cuda.Event(), torch.cuda.Event()
 
     # A step's inputs (volume, targets, poses) and results (gradients); the
     # device-resident timing uses set 0, the end-to-end pipeline both.
-    bufs = [dict(vol=vol, m2t=m2t, rot=rot, shift=shift, grad_vol=grad_vol, grad_rot=grad_rot,
-                 grad_shift=grad_shift)]
+    bufs = [dict(vol=vol, target=target, rot=rot, shift=shift, grad_vol=grad_vol,
+                 grad_rot=grad_rot, grad_shift=grad_shift)]
 
     def step(ev=None, i=0, b=None):
         if b is None:
@@ -451,39 +443,29 @@ def run_ours(args):
         V, R, T = b["vol"], b["rot"], b["shift"]
         if ev:
             ev[0].record(stream)
-        # Forward; it also saves D = phase * dS/dp for the pose gradients.
-        tp.tp_project_3d_2d_save(V, R, T, out=y, dout=D, **kw)
-        if ev:
-            ev[1].record(stream)
-        torch.add(b["m2t"], y, alpha=2.0, out=g)                  # g = 2 (y - target)
         b["grad_vol"].zero_()
         b["grad_rot"].zero_()
         b["grad_shift"].zero_()
         if ev:
+            ev[1].record(stream)
+        # Forward with the L2 data term: y, g = 2 (y - target) and the rotation
+        # and shift gradients from the forward's own derivative gather.
+        tp.tp_project_3d_2d_l2(V, R, T, b["target"], out=y, grad_out=g, grad_rot=b["grad_rot"],
+                               grad_shift=b["grad_shift"], **kw)
+        if ev:
             ev[2].record(stream)
-        g_ready.record(stream)
-        side.wait_event(g_ready)
-        if ev:
-            ev[5].record(side)
-        tp.tp_project_3d_2d_backward_saved(g, y, D, R, T, grad_rot=b["grad_rot"],
-                                           grad_shift=b["grad_shift"], stream=side, **kw_saved)
-        if ev:
-            ev[6].record(side)
-        pose_done.record(side)
+        # Volume gradient: the scatter of g (the binning of this step's poses kept).
         tp.tp_project_3d_2d_backward(g, V, R, T, grad_vol=b["grad_vol"], want_rot=False,
                                      want_shift=False, **kw)
         if ev:
             ev[3].record(stream)
-        stream.wait_event(pose_done)
-        if ev:
-            ev[4].record(stream)
 
     for i in range(args.warmup):
         flush.zero_()
         step(i=i)
     torch.cuda.synchronize()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -496,14 +478,13 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
 
-    # Per step: forward, L2 gradient + zeroing, volume gradient (main stream),
-    # rotation / shift gradients (side stream, overlapping the volume
-    # gradient), and the whole step (forward start to the join).
+    # Per step: zeroing of the gradients, the forward with the L2 term (output,
+    # residual gradient, rotation and shift gradients), the volume gradient,
+    # and the whole step.
     seg = np.array([[events[i][0].elapsed_time(events[i][1]),
                      events[i][1].elapsed_time(events[i][2]),
-                     events[i][5].elapsed_time(events[i][6]),
                      events[i][2].elapsed_time(events[i][3])] for i in range(args.steps)])
-    step_ms = np.array([events[i][0].elapsed_time(events[i][4]) for i in range(args.steps)])
+    step_ms = np.array([events[i][0].elapsed_time(events[i][3]) for i in range(args.steps)])
     total_ms = max_over_ranks(step_ms.sum(), dist, dev)
     samples = P * N * (N // 2 + 1)
     value = whole_job_rate(world, samples, args.steps, total_ms)
@@ -516,11 +497,11 @@ def run_ours(args):
     # step i+1 computes.
     h_vol = vol.cpu().pin_memory()
     h_poses = [(r.cpu().pin_memory(), t.cpu().pin_memory()) for r, t in pose_sets]
-    h_m2t = m2t.cpu().pin_memory()
+    h_target = target.cpu().pin_memory()
     bufs.append({k: torch.empty_like(t) for k, t in bufs[0].items()})
     outs = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory()
                   for t in (vol, rot, shift)) for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in (h_vol, h_poses[0][0], h_poses[0][1], h_m2t))
+    h2d = sum(t.numel() * t.element_size() for t in (h_vol, h_poses[0][0], h_poses[0][1], h_target))
     d2h = sum(t.numel() * t.element_size() for t in outs[0])
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     h2d_done = [torch.cuda.Event() for _ in range(2)]
@@ -534,7 +515,7 @@ def run_ours(args):
             b["vol"].copy_(h_vol, non_blocking=True)
             b["rot"].copy_(h_poses[i & 1][0], non_blocking=True)
             b["shift"].copy_(h_poses[i & 1][1], non_blocking=True)
-            b["m2t"].copy_(h_m2t, non_blocking=True)
+            b["target"].copy_(h_target, non_blocking=True)
         h2d_done[i & 1].record(up)
 
     def download(i):
@@ -595,17 +576,15 @@ def run_ours(args):
         torch.cuda.empty_cache()
 
     if rank == 0:
-        names = ["project_3d_2d", "l2_grad_and_zero", "pose_grad_saved (side stream)",
-                 "volume_grad_scatter"]
+        names = ["zero_gradients", "project_3d_2d_l2", "volume_grad_scatter"]
         mean_seg = seg.mean(0)
         n_in = P * in_radius_count(N, w["radius"])
         # Algorithmic HBM bytes per launch: the forward reads the volume once
-        # and writes y (8 B) and D (24 B) per stored pixel; the pose gradient
-        # reads g, y and D (40 B) per in-radius pixel; the scatter reads g
-        # (8 B per stored pixel) and reads and writes the volume gradient once.
-        kern = {"project_3d_2d": (mean_seg[0], samples * 32 + vol.numel() * 8),
-                "pose_grad_saved": (mean_seg[2], n_in * 40),
-                "volume_grad_scatter": (mean_seg[3], samples * 8 + 2 * vol.numel() * 8)}
+        # and, per stored pixel, the target (8 B) and writes y and g (16 B);
+        # the scatter reads g (8 B per stored pixel) and reads and writes the
+        # volume gradient once.
+        kern = {"project_3d_2d": (mean_seg[1], samples * 24 + vol.numel() * 8),
+                "volume_grad_scatter": (mean_seg[2], samples * 8 + 2 * vol.numel() * 8)}
         dom = max(kern, key=lambda k: kern[k][0])
         t_ms, nbytes = kern[dom]
         peak, peak_src = measured_peak_hbm()
@@ -632,7 +611,7 @@ def run_ours(args):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         smem_bytes = n_in * 64 * 8 * 2
         smem_peak = sms * 128 * clk.get("sm_mhz", 2032.0) * 1e6 / 1e9
-        smem_achieved = smem_bytes / (mean_seg[3] * 1e-3) / 1e9
+        smem_achieved = smem_bytes / (mean_seg[2] * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -654,19 +633,19 @@ def run_ours(args):
             "ncu_memory_sol": sol,
             "secondary": secondary,
             "breakdown_ms": {n: float(mean_seg[i]) for i, n in enumerate(names)},
-            "fwd_gsamples_s": samples / (mean_seg[0] * 1e-3) / 1e9,
-            "bwd_gsamples_s": samples / ((float(step_ms.mean()) - mean_seg[0]) * 1e-3) / 1e9,
+            "fwd_gsamples_s": samples / (mean_seg[1] * 1e-3) / 1e9,
+            "bwd_gsamples_s": samples / (mean_seg[2] * 1e-3) / 1e9,
             "in_radius_samples_per_step": n_in,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "copies": "every step: volume, targets, poses up; volume, rotation and shift "
                               "gradients down; pipelined with the neighbouring steps' compute "
                               "on two copy streams"},
-            # per step: forward (pose geometry, brick masks, unit plan, gather with
-            # saved derivatives and the zero fill as its prologue), the saved-path
-            # pose gradient (one streaming kernel) and the volume-gradient call
-            # (geometry, masks, plan, scatter); plus two 4-byte memsets
-            "gpu_launches": 9 * args.steps,
+            # per step: the forward with the L2 term (pose geometry, brick masks,
+            # unit plan, gather with the zero fill as its prologue) and the
+            # volume-gradient call (geometry, masks, plan, scatter); plus two
+            # 4-byte memsets
+            "gpu_launches": 8 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu_line,
         }

@@ -198,6 +198,33 @@ tp_status tp_project_3d_2d_backward_saved(const float *grad_out, const float *ou
                                           float *grad_rot, float *grad_shift, void *stream);
 
 /*
+ * tp_project_3d_2d fused with an L2 data term L = sum over all stored pixels
+ * of |out - target|^2: one pass that gives the forward output, the residual
+ * gradient and the rotation and shift gradients of L.  The pages train the
+ * projection through losses the caller writes ([de §2 "Differentiable
+ * Backpropagation"]); this entry point fuses the most common one so that
+ * the rotation and shift gradients come from the forward's own gather of the
+ * stencil derivatives, with nothing saved for a later pass.  Arguments and
+ * errors as tp_project_3d_2d, plus
+ *   target      (B, P, N, N/2+1) complex                      in
+ *   out         (B, P, N, N/2+1) complex, overwritten: the projection
+ *   grad_out    (B, P, N, N/2+1) complex, overwritten: dL/dout = 2 (out - target)
+ *               (PyTorch's complex convention), also where out is 0 by the radius
+ *   grad_rot    (Bp, P, 3, 3) float, += dL/dR (row 3 is 0), or NULL
+ *   grad_shift  (Bs, P, 2) float, += dL/dshift, or NULL; requires shift != NULL
+ * The rotation and shift gradients equal those of tp_project_3d_2d_backward
+ * for upstream gradient grad_out; the volume gradient is
+ * tp_project_3d_2d_backward of grad_out (the binning in the workspace is kept
+ * for it).  target, out and grad_out must be 8-byte aligned.
+ */
+tp_status tp_project_3d_2d_l2(const float *vol, int Bv, int Nv,
+                              const float *rot, int Bp, int P,
+                              const float *shift, int Bs,
+                              int N, tp_options opts, const float *target,
+                              float *out, float *grad_out, float *grad_rot, float *grad_shift,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * 2D -> 3D backprojection: the adjoint of tp_project_3d_2d scattered into a
  * data spectrum, plus an optional real weight spectrum [it §2 "accumulo di
  * pesi"; de §2 "Dual-Volumen-Ansatz"; ko §2 "Backward Projection"].

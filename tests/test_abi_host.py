@@ -36,7 +36,8 @@ def test_header_declares_the_operator_set():
     for name in ("tp_project_3d_2d", "tp_project_3d_2d_backward", "tp_backproject_2d_3d",
                  "tp_project_2d_2d", "tp_project_2d_2d_backward", "tp_project_3d_2d_save",
                  "tp_project_3d_2d_backward_saved", "tp_backproject_2d_3d_backward",
-                 "tp_backproject_backward_scratch_bytes", "tp_last_error", "tp_version"):
+                 "tp_backproject_backward_scratch_bytes", "tp_project_3d_2d_l2", "tp_last_error",
+                 "tp_version"):
         assert name in syms
 
 
@@ -154,6 +155,21 @@ def test_saved_forward_validation(tp):
     assert save(vol=None) == TP_ERR_NULL
     assert save(ws=None) == TP_ERR_NULL
     assert save(P=0, dout=None) == TP_OK
+
+
+def test_l2_forward_validation(tp):
+    def l2(target=A, out=A, gout=A, gr=A, gs=None, shift=None, P=4, vol=A, ws=WS):
+        return tp._fn("tp_project_3d_2d_l2")(vol, 1, 16, A, 1, P, shift, 1, 16, opts(tp), target, out,
+                                             gout, gr, gs, ws, WSB, None)
+    assert l2(target=None) == TP_ERR_NULL
+    assert "target" in tp.tp_last_error()
+    assert l2(gout=None) == TP_ERR_NULL
+    assert l2(gs=A) == TP_ERR_NULL                       # grad_shift without shift
+    assert l2(gout=MIS) == TP_ERR_ALIGN
+    assert l2(target=MIS) == TP_ERR_ALIGN
+    assert l2(gr=A + 2) == TP_ERR_ALIGN
+    assert l2(ws=None) == TP_ERR_NULL
+    assert l2(P=0, target=None, out=None, gout=None) == TP_OK
 
 
 def test_saved_backward_validation(tp):

@@ -37,15 +37,19 @@ def _raw_csv(path):
 def test_summary_merges_one_capture_per_kernel(tmp_path):
     """Exports of separate single-kernel captures merge into one summary."""
     a, b = tmp_path / "a.csv", tmp_path / "b.csv"
-    _raw_csv(a)
-    rows = list(csv.reader(open(a)))
-    with open(b, "w", newline="") as f:
-        w = csv.writer(f)
-        w.writerows(rows[:2])
-        w.writerow(["0", "k_pose_grad_saved(tp::Params)", "560", "3", "100", "73", "40"])
+    for path, row in ((a, ["0", "void tp::k_brick_project<1, 2>(tp::Params, int)", "90", "500",
+                          "560", "55", "128"]),
+                      (b, ["0", "tp::k_brick_scatter_cubic<0>(tp::Params, int)", "160", "17", "900",
+                          "82", "109"])):
+        rows = list(csv.reader(open(_raw_csv(tmp_path / "full.csv") or tmp_path / "full.csv")))
+        with open(path, "w", newline="") as f:
+            w = csv.writer(f)
+            w.writerows(rows[:2])
+            w.writerow(row)
     d = bench.ncu_summary([str(a), str(b)], str(tmp_path / "out.json"))
-    assert set(d["kernels"]) == {"project_3d_2d", "volume_grad_scatter", "pose_grad_saved"}
-    assert d["kernels"]["pose_grad_saved"]["dram_read_bytes"] == 560e6
+    assert set(d["kernels"]) == {"project_3d_2d", "volume_grad_scatter"}
+    assert d["kernels"]["project_3d_2d"]["dram_read_bytes"] == 90e6
+    assert d["kernels"]["volume_grad_scatter"]["duration_ns"] == 900e3
     assert d["from"] == ["a.csv", "b.csv"]
 
 
@@ -64,7 +68,6 @@ def test_summary_scales_units_and_keeps_the_first_launch(tmp_path):
     assert fwd["mem_sol_pct"] == 55.5 and fwd["registers"] == 126
     sc = d["kernels"]["volume_grad_scatter"]
     assert sc["dram_bytes_per_launch"] == 160e6 + 17e3        # writes in Kbyte
-    assert "pose_grad_saved" not in d["kernels"]           # not in the export
 
 
 def test_stale_summary_is_not_reported(tmp_path, monkeypatch):
