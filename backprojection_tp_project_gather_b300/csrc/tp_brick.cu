@@ -1020,54 +1020,60 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // ---------------------------------------------------------------------------
 // Backprojection / spectrum gradient (adjoint of the forward projection).
 //
-// Both kernels set up each group of 32 candidates one sample per lane
-// (ownership, stencil weights, conj(phase) * y), queue the owned samples in
-// shared memory and then spread them cooperatively over the taps.
-
-// Cubic: every warp owns a private accumulator for one octant (8^3) of a
+// Both scatter kernels give every warp a private tile for one part of a
 // brick plus the stencil's halo, so the spreading needs no atomics.  A warp
-// takes (work unit, octant) items from the global counter on its own, runs
-// through all poses of the unit that reach its octant and enumerates only
-// the samples whose floor(p) lies in it; each sample is spread by the whole
-// warp, the lanes taking its taps (jx, jy, jz) and (jx, jy, jz + 2) with
-// x, y from the lane and jz from the half-warp.  With the tile's x pitch of
-// 12 complex words the 16 lanes of a half-warp fall into distinct bank
-// pairs, so the 64-bit reads and writes of a round never conflict.  The
-// tile is folded into the stored half-spectrum with vector global atomics
-// when the item is done.
+// takes (work unit, part) items from the global counter on its own, runs
+// through all poses of the unit that reach its part and enumerates only the
+// samples whose floor(p) lies in it; the tile is folded into the stored
+// half-spectrum with vector global atomics (Friedel positions conjugated at
+// -n) when the item is done.
+
+// Cubic: one lane spreads one sample.  The owned samples of the enumeration
+// rounds are packed into a 32-slot buffer (the fraction of p, the first tap,
+// conj(phase) * y and omega); whenever it holds 32, every lane takes one and
+// spreads its 64 taps.  The tile's (x, y) layers are cut into 4 x 4 tiles of
+// 16 complex words, so word (x, y, z) sits in bank pair (x mod 4) + 4 (y mod
+// 4), and lane L visits its taps in its own order: at step (sx, sy, sz) it
+// takes the tap whose tile coordinates are congruent to (sx + L, sy + L / 4,
+// sz + L / 16) modulo 4.  The 32 lanes then touch taps of 32 distinct residue
+// triples -- 32 distinct words, wherever their samples lie -- and each
+// half-warp's 16 words fall into 16 distinct bank pairs, so every 64-bit
+// read or write of the warp takes the minimum two wavefronts.  Steps sz and
+// sz + 2 share one warp barrier: over the two, half-warp 0 touches the z
+// residues sz and sz + 2 and half-warp 1 the residues sz + 1 and sz + 3, so
+// the words of the pair are still distinct across lanes.
+//
+// The real weight tile (backprojection with the weight spectrum) pairs its
+// z layers: word (x, y, z) sits in bank 16 (z mod 2) + 4 (y mod 4) + x mod 4,
+// and since a step's two half-warps differ in the parity of z, a warp's
+// 32-bit access covers the 32 banks once.
 constexpr int kOct = kBS / 2;              // octant edge
 constexpr int kOS = kOct + 3;              // octant + cubic halo (taps x0 - 1 .. x0 + 2)
-constexpr int kOPX = 12;                   // x pitch of the tile (complex words)
-// The real weight tile is addressed with 32-bit words by the whole warp at
-// once: with pitches 12 x 12 the second half-warp's taps (jz + 1, 144 words
-// on, 16 banks away) land in the 16 banks the first half-warp leaves free.
-constexpr int kOWPY = 12;                    // y pitch of the weight tile
-constexpr int kOQW = 9;                      // floats per queued weight row (odd: no bank conflicts)
+constexpr int kCT = 12;                    // (x, y) extent of a tile layer: 3 x 3 tiles of 4 x 4
+constexpr int kCLayer = kCT * kCT;         // complex words of one z layer
+constexpr int kCWPair = 2 * kCLayer;       // weight words of a pair of z layers
 
-// Queued samples of a warp.  A lane of half-warp h reads its z weights
-// (wz[h], wz[h + 2]) with one 64-bit load from wz[], hence their order there.
-struct OctQueue {
-    float w[32][kOQW];   // per sample: wx (4), wy (4), unused
-    float4 wz[32];       // per sample: wz0, wz2, wz1, wz3
-    float4 rec[32];      // per sample: conj(phase) * y (re, im), omega, first tap (| z << 16
-                         // with weights)
+// Samples waiting to be spread by a warp, one per slot.
+struct CubicBuf {
+    float4 pos[32];   // fraction of p in x, y, z; first tap x | y << 8 | z << 16 (tile coordinates)
+    float4 val[32];   // conj(phase) * y (re, im), omega, unused
 };
 
 // A work item is one part of a unit's brick: an octant (8^3), or, with the
 // weight spectrum, half of one in z (8 x 8 x 4), so that the two tiles and
-// the queue of a warp fit 16 warps into an SM's shared memory.
+// the buffer of a warp fit 16 warps into an SM's shared memory.
 template <bool WEIGHTS>
 struct OctLayout {
-    static constexpr int WARPS = WEIGHTS ? 2 : 4;   // warps per block (blocks only share an SM)
+    static constexpr int WARPS = 4;                  // warps per block (blocks only share an SM)
     static constexpr int OZ = WEIGHTS ? kOct / 2 : kOct;   // z extent of an item's box
     static constexpr int PARTS = 4 * (kBS / OZ);     // items per work unit
     static constexpr int SZ = OZ + 3;                // z layers of the tiles
-    static constexpr int ELEMS = kOS * kOPX * SZ;    // complex words of the tile
-    static constexpr int WELEMS = kOWPY * kOPX * SZ; // words of the weight tile
+    static constexpr int ELEMS = kCLayer * SZ;       // complex words of the tile
+    static constexpr int WELEMS = WEIGHTS ? kCWPair * ((SZ + 1) / 2) : 0;   // words of the weight tile
     static constexpr size_t TILE = sizeof(float2) * ELEMS;
-    static constexpr size_t WTILE = WEIGHTS ? sizeof(float) * WELEMS : 0;
-    static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(OctQueue);
-    static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned queue");
+    static constexpr size_t WTILE = sizeof(float) * WELEMS;
+    static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(CubicBuf);
+    static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned buffer");
 };
 
 // Box of part `oct` of a brick: x and y halves from bits 0 and 1, the z
@@ -1085,9 +1091,118 @@ __device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct, int 
     return ob;
 }
 
+// Ownership test of pixel (qx, qy) for a box SIZE voxels wide in x and y and
+// SIZEZ in z: floor(p) - origin per axis, packed one per byte, and the
+// fraction of p.
+template <int SIZE, int SIZEZ>
+__device__ __forceinline__ bool own_position(const PoseGeo &g, const BrickBox &bx, int qx, int qy,
+                                             int &packed, float (&t)[3]) {
+    bool own = true;
+    packed = 0;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const float p = fmaf(g.a[a], (float)qx, g.b[a] * (float)qy);
+        const int l = split_coord(p, t[a]) - bx.o[a];
+        own = own && (unsigned)l < (unsigned)(a == 2 ? SIZEZ : SIZE);
+        packed |= (l & 0xff) << (8 * a);
+    }
+    return own;
+}
+
+__device__ __forceinline__ float2 lds_f2(unsigned a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_f2(unsigned a, float2 v) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ float lds_f1(unsigned a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_f1(unsigned a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+// Every lane spreads the sample in its buffer slot (none when !act) into the
+// warp's tile (and weight tile): shared-memory byte addresses tile, wtile.
+// Call with the whole warp after a __syncwarp that follows the buffer writes.
+template <bool WEIGHTS>
+__device__ __forceinline__ void spread_cubic(const CubicBuf &buf, unsigned tile, unsigned wtile,
+                                             bool act, unsigned *dbg) {
+    using OL = OctLayout<WEIGHTS>;
+    const int lane = threadIdx.x & 31;
+    float4 P = buf.pos[lane];
+    float4 C = buf.val[lane];
+    int b = __float_as_int(P.w);
+    int l0 = b & 0xff, l1 = (b >> 8) & 0xff, l2 = b >> 16;
+    act = act && TP_CHECK(dbg, l0 < kOct && l1 < kOct && l2 < OL::OZ, 4);
+    if (!act) {   // a lane without a sample adds zeros to in-range words
+        l0 = l1 = l2 = 0;
+        P = make_float4(0.f, 0.f, 0.f, 0.f);
+        C = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float w[3][4], r[3][4];
+    Stencil<true>::weights(P.x, w[0]);
+    Stencil<true>::weights(P.y, w[1]);
+    Stencil<true>::weights(P.z, w[2]);
+    const int cx = (lane - l0) & 3, cy = ((lane >> 2) - l1) & 3, cz = ((lane >> 4) - l2) & 3;
+    rot4(w[0], cx, r[0]);
+    rot4(w[1], cy, r[1]);
+    rot4(w[2], cz, r[2]);
+    // Byte offsets of the taps of step s on each axis.
+    unsigned ox[4], oy[4], oz[4], wox[4], woy[4], woz[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int x = l0 + ((s + cx) & 3), y = l1 + ((s + cy) & 3), z = l2 + ((s + cz) & 3);
+        ox[s] = 8u * ((x >> 2) * 16 + (x & 3));
+        oy[s] = 8u * ((y >> 2) * (4 * kCT) + 4 * (y & 3));
+        oz[s] = tile + 8u * (z * kCLayer);
+        if (WEIGHTS) {
+            wox[s] = 4u * ((x >> 2) * 32 + (x & 3));
+            woy[s] = 4u * ((y >> 2) * (8 * kCT) + 4 * (y & 3));
+            woz[s] = wtile + 4u * ((z >> 1) * kCWPair + 16 * (z & 1));
+        }
+    }
+    float2 cz2[4];
+    float czw[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        cz2[s] = make_float2(r[2][s] * C.x, r[2][s] * C.y);
+        czw[s] = r[2][s] * C.z;
+    }
+#pragma unroll
+    for (int sg = 0; sg < 2; ++sg) {
+#pragma unroll
+        for (int sy = 0; sy < 4; ++sy) {
+            const float2 c0 = make_float2(r[1][sy] * cz2[sg].x, r[1][sy] * cz2[sg].y);
+            const float2 c1 = make_float2(r[1][sy] * cz2[sg + 2].x, r[1][sy] * cz2[sg + 2].y);
+            const unsigned a0 = oy[sy] + oz[sg], a1 = oy[sy] + oz[sg + 2];
+            const float w0 = r[1][sy] * czw[sg], w1 = r[1][sy] * czw[sg + 2];
+            const unsigned b0 = woy[sy] + woz[sg], b1 = woy[sy] + woz[sg + 2];
+#pragma unroll
+            for (int sx = 0; sx < 4; ++sx) {
+                float2 v0 = lds_f2(a0 + ox[sx]), v1 = lds_f2(a1 + ox[sx]);
+                cfma(r[0][sx], c0, v0);
+                cfma(r[0][sx], c1, v1);
+                sts_f2(a0 + ox[sx], v0);
+                sts_f2(a1 + ox[sx], v1);
+                if (WEIGHTS) {
+                    const float u0 = lds_f1(b0 + wox[sx]), u1 = lds_f1(b1 + wox[sx]);
+                    sts_f1(b0 + wox[sx], fmaf(r[0][sx], w0, u0));
+                    sts_f1(b1 + wox[sx], fmaf(r[0][sx], w1, u1));
+                }
+                // The next steps' taps may be other lanes' words of these steps.
+                __syncwarp();
+            }
+        }
+    }
+}
 
 template <bool WEIGHTS>
-__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 8 : 4)
+__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, 4)
     k_brick_scatter_cubic(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
                           const float *__restrict__ omega, float2 *__restrict__ dst,
                           float *__restrict__ wdst) {
@@ -1097,22 +1212,18 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 8 : 
     char *mine = reinterpret_cast<char *>(s_oct) + (threadIdx.x >> 5) * OL::WARP_BYTES;
     float2 *acc = reinterpret_cast<float2 *>(mine);
     float *wacc = reinterpret_cast<float *>(mine + OL::TILE);
-    OctQueue &Q = *reinterpret_cast<OctQueue *>(mine + OL::TILE + OL::WTILE);
-    const int jx = lane & 3, jy = (lane >> 2) & 3, tz = lane >> 4;
-    const int toff = jx + kOPX * (jy + kOS * tz);
-    const int toff_w = jx + kOPX * (jy + kOWPY * tz);
-    constexpr int ZSTEP = 2 * kOPX * kOS;      // tile offset of taps jz + 2
-    constexpr int ZSTEP_W = 2 * kOPX * kOWPY;  // the same in the weight tile
+    CubicBuf &buf = *reinterpret_cast<CubicBuf *>(mine + OL::TILE + OL::WTILE);
+    const unsigned tile = (unsigned)__cvta_generic_to_shared(acc);
+    const unsigned wtile = (unsigned)__cvta_generic_to_shared(wacc);
+    const unsigned below = (1u << lane) - 1u;
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    constexpr int kOElems = OL::ELEMS, kOWElems = OL::WELEMS;
     const int items = OL::PARTS * (int)__ldg(sc.counters + 3 * nvol + v);
     const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
-    for (int e = lane; e < kOElems; e += 32) acc[e] = make_float2(0.f, 0.f);
-    if (WEIGHTS)
-        for (int e = lane; e < kOWElems; e += 32) wacc[e] = 0.f;
+    for (int e = lane; e < OL::ELEMS; e += 32) acc[e] = make_float2(0.f, 0.f);
+    for (int e = lane; e < OL::WELEMS; e += 32) wacc[e] = 0.f;
     __syncwarp();
     for (;;) {
         int item = 0;
@@ -1128,94 +1239,77 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, WEIGHTS ? 8 : 
         const BrickBox ob = octant_box(brick_box(rec.x, nb), part, OL::OZ);
         const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
         bool touched = false;
+        int pend = 0;   // samples in the buffer (warp-uniform)
         for (int c = rec.y; c < rec.z; ++c) {
-            for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
-                const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
-                if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
-                const PoseGeo g = load_geo(sc.geo, pid);
-                if (!pose_reaches(g, ob)) continue;
+            // The poses of the chunk that can reach this part, tested one per lane.
+            const unsigned m = __ldg(masks + c);
+            bool reach = false;
+            if ((m >> lane) & 1u) {
+                const int pid = pose_id(q, v, c * 32 + lane);
+                if (TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8))
+                    reach = pose_reaches(load_geo(sc.geo, pid), ob);
+            }
+            for (unsigned mr = __ballot_sync(0xffffffffu, reach); mr; mr &= mr - 1) {
+                const PoseGeo g = load_geo(sc.geo, pose_id(q, v, c * 32 + __ffs(mr) - 1));
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
                 for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                    int l[3];
-                    float w[3][4], d[3][4];
-                    const bool own =
-                        active && own_sample<true, false, kOct, OL::OZ>(g, ob, qx, qy, l, w, d);
+                    // The image value is loaded first, to be in flight during the
+                    // ownership test and the phase.
+                    const int iy = qy < 0 ? qy + q.N : qy;
+                    const bool in = active && TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 &&
+                                                                  qx < q.Xo && g.bp < q.B * q.P, 7);
+                    float2 cv = make_float2(0.f, 0.f);
+                    float om = 1.0f;
+                    if (in) {
+                        cv = __ldg(img + ib + iy * q.Xo + qx);
+                        if (WEIGHTS && omega) om = __ldg(omega + ib + iy * q.Xo + qx);
+                    }
+                    int packed;
+                    float t[3];
+                    const bool own = active && own_position<kOct, OL::OZ>(g, ob, qx, qy, packed, t);
                     const unsigned mask = __ballot_sync(0xffffffffu, own);
+                    if (mask == 0u) return;
+                    const int slot = pend + __popc(mask & below);
+                    float4 pos, val;
                     if (own) {
-                        const int slot = __popc(mask & ((1u << lane) - 1u));
-                        const int iy = qy < 0 ? qy + q.N : qy;
-                        const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo &&
-                                                            g.bp < q.B * q.P, 7);
-                        float2 cv = in ? __ldg(img + ib + iy * q.Xo + qx) : make_float2(0.f, 0.f);
                         if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
-                        float *wq = Q.w[slot];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            wq[j] = w[0][j];
-                            wq[4 + j] = w[1][j];
+                        pos = make_float4(t[0], t[1], t[2], __int_as_float(packed));
+                        val = make_float4(cv.x, cv.y, om, 0.f);
+                        if (slot < 32) {
+                            buf.pos[slot] = pos;
+                            buf.val[slot] = val;
                         }
-                        Q.wz[slot] = make_float4(w[2][0], w[2][2], w[2][1], w[2][3]);
-                        const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
-                        // The weight tile's first tap differs from the complex
-                        // tile's by kOPX (kOWPY - kOS) z: the z travels along.
-                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
-                                                  __int_as_float(((l[2] * kOS + l[1]) * kOPX + l[0]) |
-                                                                 (WEIGHTS ? l[2] << 16 : 0)));
                     }
-                    __syncwarp();
-                    const int nq = __popc(mask);
-                    // The next sample's queue entries are read before this
-                    // sample's tile words, hiding their latency.
-                    float wx = 0.f, wy = 0.f;
-                    float2 wz = make_float2(0.f, 0.f);
-                    float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (nq > 0) {
-                        wx = Q.w[0][jx];
-                        wy = Q.w[0][4 + jy];
-                        wz = reinterpret_cast<const float2 *>(&Q.wz[0])[tz];
-                        r4 = Q.rec[0];
-                    }
-                    for (int sq = 0; sq < nq; ++sq) {
-                        const float wxy = wx * wy;
-                        const float wt0 = wxy * wz.x, wt1 = wxy * wz.y;
-                        const float4 cur = r4;
-                        if (sq + 1 < nq) {
-                            wx = Q.w[sq + 1][jx];
-                            wy = Q.w[sq + 1][4 + jy];
-                            wz = reinterpret_cast<const float2 *>(&Q.wz[sq + 1])[tz];
-                            r4 = Q.rec[sq + 1];
-                        }
-                        const int packed = __float_as_int(cur.w);
-                        const int base = WEIGHTS ? packed & 0xffff : packed;
-                        const int idx = base + toff;
-                        const int widx = base + kOPX * (kOWPY - kOS) * (packed >> 16) + toff_w;
-                        if (TP_CHECK(q.dbg, idx >= 0 && idx + ZSTEP < kOElems, 4)) {
-                            float2 a0 = acc[idx], a1 = acc[idx + ZSTEP];
-                            const float2 cv = make_float2(cur.x, cur.y);
-                            cfma(wt0, cv, a0);
-                            cfma(wt1, cv, a1);
-                            acc[idx] = a0;
-                            acc[idx + ZSTEP] = a1;
-                        }
-                        if (WEIGHTS && TP_CHECK(q.dbg, widx >= 0 && widx + ZSTEP_W < kOWElems, 5)) {
-                            wacc[widx] = fmaf(wt0, cur.z, wacc[widx]);
-                            wacc[widx + ZSTEP_W] = fmaf(wt1, cur.z, wacc[widx + ZSTEP_W]);
-                        }
-                        // The lanes' words of a sample are distinct, but the
-                        // next sample's taps may reuse another lane's words.
+                    pend += __popc(mask);
+                    if (pend >= 32) {
                         __syncwarp();
+                        spread_cubic<WEIGHTS>(buf, tile, wtile, true, q.dbg);
+                        // Every lane has read its slot (the spread's barriers
+                        // follow the reads): the overflow moves to the front.
+                        if (own && slot >= 32) {
+                            buf.pos[slot - 32] = pos;
+                            buf.val[slot - 32] = val;
+                        }
+                        pend -= 32;
                     }
                 });
             }
         }
         if (!touched) continue;
+        if (pend > 0) {
+            __syncwarp();
+            spread_cubic<WEIGHTS>(buf, tile, wtile, lane < pend, q.dbg);
+        }
+        __syncwarp();
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0] - 1, y0 = ob.o[1] - 1, z0 = ob.o[2] - 1;
         for (int e = lane; e < kOS * kOS * OL::SZ; e += 32) {
             const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
-            const int k = (lz * kOS + ly) * kOPX + lx;
-            const int kw = (lz * kOWPY + ly) * kOPX + lx;
+            const int xy = ((ly >> 2) * (kCT / 4) + (lx >> 2)) * 16 + 4 * (ly & 3) + (lx & 3);
+            const int k = lz * kCLayer + xy;
+            const int kw = (lz >> 1) * kCWPair + xy + ((ly >> 2) * (kCT / 4) + (lx >> 2)) * 16 +
+                           16 * (lz & 1);
             const float2 cv = acc[k];
             const float wv = WEIGHTS ? wacc[kw] : 0.f;
             if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
@@ -1306,11 +1400,16 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
         const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
         bool touched = false;
         for (int c = rec.y; c < rec.z; ++c) {
-            for (unsigned m = __ldg(masks + c); m; m &= m - 1) {
-                const int pid = pose_id(q, v, c * 32 + __ffs(m) - 1);
-                if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
-                const PoseGeo g = load_geo(sc.geo, pid);
-                if (!pose_reaches(g, ob)) continue;
+            // The poses of the chunk that can reach this octant, tested one per lane.
+            const unsigned m = __ldg(masks + c);
+            bool reach = false;
+            if ((m >> lane) & 1u) {
+                const int pid = pose_id(q, v, c * 32 + lane);
+                if (TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8))
+                    reach = pose_reaches(load_geo(sc.geo, pid), ob);
+            }
+            for (unsigned mr = __ballot_sync(0xffffffffu, reach); mr; mr &= mr - 1) {
+                const PoseGeo g = load_geo(sc.geo, pose_id(q, v, c * 32 + __ffs(mr) - 1));
                 touched = true;
                 const size_t ib = (size_t)g.bp * q.plane;
                 for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
