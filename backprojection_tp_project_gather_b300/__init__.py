@@ -85,7 +85,7 @@ _SIGS = {
                                       _P, _P, _P, _P, _P, _Z, _P, _Z, _P],
     "tp_backproject_backward_scratch_bytes": [_I, _I, _I, _I, _I, _I],
 }
-_SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, TPOptions]
+_SIGS["tp_workspace_bytes"] = [_I, _I, _I, _I, _I, TPOptions]
 _SIGS["tp_debug_bounds_word"] = [_I]
 _SIGS["tp_hermitian_x0"] = [_P, _P, _I, _I, _I, ctypes.c_void_p]
 _SIGS["tp_debug_bounds_selftest"] = [_I, ctypes.c_void_p]
@@ -132,14 +132,16 @@ def tp_debug_bounds_selftest(bit: int, stream=None) -> None:
     _call("tp_debug_bounds_selftest", int(bit), _stream(stream))
 
 
-def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic"):
-    """Workspace bytes the 3D entry points need (see include/tp.h)."""
-    return int(_fn("tp_workspace_bytes")(int(Bv), int(B), int(P), int(Nv),
+def tp_workspace_bytes(Bv, B, P, Nv, interp="cubic", N=None):
+    """Workspace bytes the 3D entry points need for volume box Nv and image box N
+    (default: Nv); see include/tp.h."""
+    N = Nv if N is None else int(N)
+    return int(_fn("tp_workspace_bytes")(int(Bv), int(B), int(P), int(Nv), N,
                                          _opts(interp, 1.0, -1.0)))
 
 
-def _workspace(ws, Bv, B, P, Nv, interp, device):
-    need = tp_workspace_bytes(Bv, B, P, Nv, interp)
+def _workspace(ws, Bv, B, P, Nv, N, interp, device):
+    need = tp_workspace_bytes(Bv, B, P, Nv, interp, N)
     if ws is None:
         # A block fresh from the caching allocator may hold an old workspace
         # of the same shape; clearing its first 256 bytes (the key of the
@@ -218,7 +220,7 @@ def _forward(name, dim, src, rot, shift, N, interp, oversampling, radius, out, s
     args = [_ptr(src), Bsrc, M, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
             _opts(interp, oversampling, radius), _ptr(out)]
     if dim == 3:
-        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, interp, src.device)
+        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, N, interp, src.device)
         args += [_ptr(ws), nbytes]
     _call(name, *args, _stream(stream))
     return out
@@ -255,7 +257,7 @@ def _backward(name, dim, grad_out, src, rot, shift, interp, oversampling, radius
             _ptr(grad_shift)]
     if dim == 3:
         B = grad_out.shape[0]
-        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, interp, grad_out.device)
+        ws, nbytes = _workspace(workspace, Bsrc, B, P, M, N, interp, grad_out.device)
         args += [_ptr(ws), nbytes]
     _call(name, *args, _stream(stream))
     return grad_src, grad_rot, grad_shift
@@ -289,7 +291,7 @@ def tp_project_3d_2d_save(vol, rot, shift=None, *, N=None, interp="cubic", overs
     _need(dout, "dout", torch.complex64, 5)
     if tuple(out.shape) != shape or tuple(dout.shape) != shape + (3,):
         raise ValueError(f"out must be {shape} and dout {shape + (3,)}")
-    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, vol.device)
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, N, interp, vol.device)
     _call("tp_project_3d_2d_save", _ptr(vol), Bv, Nv, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
           _opts(interp, oversampling, radius), _ptr(out), _ptr(dout), _ptr(ws), nbytes,
           _stream(stream))
@@ -331,7 +333,7 @@ def tp_project_3d_2d_l2(vol, rot, shift, target, *, N=None, interp="cubic", over
         _need(grad_shift, "grad_shift", torch.float32, 3)
         if shift is None or grad_shift.shape != shift.shape:
             raise ValueError("grad_shift must have shift's shape")
-    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, vol.device)
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, N, interp, vol.device)
     _call("tp_project_3d_2d_l2", _ptr(vol), Bv, Nv, _ptr(rot), Bp, P, _ptr(shift), Bs, N,
           _opts(interp, oversampling, radius), _ptr(target), _ptr(out), _ptr(grad_out),
           _ptr(grad_rot), _ptr(grad_shift), _ptr(ws), nbytes, _stream(stream))
@@ -452,7 +454,7 @@ def tp_backproject_2d_3d(proj, rot, shift=None, weights=None, *, Nv=None, Bv=1, 
         _need(weight_vol, "weight_vol", torch.float32, 4)
         if tuple(weight_vol.shape) != shape:
             raise ValueError(f"weight_vol must be {shape}")
-    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, proj.device)
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, N, interp, proj.device)
     _call("tp_backproject_2d_3d", _ptr(proj), _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift),
           Bs, Bv, Nv, _opts(interp, oversampling, radius, hermitian_x0), _ptr(data_vol),
           _ptr(weight_vol),
@@ -541,7 +543,7 @@ def tp_backproject_2d_3d_backward(grad_data_vol, proj, rot, shift=None, weights=
         scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     if scratch.device.type != "cuda" or not scratch.is_contiguous():
         raise ValueError("scratch must be a contiguous CUDA tensor")
-    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, interp, dev)
+    ws, nbytes = _workspace(workspace, Bv, B, P, Nv, N, interp, dev)
     _call("tp_backproject_2d_3d_backward", _ptr(grad_data_vol), _ptr(grad_weight_vol), _ptr(proj),
           _ptr(weights), B, P, N, _ptr(rot), Bp, _ptr(shift), Bs, Bv, Nv,
           _opts(interp, oversampling, radius), _ptr(grad_proj), _ptr(grad_weights), _ptr(grad_rot),

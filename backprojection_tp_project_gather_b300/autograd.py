@@ -35,7 +35,7 @@ class _Project3D(torch.autograd.Function):
         # One workspace per call: the backward finds the forward's binning in it.
         B = max(vol.shape[0], rot.shape[0], shift.shape[0] if shift is not None else 1)
         ws = torch.empty(max(1, tp_workspace_bytes(vol.shape[0], B, rot.shape[1], vol.shape[1],
-                                                   interp)), dtype=torch.uint8, device=vol.device)
+                                                   interp, N)), dtype=torch.uint8, device=vol.device)
         if need_pose:
             out, dout = tp_project_3d_2d_save(vol, rot, shift, workspace=ws, **kw)
         else:

@@ -109,6 +109,8 @@ tp_status setup(int dim, int Bsrc, int M, const float *rot, int Bp, int P, const
     q.fN = (float)N;
     q.invN = 1.0f / (float)N;
     q.r2max = r2 > 2e9 ? 2000000000 : (int)r2;
+    q.mplane = (unsigned)((1ULL << 32) / (unsigned long long)plane);
+    q.mxo = (unsigned)((1ULL << 32) / (unsigned long long)Xo);
     q.dbg = dbg_word();
     g.dim = dim;
     g.cubic = o.interp == TP_CUBIC;
@@ -126,10 +128,16 @@ tp_status check_complex(const float *p, const char *name) {
     return TP_OK;
 }
 
-// Workspace check for the 3D operators (the 2D ones need none).
-tp_status check_workspace(const Geometry &g, void *ws, size_t ws_bytes) {
+// Workspace check for the 3D operators (the 2D ones need none).  lists: the
+// call runs the cubic scatter, whose sample lists follow the binning.
+tp_status check_workspace(const Geometry &g, void *ws, size_t ws_bytes, bool lists) {
     if (g.dim != 3) return TP_OK;
-    const size_t need = tp::brick_workspace_bytes(g.q, g.cubic);
+    if (lists && (long long)g.q.B * g.q.P * g.q.plane >= (1LL << 31))
+        return fail(TP_ERR_SHAPE, "too many output pixels for one scatter call (%lld); split the poses",
+                    (long long)g.q.B * g.q.P * g.q.plane);
+    if (lists && (long long)g.q.Bsrc * tp::brick_parts(g.q, g.cubic) >= (1LL << 31))
+        return fail(TP_ERR_SHAPE, "too many volumes of this box for one scatter call; split the batch");
+    const size_t need = lists ? tp::brick_workspace_bytes(g.q, g.cubic) : tp::brick_binning_bytes(g.q, g.cubic);
     if (!ws) return fail(TP_ERR_NULL, "workspace is required (%zu bytes, see tp_workspace_bytes)", need);
     if (!aligned(ws, 16)) return fail(TP_ERR_ALIGN, "workspace must be 16-byte aligned");
     if (ws_bytes < need)
@@ -149,7 +157,7 @@ tp_status forward(int dim, const float *src, int Bsrc, int M, const float *rot, 
     if ((st = check_complex(src, "source")) != TP_OK || (st = check_complex(out, "out")) != TP_OK)
         return st;
     if (dout && (st = check_complex(dout, "dout")) != TP_OK) return st;
-    if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
+    if ((st = check_workspace(g, ws, ws_bytes, false)) != TP_OK) return st;
     g.q.src = reinterpret_cast<const float2 *>(src);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float2 *o = reinterpret_cast<float2 *>(out);
@@ -177,7 +185,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
     if (grad_src && (st = check_complex(grad_src, "grad of the source")) != TP_OK) return st;
     if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
-    if ((st = check_workspace(g, ws, ws_bytes)) != TP_OK) return st;
+    if ((st = check_workspace(g, ws, ws_bytes, grad_src && g.cubic)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     tp::BinMode mode = tp::kBinNew;
     if (grad_rot || grad_shift) {
@@ -213,6 +221,22 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
 
 namespace tp {
 
+// Workspace bytes of the 3D operators; lists: with the cubic scatter's
+// sample lists (every operator), else the binning alone (the forward).
+size_t workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts, bool lists) {
+    if (Bv < 1 || B < 1 || P < 1 || Nv < 2 || (Nv & 1) || Nv > 4096 || N < 2 || (N & 1) || N > 4096 ||
+        Bv > B)
+        return 0;
+    tp::Params q{};
+    q.Bsrc = Bv;
+    q.B = B;
+    q.P = P;
+    q.M = Nv;
+    q.N = N;
+    const bool cubic = opts.interp == TP_CUBIC;
+    return lists ? tp::brick_workspace_bytes(q, cubic) : tp::brick_binning_bytes(q, cubic);
+}
+
 tp_status fail(tp_status st, const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -225,14 +249,8 @@ tp_status fail(tp_status st, const char *fmt, ...) {
 
 extern "C" {
 
-size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts) {
-    if (Bv < 1 || B < 1 || P < 1 || Nv < 2 || (Nv & 1) || Nv > 4096 || Bv > B) return 0;
-    tp::Params q{};
-    q.Bsrc = Bv;
-    q.B = B;
-    q.P = P;
-    q.M = Nv;
-    return tp::brick_workspace_bytes(q, opts.interp == TP_CUBIC);
+size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts) {
+    return tp::workspace_bytes(Bv, B, P, Nv, N, opts, true);
 }
 
 tp_status tp_project_3d_2d(const float *vol, int Bv, int Nv, const float *rot, int Bp, int P,
@@ -268,7 +286,7 @@ tp_status tp_project_3d_2d_l2(const float *vol, int Bv, int Nv, const float *rot
         return st;
     if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
-    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    if ((st = check_workspace(g, workspace, workspace_bytes, false)) != TP_OK) return st;
     g.q.src = reinterpret_cast<const float2 *>(vol);
     return launched(tp::launch_brick_project_l2(g.cubic, g.q, reinterpret_cast<const float2 *>(target),
                                                 reinterpret_cast<float2 *>(out),
@@ -365,7 +383,7 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
         return st;
     if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
         return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
-    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    if ((st = check_workspace(g, workspace, workspace_bytes, g.cubic)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float2 *dv = reinterpret_cast<float2 *>(data_vol);
     cudaError_t e = tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),
@@ -424,7 +442,7 @@ tp_status tp_backproject_2d_3d_backward(const float *grad_data_vol, const float 
         return fail(TP_ERR_ALIGN, "real arrays must be 4-byte aligned");
     const bool weight_terms = grad_weight_vol && (grad_weights || grad_rot);
     if (!data_terms && !weight_terms) return ok();
-    if ((st = check_workspace(g, workspace, workspace_bytes)) != TP_OK) return st;
+    if ((st = check_workspace(g, workspace, workspace_bytes, false)) != TP_OK) return st;
     const size_t need = tp_backproject_backward_scratch_bytes(Bv, B, P, N, Nv, weight_terms ? 1 : 0);
     if (!scratch) return fail(TP_ERR_NULL, "scratch is required (%zu bytes)", need);
     if (!aligned(scratch, 16)) return fail(TP_ERR_ALIGN, "scratch must be 16-byte aligned");

@@ -19,7 +19,9 @@
 //    samples into it with plain read-add-write, and adds the tile to the
 //    stored half-spectrum once per work item (Friedel positions conjugated
 //    at -n), with vector atomics because halos of neighbouring octants and
-//    other work items overlap.
+//    other work items overlap.  The cubic scatter reads its samples from
+//    lists of the output pixels sorted by brick part (a counting sort over
+//    the pixels); the linear one enumerates each reaching pose's pixels.
 //
 // Binning.  Three small passes precede every operator: one thread per pose
 // computes the pose's geometry (into the caller's workspace, where a later
@@ -30,8 +32,8 @@
 // block per volume then turns the counts into a compact list of work units
 // -- a brick and a range of chunks holding about kUnitHits reaching poses,
 // so busy bricks near the origin are split and empty bricks vanish.  The
-// main kernels take units (or, in the scatters, unit octants) from a global
-// counter in brick order, busiest first.  For one (pose, box) pair the
+// main kernels take units (or, in the linear scatter, unit octants) from a
+// global counter in brick order, busiest first.  For one (pose, box) pair the
 // owned pixels form a convex polygon in k-space: its rows come from the
 // pseudo-inverse of [a b] and each row's qx interval from the three slab
 // constraints; the enumeration is a small superset and the exact floor(p)
@@ -41,6 +43,7 @@
 // Library for PyTorch", 3D->2D projection and 2D->3D backprojection
 // [it §2 "Operazioni Supportate"; de §2 "Unterstützte Operationen"] with the
 // weight spectrum [de §2 "Dual-Volumen-Ansatz"].
+#include <algorithm>
 #include <cstddef>
 
 #include "tp_device.cuh"
@@ -115,13 +118,23 @@ struct BinKey {
 struct Scratch {
     unsigned *key;        // BinKey of the binning held in the workspace
     unsigned *changed;    // set by k_pose_geometry when key or geometry differ
-    unsigned *counters;   // [4][Bsrc]: work counters of the three main kernels, unit counts
+    unsigned *lflag;      // [0] the sample lists fit the binning held, [1] this call builds them
+    unsigned *counters;   // [6][Bsrc]: work counters of the three main kernels, unit counts,
+                          // octant and z-half item counts of the sample lists
     int4 *geo;            // B*P pose records of kGeoVec words
+    float4 *pose8;        // B*P poses: (a0, a1, a2, b0), (b1, b2, sx, sy)
     ReachGeo *reach;      // B*P poses, for the brick-mask pass
     unsigned *masks;      // [Bsrc][bricks][chunks] pose bitmasks
     int *hits;            // [Bsrc][bricks] reaching poses per brick
     int4 *units;          // [Bsrc][bricks * chunks] work units (brick, first chunk, end chunk)
+    // Sample lists (cubic scatter only; null in a forward-only workspace).
+    unsigned *lcount;     // [Bsrc][bricks * kParts] samples per brick part, then fill cursors
+    int4 *lbrick;         // [Bsrc][bricks] samples, octant items, z-half items; then their sums before
+    int4 *litems;         // [2][Bsrc][itemcap] items: (first entry, count, brick, box)
+    unsigned *llist;      // B*P*plane entries: output pixel index (b * P + p) * plane + row * Xo + kx
+    unsigned *lkey;       // B*P*plane: each in-radius pixel's key (count pass, for the fill)
     int nchunks;          // 32-pose chunks per volume
+    int itemcap;          // items per volume and kind
 };
 
 __device__ __forceinline__ void pose_geo(const Params &q, int b, int pi, PoseGeo &g) {
@@ -312,12 +325,15 @@ __global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratc
 #pragma unroll
             for (int i = 0; i < kKeyWords; ++i) sc.key[i] = key.w[i];
             atomicOr(sc.changed, 1u);
+            sc.lflag[0] = 0u;
         }
     }
     if (id >= q.B * q.P) return;
     const int b = id / q.P, pi = id - b * q.P;
     PoseGeo g;
     pose_geo(q, b, pi, g);
+    sc.pose8[2 * id] = make_float4(g.a[0], g.a[1], g.a[2], g.b[0]);
+    sc.pose8[2 * id + 1] = make_float4(g.b[1], g.b[2], g.sx, g.sy);
     {
         const float h = 0.5f * (float)kBS + kMargin;
         ReachGeo rg;
@@ -345,6 +361,7 @@ __global__ void __launch_bounds__(256) k_pose_geometry(Params q, int nbr, Scratc
         for (int j = 0; j < kGeoVec; ++j)
             rec[j] = make_int4(now[4 * j], now[4 * j + 1], now[4 * j + 2], now[4 * j + 3]);
         atomicOr(sc.changed, 1u);
+        sc.lflag[0] = 0u;
     }
 }
 
@@ -1021,27 +1038,333 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // Backprojection / spectrum gradient (adjoint of the forward projection).
 //
 // Both scatter kernels give every warp a private tile for one part of a
-// brick plus the stencil's halo, so the spreading needs no atomics.  A warp
-// takes (work unit, part) items from the global counter on its own, runs
-// through all poses of the unit that reach its part and enumerates only the
-// samples whose floor(p) lies in it; the tile is folded into the stored
-// half-spectrum with vector global atomics (Friedel positions conjugated at
-// -n) when the item is done.
+// brick plus the stencil's halo, so the spreading needs no atomics, and the
+// tile is folded into the stored half-spectrum with vector global atomics
+// (Friedel positions conjugated at -n) when the warp's work item is done.
+// The cubic scatter takes its samples from lists sorted by brick part; the
+// linear one runs through the poses of a work unit that reach its octant
+// and enumerates the samples whose floor(p) lies in it.
 
-// Cubic: one lane spreads one sample.  The owned samples of the enumeration
-// rounds are packed into a 32-slot buffer (the fraction of p, the first tap,
-// conj(phase) * y and omega); whenever it holds 32, every lane takes one and
-// spreads its 64 taps.  The tile's (x, y) layers are cut into 4 x 4 tiles of
-// 16 complex words, so word (x, y, z) sits in bank pair (x mod 4) + 4 (y mod
-// 4), and lane L visits its taps in its own order: at step (sx, sy, sz) it
-// takes the tap whose tile coordinates are congruent to (sx + L, sy + L / 4,
-// sz + L / 16) modulo 4.  The 32 lanes then touch taps of 32 distinct residue
-// triples -- 32 distinct words, wherever their samples lie -- and each
-// half-warp's 16 words fall into 16 distinct bank pairs, so every 64-bit
-// read or write of the warp takes the minimum two wavefronts.  Steps sz and
-// sz + 2 share one warp barrier: over the two, half-warp 0 touches the z
-// residues sz and sz + 2 and half-warp 1 the residues sz + 1 and sz + 3, so
-// the words of the pair are still distinct across lanes.
+// Sample lists: every in-radius output pixel whose floor(p) lies in the
+// brick grid, binned by brick part with a counting sort (count, scan, fill).
+// A brick has kParts parts, its x and y halves times its four z quarters,
+// numbered (z half, y half, x half, z quarter within the half): the two
+// parts of an octant are consecutive, and part >> 1 is the octant's index
+// for octant_box.  The lists depend on the poses alone, so a call keeps the
+// ones held in the workspace when its binning is unchanged (k_pose_geometry
+// clears lflag[0] whenever it is not).
+constexpr int kParts = 16;
+constexpr int kListChunk = 2048;   // most samples per scatter item
+constexpr int kListThreads = 1024;
+
+// Sample position of output pixel (qx, qy) of a pose: the ownership test of
+// the forward (own_sample) uses the same expression, so both agree on floor(p).
+__device__ __forceinline__ void pose8_position(const float4 &A, const float4 &Bv, int qx, int qy,
+                                               float (&p)[3]) {
+    p[0] = fmaf(A.x, (float)qx, A.w * (float)qy);
+    p[1] = fmaf(A.y, (float)qx, Bv.x * (float)qy);
+    p[2] = fmaf(A.z, (float)qx, Bv.y * (float)qy);
+}
+
+// Output pixel e = bp * plane + iy * Xo + qx as (bp, qx, qy).
+__device__ __forceinline__ unsigned split_pixel(const Params &q, unsigned e, int &qx, int &qy) {
+    const unsigned bp = udiv(e, (unsigned)q.plane, q.mplane);
+    const unsigned pix = e - bp * (unsigned)q.plane;
+    const unsigned iy = udiv(pix, (unsigned)q.Xo, q.mxo);
+    qx = (int)(pix - iy * (unsigned)q.Xo);
+    qy = row_freq((int)iy, q.N);
+    return bp;
+}
+
+// List key (volume v, brick, part) of a sample at p: the sum of one table
+// entry per axis (built by key_tables: brick index times its stride, plus
+// the part bits of the axis), negative when floor(p) lies outside the brick
+// grid on any axis (an entry of kKeyOut, whose sign bit is or-ed into the
+// sum).  The keys stay below 2^31.  floor(p) + 1.5 * 2^23, rounded down, is
+// exact for |p| < 2^22 and its bits are then floor(p) + 0x4B400000, the
+// floor of split_coord; beyond 2^22 (and for infinities and NaN) the index
+// leaves the table's range on the side of p, as split_coord's clamped floor
+// leaves the grid.
+constexpr int kKeyOut = (int)0x80000000u;   // table entry outside the grid
+
+__device__ __forceinline__ int sample_key(const int *__restrict__ tab, int nb, int vkey,
+                                          const float (&p)[3]) {
+    const int span = 16 * nb;   // table entries per axis, for floor(p) in [-8 nb, 8 nb)
+    const int bias = 0x4B400000 - 8 * nb - 1;
+    int e[3];
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        const unsigned k = (unsigned)(__float_as_int(__fadd_rd(p[d], 12582912.0f)) - bias);
+        e[d] = tab[d * (span + 2) + min(k, (unsigned)span + 1u)];   // 0 and span + 1: outside
+    }
+    const unsigned sum = (unsigned)vkey + (unsigned)e[0] + (unsigned)e[1] + (unsigned)e[2];
+    return (int)(sum | ((unsigned)(e[0] | e[1] | e[2]) & 0x80000000u));
+}
+
+// Tables of sample_key for the grid of nb bricks per axis: axis 0 adds
+// 16 i + 2 (x half), axis 1 16 nb i + 4 (y half), axis 2 16 nb^2 i +
+// 8 (z half) + (z quarter within the half), i = the brick's index (see
+// brick_coord) -- together brick * kParts + part, part = 8 (z half) +
+// 4 (y half) + 2 (x half) + (z quarter within the half).
+__device__ __forceinline__ void key_tables(int *tab, int nb) {
+    const int span = 16 * nb;
+    for (int t = threadIdx.x; t < 3 * (span + 2); t += blockDim.x) {
+        const int d = t / (span + 2), k = t - d * (span + 2);
+        int val = kKeyOut;
+        if (k >= 1 && k <= span) {
+            const int c = k - 1 - 8 * nb, bc = c >> 4, l = c & (kBS - 1);
+            const int i = (bc << 1) ^ (bc >> 31);   // 2 bc, or -2 bc - 1
+            const int stride = kParts * (d == 0 ? 1 : d == 1 ? nb : nb * nb);
+            const int bits = d == 0 ? 2 * (l >> 3) : d == 1 ? 4 * (l >> 3) : 8 * (l >> 3) + ((l >> 2) & 1);
+            val = i * stride + bits;
+        }
+        tab[t] = val;
+    }
+}
+
+// Starts a list build when the lists held do not fit the binning.
+__global__ void k_list_begin(Scratch sc) {
+    if (threadIdx.x == 0) {
+        sc.lflag[1] = sc.lflag[0] == 0u ? 1u : 0u;
+        sc.lflag[0] = 1u;
+    }
+}
+
+// The count (FILL false; the counts were cleared before the launch) and fill
+// (FILL true; the counts are then the cursors) passes over the output
+// pixels.  A warp takes one image row and gathers, 32 in-radius pixels at a
+// time, the lanes of each run of equal keys (a key that recurs after a gap
+// starts another run): the run's first lane adds its length to the key's
+// count with one atomic, and in the fill every lane writes its pixel index
+// at the cursor that atomic returned plus its place in the run.  The count
+// pass keeps each pixel's key for the fill; the fill issues the atomics of
+// kFillChunks chunks before it uses their results.
+constexpr int kFillChunks = 4;
+
+template <bool FILL>
+__global__ void __launch_bounds__(256) k_list_pass(Params q, int nb, Scratch sc) {
+    if (sc.lflag[1] == 0u) return;
+    extern __shared__ int s_tab[];
+    if (!FILL) {
+        key_tables(s_tab, nb);
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31;
+    const int rows = q.B * q.P * q.N;
+    const unsigned upto = (2u << lane) - 1u;   // lanes 0 .. lane
+    const int nbr16 = nb * nb * nb * kParts;
+    const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
+    for (int row = (blockIdx.x * 256 + threadIdx.x) >> 5; row < rows; row += (gridDim.x * 256) >> 5) {
+        const int bp = row / q.N, iy = row - bp * q.N;
+        const int qy = row_freq(iy, q.N);
+        const int rr = q.r2max - qy * qy;
+        if (rr < 0) continue;
+        // The last kx with kx^2 + ky^2 <= r2max (sqrtf corrected to the exact bound).
+        int xmax = (int)sqrtf((float)rr);
+        if ((xmax + 1) * (xmax + 1) <= rr) ++xmax;
+        if (xmax * xmax > rr) --xmax;
+        xmax = min(xmax, q.Xo - 1);
+        const unsigned e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
+        float4 A, Bv;
+        float by0 = 0.f, by1 = 0.f, by2 = 0.f;
+        int vkey = 0;
+        if (!FILL) {
+            A = __ldg(sc.pose8 + 2 * bp);
+            Bv = __ldg(sc.pose8 + 2 * bp + 1);
+            vkey = (q.Bsrc == 1) ? 0 : (bp / q.P) * nbr16;
+            // p = a qx + (b qy), as in pose8_position (b qy rounded first).
+            by0 = A.w * (float)qy;
+            by1 = Bv.x * (float)qy;
+            by2 = Bv.y * (float)qy;
+        }
+        float fx = (float)lane;
+        for (int xb = 0; xb <= xmax; xb += 32 * kFillChunks, fx += 32.0f * kFillChunks) {
+            int key[kFillChunks], leader[kFillChunks];
+            unsigned at[kFillChunks];
+#pragma unroll
+            for (int k = 0; k < kFillChunks; ++k) {
+                const int qx = xb + 32 * k + lane;
+                key[k] = -1;
+                if (qx <= xmax) {
+                    if (FILL) {
+                        key[k] = __ldg(reinterpret_cast<const int *>(sc.lkey) + e0 + qx);
+                    } else {
+                        const float f = fx + 32.0f * k;
+                        const float p[3] = {fmaf(A.x, f, by0), fmaf(A.y, f, by1), fmaf(A.z, f, by2)};
+                        key[k] = sample_key(s_tab, nb, vkey, p);
+                        sc.lkey[e0 + qx] = (unsigned)key[k];
+                    }
+                }
+                const int prev = __shfl_up_sync(0xffffffffu, key[k], 1);
+                const unsigned starts = __ballot_sync(0xffffffffu, lane == 0 || key[k] != prev);
+                leader[k] = 31 - __clz(starts & upto);
+                const unsigned after = starts & ~upto;
+                const int len = (after ? __ffs(after) - 1 : 32) - lane;   // meaningful on leaders
+                at[k] = 0u;
+                if (key[k] >= 0 && lane == leader[k]) at[k] = atomicAdd(sc.lcount + key[k], (unsigned)len);
+            }
+            if (FILL) {
+#pragma unroll
+                for (int k = 0; k < kFillChunks; ++k) {
+                    const unsigned a = __shfl_sync(0xffffffffu, at[k], leader[k]) + (unsigned)(lane - leader[k]);
+                    if (key[k] >= 0 && TP_CHECK(q.dbg, a < entries, 8))
+                        sc.llist[a] = e0 + (unsigned)(xb + 32 * k + lane);
+                }
+            }
+        }
+    }
+}
+
+// Samples, octant items and z-half items of every brick (a thread per brick).
+__global__ void __launch_bounds__(256) k_list_sums(int nbr, Scratch sc, int nvol) {
+    const int id = blockIdx.x * 256 + threadIdx.x;
+    if (sc.lflag[1] == 0u || id >= nvol * nbr) return;
+    const unsigned *cnt = sc.lcount + (size_t)id * kParts;
+    unsigned c[kParts];
+#pragma unroll
+    for (int k = 0; k < kParts; k += 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(cnt + k);
+        c[k] = u.x;
+        c[k + 1] = u.y;
+        c[k + 2] = u.z;
+        c[k + 3] = u.w;
+    }
+    int4 r = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < kParts; ++k) {
+        r.x += (int)c[k];
+        r.z += (int)((c[k] + kListChunk - 1) / kListChunk);
+    }
+#pragma unroll
+    for (int o = 0; o < kParts / 2; ++o) r.y += (int)((c[2 * o] + c[2 * o + 1] + kListChunk - 1) / kListChunk);
+    sc.lbrick[id] = r;
+}
+
+// One block per volume: exclusive sums of the bricks' figures (in place), and
+// the volume's item counts.
+__global__ void __launch_bounds__(kListThreads) k_list_scan(int nbr, Scratch sc) {
+    if (sc.lflag[1] == 0u) return;
+    __shared__ int s_w[3][kListThreads / 32];
+    const int v = blockIdx.x, nvol = gridDim.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int4 *br = sc.lbrick + (size_t)v * nbr;
+    const int per = (nbr + kListThreads - 1) / kListThreads;
+    const int j0 = threadIdx.x * per, j1 = min(nbr, j0 + per);
+    int x[3] = {0, 0, 0};
+    for (int j = j0; j < j1; ++j) {
+        const int4 r = br[j];
+        x[0] += r.x;
+        x[1] += r.y;
+        x[2] += r.z;
+    }
+    int incl[3] = {x[0], x[1], x[2]};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl[k], o);
+            if (lane >= o) incl[k] += t;
+        }
+        if (lane == 31) s_w[k][warp] = incl[k];
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            int y = s_w[k][lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, y, o);
+                if (lane >= o) y += t;
+            }
+            s_w[k][lane] = y;
+        }
+    }
+    __syncthreads();
+    int run[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) run[k] = incl[k] - x[k] + (warp > 0 ? s_w[k][warp - 1] : 0);
+    for (int j = j0; j < j1; ++j) {
+        const int4 r = br[j];
+        br[j] = make_int4(run[0], run[1], run[2], 0);
+        run[0] += r.x;
+        run[1] += r.y;
+        run[2] += r.z;
+    }
+    if (threadIdx.x == kListThreads - 1) {
+        sc.counters[4 * nvol + v] = (unsigned)min(run[1], sc.itemcap);
+        sc.counters[5 * nvol + v] = (unsigned)min(run[2], sc.itemcap);
+    }
+}
+
+// Eight threads per brick, one per octant: the list offsets of the octant's
+// two parts (the counts become the fill cursors) and its items -- a part or
+// octant with n samples gives ceil(n / kListChunk) items of consecutive
+// entries, in brick order (octant items, then z-half items, by part).
+__global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvol,
+                                                    long long vol_entries) {
+    const int id = (blockIdx.x * 256 + threadIdx.x) >> 3, o = threadIdx.x & 7;
+    if (sc.lflag[1] == 0u || id >= nvol * nbr) return;
+    const int v = id / nbr, j = id - v * nbr;
+    const int4 base = sc.lbrick[id];
+    unsigned *cnt = sc.lcount + (size_t)id * kParts;
+    unsigned c[kParts];
+#pragma unroll
+    for (int k = 0; k < kParts; k += 4) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(cnt + k);
+        c[k] = u.x;
+        c[k + 1] = u.y;
+        c[k + 2] = u.z;
+        c[k + 3] = u.w;
+    }
+    // Entries and items of the octants before this one.
+    unsigned first = (unsigned)((long long)v * vol_entries) + (unsigned)base.x;
+    int oi = base.y, hi = base.z;
+    unsigned c0 = 0u, c1 = 0u;   // this octant's two parts
+#pragma unroll
+    for (int k = 0; k < kParts / 2; ++k) {
+        if (k < o) {
+            first += c[2 * k] + c[2 * k + 1];
+            oi += (int)((c[2 * k] + c[2 * k + 1] + kListChunk - 1) / kListChunk);
+            hi += (int)((c[2 * k] + kListChunk - 1) / kListChunk) +
+                  (int)((c[2 * k + 1] + kListChunk - 1) / kListChunk);
+        }
+        if (k == o) {
+            c0 = c[2 * k];
+            c1 = c[2 * k + 1];
+        }
+    }
+    __syncwarp(0xffu << (threadIdx.x & 24));   // the brick's 8 lanes have read its counts
+    cnt[2 * o] = first;   // fill cursors
+    cnt[2 * o + 1] = first + c0;
+    int4 *oct_items = sc.litems + (size_t)v * sc.itemcap;
+    int4 *half_items = sc.litems + (size_t)(nvol + v) * sc.itemcap;
+    for (unsigned i = 0; i < c0 + c1; i += kListChunk, ++oi)
+        if (oi < sc.itemcap)   // never false: itemcap bounds the items
+            oct_items[oi] = make_int4((int)(first + i), (int)min((unsigned)kListChunk, c0 + c1 - i), j, o);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int k = 2 * o + h;
+        const int zq = ((k >> 3) << 1) | (k & 1), xy = (k >> 1) & 3;
+        const unsigned n = h ? c1 : c0, f = h ? first + c0 : first;
+        for (unsigned i = 0; i < n; i += kListChunk, ++hi)
+            if (hi < sc.itemcap)
+                half_items[hi] = make_int4((int)(f + i), (int)min((unsigned)kListChunk, n - i), j, zq * 4 + xy);
+    }
+}
+
+// Cubic: one lane spreads one sample, 32 samples of the item's list per
+// round.  The tile's (x, y) layers are cut into 4 x 4 tiles of 16 complex
+// words, so word (x, y, z) sits in bank pair (x mod 4) + 4 (y mod 4), and
+// lane L visits its taps in its own order: at step (sx, sy, sz) it takes the
+// tap whose tile coordinates are congruent to (sx + L, sy + L / 4, sz + L / 16)
+// modulo 4.  The 32 lanes then touch taps of 32 distinct residue triples --
+// 32 distinct words, wherever their samples lie -- and each half-warp's 16
+// words fall into 16 distinct bank pairs, so every 64-bit read or write of
+// the warp takes the minimum two wavefronts.  Steps sz and sz + 2 share one
+// warp barrier: over the two, half-warp 0 touches the z residues sz and
+// sz + 2 and half-warp 1 the residues sz + 1 and sz + 3, so the words of the
+// pair are still distinct across lanes.
 //
 // The real weight tile (backprojection with the weight spectrum) pairs its
 // z layers: word (x, y, z) sits in bank 16 (z mod 2) + 4 (y mod 4) + x mod 4,
@@ -1053,27 +1376,20 @@ constexpr int kCT = 12;                    // (x, y) extent of a tile layer: 3 x
 constexpr int kCLayer = kCT * kCT;         // complex words of one z layer
 constexpr int kCWPair = 2 * kCLayer;       // weight words of a pair of z layers
 
-// Samples waiting to be spread by a warp, one per slot.
-struct CubicBuf {
-    float4 pos[32];   // fraction of p in x, y, z; first tap x | y << 8 | z << 16 (tile coordinates)
-    float4 val[32];   // conj(phase) * y (re, im), omega, unused
-};
-
-// A work item is one part of a unit's brick: an octant (8^3), or, with the
-// weight spectrum, half of one in z (8 x 8 x 4), so that the two tiles and
-// the buffer of a warp fit 16 warps into an SM's shared memory.
+// A work item covers one part of a brick: an octant (8^3), or, with the
+// weight spectrum, half of one in z (8 x 8 x 4), so that the two tiles of a
+// warp fit 16 warps into an SM's shared memory.
 template <bool WEIGHTS>
 struct OctLayout {
     static constexpr int WARPS = 4;                  // warps per block (blocks only share an SM)
     static constexpr int OZ = WEIGHTS ? kOct / 2 : kOct;   // z extent of an item's box
-    static constexpr int PARTS = 4 * (kBS / OZ);     // items per work unit
     static constexpr int SZ = OZ + 3;                // z layers of the tiles
     static constexpr int ELEMS = kCLayer * SZ;       // complex words of the tile
     static constexpr int WELEMS = WEIGHTS ? kCWPair * ((SZ + 1) / 2) : 0;   // words of the weight tile
     static constexpr size_t TILE = sizeof(float2) * ELEMS;
     static constexpr size_t WTILE = sizeof(float) * WELEMS;
-    static constexpr size_t WARP_BYTES = TILE + WTILE + sizeof(CubicBuf);
-    static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned buffer");
+    static constexpr size_t WARP_BYTES = TILE + WTILE;
+    static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned tiles");
 };
 
 // Box of part `oct` of a brick: x and y halves from bits 0 and 1, the z
@@ -1089,24 +1405,6 @@ __device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct, int 
         ob.hi[d] = (float)(ob.o[d] + ext[d]) + kMargin;
     }
     return ob;
-}
-
-// Ownership test of pixel (qx, qy) for a box SIZE voxels wide in x and y and
-// SIZEZ in z: floor(p) - origin per axis, packed one per byte, and the
-// fraction of p.
-template <int SIZE, int SIZEZ>
-__device__ __forceinline__ bool own_position(const PoseGeo &g, const BrickBox &bx, int qx, int qy,
-                                             int &packed, float (&t)[3]) {
-    bool own = true;
-    packed = 0;
-#pragma unroll
-    for (int a = 0; a < 3; ++a) {
-        const float p = fmaf(g.a[a], (float)qx, g.b[a] * (float)qy);
-        const int l = split_coord(p, t[a]) - bx.o[a];
-        own = own && (unsigned)l < (unsigned)(a == 2 ? SIZEZ : SIZE);
-        packed |= (l & 0xff) << (8 * a);
-    }
-    return own;
 }
 
 __device__ __forceinline__ float2 lds_f2(unsigned a) {
@@ -1126,28 +1424,26 @@ __device__ __forceinline__ void sts_f1(unsigned a, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 
-// Every lane spreads the sample in its buffer slot (none when !act) into the
-// warp's tile (and weight tile): shared-memory byte addresses tile, wtile.
-// Call with the whole warp after a __syncwarp that follows the buffer writes.
+// Every lane spreads its sample into the warp's tile (and weight tile):
+// first tap (l0, l1, l2) in tile coordinates (each in [0, 8), l2 in
+// [0, OZ)), fraction t of p, value c = conj(phase) * y, weight om; a lane
+// with !act adds zeros to in-range words.  tile and wtile are shared-memory
+// byte addresses.  Call with the whole warp.
 template <bool WEIGHTS>
-__device__ __forceinline__ void spread_cubic(const CubicBuf &buf, unsigned tile, unsigned wtile,
-                                             bool act, unsigned *dbg) {
-    using OL = OctLayout<WEIGHTS>;
+__device__ __forceinline__ void spread_cubic(int l0, int l1, int l2, const float (&tf)[3], float2 c,
+                                             float om, unsigned tile, unsigned wtile, bool act) {
     const int lane = threadIdx.x & 31;
-    float4 P = buf.pos[lane];
-    float4 C = buf.val[lane];
-    int b = __float_as_int(P.w);
-    int l0 = b & 0xff, l1 = (b >> 8) & 0xff, l2 = b >> 16;
-    act = act && TP_CHECK(dbg, l0 < kOct && l1 < kOct && l2 < OL::OZ, 4);
-    if (!act) {   // a lane without a sample adds zeros to in-range words
+    float t[3] = {tf[0], tf[1], tf[2]};
+    if (!act) {
         l0 = l1 = l2 = 0;
-        P = make_float4(0.f, 0.f, 0.f, 0.f);
-        C = make_float4(0.f, 0.f, 0.f, 0.f);
+        t[0] = t[1] = t[2] = 0.f;
+        c = make_float2(0.f, 0.f);
+        om = 0.f;
     }
     float w[3][4], r[3][4];
-    Stencil<true>::weights(P.x, w[0]);
-    Stencil<true>::weights(P.y, w[1]);
-    Stencil<true>::weights(P.z, w[2]);
+    Stencil<true>::weights(t[0], w[0]);
+    Stencil<true>::weights(t[1], w[1]);
+    Stencil<true>::weights(t[2], w[2]);
     const int cx = (lane - l0) & 3, cy = ((lane >> 2) - l1) & 3, cz = ((lane >> 4) - l2) & 3;
     rot4(w[0], cx, r[0]);
     rot4(w[1], cy, r[1]);
@@ -1170,8 +1466,8 @@ __device__ __forceinline__ void spread_cubic(const CubicBuf &buf, unsigned tile,
     float czw[4];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-        cz2[s] = make_float2(r[2][s] * C.x, r[2][s] * C.y);
-        czw[s] = r[2][s] * C.z;
+        cz2[s] = make_float2(r[2][s] * c.x, r[2][s] * c.y);
+        czw[s] = r[2][s] * om;
     }
 #pragma unroll
     for (int sg = 0; sg < 2; ++sg) {
@@ -1212,14 +1508,13 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, 4)
     char *mine = reinterpret_cast<char *>(s_oct) + (threadIdx.x >> 5) * OL::WARP_BYTES;
     float2 *acc = reinterpret_cast<float2 *>(mine);
     float *wacc = reinterpret_cast<float *>(mine + OL::TILE);
-    CubicBuf &buf = *reinterpret_cast<CubicBuf *>(mine + OL::TILE + OL::WTILE);
     const unsigned tile = (unsigned)__cvta_generic_to_shared(acc);
     const unsigned wtile = (unsigned)__cvta_generic_to_shared(wacc);
-    const unsigned below = (1u << lane) - 1u;
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int items = OL::PARTS * (int)__ldg(sc.counters + 3 * nvol + v);
-    const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
+    const int nitems = (int)__ldg(sc.counters + (WEIGHTS ? 5 : 4) * nvol + v);
+    const int4 *items = sc.litems + (size_t)((WEIGHTS ? nvol : 0) + v) * sc.itemcap;
+    const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
     for (int e = lane; e < OL::ELEMS; e += 32) acc[e] = make_float2(0.f, 0.f);
@@ -1229,87 +1524,46 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, 4)
         int item = 0;
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
-        if (item >= items) break;
-        const int ui = item / OL::PARTS, part = item - ui * OL::PARTS;
-        if (!TP_CHECK(q.dbg, ui < nbr * sc.nchunks, 8)) break;
-        const int4 rec = __ldg(units + ui);
-        if (!TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
-                                 rec.z <= sc.nchunks, 8))
-            break;
-        const BrickBox ob = octant_box(brick_box(rec.x, nb), part, OL::OZ);
-        const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
-        bool touched = false;
-        int pend = 0;   // samples in the buffer (warp-uniform)
-        for (int c = rec.y; c < rec.z; ++c) {
-            // The poses of the chunk that can reach this part, tested one per lane.
-            const unsigned m = __ldg(masks + c);
-            bool reach = false;
-            if ((m >> lane) & 1u) {
-                const int pid = pose_id(q, v, c * 32 + lane);
-                if (TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8))
-                    reach = pose_reaches(load_geo(sc.geo, pid), ob);
+        if (item >= nitems) break;
+        const int4 it = __ldg(items + item);   // first entry, count, brick, box
+        if (!TP_CHECK(q.dbg, it.z >= 0 && it.z < nbr && it.y > 0 && it.y <= kListChunk &&
+                                 (unsigned)it.x + (unsigned)it.y <= entries, 8))
+            continue;
+        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w, OL::OZ);
+        for (int r = 0; r < it.y; r += 32) {
+            bool act = r + lane < it.y;
+            const unsigned e = act ? __ldg(sc.llist + it.x + r + lane) : 0u;
+            act = act && TP_CHECK(q.dbg, e < entries, 8);
+            float2 cv = make_float2(0.f, 0.f);
+            float om = 1.0f;
+            if (act) {
+                cv = __ldg(img + e);
+                if (WEIGHTS && omega) om = __ldg(omega + e);
             }
-            for (unsigned mr = __ballot_sync(0xffffffffu, reach); mr; mr &= mr - 1) {
-                const PoseGeo g = load_geo(sc.geo, pose_id(q, v, c * 32 + __ffs(mr) - 1));
-                touched = true;
-                const size_t ib = (size_t)g.bp * q.plane;
-                for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                    // The image value is loaded first, to be in flight during the
-                    // ownership test and the phase.
-                    const int iy = qy < 0 ? qy + q.N : qy;
-                    const bool in = active && TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 &&
-                                                                  qx < q.Xo && g.bp < q.B * q.P, 7);
-                    float2 cv = make_float2(0.f, 0.f);
-                    float om = 1.0f;
-                    if (in) {
-                        cv = __ldg(img + ib + iy * q.Xo + qx);
-                        if (WEIGHTS && omega) om = __ldg(omega + ib + iy * q.Xo + qx);
-                    }
-                    int packed;
-                    float t[3];
-                    const bool own = active && own_position<kOct, OL::OZ>(g, ob, qx, qy, packed, t);
-                    const unsigned mask = __ballot_sync(0xffffffffu, own);
-                    if (mask == 0u) return;
-                    const int slot = pend + __popc(mask & below);
-                    float4 pos, val;
-                    if (own) {
-                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
-                        pos = make_float4(t[0], t[1], t[2], __int_as_float(packed));
-                        val = make_float4(cv.x, cv.y, om, 0.f);
-                        if (slot < 32) {
-                            buf.pos[slot] = pos;
-                            buf.val[slot] = val;
-                        }
-                    }
-                    pend += __popc(mask);
-                    if (pend >= 32) {
-                        __syncwarp();
-                        spread_cubic<WEIGHTS>(buf, tile, wtile, true, q.dbg);
-                        // Every lane has read its slot (the spread's barriers
-                        // follow the reads): the overflow moves to the front.
-                        if (own && slot >= 32) {
-                            buf.pos[slot - 32] = pos;
-                            buf.val[slot - 32] = val;
-                        }
-                        pend -= 32;
-                    }
-                });
-            }
-        }
-        if (!touched) continue;
-        if (pend > 0) {
-            __syncwarp();
-            spread_cubic<WEIGHTS>(buf, tile, wtile, lane < pend, q.dbg);
+            int qx, qy;
+            const unsigned bp = split_pixel(q, act ? e : 0u, qx, qy);
+            const float4 A = __ldg(sc.pose8 + 2 * bp), Bv = __ldg(sc.pose8 + 2 * bp + 1);
+            float p[3], t[3];
+            pose8_position(A, Bv, qx, qy, p);
+            const int l0 = split_coord(p[0], t[0]) - ob.o[0];
+            const int l1 = split_coord(p[1], t[1]) - ob.o[1];
+            const int l2 = split_coord(p[2], t[2]) - ob.o[2];
+            // The list put the sample in this box (same position arithmetic);
+            // the test keeps every tile access in range whatever happens.
+            const bool inbox = (unsigned)l0 < (unsigned)kOct && (unsigned)l1 < (unsigned)kOct &&
+                               (unsigned)l2 < (unsigned)OL::OZ;
+            act = act && TP_CHECK(q.dbg, inbox, 4) && inbox;
+            if (act && q.shift) cv = cmul_conj_a(shift_phase(qx, qy, Bv.z, Bv.w, q.fN, q.invN), cv);
+            spread_cubic<WEIGHTS>(l0, l1, l2, t, cv, om, tile, wtile, act);
         }
         __syncwarp();
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0] - 1, y0 = ob.o[1] - 1, z0 = ob.o[2] - 1;
         for (int e = lane; e < kOS * kOS * OL::SZ; e += 32) {
             const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
-            const int xy = ((ly >> 2) * (kCT / 4) + (lx >> 2)) * 16 + 4 * (ly & 3) + (lx & 3);
-            const int k = lz * kCLayer + xy;
-            const int kw = (lz >> 1) * kCWPair + xy + ((ly >> 2) * (kCT / 4) + (lx >> 2)) * 16 +
-                           16 * (lz & 1);
+            const int tl = (ly >> 2) * (kCT / 4) + (lx >> 2), in = 4 * (ly & 3) + (lx & 3);
+            const int k = lz * kCLayer + tl * 16 + in;
+            const int kw = (lz >> 1) * kCWPair + tl * 32 + 16 * (lz & 1) + in;
             const float2 cv = acc[k];
             const float wv = WEIGHTS ? wacc[kw] : 0.f;
             if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
@@ -1502,23 +1756,42 @@ int bricks_per_axis(int M, bool cubic) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t counters, geo, reach, masks, hits, units, total;
-    int nb, nchunks;
+    size_t counters, geo, pose8, reach, masks, hits, units, binning;   // the binning
+    size_t lcount, lbrick, litems, llist, lkey, total;                // + the sample lists
+    int nb, nchunks, itemcap;
+    long long vol_entries;   // list entries per volume (its images' pixels)
 };
 
+// Workspace layout: the binning every 3D operator uses, then (cubic only) the
+// sample lists of the scatter, sized for every output pixel.
 Layout layout(const Params &q, bool cubic) {
     Layout L;
     L.nb = bricks_per_axis(q.M, cubic);
     const size_t nbr = (size_t)L.nb * L.nb * L.nb;
     const long long Pv = (q.Bsrc == 1) ? (long long)q.B * q.P : q.P;
+    const size_t poses = (size_t)q.B * q.P;
     L.nchunks = (int)((Pv + 31) / 32);
-    L.counters = 256;                                         // key and flag first
-    L.geo = L.counters + align256(sizeof(unsigned) * 4 * (size_t)q.Bsrc);
-    L.reach = L.geo + align256(sizeof(int4) * kGeoVec * (size_t)q.B * q.P);
-    L.masks = L.reach + align256(sizeof(ReachGeo) * (size_t)q.B * q.P);
+    L.counters = 256;                                         // key and flags first
+    L.geo = L.counters + align256(sizeof(unsigned) * 6 * (size_t)q.Bsrc);
+    L.pose8 = L.geo + align256(sizeof(int4) * kGeoVec * poses);
+    L.reach = L.pose8 + align256(2 * sizeof(float4) * poses);
+    L.masks = L.reach + align256(sizeof(ReachGeo) * poses);
     L.hits = L.masks + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.units = L.hits + align256(sizeof(int) * (size_t)q.Bsrc * nbr);
-    L.total = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
+    L.binning = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
+    L.vol_entries = Pv * (long long)q.N * (q.N / 2 + 1);
+    L.itemcap = 0;
+    L.lcount = L.lbrick = L.litems = L.llist = L.lkey = 0;
+    L.total = L.binning;
+    if (cubic) {
+        L.itemcap = (int)(nbr * kParts + L.vol_entries / kListChunk + 1);
+        L.lcount = L.binning;
+        L.lbrick = L.lcount + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * kParts);
+        L.litems = L.lbrick + align256(sizeof(int4) * (size_t)q.Bsrc * nbr);
+        L.llist = L.litems + align256(sizeof(int4) * 2 * (size_t)q.Bsrc * L.itemcap);
+        L.lkey = L.llist + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
+        L.total = L.lkey + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
+    }
     return L;
 }
 
@@ -1527,13 +1800,21 @@ Scratch scratch_in(void *ws, const Layout &L) {
     char *base = static_cast<char *>(ws);
     sc.key = reinterpret_cast<unsigned *>(base);
     sc.changed = sc.key + kKeyWords;
+    sc.lflag = sc.changed + 1;
     sc.counters = reinterpret_cast<unsigned *>(base + L.counters);
     sc.geo = reinterpret_cast<int4 *>(base + L.geo);
+    sc.pose8 = reinterpret_cast<float4 *>(base + L.pose8);
     sc.reach = reinterpret_cast<ReachGeo *>(base + L.reach);
     sc.masks = reinterpret_cast<unsigned *>(base + L.masks);
     sc.hits = reinterpret_cast<int *>(base + L.hits);
     sc.units = reinterpret_cast<int4 *>(base + L.units);
+    sc.lcount = L.lcount ? reinterpret_cast<unsigned *>(base + L.lcount) : nullptr;
+    sc.lbrick = L.lbrick ? reinterpret_cast<int4 *>(base + L.lbrick) : nullptr;
+    sc.litems = L.litems ? reinterpret_cast<int4 *>(base + L.litems) : nullptr;
+    sc.llist = L.llist ? reinterpret_cast<unsigned *>(base + L.llist) : nullptr;
+    sc.lkey = L.lkey ? reinterpret_cast<unsigned *>(base + L.lkey) : nullptr;
     sc.nchunks = L.nchunks;
+    sc.itemcap = L.itemcap;
     return sc;
 }
 
@@ -1656,6 +1937,31 @@ cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *om
     return cudaGetLastError();
 }
 
+// The sample lists of the cubic scatter, unless the workspace holds the ones
+// of this binning (the kernels after k_list_begin then return at once).
+cudaError_t build_lists(const Params &q, const Layout &L, const Scratch &sc, cudaStream_t st) {
+    const int nbr = L.nb * L.nb * L.nb;
+    cudaError_t e = cudaMemsetAsync(sc.lcount, 0, sizeof(unsigned) * (size_t)q.Bsrc * nbr * kParts, st);
+    if (e != cudaSuccess) return e;
+    k_list_begin<<<1, 32, 0, st>>>(sc);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long rows = (long long)q.B * q.P * q.N;
+    const unsigned blocks = (unsigned)std::min<long long>((rows + 7) / 8, 16LL * sms);
+    const unsigned bricks = (unsigned)(((long long)q.Bsrc * nbr + 255) / 256);
+    if (blocks == 0) return cudaGetLastError();
+    const size_t tab = sizeof(int) * 3 * (16 * L.nb + 2);
+    if ((e = cudaFuncSetAttribute(k_list_pass<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab)) !=
+        cudaSuccess)
+        return e;
+    k_list_pass<false><<<blocks, 256, tab, st>>>(q, L.nb, sc);
+    k_list_sums<<<bricks, 256, 0, st>>>(nbr, sc, q.Bsrc);
+    k_list_scan<<<q.Bsrc, kListThreads, 0, st>>>(nbr, sc);
+    k_list_items<<<8 * bricks, 256, 0, st>>>(nbr, sc, q.Bsrc, L.vol_entries);
+    k_list_pass<true><<<blocks, 256, 0, st>>>(q, L.nb, sc);
+    return cudaGetLastError();
+}
+
 template <bool WEIGHTS>
 cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
                             float *wdst, void *ws, BinMode mode, cudaStream_t st) {
@@ -1668,6 +1974,7 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
+    if ((e = build_lists(q, L, sc, st)) != cudaSuccess) return e;
     kern<<<warp_grid(q, (const void *)kern, threads, smem), threads, smem, st>>>(q, L.nb, sc, img,
                                                                                omega, dst, wdst);
     return cudaGetLastError();
@@ -1676,6 +1983,13 @@ cudaError_t scatter_cubic_t(const Params &q, const float2 *img, const float *ome
 }  // namespace
 
 size_t brick_workspace_bytes(const Params &q, bool cubic) { return layout(q, cubic).total; }
+
+size_t brick_binning_bytes(const Params &q, bool cubic) { return layout(q, cubic).binning; }
+
+long long brick_parts(const Params &q, bool cubic) {
+    const long long nb = bricks_per_axis(q.M, cubic);
+    return nb * nb * nb * kParts;
+}
 
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  BinMode mode, cudaStream_t st) {

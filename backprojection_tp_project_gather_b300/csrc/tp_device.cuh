@@ -37,6 +37,7 @@ struct Params {
     float fN;              // N as a float
     float invN;            // 1 / N
     int r2max;             // pixels with kx^2 + ky^2 > r2max are outside the radius
+    unsigned mplane, mxo;  // floor(2^32 / plane), floor(2^32 / Xo): see udiv
     unsigned *dbg;         // bounds-check word of a TP_DEBUG_BOUNDS build, else null
 };
 
@@ -118,6 +119,15 @@ __device__ __forceinline__ int split_coord(float p, float &t) {
     const float f = floorf(pc);
     t = pc - f;
     return (int)f;
+}
+
+// n / d for n < 2^31 and d >= 2, given m = floor(2^32 / d): umulhi(n, m) is
+// n / d or one less (m underestimates 2^32 / d by less than one, n by less
+// than 2^32), and one comparison of the remainder corrects it.
+__device__ __forceinline__ unsigned udiv(unsigned n, unsigned d, unsigned m) {
+    unsigned qt = __umulhi(n, m);
+    if (n - qt * d >= d) ++qt;
+    return qt;
 }
 
 // Row of frequency f (valid for -M/2 <= f < M/2) in rfftn order.

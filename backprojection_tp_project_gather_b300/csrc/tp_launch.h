@@ -44,7 +44,11 @@ cudaError_t launch_scatter_2d(bool cubic, const Params &q, const float2 *img, fl
 // binning an earlier launch of the same call made.  With dout the forward
 // also writes D_a = phase * dS/dp_a, three complex values per output pixel.
 enum BinMode { kBinNew = 0, kBinSameCall = 1 };
-size_t brick_workspace_bytes(const Params &q, bool cubic);
+size_t brick_workspace_bytes(const Params &q, bool cubic);   // every 3D operator
+size_t brick_binning_bytes(const Params &q, bool cubic);     // the forward and pose gradients
+long long brick_parts(const Params &q, bool cubic);          // list keys of one volume
+// tp_workspace_bytes with or without the cubic scatter's sample lists.
+size_t workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts, bool lists);
 cudaError_t launch_brick_project(bool cubic, const Params &q, float2 *out, float2 *dout, void *ws,
                                  BinMode mode, cudaStream_t st);
 // The forward fused with an L2 data term (always bins its poses): writes out

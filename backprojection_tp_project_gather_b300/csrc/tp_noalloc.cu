@@ -73,7 +73,7 @@ tp_status tp_project_3d_2d_noalloc(const float *vol, int Bv, int Nv, const float
                                         0, stream);
     int B = Bv > Bp ? Bv : Bp;
     if (shift && Bs > B) B = Bs;
-    const size_t need = tp_workspace_bytes(Bv, B, P, Nv, opts);
+    const size_t need = tp::workspace_bytes(Bv, B, P, Nv, N, opts, false);   // the forward's part
     if (need > kMaxScratch)
         return tp::fail(TP_ERR_SHAPE,
                         "tp_project_3d_2d_noalloc: this problem needs %zu bytes of scratch, the "

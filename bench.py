@@ -642,10 +642,11 @@ def run_ours(args):
                               "gradients down; pipelined with the neighbouring steps' compute "
                               "on two copy streams"},
             # per step: the forward with the L2 term (pose geometry, brick masks,
-            # unit plan, gather with the zero fill as its prologue) and the
-            # volume-gradient call (geometry, masks, plan, scatter); plus two
-            # 4-byte memsets
-            "gpu_launches": 8 * args.steps,
+            # unit plan, gather with the zero fill as its prologue: 4) and the
+            # volume-gradient call (geometry, masks, plan: 3; the sample lists
+            # of this step's poses: begin, count, sums, scan, items, fill: 6;
+            # the scatter: 1); plus three memsets
+            "gpu_launches": 14 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu_line,
         }

@@ -62,12 +62,18 @@
  * sizes (its key and the pose records compared on the device, bit for bit:
  * for example the backward call after the forward call of one step) keeps
  * the brick masks and work units stored there instead of recomputing them;
- * any difference recomputes them.  So the first 256 bytes of a workspace
- * that is new to the library, or whose memory served anything else since
- * its last call, must be zero (the rest needs no initialisation): memory
- * recycled by an allocator can hold the key and poses of an old workspace
- * but other data in its masks.  It must not be used by two calls that can
- * run at the same time (one workspace per stream).
+ * any difference recomputes them.  With cubic interpolation the scatters
+ * (backprojection, spectrum gradient) also sort the in-radius output pixels
+ * by brick part into lists kept there under the same rule; the forward
+ * entry points and the pose-gradient-only backward need only the binning,
+ * the first part of the workspace (they accept any size that holds it).  So
+ * the first 256 bytes of a workspace that is new to the library, or whose
+ * memory served anything else since its last call, must be zero (the rest
+ * needs no initialisation): memory recycled by an allocator can hold the
+ * key and poses of an old workspace but other data in its masks.  It must
+ * not be used by two calls that can run at the same time (one workspace
+ * per stream).  A cubic scatter call handles fewer than 2^31 output pixels
+ * (B * P * N * (N/2+1)); larger ones fail with TP_ERR_SHAPE.
  *
  * Errors.  Each call returns a tp_status.  Argument errors are detected
  * before anything is enqueued; TP_ERR_CUDA reports a launch failure.  No
@@ -323,11 +329,13 @@ tp_status tp_hermitian_x0(float *spec, float *weight, int B, int N, int dim, voi
 
 /*
  * Bytes of workspace the 3D entry points need for a volume batch Bv, batch
- * B (Bv is 1 or B), P poses per batch element, volume box Nv and the
- * interpolation of opts; the same for all three of them (the backward uses
- * it for both of its passes).  Returns 0 for invalid sizes.
+ * B (Bv is 1 or B), P poses per batch element, volume box Nv, image box N
+ * and the interpolation of opts: enough for every 3D entry point on these
+ * sizes (the backward uses it for both of its passes).  With cubic
+ * interpolation this includes 4 bytes per output pixel (B * P * N *
+ * (N/2+1)) for the scatter's sample lists.  Returns 0 for invalid sizes.
  */
-size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts);
+size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts);
 
 /*
  * tp_project_3d_2d without a workspace, for callers that cannot allocate
@@ -336,8 +344,9 @@ size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, tp_options opts);
  * is an interface convenience of this library.  Arguments and results are
  * those of tp_project_3d_2d.  The scratch lives in a fixed 16 MiB array in
  * the library's device memory, reserved on every GPU that loads the
- * library until the process exits; problems needing more scratch than that
- * (tp_workspace_bytes) fail with TP_ERR_SHAPE (tp_last_error says why).
+ * library until the process exits; problems whose binning (the forward's
+ * part of tp_workspace_bytes) needs more than that fail with TP_ERR_SHAPE
+ * (tp_last_error says why).
  * All calls share the array: calls that can overlap on the GPU race and
  * must be serialised by the caller.  The first call on each device looks
  * the array up (and may load the module); make it before any stream

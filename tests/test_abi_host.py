@@ -223,6 +223,12 @@ def test_workspace_size_query(tp):
     assert 0 < small < big
     assert tp.tp_workspace_bytes(1, 1, 8, 31, "cubic") == 0      # odd box
     assert tp.tp_workspace_bytes(2, 1, 8, 32, "cubic") == 0      # Bv > B
+    assert tp.tp_workspace_bytes(1, 1, 8, 32, "cubic", N=31) == 0   # odd image box
+    # The cubic scatter's sample lists: 4 bytes per output pixel.
+    grow = tp.tp_workspace_bytes(1, 1, 8, 32, "cubic", N=64) - small
+    assert grow >= 4 * 8 * (64 * 33 - 32 * 17)
+    lin = tp.tp_workspace_bytes(1, 1, 8, 32, "linear")
+    assert lin == tp.tp_workspace_bytes(1, 1, 8, 32, "linear", N=64) < small
 
 
 def test_binding_rejects_cpu_tensors(tp):
