@@ -132,7 +132,8 @@ struct Scratch {
     int4 *lbrick;         // [Bsrc][bricks] samples, octant items, z-half items; then their sums before
     int4 *litems;         // [2][Bsrc][itemcap] items: (first entry, count, brick, box)
     unsigned *llist;      // B*P*plane entries: output pixel index (b * P + p) * plane + row * Xo + kx
-    unsigned *lkey;       // B*P*plane: each in-radius pixel's key (count pass, for the fill)
+    int2 *lkey;           // B*P*plane: each in-radius pixel's key and place in the key's list
+    int4 *lblock;         // [Bsrc][brick blocks] the sums of k_list_sums' blocks
     int nchunks;          // 32-pose chunks per volume
     int itemcap;          // items per volume and kind
 };
@@ -1055,7 +1056,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // clears lflag[0] whenever it is not).
 constexpr int kParts = 16;
 constexpr int kListChunk = 2048;   // most samples per scatter item
-constexpr int kListThreads = 1024;
 
 // Sample position of output pixel (qx, qy) of a pose: the ownership test of
 // the forward (own_sample) uses the same expression, so both agree on floor(p).
@@ -1130,30 +1130,24 @@ __global__ void k_list_begin(Scratch sc) {
     }
 }
 
-// The count (FILL false; the counts were cleared before the launch) and fill
-// (FILL true; the counts are then the cursors) passes over the output
-// pixels.  A warp takes one image row and gathers, 32 in-radius pixels at a
+// The count pass over the output pixels (the counts were cleared before the
+// launch).  A warp takes one image row and gathers, 32 in-radius pixels at a
 // time, the lanes of each run of equal keys (a key that recurs after a gap
 // starts another run): the run's first lane adds its length to the key's
-// count with one atomic, and in the fill every lane writes its pixel index
-// at the cursor that atomic returned plus its place in the run.  The count
-// pass keeps each pixel's key for the fill; the fill issues the atomics of
-// kFillChunks chunks before it uses their results.
-constexpr int kFillChunks = 4;
+// count with one atomic, whose result places the run in the key's list, and
+// every pixel keeps its key and its place for the fill.  The atomics of
+// kListChunks chunks are issued before their results are used.
+constexpr int kListChunks = 4;
 
-template <bool FILL>
-__global__ void __launch_bounds__(256) k_list_pass(Params q, int nb, Scratch sc) {
+__global__ void __launch_bounds__(256) k_list_count(Params q, int nb, Scratch sc) {
     if (sc.lflag[1] == 0u) return;
     extern __shared__ int s_tab[];
-    if (!FILL) {
-        key_tables(s_tab, nb);
-        __syncthreads();
-    }
+    key_tables(s_tab, nb);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int rows = q.B * q.P * q.N;
     const unsigned upto = (2u << lane) - 1u;   // lanes 0 .. lane
     const int nbr16 = nb * nb * nb * kParts;
-    const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     for (int row = (blockIdx.x * 256 + threadIdx.x) >> 5; row < rows; row += (gridDim.x * 256) >> 5) {
         const int bp = row / q.N, iy = row - bp * q.N;
         const int qy = row_freq(iy, q.N);
@@ -1165,35 +1159,22 @@ __global__ void __launch_bounds__(256) k_list_pass(Params q, int nb, Scratch sc)
         if (xmax * xmax > rr) --xmax;
         xmax = min(xmax, q.Xo - 1);
         const unsigned e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
-        float4 A, Bv;
-        float by0 = 0.f, by1 = 0.f, by2 = 0.f;
-        int vkey = 0;
-        if (!FILL) {
-            A = __ldg(sc.pose8 + 2 * bp);
-            Bv = __ldg(sc.pose8 + 2 * bp + 1);
-            vkey = (q.Bsrc == 1) ? 0 : (bp / q.P) * nbr16;
-            // p = a qx + (b qy), as in pose8_position (b qy rounded first).
-            by0 = A.w * (float)qy;
-            by1 = Bv.x * (float)qy;
-            by2 = Bv.y * (float)qy;
-        }
+        const float4 A = __ldg(sc.pose8 + 2 * bp), Bv = __ldg(sc.pose8 + 2 * bp + 1);
+        const int vkey = (q.Bsrc == 1) ? 0 : (bp / q.P) * nbr16;
+        // p = a qx + (b qy), as in pose8_position (b qy rounded first).
+        const float by0 = A.w * (float)qy, by1 = Bv.x * (float)qy, by2 = Bv.y * (float)qy;
         float fx = (float)lane;
-        for (int xb = 0; xb <= xmax; xb += 32 * kFillChunks, fx += 32.0f * kFillChunks) {
-            int key[kFillChunks], leader[kFillChunks];
-            unsigned at[kFillChunks];
+        for (int xb = 0; xb <= xmax; xb += 32 * kListChunks, fx += 32.0f * kListChunks) {
+            int key[kListChunks], leader[kListChunks];
+            unsigned at[kListChunks];
 #pragma unroll
-            for (int k = 0; k < kFillChunks; ++k) {
+            for (int k = 0; k < kListChunks; ++k) {
                 const int qx = xb + 32 * k + lane;
                 key[k] = -1;
                 if (qx <= xmax) {
-                    if (FILL) {
-                        key[k] = __ldg(reinterpret_cast<const int *>(sc.lkey) + e0 + qx);
-                    } else {
-                        const float f = fx + 32.0f * k;
-                        const float p[3] = {fmaf(A.x, f, by0), fmaf(A.y, f, by1), fmaf(A.z, f, by2)};
-                        key[k] = sample_key(s_tab, nb, vkey, p);
-                        sc.lkey[e0 + qx] = (unsigned)key[k];
-                    }
+                    const float f = fx + 32.0f * k;
+                    const float p[3] = {fmaf(A.x, f, by0), fmaf(A.y, f, by1), fmaf(A.z, f, by2)};
+                    key[k] = sample_key(s_tab, nb, vkey, p);
                 }
                 const int prev = __shfl_up_sync(0xffffffffu, key[k], 1);
                 const unsigned starts = __ballot_sync(0xffffffffu, lane == 0 || key[k] != prev);
@@ -1203,59 +1184,83 @@ __global__ void __launch_bounds__(256) k_list_pass(Params q, int nb, Scratch sc)
                 at[k] = 0u;
                 if (key[k] >= 0 && lane == leader[k]) at[k] = atomicAdd(sc.lcount + key[k], (unsigned)len);
             }
-            if (FILL) {
 #pragma unroll
-                for (int k = 0; k < kFillChunks; ++k) {
-                    const unsigned a = __shfl_sync(0xffffffffu, at[k], leader[k]) + (unsigned)(lane - leader[k]);
-                    if (key[k] >= 0 && TP_CHECK(q.dbg, a < entries, 8))
-                        sc.llist[a] = e0 + (unsigned)(xb + 32 * k + lane);
-                }
+            for (int k = 0; k < kListChunks; ++k) {
+                const unsigned rank = __shfl_sync(0xffffffffu, at[k], leader[k]) + (unsigned)(lane - leader[k]);
+                const int qx = xb + 32 * k + lane;
+                if (qx <= xmax) sc.lkey[e0 + qx] = make_int2(key[k], (int)rank);
             }
         }
     }
 }
 
-// Samples, octant items and z-half items of every brick (a thread per brick).
-__global__ void __launch_bounds__(256) k_list_sums(int nbr, Scratch sc, int nvol) {
-    const int id = blockIdx.x * 256 + threadIdx.x;
-    if (sc.lflag[1] == 0u || id >= nvol * nbr) return;
-    const unsigned *cnt = sc.lcount + (size_t)id * kParts;
-    unsigned c[kParts];
+// The fill pass (the counts are the parts' first entries now): every
+// in-radius pixel with a key is written at its key's first entry plus its
+// place.  A warp takes one image row, 32 pixels at a time.
+__global__ void __launch_bounds__(256) k_list_fill(Params q, Scratch sc) {
+    if (sc.lflag[1] == 0u) return;
+    const int lane = threadIdx.x & 31;
+    const int rows = q.B * q.P * q.N;
+    const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
+    for (int row = (blockIdx.x * 256 + threadIdx.x) >> 5; row < rows; row += (gridDim.x * 256) >> 5) {
+        const int bp = row / q.N, iy = row - bp * q.N;
+        const int qy = row_freq(iy, q.N);
+        const int rr = q.r2max - qy * qy;
+        if (rr < 0) continue;
+        int xmax = (int)sqrtf((float)rr);
+        if ((xmax + 1) * (xmax + 1) <= rr) ++xmax;
+        if (xmax * xmax > rr) --xmax;
+        xmax = min(xmax, q.Xo - 1);
+        const unsigned e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
+        // kListChunks chunks at a time: their loads are all in flight before
+        // the first store.
+        for (int xb = lane; xb <= xmax; xb += 32 * kListChunks) {
+            int2 kr[kListChunks];
+            unsigned first[kListChunks];
 #pragma unroll
-    for (int k = 0; k < kParts; k += 4) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(cnt + k);
-        c[k] = u.x;
-        c[k + 1] = u.y;
-        c[k + 2] = u.z;
-        c[k + 3] = u.w;
+            for (int k = 0; k < kListChunks; ++k)
+                kr[k] = xb + 32 * k <= xmax ? __ldg(sc.lkey + e0 + xb + 32 * k) : make_int2(-1, 0);
+#pragma unroll
+            for (int k = 0; k < kListChunks; ++k) first[k] = kr[k].x >= 0 ? __ldg(sc.lcount + kr[k].x) : 0u;
+#pragma unroll
+            for (int k = 0; k < kListChunks; ++k) {
+                const unsigned at = first[k] + (unsigned)kr[k].y;
+                if (kr[k].x >= 0 && TP_CHECK(q.dbg, at < entries, 8)) sc.llist[at] = e0 + (unsigned)(xb + 32 * k);
+            }
+        }
     }
-    int4 r = make_int4(0, 0, 0, 0);
-#pragma unroll
-    for (int k = 0; k < kParts; ++k) {
-        r.x += (int)c[k];
-        r.z += (int)((c[k] + kListChunk - 1) / kListChunk);
-    }
-#pragma unroll
-    for (int o = 0; o < kParts / 2; ++o) r.y += (int)((c[2 * o] + c[2 * o + 1] + kListChunk - 1) / kListChunk);
-    sc.lbrick[id] = r;
 }
 
-// One block per volume: exclusive sums of the bricks' figures (in place), and
-// the volume's item counts.
-__global__ void __launch_bounds__(kListThreads) k_list_scan(int nbr, Scratch sc) {
+// Samples, octant items and z-half items of every brick, and their sums
+// before it within its block of kSumBlock bricks (the block's totals go to
+// lblock).  Grid: (blocks of bricks, volumes).
+constexpr int kSumBlock = 256;
+
+__global__ void __launch_bounds__(kSumBlock) k_list_sums(int nbr, Scratch sc) {
     if (sc.lflag[1] == 0u) return;
-    __shared__ int s_w[3][kListThreads / 32];
-    const int v = blockIdx.x, nvol = gridDim.x;
+    __shared__ int s_w[3][kSumBlock / 32];
+    const int v = blockIdx.y, j = blockIdx.x * kSumBlock + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int4 *br = sc.lbrick + (size_t)v * nbr;
-    const int per = (nbr + kListThreads - 1) / kListThreads;
-    const int j0 = threadIdx.x * per, j1 = min(nbr, j0 + per);
     int x[3] = {0, 0, 0};
-    for (int j = j0; j < j1; ++j) {
-        const int4 r = br[j];
-        x[0] += r.x;
-        x[1] += r.y;
-        x[2] += r.z;
+    if (j < nbr) {
+        const unsigned *cnt = sc.lcount + ((size_t)v * nbr + j) * kParts;
+        unsigned c[kParts];
+#pragma unroll
+        for (int k = 0; k < kParts; k += 4) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(cnt + k);
+            c[k] = u.x;
+            c[k + 1] = u.y;
+            c[k + 2] = u.z;
+            c[k + 3] = u.w;
+        }
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) {
+            x[0] += (int)c[k];
+            x[2] += (int)((c[k] + kListChunk - 1) / kListChunk);
+        }
+#pragma unroll
+        for (int o = 0; o < kParts / 2; ++o)
+            x[1] += (int)((c[2 * o] + c[2 * o + 1] + kListChunk - 1) / kListChunk);
     }
     int incl[3] = {x[0], x[1], x[2]};
 #pragma unroll
@@ -1268,33 +1273,16 @@ __global__ void __launch_bounds__(kListThreads) k_list_scan(int nbr, Scratch sc)
         if (lane == 31) s_w[k][warp] = incl[k];
     }
     __syncthreads();
-    if (warp == 0) {
+    int before[3] = {0, 0, 0};
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            int y = s_w[k][lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, y, o);
-                if (lane >= o) y += t;
-            }
-            s_w[k][lane] = y;
-        }
-    }
-    __syncthreads();
-    int run[3];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) run[k] = incl[k] - x[k] + (warp > 0 ? s_w[k][warp - 1] : 0);
-    for (int j = j0; j < j1; ++j) {
-        const int4 r = br[j];
-        br[j] = make_int4(run[0], run[1], run[2], 0);
-        run[0] += r.x;
-        run[1] += r.y;
-        run[2] += r.z;
-    }
-    if (threadIdx.x == kListThreads - 1) {
-        sc.counters[4 * nvol + v] = (unsigned)min(run[1], sc.itemcap);
-        sc.counters[5 * nvol + v] = (unsigned)min(run[2], sc.itemcap);
-    }
+    for (int k = 0; k < 3; ++k)
+        for (int w = 0; w < warp; ++w) before[k] += s_w[k][w];
+    if (j < nbr)
+        sc.lbrick[(size_t)v * nbr + j] =
+            make_int4(before[0] + incl[0] - x[0], before[1] + incl[1] - x[1], before[2] + incl[2] - x[2], 0);
+    if (threadIdx.x == kSumBlock - 1)
+        sc.lblock[(size_t)v * gridDim.x + blockIdx.x] =
+            make_int4(before[0] + incl[0], before[1] + incl[1], before[2] + incl[2], 0);
 }
 
 // Eight threads per brick, one per octant: the list offsets of the octant's
@@ -1306,7 +1294,16 @@ __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvo
     const int id = (blockIdx.x * 256 + threadIdx.x) >> 3, o = threadIdx.x & 7;
     if (sc.lflag[1] == 0u || id >= nvol * nbr) return;
     const int v = id / nbr, j = id - v * nbr;
-    const int4 base = sc.lbrick[id];
+    // The brick's sums before it: within its block of bricks, plus the
+    // totals of the volume's blocks before that one.
+    int4 base = sc.lbrick[id];
+    const int nblk = (nbr + kSumBlock - 1) / kSumBlock;
+    for (int b = 0; b < j / kSumBlock; ++b) {
+        const int4 t = sc.lblock[(size_t)v * nblk + b];
+        base.x += t.x;
+        base.y += t.y;
+        base.z += t.z;
+    }
     unsigned *cnt = sc.lcount + (size_t)id * kParts;
     unsigned c[kParts];
 #pragma unroll
@@ -1351,6 +1348,10 @@ __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvo
             if (hi < sc.itemcap)
                 half_items[hi] = make_int4((int)(f + i), (int)min((unsigned)kListChunk, n - i), j, zq * 4 + xy);
     }
+    if (j == nbr - 1 && o == kParts / 2 - 1) {   // the volume's last items: their counts
+        sc.counters[4 * nvol + v] = (unsigned)min(oi, sc.itemcap);
+        sc.counters[5 * nvol + v] = (unsigned)min(hi, sc.itemcap);
+    }
 }
 
 // Cubic: one lane spreads one sample, 32 samples of the item's list per
@@ -1382,7 +1383,8 @@ constexpr int kCWPair = 2 * kCLayer;       // weight words of a pair of z layers
 template <bool WEIGHTS>
 struct OctLayout {
     static constexpr int WARPS = 4;                  // warps per block (blocks only share an SM)
-    static constexpr int OZ = WEIGHTS ? kOct / 2 : kOct;   // z extent of an item's box
+    static constexpr int OZ = kOct / 2;              // z extent of an item's box
+    static constexpr int BLOCKS = WEIGHTS ? 4 : 6;   // resident blocks per SM
     static constexpr int SZ = OZ + 3;                // z layers of the tiles
     static constexpr int ELEMS = kCLayer * SZ;       // complex words of the tile
     static constexpr int WELEMS = WEIGHTS ? kCWPair * ((SZ + 1) / 2) : 0;   // words of the weight tile
@@ -1498,7 +1500,7 @@ __device__ __forceinline__ void spread_cubic(int l0, int l1, int l2, const float
 }
 
 template <bool WEIGHTS>
-__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, 4)
+__global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIGHTS>::BLOCKS)
     k_brick_scatter_cubic(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
                           const float *__restrict__ omega, float2 *__restrict__ dst,
                           float *__restrict__ wdst) {
@@ -1512,8 +1514,8 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, 4)
     const unsigned wtile = (unsigned)__cvta_generic_to_shared(wacc);
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int nitems = (int)__ldg(sc.counters + (WEIGHTS ? 5 : 4) * nvol + v);
-    const int4 *items = sc.litems + (size_t)((WEIGHTS ? nvol : 0) + v) * sc.itemcap;
+    const int nitems = (int)__ldg(sc.counters + (OL::OZ == kOct ? 4 : 5) * nvol + v);
+    const int4 *items = sc.litems + (size_t)((OL::OZ == kOct ? 0 : nvol) + v) * sc.itemcap;
     const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
@@ -1757,7 +1759,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t counters, geo, pose8, reach, masks, hits, units, binning;   // the binning
-    size_t lcount, lbrick, litems, llist, lkey, total;                // + the sample lists
+    size_t lcount, lbrick, litems, llist, lkey, lblock, total;        // + the sample lists
     int nb, nchunks, itemcap;
     long long vol_entries;   // list entries per volume (its images' pixels)
 };
@@ -1781,7 +1783,7 @@ Layout layout(const Params &q, bool cubic) {
     L.binning = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.vol_entries = Pv * (long long)q.N * (q.N / 2 + 1);
     L.itemcap = 0;
-    L.lcount = L.lbrick = L.litems = L.llist = L.lkey = 0;
+    L.lcount = L.lbrick = L.litems = L.llist = L.lkey = L.lblock = 0;
     L.total = L.binning;
     if (cubic) {
         L.itemcap = (int)(nbr * kParts + L.vol_entries / kListChunk + 1);
@@ -1790,7 +1792,8 @@ Layout layout(const Params &q, bool cubic) {
         L.litems = L.lbrick + align256(sizeof(int4) * (size_t)q.Bsrc * nbr);
         L.llist = L.litems + align256(sizeof(int4) * 2 * (size_t)q.Bsrc * L.itemcap);
         L.lkey = L.llist + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
-        L.total = L.lkey + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
+        L.lblock = L.lkey + align256(sizeof(int2) * (size_t)(L.vol_entries * q.Bsrc));
+        L.total = L.lblock + align256(sizeof(int4) * (size_t)q.Bsrc * ((nbr + kSumBlock - 1) / kSumBlock));
     }
     return L;
 }
@@ -1812,7 +1815,8 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.lbrick = L.lbrick ? reinterpret_cast<int4 *>(base + L.lbrick) : nullptr;
     sc.litems = L.litems ? reinterpret_cast<int4 *>(base + L.litems) : nullptr;
     sc.llist = L.llist ? reinterpret_cast<unsigned *>(base + L.llist) : nullptr;
-    sc.lkey = L.lkey ? reinterpret_cast<unsigned *>(base + L.lkey) : nullptr;
+    sc.lkey = L.lkey ? reinterpret_cast<int2 *>(base + L.lkey) : nullptr;
+    sc.lblock = L.lblock ? reinterpret_cast<int4 *>(base + L.lblock) : nullptr;
     sc.nchunks = L.nchunks;
     sc.itemcap = L.itemcap;
     return sc;
@@ -1951,14 +1955,13 @@ cudaError_t build_lists(const Params &q, const Layout &L, const Scratch &sc, cud
     const unsigned bricks = (unsigned)(((long long)q.Bsrc * nbr + 255) / 256);
     if (blocks == 0) return cudaGetLastError();
     const size_t tab = sizeof(int) * 3 * (16 * L.nb + 2);
-    if ((e = cudaFuncSetAttribute(k_list_pass<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab)) !=
+    if ((e = cudaFuncSetAttribute(k_list_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab)) !=
         cudaSuccess)
         return e;
-    k_list_pass<false><<<blocks, 256, tab, st>>>(q, L.nb, sc);
-    k_list_sums<<<bricks, 256, 0, st>>>(nbr, sc, q.Bsrc);
-    k_list_scan<<<q.Bsrc, kListThreads, 0, st>>>(nbr, sc);
+    k_list_count<<<blocks, 256, tab, st>>>(q, L.nb, sc);
+    k_list_sums<<<dim3((unsigned)((nbr + kSumBlock - 1) / kSumBlock), (unsigned)q.Bsrc), kSumBlock, 0, st>>>(nbr, sc);
     k_list_items<<<8 * bricks, 256, 0, st>>>(nbr, sc, q.Bsrc, L.vol_entries);
-    k_list_pass<true><<<blocks, 256, 0, st>>>(q, L.nb, sc);
+    k_list_fill<<<blocks, 256, 0, st>>>(q, sc);
     return cudaGetLastError();
 }
 
