@@ -31,8 +31,9 @@ namespace {
 // prefix sum packing the candidates into 32-lane rounds) and spreads the
 // owned ones into a private tile with plain read-add-write.  Cubic: each lane
 // spreads its own sample's 16 taps in a lane-rotated order that keeps the 16
-// lanes of a pass on 16 different words (lanes 0-15, then 16-31), with no
-// queue.  Linear: owned samples are queued and tap lanes (jx, jy) spread
+// lanes of a half-warp on 16 different words; each half-warp has a tile of its
+// own, so both spread at once, and the fold adds the two.  Linear: owned
+// samples are queued and tap lanes (jx, jy) spread
 // several samples per round, one at a time in a round where two of their
 // stencils meet (stencils_meet).  The tile is then added to the stored
 // half-spectrum with one vector atomic per touched word (Friedel positions
@@ -42,8 +43,8 @@ constexpr int kTileWarps = 4;
 constexpr float kTileMargin = 0.01f;
 
 // The warp's tile.  Cubic: 20 x 20 words in 4 x 4 tiles of 16 complex words,
-// so word (x, y) sits in bank pair (x mod 4) + 4 (y mod 4).  Linear: row-major
-// 17 x 18 (x pitch 18).
+// so word (x, y) sits in bank pair (x mod 4) + 4 (y mod 4), one tile per
+// half-warp.  Linear: row-major 17 x 18 (x pitch 18).
 template <bool CUBIC>
 struct Tile2 {
     using St = Stencil<CUBIC>;
@@ -55,7 +56,8 @@ struct Tile2 {
     // stencils rarely meet; a round in which two of them do is spread one
     // sample at a time.
     static constexpr int SPS = 32 / LANES;
-    static constexpr size_t TILE_BYTES = sizeof(float2) * ELEMS;
+    static constexpr int COPIES = CUBIC ? 2 : 1;          // tiles per warp
+    static constexpr size_t TILE_BYTES = sizeof(float2) * ELEMS * COPIES;
     static constexpr size_t QUEUE_BYTES = CUBIC ? 0 : sizeof(float) * 32 * 9 + sizeof(float4) * 32;
     static constexpr size_t WARP_BYTES = TILE_BYTES + QUEUE_BYTES;
     static_assert(TILE_BYTES % 16 == 0, "16-byte aligned queue");
@@ -116,7 +118,8 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
     float2 *V = dst + (q.Bsrc == 1 ? (size_t)0 : (size_t)b * q.src_stride);
     const float sx = ps.sx, sy = ps.sy;
 
-    for (int e = lane; e < T::ELEMS; e += 32) acc[e] = make_float2(0.f, 0.f);
+    for (int e = lane; e < T::ELEMS * T::COPIES; e += 32) acc[e] = make_float2(0.f, 0.f);
+    float2 *const mytile = acc + (T::COPIES == 2 ? (lane >> 4) * T::ELEMS : 0);   // this half-warp's tile
     if (threadIdx.x == 0) s_next = 0;
     __syncthreads();
     for (;;) {
@@ -207,10 +210,10 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                 }
                 const unsigned mask = __ballot_sync(0xffffffffu, own);
                 if constexpr (CUBIC) {
-                    // Each lane spreads its own sample's 16 taps, lanes 0-15 and
-                    // then lanes 16-31.  At step (sx, sy) lane L takes the tap
+                    // Each lane spreads its own sample's 16 taps into its
+                    // half-warp's tile.  At step (sx, sy) lane L takes the tap
                     // whose x is (sx + L) mod 4 and y (sy + L / 4) mod 4: the 16
-                    // lanes of a pass touch 16 different bank pairs, hence 16
+                    // lanes of a half-warp touch 16 different bank pairs, hence 16
                     // different words, so the plain read-add-write never races;
                     // the warp synchronises between steps because the stencils of
                     // different lanes' samples meet at different steps.
@@ -235,21 +238,17 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                             cy[i] = make_float2(wy[i] * cv.x, wy[i] * cv.y);
                         }
                     }
-                    for (int pass = 0; pass < 2; ++pass) {
-                        if (((mask >> (16 * pass)) & 0xffffu) == 0u) continue;   // warp-uniform
-                        const bool now = own && (lane >> 4) == pass;
 #pragma unroll
-                        for (int sy2 = 0; sy2 < 4; ++sy2) {
+                    for (int sy2 = 0; sy2 < 4; ++sy2) {
 #pragma unroll
-                            for (int sx2 = 0; sx2 < 4; ++sx2) {
-                                const int at = toy[sy2] + tox[sx2];
-                                if (now && TP_CHECK(q.dbg, at >= 0 && at < T::ELEMS, 4)) {
-                                    float2 a = acc[at];
-                                    cfma(wx[sx2], cy[sy2], a);
-                                    acc[at] = a;
-                                }
-                                __syncwarp();
+                        for (int sx2 = 0; sx2 < 4; ++sx2) {
+                            const int at = toy[sy2] + tox[sx2];
+                            if (own && TP_CHECK(q.dbg, at >= 0 && at < T::ELEMS, 4)) {
+                                float2 a = mytile[at];
+                                cfma(wx[sx2], cy[sy2], a);
+                                mytile[at] = a;
                             }
+                            __syncwarp();
                         }
                     }
                     continue;
@@ -308,7 +307,12 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
         for (int e = lane; e < T::S * T::S; e += 32) {
             const int lx = e % T::S, ly = e / T::S;
             const int k = T::index(lx, ly);
-            const float2 cv = acc[k];
+            float2 cv = acc[k];
+            if (T::COPIES == 2) {   // the two half-warps' tiles
+                const float2 c2 = acc[k + T::ELEMS];
+                cv = make_float2(cv.x + c2.x, cv.y + c2.y);
+                acc[k + T::ELEMS] = make_float2(0.f, 0.f);
+            }
             if (cv.x == 0.f && cv.y == 0.f) continue;
             acc[k] = make_float2(0.f, 0.f);
             int nx = x0 + lx, ny = y0 + ly;
