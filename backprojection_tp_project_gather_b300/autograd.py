@@ -36,6 +36,7 @@ class _Project3D(torch.autograd.Function):
         B = max(vol.shape[0], rot.shape[0], shift.shape[0] if shift is not None else 1)
         ws = torch.empty(max(1, tp_workspace_bytes(vol.shape[0], B, rot.shape[1], vol.shape[1],
                                                    interp, N)), dtype=torch.uint8, device=vol.device)
+        ws[:256].zero_()   # a recycled block may hold an old binning's key
         if need_pose:
             out, dout = tp_project_3d_2d_save(vol, rot, shift, workspace=ws, **kw)
         else:

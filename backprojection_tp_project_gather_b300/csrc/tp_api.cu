@@ -129,7 +129,7 @@ tp_status check_complex(const float *p, const char *name) {
 }
 
 // Workspace check for the 3D operators (the 2D ones need none).  lists: the
-// call runs the cubic scatter, whose sample lists follow the binning.
+// call runs a scatter, whose sample lists follow the binning.
 tp_status check_workspace(const Geometry &g, void *ws, size_t ws_bytes, bool lists) {
     if (g.dim != 3) return TP_OK;
     if (lists && (long long)g.q.B * g.q.P * g.q.plane >= (1LL << 31))
@@ -185,7 +185,7 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
     if (grad_src && (st = check_complex(grad_src, "grad of the source")) != TP_OK) return st;
     if ((grad_rot && !aligned(grad_rot, 4)) || (grad_shift && !aligned(grad_shift, 4)))
         return fail(TP_ERR_ALIGN, "grad_rot / grad_shift must be 4-byte aligned");
-    if ((st = check_workspace(g, ws, ws_bytes, grad_src && g.cubic)) != TP_OK) return st;
+    if ((st = check_workspace(g, ws, ws_bytes, grad_src != nullptr)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     tp::BinMode mode = tp::kBinNew;
     if (grad_rot || grad_shift) {
@@ -221,8 +221,8 @@ tp_status backward(int dim, const float *grad_out, const float *src, int Bsrc, i
 
 namespace tp {
 
-// Workspace bytes of the 3D operators; lists: with the cubic scatter's
-// sample lists (every operator), else the binning alone (the forward).
+// Workspace bytes of the 3D operators; lists: with the scatters' sample
+// lists (every operator), else the binning alone (the forward).
 size_t workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts, bool lists) {
     if (Bv < 1 || B < 1 || P < 1 || Nv < 2 || (Nv & 1) || Nv > 4096 || N < 2 || (N & 1) || N > 4096 ||
         Bv > B)
@@ -383,7 +383,7 @@ tp_status tp_backproject_2d_3d(const float *proj, const float *weights, int B, i
         return st;
     if ((weights && !aligned(weights, 4)) || (weight_vol && !aligned(weight_vol, 4)))
         return fail(TP_ERR_ALIGN, "weights / weight_vol must be 4-byte aligned");
-    if ((st = check_workspace(g, workspace, workspace_bytes, g.cubic)) != TP_OK) return st;
+    if ((st = check_workspace(g, workspace, workspace_bytes, true)) != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float2 *dv = reinterpret_cast<float2 *>(data_vol);
     cudaError_t e = tp::launch_brick_scatter(g.cubic, g.q, reinterpret_cast<const float2 *>(proj),

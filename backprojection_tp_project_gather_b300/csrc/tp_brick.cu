@@ -19,9 +19,9 @@
 //    samples into it with plain read-add-write, and adds the tile to the
 //    stored half-spectrum once per work item (Friedel positions conjugated
 //    at -n), with vector atomics because halos of neighbouring octants and
-//    other work items overlap.  The cubic scatter reads its samples from
-//    lists of the output pixels sorted by brick part (a counting sort over
-//    the pixels); the linear one enumerates each reaching pose's pixels.
+//    other work items overlap.  The scatters read their samples from lists
+//    of the output pixels sorted by brick part (a counting sort over the
+//    pixels).
 //
 // Binning.  Three small passes precede every operator: one thread per pose
 // computes the pose's geometry (into the caller's workspace, where a later
@@ -32,8 +32,7 @@
 // block per volume then turns the counts into a compact list of work units
 // -- a brick and a range of chunks holding about kUnitHits reaching poses,
 // so busy bricks near the origin are split and empty bricks vanish.  The
-// main kernels take units (or, in the linear scatter, unit octants) from a
-// global counter in brick order, busiest first.  For one (pose, box) pair the
+// gathers take units from a global counter in brick order, busiest first.  For one (pose, box) pair the
 // owned pixels form a convex polygon in k-space: its rows come from the
 // pseudo-inverse of [a b] and each row's qx interval from the three slab
 // constraints; the enumeration is a small superset and the exact floor(p)
@@ -194,28 +193,6 @@ __device__ __forceinline__ BrickBox brick_box(int linear, int nb) {
         bx.hi[d] = (float)(bx.o[d] + kBS) + kMargin;
     }
     return bx;
-}
-
-// Can an in-radius sample of the pose have its position p in the box?  The
-// plane must meet the box, the half-plane qx >= 0 must reach it, and the box
-// must come within the pose's reach of the origin.
-__device__ __forceinline__ bool pose_reaches(const PoseGeo &g, const BrickBox &bx) {
-    float c[3], h[3], dist2 = 0.f;
-#pragma unroll
-    for (int d = 0; d < 3; ++d) {
-        c[d] = 0.5f * (bx.lo[d] + bx.hi[d]);
-        h[d] = 0.5f * (bx.hi[d] - bx.lo[d]);
-        const float e = fmaxf(fabsf(c[d]) - h[d], 0.f);
-        dist2 += e * e;
-    }
-    if (dist2 > g.reach * g.reach) return false;
-    if (g.degenerate) return true;
-    const float cn = g.n[0] * c[0] + g.n[1] * c[1] + g.n[2] * c[2];
-    const float hn = fabsf(g.n[0]) * h[0] + fabsf(g.n[1]) * h[1] + fabsf(g.n[2]) * h[2];
-    if (fabsf(cn) > hn * 1.0001f + 1e-6f) return false;
-    const float cv = g.v[0] * c[0] + g.v[1] * c[1] + g.v[2] * c[2];
-    const float hv = fabsf(g.v[0]) * h[0] + fabsf(g.v[1]) * h[1] + fabsf(g.v[2]) * h[2];
-    return cv + hv >= -0.01f;
 }
 
 // Calls f(qx, qy, active) on every lane for groups of 32 candidate pixels:
@@ -390,8 +367,10 @@ __device__ __forceinline__ float geo_reach(const int4 *geo, int pid) {
 }
 
 // Bit l of mask (volume, brick, chunk) = pose 32*chunk + l of the volume's
-// list can reach the brick (the test of pose_reaches, with the per-pose
-// constants of ReachGeo); the brick's count grows by the number of set bits.
+// list can reach the brick: the box must come within the pose's reach of the
+// origin, the plane must meet it and the half-plane qx >= 0 must reach it
+// (with the per-pose constants of ReachGeo); the brick's count grows by the
+// number of set bits.
 // A lane owns one brick and runs through the chunk's 32 poses, whose
 // records every lane of the warp reads at once.
 __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
@@ -1042,9 +1021,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // brick plus the stencil's halo, so the spreading needs no atomics, and the
 // tile is folded into the stored half-spectrum with vector global atomics
 // (Friedel positions conjugated at -n) when the warp's work item is done.
-// The cubic scatter takes its samples from lists sorted by brick part; the
-// linear one runs through the poses of a work unit that reach its octant
-// and enumerates the samples whose floor(p) lies in it.
+// Both take their samples from lists of the output pixels sorted by brick
+// part.
 
 // Sample lists: every in-radius output pixel whose floor(p) lies in the
 // brick grid, binned by brick part with a counting sort (count, scan, fill).
@@ -1633,8 +1611,9 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
     const int toff = jx + kLPX * (jy + kLPY * jz);
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int items = 8 * (int)__ldg(sc.counters + 3 * nvol + v);
-    const int4 *units = sc.units + (size_t)v * nbr * sc.nchunks;
+    const int nitems = (int)__ldg(sc.counters + 4 * nvol + v);
+    const int4 *items = sc.litems + (size_t)v * sc.itemcap;
+    const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
     for (int e = lane; e < kLElems; e += 32) {
@@ -1646,81 +1625,75 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
         int item = 0;
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
-        if (item >= items) break;
-        if (!TP_CHECK(q.dbg, (item >> 3) < nbr * sc.nchunks, 8)) break;
-        const int4 rec = __ldg(units + (item >> 3));
-        if (!TP_CHECK(q.dbg, rec.x >= 0 && rec.x < nbr && rec.y >= 0 && rec.y <= rec.z &&
-                                 rec.z <= sc.nchunks, 8))
-            break;
-        const BrickBox ob = octant_box(brick_box(rec.x, nb), item & 7);
-        const unsigned *masks = sc.masks + ((size_t)v * nbr + rec.x) * sc.nchunks;
-        bool touched = false;
-        for (int c = rec.y; c < rec.z; ++c) {
-            // The poses of the chunk that can reach this octant, tested one per lane.
-            const unsigned m = __ldg(masks + c);
-            bool reach = false;
-            if ((m >> lane) & 1u) {
-                const int pid = pose_id(q, v, c * 32 + lane);
-                if (TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8))
-                    reach = pose_reaches(load_geo(sc.geo, pid), ob);
-            }
-            for (unsigned mr = __ballot_sync(0xffffffffu, reach); mr; mr &= mr - 1) {
-                const PoseGeo g = load_geo(sc.geo, pose_id(q, v, c * 32 + __ffs(mr) - 1));
-                touched = true;
-                const size_t ib = (size_t)g.bp * q.plane;
-                for_pixels_in_box(g, ob, q.N, q.r2max, [&](int qx, int qy, bool active) {
-                    int l[3];
-                    float w[3][4], d[3][4];
-                    const bool own = active && own_sample<false, false, kOct>(g, ob, qx, qy, l, w, d);
-                    const unsigned mask = __ballot_sync(0xffffffffu, own);
-                    if (own) {
-                        const int slot = __popc(mask & ((1u << lane) - 1u));
-                        const int iy = qy < 0 ? qy + q.N : qy;
-                        const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo &&
-                                                            g.bp < q.B * q.P, 7);
-                        float2 cv = in ? __ldg(img + ib + iy * q.Xo + qx) : make_float2(0.f, 0.f);
-                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, g.sx, g.sy, q.fN, q.invN), cv);
-                        float *wq = Q.w[slot];
+        if (item >= nitems) break;
+        const int4 it = __ldg(items + item);   // first entry, count, brick, octant
+        if (!TP_CHECK(q.dbg, it.z >= 0 && it.z < nbr && it.y > 0 && it.y <= kListChunk &&
+                                 (unsigned)it.x + (unsigned)it.y <= entries, 8))
+            continue;
+        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w);
+        for (int r0 = 0; r0 < it.y; r0 += 32) {
+            // Each lane sets up one sample of the list and queues it.
+            bool own = r0 + lane < it.y;
+            const unsigned e = own ? __ldg(sc.llist + it.x + r0 + lane) : 0u;
+            own = own && TP_CHECK(q.dbg, e < entries, 8);
+            int qx, qy;
+            const unsigned bp = split_pixel(q, own ? e : 0u, qx, qy);
+            float2 cv = own ? __ldg(img + e) : make_float2(0.f, 0.f);
+            const float om = (WEIGHTS && omega && own) ? __ldg(omega + e) : 1.0f;
+            const float4 A = __ldg(sc.pose8 + 2 * bp), Bv = __ldg(sc.pose8 + 2 * bp + 1);
+            float p[3], w[3][2];
+            int l[3];
+            pose8_position(A, Bv, qx, qy, p);
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) wq[t] = w[0][t & 1] * w[1][(t >> 1) & 1] * w[2][t >> 2];
-                        wq[8] = __int_as_float(l[0] | (l[1] << 8) | (l[2] << 16));
-                        const float om = (WEIGHTS && omega && in) ? __ldg(omega + ib + iy * q.Xo + qx) : 1.0f;
-                        Q.rec[slot] = make_float4(cv.x, cv.y, om,
-                                                  __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
-                    }
-                    __syncwarp();
-                    const int nq = __popc(mask);
-                    const int R = (nq + 3) >> 2;
-                    for (int r = 0; r < R; ++r) {
-                        const int sq = r + R * grp;
-                        const bool act = sq < nq;
-                        float wt = 0.f;
-                        float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
-                        int idx = 0, at = kFarAway;
-                        if (act) {
-                            wt = Q.w[sq][lane & 7];
-                            at = __float_as_int(Q.w[sq][8]);
-                            cur = Q.rec[sq];
-                            idx = __float_as_int(cur.w) + toff;
-                        }
-                        const bool clash = stencils_meet<4, 3>(at, 8, 2);
-                        for (int k = 0; k < 4; ++k) {
-                            if (act && (!clash || grp == k) &&
-                                TP_CHECK(q.dbg, idx >= 0 && idx < kLElems, 4)) {
-                                float2 a = acc[idx];
-                                cfma(wt, make_float2(cur.x, cur.y), a);
-                                acc[idx] = a;
-                                if (WEIGHTS) wacc[idx] = fmaf(wt, cur.z, wacc[idx]);
-                            }
-                            __syncwarp();
-                            if (!clash) break;
-                        }
-                    }
-                    __syncwarp();
-                });
+            for (int a = 0; a < 3; ++a) {
+                float t;
+                l[a] = split_coord(p[a], t) - ob.o[a];
+                Stencil<false>::weights(t, w[a]);
             }
+            // The list put the sample in this octant (same position arithmetic);
+            // the test keeps every tile access in range whatever happens.
+            const bool inbox = (unsigned)l[0] < (unsigned)kOct && (unsigned)l[1] < (unsigned)kOct &&
+                               (unsigned)l[2] < (unsigned)kOct;
+            own = own && TP_CHECK(q.dbg, inbox, 4) && inbox;
+            const unsigned mask = __ballot_sync(0xffffffffu, own);
+            if (own) {
+                if (q.shift) cv = cmul_conj_a(shift_phase(qx, qy, Bv.z, Bv.w, q.fN, q.invN), cv);
+                const int slot = __popc(mask & ((1u << lane) - 1u));
+                float *wq = Q.w[slot];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) wq[t] = w[0][t & 1] * w[1][(t >> 1) & 1] * w[2][t >> 2];
+                wq[8] = __int_as_float(l[0] | (l[1] << 8) | (l[2] << 16));
+                Q.rec[slot] = make_float4(cv.x, cv.y, om, __int_as_float((l[2] * kLPY + l[1]) * kLPX + l[0]));
+            }
+            __syncwarp();
+            const int nq = __popc(mask);
+            const int R = (nq + 3) >> 2;
+            for (int r = 0; r < R; ++r) {
+                const int sq = r + R * grp;
+                const bool act = sq < nq;
+                float wt = 0.f;
+                float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
+                int idx = 0, at = kFarAway;
+                if (act) {
+                    wt = Q.w[sq][lane & 7];
+                    at = __float_as_int(Q.w[sq][8]);
+                    cur = Q.rec[sq];
+                    idx = __float_as_int(cur.w) + toff;
+                }
+                const bool clash = stencils_meet<4, 3>(at, 8, 2);
+                for (int k = 0; k < 4; ++k) {
+                    if (act && (!clash || grp == k) && TP_CHECK(q.dbg, idx >= 0 && idx < kLElems, 4)) {
+                        float2 a = acc[idx];
+                        cfma(wt, make_float2(cur.x, cur.y), a);
+                        acc[idx] = a;
+                        if (WEIGHTS) wacc[idx] = fmaf(wt, cur.z, wacc[idx]);
+                    }
+                    __syncwarp();
+                    if (!clash) break;
+                }
+            }
+            __syncwarp();
         }
-        if (!touched) continue;
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0], y0 = ob.o[1], z0 = ob.o[2];
         for (int e = lane; e < kLS * kLS * kLS; e += 32) {
@@ -1764,8 +1737,8 @@ struct Layout {
     long long vol_entries;   // list entries per volume (its images' pixels)
 };
 
-// Workspace layout: the binning every 3D operator uses, then (cubic only) the
-// sample lists of the scatter, sized for every output pixel.
+// Workspace layout: the binning every 3D operator uses, then the sample lists
+// of the scatters, sized for every output pixel.
 Layout layout(const Params &q, bool cubic) {
     Layout L;
     L.nb = bricks_per_axis(q.M, cubic);
@@ -1785,7 +1758,7 @@ Layout layout(const Params &q, bool cubic) {
     L.itemcap = 0;
     L.lcount = L.lbrick = L.litems = L.llist = L.lkey = L.lblock = 0;
     L.total = L.binning;
-    if (cubic) {
+    {
         L.itemcap = (int)(nbr * kParts + L.vol_entries / kListChunk + 1);
         L.lcount = L.binning;
         L.lbrick = L.lcount + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * kParts);
@@ -1924,24 +1897,7 @@ cudaError_t pose_grad_t(const Params &q, const float2 *g, float *grot, float *gs
     return cudaGetLastError();
 }
 
-template <bool WEIGHTS>
-cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
-                             float *wdst, void *ws, BinMode mode, cudaStream_t st) {
-    using LL = LinLayout<WEIGHTS>;
-    const Layout L = layout(q, false);
-    const Scratch sc = scratch_in(ws, L);
-    const int threads = 32 * LL::WARPS;
-    const size_t smem = LL::WARP_BYTES * LL::WARPS;
-    auto kern = k_brick_scatter_linear<WEIGHTS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
-    kern<<<warp_grid(q, (const void *)kern, threads, smem), threads, smem, st>>>(q, L.nb, sc, img,
-                                                                               omega, dst, wdst);
-    return cudaGetLastError();
-}
-
-// The sample lists of the cubic scatter, unless the workspace holds the ones
+// The sample lists of the scatters, unless the workspace holds the ones
 // of this binning (the kernels after k_list_begin then return at once).
 cudaError_t build_lists(const Params &q, const Layout &L, const Scratch &sc, cudaStream_t st) {
     const int nbr = L.nb * L.nb * L.nb;
@@ -1962,6 +1918,24 @@ cudaError_t build_lists(const Params &q, const Layout &L, const Scratch &sc, cud
     k_list_sums<<<dim3((unsigned)((nbr + kSumBlock - 1) / kSumBlock), (unsigned)q.Bsrc), kSumBlock, 0, st>>>(nbr, sc);
     k_list_items<<<8 * bricks, 256, 0, st>>>(nbr, sc, q.Bsrc, L.vol_entries);
     k_list_fill<<<blocks, 256, 0, st>>>(q, sc);
+    return cudaGetLastError();
+}
+
+template <bool WEIGHTS>
+cudaError_t scatter_linear_t(const Params &q, const float2 *img, const float *omega, float2 *dst,
+                             float *wdst, void *ws, BinMode mode, cudaStream_t st) {
+    using LL = LinLayout<WEIGHTS>;
+    const Layout L = layout(q, false);
+    const Scratch sc = scratch_in(ws, L);
+    const int threads = 32 * LL::WARPS;
+    const size_t smem = LL::WARP_BYTES * LL::WARPS;
+    auto kern = k_brick_scatter_linear<WEIGHTS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare(q, L, sc, 2, mode, st)) != cudaSuccess) return e;
+    if ((e = build_lists(q, L, sc, st)) != cudaSuccess) return e;
+    kern<<<warp_grid(q, (const void *)kern, threads, smem), threads, smem, st>>>(q, L.nb, sc, img,
+                                                                               omega, dst, wdst);
     return cudaGetLastError();
 }
 

@@ -710,20 +710,28 @@ def backproject_setup(tp, dev, interp, backward=False, images=None):
     n, N = w["P"], w["box"]
     samples = n * N * (N // 2 + 1)
     proj = torch.from_numpy(w["proj"]).to(dev)
-    rot = torch.from_numpy(w["rot"]).to(dev)
+    # Two pose sets used in turn, so that every call bins its poses and sorts
+    # its samples anew (a workspace keeps them only for unchanged poses).
+    rots = [torch.from_numpy(w["rot"]).to(dev),
+            torch.from_numpy(synth.random_rotations(n, synth.streams(7005, 1)[0])
+                             .reshape(w["rot"].shape).astype(np.float32)).to(dev)]
+    rot = rots[0]
     kw = dict(interp=interp, oversampling=1.0, radius=w["radius"])
     shape = (1, N, N, N // 2 + 1)
     ws = torch.zeros(tp.tp_workspace_bytes(1, 1, n, N, interp), dtype=torch.uint8, device=dev)
     vol_bytes = 8 * N * N * (N // 2 + 1)
     cfg = {"workload": f"backproject-box{N}-{n}img-{interp}", "box": N, "images": n,
            "interp": interp, "radius": w["radius"], "weights": "1 (default)",
+           "poses": "two seeded pose sets in turn: every call bins its poses and sorts its "
+                    "samples",
            "l2_cache": "flushed between steps (256 MB write)"}
     if not backward:
         data = torch.zeros(shape, dtype=torch.complex64, device=dev)
         wvol = torch.zeros(shape, dtype=torch.float32, device=dev)
 
         def step(i):
-            tp.tp_backproject_2d_3d(proj, rot, data_vol=data, weight_vol=wvol, workspace=ws, **kw)
+            tp.tp_backproject_2d_3d(proj, rots[i & 1], data_vol=data, weight_vol=wvol, workspace=ws,
+                                    **kw)
         nbytes = samples * 8 + 2 * vol_bytes + 2 * vol_bytes // 2
         metric = "backprojected Fourier samples/sec (Gsamples/s), data + weight spectra"
     else:
@@ -738,7 +746,7 @@ def backproject_setup(tp, dev, interp, backward=False, images=None):
 
         def step(i):
             gr.zero_()
-            tp.tp_backproject_2d_3d_backward(G, proj, rot, grad_weight_vol=GW, grad_proj=gp,
+            tp.tp_backproject_2d_3d_backward(G, proj, rots[i & 1], grad_weight_vol=GW, grad_proj=gp,
                                              grad_weights=gw, grad_rot=gr, scratch=sc,
                                              workspace=ws, **kw)
         # data: spectrum read, y and D written (32 B), images read with y and

@@ -62,9 +62,9 @@
  * sizes (its key and the pose records compared on the device, bit for bit:
  * for example the backward call after the forward call of one step) keeps
  * the brick masks and work units stored there instead of recomputing them;
- * any difference recomputes them.  With cubic interpolation the scatters
- * (backprojection, spectrum gradient) also sort the in-radius output pixels
- * by brick part into lists kept there under the same rule; the forward
+ * any difference recomputes them.  The scatters (backprojection, spectrum
+ * gradient) also sort the in-radius output pixels by brick part into lists
+ * kept there under the same rule; the forward
  * entry points and the pose-gradient-only backward need only the binning,
  * the first part of the workspace (they accept any size that holds it).  So
  * the first 256 bytes of a workspace that is new to the library, or whose
@@ -72,7 +72,7 @@
  * needs no initialisation): memory recycled by an allocator can hold the
  * key and poses of an old workspace but other data in its masks.  It must
  * not be used by two calls that can run at the same time (one workspace
- * per stream).  A cubic scatter call handles fewer than 2^31 output pixels
+ * per stream).  A scatter call handles fewer than 2^31 output pixels
  * (B * P * N * (N/2+1)); larger ones fail with TP_ERR_SHAPE.
  *
  * Errors.  Each call returns a tp_status.  Argument errors are detected
@@ -331,9 +331,9 @@ tp_status tp_hermitian_x0(float *spec, float *weight, int B, int N, int dim, voi
  * Bytes of workspace the 3D entry points need for a volume batch Bv, batch
  * B (Bv is 1 or B), P poses per batch element, volume box Nv, image box N
  * and the interpolation of opts: enough for every 3D entry point on these
- * sizes (the backward uses it for both of its passes).  With cubic
- * interpolation this includes 4 bytes per output pixel (B * P * N *
- * (N/2+1)) for the scatter's sample lists.  Returns 0 for invalid sizes.
+ * sizes (the backward uses it for both of its passes).  This includes
+ * 12 bytes per output pixel (B * P * N * (N/2+1)) for the scatters' sample
+ * lists.  Returns 0 for invalid sizes.
  */
 size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts);
 

@@ -228,7 +228,7 @@ def test_workspace_size_query(tp):
     grow = tp.tp_workspace_bytes(1, 1, 8, 32, "cubic", N=64) - small
     assert grow >= 4 * 8 * (64 * 33 - 32 * 17)
     lin = tp.tp_workspace_bytes(1, 1, 8, 32, "linear")
-    assert lin == tp.tp_workspace_bytes(1, 1, 8, 32, "linear", N=64) < small
+    assert 0 < lin < tp.tp_workspace_bytes(1, 1, 8, 32, "linear", N=64)
 
 
 def test_binding_rejects_cpu_tensors(tp):

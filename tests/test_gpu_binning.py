@@ -127,3 +127,60 @@ def test_alternating_pose_sets_many_calls(tp, ws):
     rv, _, _ = oracle.project_backward(3, g, vol, R2, shift=t2, need_rot=False, need_shift=False,
                                        **CUBIC)
     assert rel(host(gv), rv) <= ATOMIC_TOL
+
+
+def _bp(tp, proj, R, t, om, ws, **kw):
+    kw = {**CUBIC, **kw}
+    d, w = tp.tp_backproject_2d_3d(dev(proj), dev(R), dev(t), dev(om), Nv=M, workspace=ws, **kw)
+    return host(d), host(w)
+
+
+def test_scatter_sample_lists_kept_and_rebuilt(tp, ws):
+    # The cubic scatters sort the output pixels into lists kept in the
+    # workspace with the binning: reused for the same poses, rebuilt after a
+    # call on other poses, after poses changed in place and for another image
+    # box; a kept list must never serve other poses.
+    rng = np.random.default_rng(8)
+    _, R, t, proj = _problem(8)
+    _, R2, t2, _ = _problem(9)
+    om = rng.uniform(0.5, 1.5, proj.shape).astype(np.float32)
+    ref = oracle.backproject(3, proj, R, shift=t, M=M, weights=om, **CUBIC)
+    for _ in range(2):   # built, then kept
+        d, w = _bp(tp, proj, R, t, om, ws)
+        assert rel(d, ref[0]) <= ATOMIC_TOL and rel(w, ref[1]) <= ATOMIC_TOL
+    vol = crandn(rng, (1, M, M, M // 2 + 1))
+    _fwd(tp, vol, R2, t2, ws)   # other poses: the binning and the lists change
+    d, w = _bp(tp, proj, R, t, om, ws)
+    assert rel(d, ref[0]) <= ATOMIC_TOL and rel(w, ref[1]) <= ATOMIC_TOL
+    # One rotation changed in place between two calls.
+    dR, dt, dp, dom = dev(R), dev(t), dev(proj), dev(om)
+    tp.tp_backproject_2d_3d(dp, dR, dt, dom, Nv=M, workspace=ws, **CUBIC)
+    dR[0, 1] = dR[0, 1] @ torch.tensor([[0.0, 0.0, 1.0], [0.0, 1.0, 0.0], [-1.0, 0.0, 0.0]],
+                                       device="cuda")
+    d, w = tp.tp_backproject_2d_3d(dp, dR, dt, dom, Nv=M, workspace=ws, **CUBIC)
+    ref2 = oracle.backproject(3, proj, host(dR), shift=t, M=M, weights=om, **CUBIC)
+    assert rel(host(d), ref2[0]) <= ATOMIC_TOL and rel(host(w), ref2[1]) <= ATOMIC_TOL
+    # Volume gradient of a smaller image box on the same workspace, then the
+    # original box again.
+    g16 = crandn(rng, (1, P, 16, 9))
+    gv, _, _ = tp.tp_project_3d_2d_backward(dev(g16), dev(vol), dev(R), dev(t), workspace=ws,
+                                            want_rot=False, want_shift=False, **CUBIC)
+    rv, _, _ = oracle.project_backward(3, g16, vol, R, shift=t, need_rot=False,
+                                       need_shift=False, **CUBIC)
+    assert rel(host(gv), rv) <= ATOMIC_TOL
+    d, w = _bp(tp, proj, R, t, om, ws)
+    assert rel(d, ref[0]) <= ATOMIC_TOL and rel(w, ref[1]) <= ATOMIC_TOL
+
+
+def test_scatter_sample_lists_in_a_workspace_of_random_bytes(tp):
+    # Random contents, including the list flags: the key cannot match, so the
+    # binning and the lists are rebuilt.
+    _, R, t, proj = _problem(10)
+    om = np.ones(proj.shape, np.float32)
+    ref = oracle.backproject(3, proj, R, shift=t, M=M, weights=om, **CUBIC)
+    for seed in range(3):
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        n = tp.tp_workspace_bytes(1, 1, P, M, "cubic")
+        ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=gen)
+        d, w = _bp(tp, proj, R, t, om, ws)
+        assert rel(d, ref[0]) <= ATOMIC_TOL and rel(w, ref[1]) <= ATOMIC_TOL
