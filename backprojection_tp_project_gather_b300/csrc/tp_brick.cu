@@ -481,6 +481,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan_units(int nbr, Scratch sc
 // brick, with their geometry copied into shared memory.
 struct UnitTable {
     PoseGeo pose[kUnitPoses];
+    float key[kUnitPoses];             // plane-to-brick-centre distance, relative: small = many samples
+    unsigned short order[kUnitPoses];  // entries of pose[] by increasing key
     unsigned mask[32];   // masks of the batch's chunks
     int base[32];        // table offset of each chunk's first pose
     int nhit;            // entries of pose[]
@@ -508,9 +510,12 @@ __device__ __forceinline__ bool next_unit(const Params &q, const Scratch &sc, in
 // Load the reaching poses of the unit's chunks, from chunk c on, into the
 // table (block-wide): as many whole chunks (at most 32) as fit into its
 // kUnitPoses entries.  Returns the first chunk not loaded; t.nhit holds the
-// number of poses loaded.
+// number of poses loaded.  The warps take the poses in t.order: the planes
+// nearest the brick's centre (the largest sections, the most samples) first,
+// so that the poses left when the first warps run out of work are small ones.
 __device__ __forceinline__ int load_batch(const Params &q, const Scratch &sc, int nbr, int v,
-                                          int brick, int c, int c1, UnitTable &t) {
+                                          int brick, const BrickBox &bx, int c, int c1,
+                                          UnitTable &t) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned *masks = sc.masks + ((size_t)v * nbr + brick) * sc.nchunks;
     if (warp == 0) {
@@ -545,18 +550,37 @@ __device__ __forceinline__ int load_batch(const Params &q, const Scratch &sc, in
             int *dst = reinterpret_cast<int *>(&t.pose[at]);
 #pragma unroll
             for (int k = 0; k < kGeoWords; ++k) dst[k] = src[k];
+            float cn = 0.f, sn = 0.f;
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                cn += g.n[d] * 0.5f * (bx.lo[d] + bx.hi[d]);
+                sn += fabsf(g.n[d]);
+            }
+            t.key[at] = fabsf(cn) / fmaxf(sn, 1e-30f);
         }
+    }
+    __syncthreads();
+    const int nhit = t.nhit;
+    for (int i = threadIdx.x; i < nhit; i += kThreads) {
+        const float ki = t.key[i];
+        int rank = 0;
+        for (int j = 0; j < nhit; ++j) {
+            const float kj = t.key[j];
+            rank += (kj < ki || (kj == ki && j < i)) ? 1 : 0;
+        }
+        t.order[rank] = (unsigned short)i;
     }
     __syncthreads();
     return c + nchunk;
 }
 
-// Next listed pose for the calling warp, or -1 when the list is exhausted.
+// Next listed pose for the calling warp (its entry of t.pose), or -1 when
+// the list is exhausted.
 __device__ __forceinline__ int next_pose(UnitTable &t) {
     int k = 0;
     if ((threadIdx.x & 31) == 0) k = atomicAdd(&t.next, 1);
     k = __shfl_sync(0xffffffffu, k, 0);
-    return k < t.nhit ? k : -1;
+    return k < t.nhit ? (int)t.order[k] : -1;
 }
 
 __device__ __forceinline__ bool stored(int x, int y, int z, int half) {
@@ -862,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kPlain ? 3 : 2)
         const BrickBox bx = brick_box(rec.x, nb);
         stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol, q.dbg);
         for (int c0 = rec.y; c0 < rec.z;) {
-            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
+            c0 = load_batch(q, sc, nbr, v, rec.x, bx, c0, rec.z, s_tab);
             for (int k; (k = next_pose(s_tab)) >= 0;) {
                 const PoseGeo &g = s_tab.pose[k];
                 const size_t ob = (size_t)g.bp * q.plane;
@@ -956,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
         const BrickBox bx = brick_box(rec.x, nb);
         stage<CUBIC>(q.src + (size_t)v * q.src_stride, q.M, q.Xs, bx, s_vol, q.dbg);
         for (int c0 = rec.y; c0 < rec.z;) {
-            c0 = load_batch(q, sc, nbr, v, rec.x, c0, rec.z, s_tab);
+            c0 = load_batch(q, sc, nbr, v, rec.x, bx, c0, rec.z, s_tab);
             for (int k; (k = next_pose(s_tab)) >= 0;) {
                 const PoseGeo &g = s_tab.pose[k];
                 float acc[8];
