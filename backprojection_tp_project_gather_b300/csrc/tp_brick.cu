@@ -375,6 +375,10 @@ __device__ __forceinline__ float geo_reach(const int4 *geo, int pid) {
 // records every lane of the warp reads at once.
 __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch sc) {
     if (*sc.changed == 0u) return;
+    // The chunk's 32 reach records, each lane loading one, so that their
+    // loads are in flight together.
+    __shared__ ReachGeo s_rg[8][32];
+    ReachGeo *const rgs = s_rg[threadIdx.x >> 5];
     const int nbr = nb * nb * nb;
     const int nchunks = sc.nchunks;
     const int groups = (nbr + 31) / 32;
@@ -397,16 +401,26 @@ __global__ void __launch_bounds__(256) k_brick_masks(Params q, int nb, Scratch s
             e2 += e * e;
         }
         const int np = min(32, Pv - c * 32);
+        __syncwarp();   // the previous chunk's records have been read
+        if (lane < np) {
+            const int pid = pose_id(q, v, c * 32 + lane);
+            if (TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) {
+                const ReachGeo *rg = sc.reach + pid;
+                rgs[lane].n = __ldg(&rg->n);
+                rgs[lane].v = __ldg(&rg->v);
+                rgs[lane].r = __ldg(&rg->r);
+            } else {
+                rgs[lane].r = make_float4(-1.f, 0.f, 0.f, 0.f);   // reaches nothing
+            }
+        }
+        __syncwarp();
         unsigned m = 0u;
         for (int k = 0; k < np; ++k) {
-            const int pid = pose_id(q, v, c * 32 + k);
-            if (!TP_CHECK(q.dbg, pid >= 0 && pid < q.B * q.P, 8)) continue;
-            const ReachGeo *rg = sc.reach + pid;
-            const float4 rr = __ldg(&rg->r);
+            const float4 rr = rgs[k].r;
             if (e2 > rr.x) continue;
             bool hit = rr.y != 0.f;   // degenerate poses reach every brick within reach
             if (!hit) {
-                const float4 nn = __ldg(&rg->n), vv = __ldg(&rg->v);
+                const float4 nn = rgs[k].n, vv = rgs[k].v;
                 const float cn = nn.x * cen[0] + nn.y * cen[1] + nn.z * cen[2];
                 const float cv = vv.x * cen[0] + vv.y * cen[1] + vv.z * cen[2];
                 hit = fabsf(cn) <= nn.w * 1.0001f + 1e-6f && cv + vv.w >= -0.01f;
