@@ -1604,18 +1604,20 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIG
     }
 }
 
-// Linear: the same warp-private octant tiles, here 8^3 plus the one-voxel
-// halo of the taps x0, x0 + 1, stored as 9 x 10 x 10 complex words (x and y
-// pitches 10: the 8 taps of one sample fall into 8 distinct bank pairs).  A
-// round spreads four queued samples at once, the lanes of group g = lane / 8
+// Linear: warp-private tiles of one z-half part (8 x 8 x 4 tap origins) plus
+// the one-voxel halo of the taps x0, x0 + 1, stored as 9 x 9 x 5 words with x
+// and y pitches 10 (the 8 taps of one sample fall into 8 distinct bank
+// pairs); the tiles and queue of a warp take 7.7 KB, so 32 warps share an SM.
+// A round spreads four queued samples at once, the lanes of group g = lane / 8
 // taking the 8 taps of sample r + R g (R = rounds of the queue).  Samples R
 // slots apart rarely share a voxel; a round in which two of them do (their
-// octant coordinates, exchanged by shuffles, differ by less than 2 on every
+// tile coordinates, exchanged by shuffles, differ by less than 2 on every
 // axis) is spread one sample at a time, so the plain read-add-write never
 // races.
-constexpr int kLS = kOct + 1;               // octant + linear halo
+constexpr int kLS = kOct + 1;               // part + linear halo in x and y
+constexpr int kLZ = kOct / 2 + 1;           // the same in z
 constexpr int kLPX = 10, kLPY = 10;         // x and y pitches of the tile
-constexpr int kLElems = kLS * kLPY * kLPX;  // complex words of the tile
+constexpr int kLElems = kLZ * kLPY * kLPX;  // complex words of the tile
 constexpr int kLQW = 9;                     // floats per queued weight row (odd)
 
 struct LinQueue {
@@ -1634,7 +1636,7 @@ struct LinLayout {
 };
 
 template <bool WEIGHTS>
-__global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 6)
+__global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, 8)
     k_brick_scatter_linear(Params q, int nb, Scratch sc, const float2 *__restrict__ img,
                            const float *__restrict__ omega, float2 *__restrict__ dst,
                            float *__restrict__ wdst) {
@@ -1649,8 +1651,8 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
     const int toff = jx + kLPX * (jy + kLPY * jz);
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int nitems = (int)__ldg(sc.counters + 4 * nvol + v);
-    const int4 *items = sc.litems + (size_t)v * sc.itemcap;
+    const int nitems = (int)__ldg(sc.counters + 5 * nvol + v);   // z-half parts
+    const int4 *items = sc.litems + (size_t)(nvol + v) * sc.itemcap;
     const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
@@ -1664,11 +1666,11 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= nitems) break;
-        const int4 it = __ldg(items + item);   // first entry, count, brick, octant
+        const int4 it = __ldg(items + item);   // first entry, count, brick, part
         if (!TP_CHECK(q.dbg, it.z >= 0 && it.z < nbr && it.y > 0 && it.y <= kListChunk &&
                                  (unsigned)it.x + (unsigned)it.y <= entries, 8))
             continue;
-        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w);
+        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w, kOct / 2);
         for (int r0 = 0; r0 < it.y; r0 += 32) {
             // Each lane sets up one sample of the list and queues it.
             bool own = r0 + lane < it.y;
@@ -1688,10 +1690,10 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
                 l[a] = split_coord(p[a], t) - ob.o[a];
                 Stencil<false>::weights(t, w[a]);
             }
-            // The list put the sample in this octant (same position arithmetic);
+            // The list put the sample in this part (same position arithmetic);
             // the test keeps every tile access in range whatever happens.
             const bool inbox = (unsigned)l[0] < (unsigned)kOct && (unsigned)l[1] < (unsigned)kOct &&
-                               (unsigned)l[2] < (unsigned)kOct;
+                               (unsigned)l[2] < (unsigned)(kOct / 2);
             own = own && TP_CHECK(q.dbg, inbox, 4) && inbox;
             const unsigned mask = __ballot_sync(0xffffffffu, own);
             if (own) {
@@ -1734,7 +1736,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, WEIGHTS ? 4 : 
         }
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0], y0 = ob.o[1], z0 = ob.o[2];
-        for (int e = lane; e < kLS * kLS * kLS; e += 32) {
+        for (int e = lane; e < kLS * kLS * kLZ; e += 32) {
             const int lx = e % kLS, ly = (e / kLS) % kLS, lz = e / (kLS * kLS);
             const int k = (lz * kLPY + ly) * kLPX + lx;
             const float2 cv = acc[k];
