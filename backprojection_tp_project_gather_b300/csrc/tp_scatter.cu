@@ -24,8 +24,9 @@ namespace {
 // (F(n) = V[n] for n_x >= 0, conj(V[-n]) for n_x < 0, zero outside the
 // stored range) and cut into kTile x kTile tiles.  A sample belongs to the
 // tile that holds floor(p), so its stencil lies in the tile plus a halo of
-// LO + HI.  One block per output image; its warps take the image's tiles
-// from a counter in shared memory.  A warp enumerates the image's pixels
+// LO + HI.  kSplit blocks per output image, each with an interleaved quarter
+// of its tiles; a block's warps take their tiles from a counter in shared
+// memory.  A warp enumerates the image's pixels
 // whose sample position falls in its tile (rows from the inverse of
 // [a b], each row's qx interval from the two slab constraints, a warp
 // prefix sum packing the candidates into 32-lane rounds) and spreads the
@@ -40,6 +41,7 @@ namespace {
 // conjugated at -n).
 constexpr int kTile = 16;
 constexpr int kTileWarps = 4;
+constexpr int kSplit = 4;   // blocks per image: shorter blocks, a smaller last wave
 constexpr float kTileMargin = 0.01f;
 
 // The warp's tile.  Cubic: 20 x 20 words in 4 x 4 tiles of 16 complex words,
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
         ry[i] = (i + (lane >> 2)) & 3;
     }
 
-    const int bp = blockIdx.x;
+    // kSplit blocks per image, block s taking the image's tiles s, s + kSplit, ...
+    const int bp = blockIdx.x / kSplit, sub = blockIdx.x - bp * kSplit;
     const int b = bp / q.P, pi = bp - b * q.P;
     const Pose<2> ps = load_pose<2>(q, b, pi);
     const float a0 = ps.a[0], a1 = ps.a[1], b0 = ps.b[0], b1 = ps.b[1];   // p = a qx + b qy
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
     for (;;) {
         int t = 0;
         if (lane == 0) t = atomicAdd(&s_next, 1);
-        t = __shfl_sync(0xffffffffu, t, 0);
+        t = __shfl_sync(0xffffffffu, t, 0) * kSplit + sub;
         if (t >= nt * nt) break;
         const int ox = (tlo + t % nt) * kTile, oy = (tlo + t / nt) * kTile;
         const float lo0 = (float)ox - kTileMargin, hi0 = (float)(ox + kTile) + kTileMargin;
@@ -339,7 +342,7 @@ cudaError_t launch_scatter2d_tiles(const Params &q, const float2 *img, float2 *d
     auto kern = k_scatter2d_tiles<CUBIC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)images, 32 * kTileWarps, smem, st>>>(q, img, dst);
+    kern<<<(unsigned)(images * kSplit), 32 * kTileWarps, smem, st>>>(q, img, dst);
     return cudaGetLastError();
 }
 
