@@ -57,6 +57,8 @@ def parse_args():
                          "the float64 volume gradient of the whole 256^3 spectrum)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step's launches one by one instead of replaying a CUDA graph")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary figures of the headline line (2D step, box-256 "
                          "backprojection)")
@@ -465,6 +467,17 @@ def run_ours(args):
         step(i=i)
     torch.cuda.synchronize()
 
+    # The step's launches (zeroing, forward, volume gradient: all on the
+    # device, the binning decisions included) are captured once as a CUDA
+    # graph and replayed every timed step; the pose estimates are copied in
+    # before each replay, untimed.  --eager times the launches one by one.
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(b=bufs[0])
+        torch.cuda.synchronize()
+
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
@@ -472,19 +485,32 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.zero_()                                            # L2 flush, untimed
-            step(events[i], i=args.warmup + i)
+            if graph is None:
+                step(events[i], i=args.warmup + i)
+            else:
+                bufs[0]["rot"].copy_(pose_sets[(args.warmup + i) & 1][0])
+                bufs[0]["shift"].copy_(pose_sets[(args.warmup + i) & 1][1])
+                events[i][0].record(stream)
+                graph.replay()
+                events[i][3].record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    step_ms = np.array([events[i][0].elapsed_time(events[i][3]) for i in range(args.steps)])
 
     # Per step: zeroing of the gradients, the forward with the L2 term (output,
-    # residual gradient, rotation and shift gradients), the volume gradient,
-    # and the whole step.
-    seg = np.array([[events[i][0].elapsed_time(events[i][1]),
-                     events[i][1].elapsed_time(events[i][2]),
-                     events[i][2].elapsed_time(events[i][3])] for i in range(args.steps)])
-    step_ms = np.array([events[i][0].elapsed_time(events[i][3]) for i in range(args.steps)])
+    # residual gradient, rotation and shift gradients), the volume gradient:
+    # from launches one by one (a replayed graph has no events inside).
+    nb = min(args.steps, 20)
+    bevents = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    for i in range(nb):
+        flush.zero_()
+        step(bevents[i], i=args.warmup + args.steps + i)
+    torch.cuda.synchronize()
+    seg = np.array([[bevents[i][0].elapsed_time(bevents[i][1]),
+                     bevents[i][1].elapsed_time(bevents[i][2]),
+                     bevents[i][2].elapsed_time(bevents[i][3])] for i in range(nb)])
     total_ms = max_over_ranks(step_ms.sum(), dist, dev)
     samples = P * N * (N // 2 + 1)
     value = whole_job_rate(world, samples, args.steps, total_ms)
@@ -617,7 +643,10 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded Gaussian-blob volume, uniform SO(3) poses, noisy targets)",
-            "config": config_dict(w, P),
+            "config": {**config_dict(w, P),
+                       "launch": ("step launches one by one" if args.eager else
+                                  "step captured once as a CUDA graph, replayed every step "
+                                  "(breakdown_ms from launches one by one)")},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic,
