@@ -1433,6 +1433,34 @@ __device__ __forceinline__ float2 lds_f2(unsigned a) {
 __device__ __forceinline__ void sts_f2(unsigned a, float2 v) {
     asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
 }
+// The same, made only when p is set (the partial rounds' lanes without a
+// sample make no shared-memory access at all).
+__device__ __forceinline__ float2 lds_f2_if(unsigned a, bool p) {
+    float2 v = make_float2(0.f, 0.f);
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %3, 0;\n @q ld.shared.v2.f32 {%0, %1}, [%2];\n}"
+                 : "+f"(v.x), "+f"(v.y)
+                 : "r"(a), "r"((unsigned)p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_f2_if(unsigned a, float2 v, bool p) {
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %3, 0;\n @q st.shared.v2.f32 [%0], {%1, %2};\n}"
+                 ::"r"(a), "f"(v.x), "f"(v.y), "r"((unsigned)p)
+                 : "memory");
+}
+__device__ __forceinline__ float lds_f1_if(unsigned a, bool p) {
+    float v = 0.f;
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.shared.f32 %0, [%1];\n}"
+                 : "+f"(v)
+                 : "r"(a), "r"((unsigned)p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_f1_if(unsigned a, float v, bool p) {
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.shared.f32 [%0], %1;\n}"
+                 ::"r"(a), "f"(v), "r"((unsigned)p)
+                 : "memory");
+}
 __device__ __forceinline__ float lds_f1(unsigned a) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
@@ -1444,10 +1472,12 @@ __device__ __forceinline__ void sts_f1(unsigned a, float v) {
 
 // Every lane spreads its sample into the warp's tile (and weight tile):
 // first tap (l0, l1, l2) in tile coordinates (each in [0, 8), l2 in
-// [0, OZ)), fraction t of p, value c = conj(phase) * y, weight om; a lane
-// with !act adds zeros to in-range words.  tile and wtile are shared-memory
-// byte addresses.  Call with the whole warp.
-template <bool WEIGHTS>
+// [0, OZ)), fraction t of p, value c = conj(phase) * y, weight om.  A lane
+// with !act adds zeros to in-range words, or, with PARTIAL, makes no access
+// (the last round of an item; its predicated accesses cost an instruction
+// each).  tile and wtile are shared-memory byte addresses.  Call with the
+// whole warp.
+template <bool WEIGHTS, bool PARTIAL>
 __device__ __forceinline__ void spread_cubic(int l0, int l1, int l2, const float (&tf)[3], float2 c,
                                              float om, unsigned tile, unsigned wtile, bool act) {
     const int lane = threadIdx.x & 31;
@@ -1498,15 +1528,33 @@ __device__ __forceinline__ void spread_cubic(int l0, int l1, int l2, const float
             const unsigned b0 = woy[sy] + woz[sg], b1 = woy[sy] + woz[sg + 2];
 #pragma unroll
             for (int sx = 0; sx < 4; ++sx) {
-                float2 v0 = lds_f2(a0 + ox[sx]), v1 = lds_f2(a1 + ox[sx]);
+                float2 v0, v1;
+                if (PARTIAL) {
+                    v0 = lds_f2_if(a0 + ox[sx], act);
+                    v1 = lds_f2_if(a1 + ox[sx], act);
+                } else {
+                    v0 = lds_f2(a0 + ox[sx]);
+                    v1 = lds_f2(a1 + ox[sx]);
+                }
                 cfma(r[0][sx], c0, v0);
                 cfma(r[0][sx], c1, v1);
-                sts_f2(a0 + ox[sx], v0);
-                sts_f2(a1 + ox[sx], v1);
+                if (PARTIAL) {
+                    sts_f2_if(a0 + ox[sx], v0, act);
+                    sts_f2_if(a1 + ox[sx], v1, act);
+                } else {
+                    sts_f2(a0 + ox[sx], v0);
+                    sts_f2(a1 + ox[sx], v1);
+                }
                 if (WEIGHTS) {
-                    const float u0 = lds_f1(b0 + wox[sx]), u1 = lds_f1(b1 + wox[sx]);
-                    sts_f1(b0 + wox[sx], fmaf(r[0][sx], w0, u0));
-                    sts_f1(b1 + wox[sx], fmaf(r[0][sx], w1, u1));
+                    if (PARTIAL) {
+                        const float u0 = lds_f1_if(b0 + wox[sx], act), u1 = lds_f1_if(b1 + wox[sx], act);
+                        sts_f1_if(b0 + wox[sx], fmaf(r[0][sx], w0, u0), act);
+                        sts_f1_if(b1 + wox[sx], fmaf(r[0][sx], w1, u1), act);
+                    } else {
+                        const float u0 = lds_f1(b0 + wox[sx]), u1 = lds_f1(b1 + wox[sx]);
+                        sts_f1(b0 + wox[sx], fmaf(r[0][sx], w0, u0));
+                        sts_f1(b1 + wox[sx], fmaf(r[0][sx], w1, u1));
+                    }
                 }
                 // The next steps' taps may be other lanes' words of these steps.
                 __syncwarp();
@@ -1572,7 +1620,10 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIG
                                (unsigned)l2 < (unsigned)OL::OZ;
             act = act && TP_CHECK(q.dbg, inbox, 4) && inbox;
             if (act && q.shift) cv = cmul_conj_a(shift_phase(qx, qy, Bv.z, Bv.w, q.fN, q.invN), cv);
-            spread_cubic<WEIGHTS>(l0, l1, l2, t, cv, om, tile, wtile, act);
+            if (r + 32 <= it.y)
+                spread_cubic<WEIGHTS, false>(l0, l1, l2, t, cv, om, tile, wtile, act);
+            else   // the item's last, partly filled round
+                spread_cubic<WEIGHTS, true>(l0, l1, l2, t, cv, om, tile, wtile, act);
         }
         __syncwarp();
         // Fold the tile into the stored half-spectrum and clear it.
