@@ -15,11 +15,11 @@
 //    shared memory with one branch-free code path (for cubic in a tiled
 //    layout and a per-lane tap order free of bank conflicts);
 //  - scatter (backprojection, spectrum gradient): every warp owns a private
-//    tile for one octant of a brick plus the stencil halo, spreads its
-//    samples into it with plain read-add-write, and adds the tile to the
-//    stored half-spectrum once per work item (Friedel positions conjugated
-//    at -n), with vector atomics because halos of neighbouring octants and
-//    other work items overlap.  The scatters read their samples from lists
+//    tile for one part of a brick (an x and y half and a z quarter) plus the
+//    stencil halo, spreads its samples into it with plain read-add-write,
+//    and adds the tile to the stored half-spectrum once per work item
+//    (Friedel positions conjugated at -n), with vector atomics because halos
+//    of neighbouring parts and other work items overlap.  The scatters read their samples from lists
 //    of the output pixels sorted by brick part (a counting sort over the
 //    pixels).
 //
@@ -118,8 +118,8 @@ struct Scratch {
     unsigned *key;        // BinKey of the binning held in the workspace
     unsigned *changed;    // set by k_pose_geometry when key or geometry differ
     unsigned *lflag;      // [0] the sample lists fit the binning held, [1] this call builds them
-    unsigned *counters;   // [6][Bsrc]: work counters of the three main kernels, unit counts,
-                          // octant and z-half item counts of the sample lists
+    unsigned *counters;   // [5][Bsrc]: work counters of the three main kernels, unit counts,
+                          // item counts of the sample lists
     int4 *geo;            // B*P pose records of kGeoVec words
     float4 *pose8;        // B*P poses: (a0, a1, a2, b0), (b1, b2, sx, sy)
     ReachGeo *reach;      // B*P poses, for the brick-mask pass
@@ -128,11 +128,11 @@ struct Scratch {
     int4 *units;          // [Bsrc][bricks * chunks] work units (brick, first chunk, end chunk)
     // Sample lists (cubic scatter only; null in a forward-only workspace).
     unsigned *lcount;     // [Bsrc][bricks * kParts] samples per brick part, then fill cursors
-    int4 *lbrick;         // [Bsrc][bricks] samples, octant items, z-half items; then their sums before
-    int4 *litems;         // [2][Bsrc][itemcap] items: (first entry, count, brick, box)
+    int2 *lbrick;         // [Bsrc][bricks] samples and items, then their sums before
+    int4 *litems;         // [Bsrc][itemcap] items: (first entry, count, brick, part box)
     unsigned *llist;      // B*P*plane entries: output pixel index (b * P + p) * plane + row * Xo + kx
     int2 *lkey;           // B*P*plane: each in-radius pixel's key and place in the key's list
-    int4 *lblock;         // [Bsrc][brick blocks] the sums of k_list_sums' blocks
+    int2 *lblock;         // [Bsrc][brick blocks] the sums of k_list_sums' blocks
     int nchunks;          // 32-pose chunks per volume
     int itemcap;          // items per volume and kind
 };
@@ -1065,9 +1065,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_brick_pose_grad(Params q, int n
 // Sample lists: every in-radius output pixel whose floor(p) lies in the
 // brick grid, binned by brick part with a counting sort (count, scan, fill).
 // A brick has kParts parts, its x and y halves times its four z quarters,
-// numbered (z half, y half, x half, z quarter within the half): the two
-// parts of an octant are consecutive, and part >> 1 is the octant's index
-// for octant_box.  The lists depend on the poses alone, so a call keeps the
+// numbered (z half, y half, x half, z quarter within the half), so the two
+// parts of an octant are consecutive; a work item names its part's box by
+// 4 z quarter + 2 y half + x half (part_box).  The lists depend on the poses alone, so a call keeps the
 // ones held in the workspace when its binning is unchanged (k_pose_geometry
 // clears lflag[0] whenever it is not).
 constexpr int kParts = 16;
@@ -1247,40 +1247,34 @@ __global__ void __launch_bounds__(256) k_list_fill(Params q, Scratch sc) {
     }
 }
 
-// Samples, octant items and z-half items of every brick, and their sums
-// before it within its block of kSumBlock bricks (the block's totals go to
-// lblock).  Grid: (blocks of bricks, volumes).
+// Samples and items (parts with n samples give ceil(n / kListChunk) items)
+// of every brick, and their sums before it within its block of kSumBlock
+// bricks (the block's totals go to lblock).  Grid: (blocks of bricks,
+// volumes).
 constexpr int kSumBlock = 256;
 
 __global__ void __launch_bounds__(kSumBlock) k_list_sums(int nbr, Scratch sc) {
     if (sc.lflag[1] == 0u) return;
-    __shared__ int s_w[3][kSumBlock / 32];
+    __shared__ int s_w[2][kSumBlock / 32];
     const int v = blockIdx.y, j = blockIdx.x * kSumBlock + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x[3] = {0, 0, 0};
+    int x[2] = {0, 0};
     if (j < nbr) {
         const unsigned *cnt = sc.lcount + ((size_t)v * nbr + j) * kParts;
-        unsigned c[kParts];
 #pragma unroll
         for (int k = 0; k < kParts; k += 4) {
             const uint4 u = *reinterpret_cast<const uint4 *>(cnt + k);
-            c[k] = u.x;
-            c[k + 1] = u.y;
-            c[k + 2] = u.z;
-            c[k + 3] = u.w;
-        }
+            const unsigned c[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int k = 0; k < kParts; ++k) {
-            x[0] += (int)c[k];
-            x[2] += (int)((c[k] + kListChunk - 1) / kListChunk);
+            for (int i = 0; i < 4; ++i) {
+                x[0] += (int)c[i];
+                x[1] += (int)((c[i] + kListChunk - 1) / kListChunk);
+            }
         }
-#pragma unroll
-        for (int o = 0; o < kParts / 2; ++o)
-            x[1] += (int)((c[2 * o] + c[2 * o + 1] + kListChunk - 1) / kListChunk);
     }
-    int incl[3] = {x[0], x[1], x[2]};
+    int incl[2] = {x[0], x[1]};
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < 2; ++k) {
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, incl[k], o);
@@ -1289,22 +1283,21 @@ __global__ void __launch_bounds__(kSumBlock) k_list_sums(int nbr, Scratch sc) {
         if (lane == 31) s_w[k][warp] = incl[k];
     }
     __syncthreads();
-    int before[3] = {0, 0, 0};
+    int before[2] = {0, 0};
 #pragma unroll
-    for (int k = 0; k < 3; ++k)
+    for (int k = 0; k < 2; ++k)
         for (int w = 0; w < warp; ++w) before[k] += s_w[k][w];
     if (j < nbr)
         sc.lbrick[(size_t)v * nbr + j] =
-            make_int4(before[0] + incl[0] - x[0], before[1] + incl[1] - x[1], before[2] + incl[2] - x[2], 0);
+            make_int2(before[0] + incl[0] - x[0], before[1] + incl[1] - x[1]);
     if (threadIdx.x == kSumBlock - 1)
-        sc.lblock[(size_t)v * gridDim.x + blockIdx.x] =
-            make_int4(before[0] + incl[0], before[1] + incl[1], before[2] + incl[2], 0);
+        sc.lblock[(size_t)v * gridDim.x + blockIdx.x] = make_int2(before[0] + incl[0], before[1] + incl[1]);
 }
 
-// Eight threads per brick, one per octant: the list offsets of the octant's
-// two parts (the counts become the fill cursors) and its items -- a part or
-// octant with n samples gives ceil(n / kListChunk) items of consecutive
-// entries, in brick order (octant items, then z-half items, by part).
+// Eight threads per brick, each taking two consecutive parts (an octant's):
+// their list offsets (the counts become the fill cursors) and their items --
+// a part with n samples gives ceil(n / kListChunk) items of consecutive
+// entries, in brick and part order.
 __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvol,
                                                     long long vol_entries) {
     const int id = (blockIdx.x * 256 + threadIdx.x) >> 3, o = threadIdx.x & 7;
@@ -1312,13 +1305,12 @@ __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvo
     const int v = id / nbr, j = id - v * nbr;
     // The brick's sums before it: within its block of bricks, plus the
     // totals of the volume's blocks before that one.
-    int4 base = sc.lbrick[id];
+    int2 base = sc.lbrick[id];
     const int nblk = (nbr + kSumBlock - 1) / kSumBlock;
     for (int b = 0; b < j / kSumBlock; ++b) {
-        const int4 t = sc.lblock[(size_t)v * nblk + b];
+        const int2 t = sc.lblock[(size_t)v * nblk + b];
         base.x += t.x;
         base.y += t.y;
-        base.z += t.z;
     }
     unsigned *cnt = sc.lcount + (size_t)id * kParts;
     unsigned c[kParts];
@@ -1330,16 +1322,15 @@ __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvo
         c[k + 2] = u.z;
         c[k + 3] = u.w;
     }
-    // Entries and items of the octants before this one.
+    // Entries and items of the parts before this thread's two.
     unsigned first = (unsigned)((long long)v * vol_entries) + (unsigned)base.x;
-    int oi = base.y, hi = base.z;
-    unsigned c0 = 0u, c1 = 0u;   // this octant's two parts
+    int it = base.y;
+    unsigned c0 = 0u, c1 = 0u;   // this thread's two parts
 #pragma unroll
     for (int k = 0; k < kParts / 2; ++k) {
         if (k < o) {
             first += c[2 * k] + c[2 * k + 1];
-            oi += (int)((c[2 * k] + c[2 * k + 1] + kListChunk - 1) / kListChunk);
-            hi += (int)((c[2 * k] + kListChunk - 1) / kListChunk) +
+            it += (int)((c[2 * k] + kListChunk - 1) / kListChunk) +
                   (int)((c[2 * k + 1] + kListChunk - 1) / kListChunk);
         }
         if (k == o) {
@@ -1350,24 +1341,18 @@ __global__ void __launch_bounds__(256) k_list_items(int nbr, Scratch sc, int nvo
     __syncwarp(0xffu << (threadIdx.x & 24));   // the brick's 8 lanes have read its counts
     cnt[2 * o] = first;   // fill cursors
     cnt[2 * o + 1] = first + c0;
-    int4 *oct_items = sc.litems + (size_t)v * sc.itemcap;
-    int4 *half_items = sc.litems + (size_t)(nvol + v) * sc.itemcap;
-    for (unsigned i = 0; i < c0 + c1; i += kListChunk, ++oi)
-        if (oi < sc.itemcap)   // never false: itemcap bounds the items
-            oct_items[oi] = make_int4((int)(first + i), (int)min((unsigned)kListChunk, c0 + c1 - i), j, o);
+    int4 *items = sc.litems + (size_t)v * sc.itemcap;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int k = 2 * o + h;
         const int zq = ((k >> 3) << 1) | (k & 1), xy = (k >> 1) & 3;
         const unsigned n = h ? c1 : c0, f = h ? first + c0 : first;
-        for (unsigned i = 0; i < n; i += kListChunk, ++hi)
-            if (hi < sc.itemcap)
-                half_items[hi] = make_int4((int)(f + i), (int)min((unsigned)kListChunk, n - i), j, zq * 4 + xy);
+        for (unsigned i = 0; i < n; i += kListChunk, ++it)
+            if (it < sc.itemcap)   // never false: itemcap bounds the items
+                items[it] = make_int4((int)(f + i), (int)min((unsigned)kListChunk, n - i), j, zq * 4 + xy);
     }
-    if (j == nbr - 1 && o == kParts / 2 - 1) {   // the volume's last items: their counts
-        sc.counters[4 * nvol + v] = (unsigned)min(oi, sc.itemcap);
-        sc.counters[5 * nvol + v] = (unsigned)min(hi, sc.itemcap);
-    }
+    if (j == nbr - 1 && o == kParts / 2 - 1)   // the volume's last items: their count
+        sc.counters[4 * nvol + v] = (unsigned)min(it, sc.itemcap);
 }
 
 // Cubic: one lane spreads one sample, 32 samples of the item's list per
@@ -1393,9 +1378,10 @@ constexpr int kCT = 12;                    // (x, y) extent of a tile layer: 3 x
 constexpr int kCLayer = kCT * kCT;         // complex words of one z layer
 constexpr int kCWPair = 2 * kCLayer;       // weight words of a pair of z layers
 
-// A work item covers one part of a brick: an octant (8^3), or, with the
-// weight spectrum, half of one in z (8 x 8 x 4), so that the two tiles of a
-// warp fit 16 warps into an SM's shared memory.
+// A work item covers one list part of a brick: half an octant in z
+// (8 x 8 x 4 tap origins).  Its tile (12 x 12 x 7 complex words, 8.1 KB) lets
+// 24 warps share an SM; with the weight spectrum the two tiles take 12.7 KB
+// and 16 warps do.
 template <bool WEIGHTS>
 struct OctLayout {
     static constexpr int WARPS = 4;                  // warps per block (blocks only share an SM)
@@ -1410,12 +1396,13 @@ struct OctLayout {
     static_assert(TILE % 16 == 0 && WTILE % 16 == 0, "16-byte aligned tiles");
 };
 
-// Box of part `oct` of a brick: x and y halves from bits 0 and 1, the z
-// slice of depth oz from the bits above.
-__device__ __forceinline__ BrickBox octant_box(const BrickBox &bx, int oct, int oz = kOct) {
+// Box of list part `w` of a brick: x and y halves from bits 0 and 1, the z
+// quarter from the bits above.
+__device__ __forceinline__ BrickBox part_box(const BrickBox &bx, int w) {
+    constexpr int kQ = kOct / 2;   // z extent of a part
     BrickBox ob;
-    const int off[3] = {kOct * (oct & 1), kOct * ((oct >> 1) & 1), oz * (oct >> 2)};
-    const int ext[3] = {kOct, kOct, oz};
+    const int off[3] = {kOct * (w & 1), kOct * ((w >> 1) & 1), kQ * (w >> 2)};
+    const int ext[3] = {kOct, kOct, kQ};
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
         ob.o[d] = bx.o[d] + off[d];
@@ -1578,8 +1565,8 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIG
     const unsigned wtile = (unsigned)__cvta_generic_to_shared(wacc);
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int nitems = (int)__ldg(sc.counters + (OL::OZ == kOct ? 4 : 5) * nvol + v);
-    const int4 *items = sc.litems + (size_t)((OL::OZ == kOct ? 0 : nvol) + v) * sc.itemcap;
+    const int nitems = (int)__ldg(sc.counters + 4 * nvol + v);
+    const int4 *items = sc.litems + (size_t)v * sc.itemcap;
     const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
@@ -1591,11 +1578,11 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIG
         if (lane == 0) item = (int)atomicAdd(sc.counters + 2 * nvol + v, 1u);
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item >= nitems) break;
-        const int4 it = __ldg(items + item);   // first entry, count, brick, box
+        const int4 it = __ldg(items + item);   // first entry, count, brick, part
         if (!TP_CHECK(q.dbg, it.z >= 0 && it.z < nbr && it.y > 0 && it.y <= kListChunk &&
                                  (unsigned)it.x + (unsigned)it.y <= entries, 8))
             continue;
-        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w, OL::OZ);
+        const BrickBox ob = part_box(brick_box(it.z, nb), it.w);
         for (int r = 0; r < it.y; r += 32) {
             bool act = r + lane < it.y;
             const unsigned e = act ? __ldg(sc.llist + it.x + r + lane) : 0u;
@@ -1702,8 +1689,8 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, 8)
     const int toff = jx + kLPX * (jy + kLPY * jz);
     const int half = q.M >> 1;
     const int v = blockIdx.z, nvol = gridDim.z, nbr = nb * nb * nb;
-    const int nitems = (int)__ldg(sc.counters + 5 * nvol + v);   // z-half parts
-    const int4 *items = sc.litems + (size_t)(nvol + v) * sc.itemcap;
+    const int nitems = (int)__ldg(sc.counters + 4 * nvol + v);
+    const int4 *items = sc.litems + (size_t)v * sc.itemcap;
     const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     float2 *Vd = dst + (size_t)v * q.src_stride;
     float *Wd = WEIGHTS && wdst ? wdst + (size_t)v * q.src_stride : nullptr;
@@ -1721,7 +1708,7 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, 8)
         if (!TP_CHECK(q.dbg, it.z >= 0 && it.z < nbr && it.y > 0 && it.y <= kListChunk &&
                                  (unsigned)it.x + (unsigned)it.y <= entries, 8))
             continue;
-        const BrickBox ob = octant_box(brick_box(it.z, nb), it.w, kOct / 2);
+        const BrickBox ob = part_box(brick_box(it.z, nb), it.w);
         for (int r0 = 0; r0 < it.y; r0 += 32) {
             // Each lane sets up one sample of the list and queues it.
             bool own = r0 + lane < it.y;
@@ -1838,7 +1825,7 @@ Layout layout(const Params &q, bool cubic) {
     const size_t poses = (size_t)q.B * q.P;
     L.nchunks = (int)((Pv + 31) / 32);
     L.counters = 256;                                         // key and flags first
-    L.geo = L.counters + align256(sizeof(unsigned) * 6 * (size_t)q.Bsrc);
+    L.geo = L.counters + align256(sizeof(unsigned) * 5 * (size_t)q.Bsrc);
     L.pose8 = L.geo + align256(sizeof(int4) * kGeoVec * poses);
     L.reach = L.pose8 + align256(2 * sizeof(float4) * poses);
     L.masks = L.reach + align256(sizeof(ReachGeo) * poses);
@@ -1853,11 +1840,11 @@ Layout layout(const Params &q, bool cubic) {
         L.itemcap = (int)(nbr * kParts + L.vol_entries / kListChunk + 1);
         L.lcount = L.binning;
         L.lbrick = L.lcount + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * kParts);
-        L.litems = L.lbrick + align256(sizeof(int4) * (size_t)q.Bsrc * nbr);
-        L.llist = L.litems + align256(sizeof(int4) * 2 * (size_t)q.Bsrc * L.itemcap);
+        L.litems = L.lbrick + align256(sizeof(int2) * (size_t)q.Bsrc * nbr);
+        L.llist = L.litems + align256(sizeof(int4) * (size_t)q.Bsrc * L.itemcap);
         L.lkey = L.llist + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
         L.lblock = L.lkey + align256(sizeof(int2) * (size_t)(L.vol_entries * q.Bsrc));
-        L.total = L.lblock + align256(sizeof(int4) * (size_t)q.Bsrc * ((nbr + kSumBlock - 1) / kSumBlock));
+        L.total = L.lblock + align256(sizeof(int2) * (size_t)q.Bsrc * ((nbr + kSumBlock - 1) / kSumBlock));
     }
     return L;
 }
@@ -1876,11 +1863,11 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.hits = reinterpret_cast<int *>(base + L.hits);
     sc.units = reinterpret_cast<int4 *>(base + L.units);
     sc.lcount = L.lcount ? reinterpret_cast<unsigned *>(base + L.lcount) : nullptr;
-    sc.lbrick = L.lbrick ? reinterpret_cast<int4 *>(base + L.lbrick) : nullptr;
+    sc.lbrick = L.lbrick ? reinterpret_cast<int2 *>(base + L.lbrick) : nullptr;
     sc.litems = L.litems ? reinterpret_cast<int4 *>(base + L.litems) : nullptr;
     sc.llist = L.llist ? reinterpret_cast<unsigned *>(base + L.llist) : nullptr;
     sc.lkey = L.lkey ? reinterpret_cast<int2 *>(base + L.lkey) : nullptr;
-    sc.lblock = L.lblock ? reinterpret_cast<int4 *>(base + L.lblock) : nullptr;
+    sc.lblock = L.lblock ? reinterpret_cast<int2 *>(base + L.lblock) : nullptr;
     sc.nchunks = L.nchunks;
     sc.itemcap = L.itemcap;
     return sc;
@@ -1946,7 +1933,7 @@ dim3 main_grid(const Params &q, const void *kern, size_t smem) {
     return dim3((unsigned)per, 1, (unsigned)q.Bsrc);
 }
 
-// Blocks of a kernel whose warps take work items on their own (the octant
+// Blocks of a kernel whose warps take work items on their own (the list-fed
 // scatters): every resident block, shared out over the volumes.
 dim3 warp_grid(const Params &q, const void *kern, int threads, size_t smem) {
     int dev = 0, sms = 148, per_sm = 1;

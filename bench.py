@@ -673,9 +673,9 @@ def run_ours(args):
             # per step: the forward with the L2 term (pose geometry, brick masks,
             # unit plan, gather with the zero fill as its prologue: 4) and the
             # volume-gradient call (geometry, masks, plan: 3; the sample lists
-            # of this step's poses: begin, count, sums, scan, items, fill: 6;
-            # the scatter: 1); plus three memsets
-            "gpu_launches": 14 * args.steps,
+            # of this step's poses: begin, count, sums, items, fill: 5; the
+            # scatter: 1), as the step's ncu launch list shows
+            "gpu_launches": 13 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu_line,
         }
