@@ -4,24 +4,33 @@
 // A 2D half-spectrum of box M (M x (M/2+1) complex) is small enough that a
 // thread block can hold its Friedel-completed "virtual" plane -- F(n) = V[n]
 // for n_x >= 0, conj(V[-n]) for n_x < 0, zero outside the stored range
-// [ar §2 "التمرير الأمامي"; ko §2 "Friedel 대칭성 처리"] -- over every
-// position a stencil can reach while touching the stored range.  Every
-// sample then reads its taps from shared memory on one branch-free path.
+// [ar §2 "التمرير الأمامي"; ko §2 "Friedel 대칭성 처리"] -- over the stored
+// columns and a strip of the Friedel side.  Every sample then reads its taps
+// from shared memory on one branch-free path.
 //
-//  - Layout.  The plane covers n in [X0, X0 + W)^2 with X0 = -(M/2 + 4) and W
-//    the next multiple of 4 of M + 8, so a stencil (taps floor(p) - LO ..
-//    floor(p) + HI) that leaves the region lies wholly outside the stored
-//    range and reads zero.  It is cut into 4 x 4 tiles of 16 complex words
-//    (one 128-byte row of banks): element (x, y) sits in bank pair
+//  - Half plane.  The plane covers columns n_x in [-4, WX - 4) (WX the next
+//    multiple of 4 of M/2 + 8) and rows n_y in [Y0, Y0 + WY) (Y0 = -(M/2 + 4),
+//    WY the next multiple of 4 of M + 8), so a stencil (taps floor(p) - LO ..
+//    floor(p) + HI) with p_x >= -2 that leaves the region lies wholly outside
+//    the stored range and reads zero.  A sample with p_x < -2 is taken at -p:
+//    all its taps lie at n_x <= -1, where F(n) = conj(F(-n)) holds by
+//    construction, and the stencil weights are even, so S(p) = conj(S(-p))
+//    and dS/dp(p) = -conj(dS/dp(-p)) exactly; its mirror's taps all lie at
+//    n_x >= 1, away from the stored n_x = 0 column, which need not be
+//    Hermitian.
+//  - Layout.  The plane is cut into 4 x 4 tiles of 16 complex words (one
+//    128-byte row of banks): element (x, y) sits in bank pair
 //    (x mod 4) + 4 (y mod 4).  For cubic, lane L visits its 16 taps in its own
 //    order -- at step (sx, sy) the tap in bank pair ((sx + L) mod 4) +
 //    4 ((sy + L / 4) mod 4) -- so the 16 lanes of a half-warp never share a
 //    bank pair and every 64-bit load takes the minimum two wavefronts.
-//  - Staging.  A block copies the raw stored image into a second shared
-//    buffer with 16-byte (else 8-byte) cp.async, then unpacks it into the
-//    tiled virtual plane, conjugating the Friedel side.  The copy of the
-//    block's NEXT source image is issued before the current one is used, so
-//    it lands while the block computes.
+//  - Staging.  A block holds two planes.  Each stored element of a source is
+//    copied straight to its place in the tiled plane with an 8-byte
+//    cp.async; once it landed, the three Friedel columns n_x = -1, -2, -3 are
+//    filled from the plane itself.  Every other word is zero for every source
+//    and is cleared once, at the start.  The copy of the block's NEXT source
+//    image goes into the other plane before the current one is used, so it
+//    lands while the block computes.
 //  - Work.  The poses of each source image are cut into items; a persistent
 //    block takes a contiguous range of items (consecutive items mostly share
 //    their source, which then stays staged).  Threads take output pixels in
@@ -57,12 +66,16 @@ namespace {
 constexpr int kPlaneThreads = 512;
 constexpr int kPlaneWarps = kPlaneThreads / 32;
 
-// Geometry of the staged virtual plane of a box-M source.
+// Geometry of the staged half plane of a box-M source.
+constexpr int kPlaneX0 = -4;      // virtual column of local column 0
+constexpr float kMirror = -2.0f;  // samples with p_x below this are taken at -p
+
 struct PlaneGeo {
     int M, half, Xs;   // source box, M/2, M/2 + 1
-    int X0;            // virtual coordinate of local index 0 (both axes)
-    int W;             // local extent (both axes), a multiple of 4
-    int TW;            // tiles per row (W / 4)
+    int Y0;            // virtual row of local row 0
+    int WX, WY;        // local extents, multiples of 4
+    int TWX;           // tiles per row (WX / 4)
+    int words;         // complex words of one plane (WX * WY)
     int raw_words;     // complex words of one stored source image (M * Xs)
 };
 
@@ -71,9 +84,11 @@ __host__ __device__ inline PlaneGeo plane_geo(int M) {
     g.M = M;
     g.half = M / 2;
     g.Xs = M / 2 + 1;
-    g.X0 = -(M / 2 + 4);
-    g.W = ((M + 8) + 3) & ~3;
-    g.TW = g.W / 4;
+    g.Y0 = -(M / 2 + 4);
+    g.WX = ((M / 2 + 8) + 3) & ~3;
+    g.WY = ((M + 8) + 3) & ~3;
+    g.TWX = g.WX / 4;
+    g.words = g.WX * g.WY;
     g.raw_words = M * g.Xs;
     return g;
 }
@@ -83,18 +98,16 @@ __host__ __device__ inline PlaneGeo plane_geo(int M) {
 // aligned.
 __host__ __device__ inline int table_words(int N) { return (N + N / 2 + 1 + 1) & ~1; }
 
-// Shared memory of a launch: the plane, the phase tables and, for the
-// gathers, the raw buffer of the next source image (16-byte aligned: W^2 and
-// the table words are even).
-__host__ __device__ inline size_t plane_smem_bytes(int M, int N, bool raw) {
+// Shared memory of a launch: two planes and the phase tables (16-byte
+// aligned: the plane words are a multiple of 16).
+__host__ __device__ inline size_t plane_smem_bytes(int M, int N) {
     const PlaneGeo g = plane_geo(M);
-    return sizeof(float2) * ((size_t)g.W * g.W + (size_t)table_words(N) +
-                             (raw ? (size_t)g.raw_words : 0));
+    return sizeof(float2) * (2 * (size_t)g.words + (size_t)table_words(N));
 }
 
 // Tiled index of local element (lx, ly).
 __device__ __forceinline__ int tidx(const PlaneGeo &g, int lx, int ly) {
-    return ((ly >> 2) * g.TW + (lx >> 2)) * 16 + (lx & 3) + 4 * (ly & 3);
+    return ((ly >> 2) * g.TWX + (lx >> 2)) * 16 + (lx & 3) + 4 * (ly & 3);
 }
 
 // Quotient and remainder of e by d (e < 2^24, inv = 1/d rounded) without an
@@ -113,51 +126,43 @@ __device__ __forceinline__ int divmod(int e, int d, float inv, int &rem) {
     return quo;
 }
 
-// Issue the copy of one stored source image (raw_words complex words at src)
-// into the raw buffer and commit it as one group.
-__device__ __forceinline__ void issue_raw_copy(const float2 *src, int words, float2 *raw,
-                                               bool vec16) {
-    const unsigned sbase = (unsigned)__cvta_generic_to_shared(raw);
-    if (vec16) {
-        // words is even (M even), so the image is a whole number of 16-byte chunks.
-        const int chunks = words >> 1;
-        for (int c = threadIdx.x; c < chunks; c += kPlaneThreads)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16u * c),
-                         "l"(src + 2 * c)
+// Issue the copy of one stored source image (raw_words complex words at src,
+// row-major M x Xs) into plane: element (r, x) goes to virtual (x, y) with
+// y = r for r < M/2, r - M above.  One commit group.
+__device__ __forceinline__ void issue_plane_copy(const PlaneGeo &g, const float2 *src,
+                                                 float2 *plane, unsigned *dbg) {
+    const unsigned sbase = (unsigned)__cvta_generic_to_shared(plane);
+    int r, x;
+    r = divmod(threadIdx.x, g.Xs, 1.0f / (float)g.Xs, x);
+    const int dq = kPlaneThreads / g.Xs, dr = kPlaneThreads - dq * g.Xs;
+    for (int e = threadIdx.x; e < g.raw_words; e += kPlaneThreads) {
+        const int y = r < g.half ? r : r - g.M;
+        const int at = tidx(g, x - kPlaneX0, y - g.Y0);
+        if (TP_CHECK(dbg, at >= 0 && at < g.words, 1))
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(sbase + 8u * at),
+                         "l"(src + e)
                          : "memory");
-    } else {
-        for (int c = threadIdx.x; c < words; c += kPlaneThreads)
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(sbase + 8u * c),
-                         "l"(src + c)
-                         : "memory");
+        x += dr;
+        r += dq;
+        if (x >= g.Xs) {
+            x -= g.Xs;
+            ++r;
+        }
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
-// Fill the tiled virtual plane from the raw stored image: direct side
-// n_x >= 0 reads V[n], Friedel side conj(V[-n]); zero outside the stored
-// range.  Half-warps take whole 4 x 4 tiles, so their writes are 16
-// consecutive words.
-__device__ __forceinline__ void unpack_plane(const PlaneGeo &g, const float2 *raw, float2 *plane,
-                                             unsigned *dbg) {
-    const int ntiles = g.TW * g.TW;
-    const float inv = 1.0f / (float)g.TW;
-    for (int t = threadIdx.x >> 4; t < ntiles; t += kPlaneThreads >> 4) {
-        int tx;
-        const int ty = divmod(t, g.TW, inv, tx);
-        const int r = threadIdx.x & 15;
-        const int vx = g.X0 + 4 * tx + (r & 3), vy = g.X0 + 4 * ty + (r >> 2);
-        const bool cj = vx < 0;
-        const int mx = cj ? -vx : vx, my = cj ? -vy : vy;
-        float2 v = make_float2(0.f, 0.f);
-        if (mx <= g.half && row_ok(my, g.half)) {
-            const int at = wrap_row(my, g.M) * g.Xs + mx;
-            if (TP_CHECK(dbg, at >= 0 && at < g.raw_words, 0)) {
-                v = raw[at];
-                if (cj) v.y = -v.y;
-            }
-        }
-        plane[16 * t + r] = v;
+// The Friedel columns n_x = -1, -2, -3 of a landed plane: F(n) = conj(F(-n)),
+// for the rows whose mirror -n_y is stored (-M/2 < n_y <= M/2); the other
+// rows of these columns stay zero.
+__device__ __forceinline__ void friedel_columns(const PlaneGeo &g, float2 *plane, unsigned *dbg) {
+    for (int i = threadIdx.x; i < 3 * g.M; i += kPlaneThreads) {
+        const int c = i / g.M;
+        const int nx = -1 - c, ny = i - c * g.M - g.half + 1;   // ny in (-M/2, M/2]
+        const int from = tidx(g, -nx - kPlaneX0, -ny - g.Y0), to = tidx(g, nx - kPlaneX0, ny - g.Y0);
+        if (!TP_CHECK(dbg, from >= 0 && from < g.words && to >= 0 && to < g.words, 1)) continue;
+        const float2 v = plane[from];
+        plane[to] = make_float2(v.x, -v.y);
     }
 }
 
@@ -206,7 +211,7 @@ __device__ __forceinline__ void gather_plane(const PlaneGeo &g, const LaneRes &r
                                              float2 &S, float2 (&dS)[2], unsigned *dbg) {
     S = make_float2(0.f, 0.f);
     dS[0] = dS[1] = S;
-    const int total = g.W * g.W;
+    const int total = g.words;
     if constexpr (CUBIC) {
         const int lane = threadIdx.x & 31;
         const int cx = (lane - lx) & 3, cy = ((lane >> 2) - ly) & 3;
@@ -221,7 +226,7 @@ __device__ __forceinline__ void gather_plane(const PlaneGeo &g, const LaneRes &r
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             ox[i] = ((lx + 3 - res.rx[i]) >> 2) * 16 + res.rx[i];
-            oy[i] = ((ly + 3 - res.ry[i]) >> 2) * (16 * g.TW) + 4 * res.ry[i];
+            oy[i] = ((ly + 3 - res.ry[i]) >> 2) * (16 * g.TWX) + 4 * res.ry[i];
         }
 #pragma unroll
         for (int sy = 0; sy < 4; ++sy) {
@@ -275,42 +280,52 @@ __device__ __forceinline__ int image_of(const Params &q, int v, int j) {
     return (q.Bsrc == 1) ? j : v * q.P + j;
 }
 
-// Stencil of the pixel (kx, ky) of pose ps: local tap origin and weights.
+// Stencil of the pixel (kx, ky) of pose ps: local tap origin and weights,
+// at -p when p_x < kMirror (mir; the caller conjugates what it gathers).
 // Returns false when the stencil leaves the staged region, i.e. lies wholly
 // outside the stored range.
 template <bool CUBIC, bool DERIV>
 __device__ __forceinline__ bool stencil_at(const PlaneGeo &g, const Pose<2> &ps, int kx, int ky,
-                                           int &lx, int &ly, float (&w)[2][4], float (&d)[2][4]) {
+                                           int &lx, int &ly, bool &mir, float (&w)[2][4],
+                                           float (&d)[2][4]) {
     using St = Stencil<CUBIC>;
     float t;
-    const float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)ky);
-    const float py = fmaf(ps.a[1], (float)kx, ps.b[1] * (float)ky);
-    lx = split_coord(px, t) - St::LO - g.X0;
+    float px = fmaf(ps.a[0], (float)kx, ps.b[0] * (float)ky);
+    float py = fmaf(ps.a[1], (float)kx, ps.b[1] * (float)ky);
+    mir = px < kMirror;
+    if (mir) {
+        px = -px;
+        py = -py;
+    }
+    lx = split_coord(px, t) - St::LO - kPlaneX0;
     St::weights(t, w[0]);
     if (DERIV) St::derivs(t, d[0]);
-    ly = split_coord(py, t) - St::LO - g.X0;
+    ly = split_coord(py, t) - St::LO - g.Y0;
     St::weights(t, w[1]);
     if (DERIV) St::derivs(t, d[1]);
-    const unsigned lim = (unsigned)(g.W - (St::LO + St::HI + 1));
-    return (unsigned)lx <= lim && (unsigned)ly <= lim;
+    constexpr int span = St::LO + St::HI + 1;
+    return (unsigned)lx <= (unsigned)(g.WX - span) && (unsigned)ly <= (unsigned)(g.WY - span);
 }
 
 template <bool CUBIC, bool GRAD>
 __global__ void __launch_bounds__(kPlaneThreads, 1)
-    k_plane2d(Params q, Items it, bool vec16, float2 *__restrict__ out,
+    k_plane2d(Params q, Items it, float2 *__restrict__ out,
               const float2 *__restrict__ g_out, float *__restrict__ grad_rot,
               float *__restrict__ grad_shift) {
     extern __shared__ float4 s_plane4[];
     __shared__ float s_red[kPlaneWarps][6];
     const PlaneGeo g = plane_geo(q.M);
-    float2 *plane = reinterpret_cast<float2 *>(s_plane4);
-    float2 *phx = plane + (size_t)g.W * g.W;
+    float2 *planes = reinterpret_cast<float2 *>(s_plane4);   // two planes
+    float2 *phx = planes + 2 * (size_t)g.words;
     float2 *phy = phx + q.Xo;
-    float2 *raw = phx + table_words(q.N);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int first = (int)((long long)it.count * blockIdx.x / gridDim.x);
     const int last = (int)((long long)it.count * (blockIdx.x + 1) / gridDim.x);
     if (first >= last) return;
+    // The words no copy writes are zero for every source: clear both planes once.
+    for (int i = threadIdx.x; i < g.words; i += kPlaneThreads)   // 2 planes = g.words float4
+        s_plane4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
     const int npix = q.N * q.Xo;
     const LaneRes res = lane_residues();
     // Pixel e = threadIdx.x + k * kPlaneThreads as (row, column), advanced
@@ -318,21 +333,27 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
     int iy0, kx0;
     iy0 = divmod(threadIdx.x, q.Xo, 1.0f / (float)q.Xo, kx0);
     const int dq = kPlaneThreads / q.Xo, dr = kPlaneThreads - dq * q.Xo;
-    int staged = -1;   // source held in the plane
-    issue_raw_copy(q.src + (size_t)(first / it.per_src) * q.src_stride, g.raw_words, raw, vec16);
+    int staged = -1;   // source held in plane `cur`
+    int cur = 0;       // plane receiving (then holding) the next source
+    issue_plane_copy(g, q.src + (size_t)(first / it.per_src) * q.src_stride, planes, q.dbg);
+    const float2 *plane = planes;
     for (int i = first; i < last; ++i) {
         const int v = i / it.per_src;
         if (v != staged) {
+            // Sources come in increasing order and the copy in flight is
+            // always the next one's, into plane `cur`.
             asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-            __syncthreads();   // raw landed for every thread; the plane is free
-            unpack_plane(g, raw, plane, q.dbg);
+            __syncthreads();   // landed for every thread; the other plane is no longer read
+            friedel_columns(g, planes + (size_t)cur * g.words, q.dbg);
+            plane = planes + (size_t)cur * g.words;
             staged = v;
-            __syncthreads();   // plane complete; raw free again
-            // Prefetch the next different source while this one is used.
+            __syncthreads();   // plane complete
+            // Prefetch the next different source into the other plane.
             for (int k = i + 1; k < last; ++k)
                 if (k / it.per_src != v) {
-                    issue_raw_copy(q.src + (size_t)(k / it.per_src) * q.src_stride, g.raw_words,
-                                   raw, vec16);
+                    cur ^= 1;
+                    issue_plane_copy(g, q.src + (size_t)(k / it.per_src) * q.src_stride,
+                                     planes + (size_t)cur * g.words, q.dbg);
                     break;
                 }
         }
@@ -369,9 +390,16 @@ __global__ void __launch_bounds__(kPlaneThreads, 1)
                 if (GRAD) gv = __ldg(g_out + ob + e);   // in flight during the gather
                 float w[2][4], d[2][4];
                 int lx, ly;
+                bool mir;
                 float2 S = make_float2(0.f, 0.f), dS[2] = {S, S};
-                if (stencil_at<CUBIC, GRAD>(g, ps, rx, ky, lx, ly, w, d))
+                if (stencil_at<CUBIC, GRAD>(g, ps, rx, ky, lx, ly, mir, w, d)) {
                     gather_plane<CUBIC, GRAD>(g, res, plane, lx, ly, w, d, S, dS, q.dbg);
+                    if (mir) {   // S(p) = conj(S(-p)), dS/dp(p) = -conj(dS/dp(-p))
+                        S.y = -S.y;
+                        dS[0].x = -dS[0].x;
+                        dS[1].x = -dS[1].x;
+                    }
+                }
                 const float2 ph = q.shift ? cmul(phx[rx], phy[ry]) : make_float2(1.f, 0.f);
                 if (!GRAD) {
                     out[ob + e] = cmul(ph, S);
@@ -443,15 +471,14 @@ template <bool CUBIC, bool GRAD>
 cudaError_t plane_launch(const Params &q, float2 *out, const float2 *g, float *grot, float *gshift,
                          cudaStream_t st) {
     if ((long long)q.B * q.P == 0) return cudaSuccess;
-    const size_t smem = plane_smem_bytes(q.M, q.N, true);
+    const size_t smem = plane_smem_bytes(q.M, q.N);
     auto kern = k_plane2d<CUBIC, GRAD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const Items it = make_items(q, sms);
     const int blocks = it.count < sms ? it.count : sms;
-    const bool vec16 = (reinterpret_cast<uintptr_t>(q.src) & 15) == 0 && (q.src_stride & 1) == 0;
-    kern<<<blocks, kPlaneThreads, smem, st>>>(q, it, vec16, out, g, grot, gshift);
+    kern<<<blocks, kPlaneThreads, smem, st>>>(q, it, out, g, grot, gshift);
     return cudaGetLastError();
 }
 
@@ -463,7 +490,7 @@ bool plane2d_fits(int M, int N) {
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return false;
     // The static reduction array and a margin for the runtime's own use.
-    return plane_smem_bytes(M, N, true) + 1024 <= (size_t)optin;
+    return plane_smem_bytes(M, N) + 1024 <= (size_t)optin;
 }
 
 cudaError_t launch_plane2d_project(bool cubic, const Params &q, float2 *out, cudaStream_t st) {

@@ -485,14 +485,14 @@ def test_dense_3d_volume_gradient(tp, interp):
 
 
 # ---------------------------------------------------------------------------
-# The 2D operators stage the whole Friedel-completed source plane in shared
-# memory when it fits (sources up to box 132 on a 227 KB block) and fall back to the
-# per-sample kernels above that.  These cases cover both sides of the limit,
-# a source pointer that is only 8-byte aligned (the staging copies 8 bytes at
-# a time then), a shared source whose many poses are cut into work items,
-# and several poses per source image.
+# The 2D operators stage two Friedel-completed half planes of the source in
+# shared memory when they fit (sources up to box 152 on a 227 KB block) and
+# fall back to the per-sample kernels above that.  These cases cover both
+# sides of the limit, a source pointer that is only 8-byte aligned, a shared
+# source whose many poses are cut into work items, and several poses per
+# source image.
 @pytest.mark.parametrize("M,N,s", [(128, 64, 0.5), (130, 130, 1.0), (132, 96, 0.7),
-                                   (134, 134, 1.0), (256, 64, 0.25)])
+                                   (152, 152, 1.0), (154, 120, 0.8), (256, 64, 0.25)])
 @pytest.mark.parametrize("interp", ["linear", "cubic"])
 def test_2d_staged_plane_limits(tp, M, N, s, interp):
     rng = np.random.default_rng(M + N)
