@@ -131,7 +131,7 @@ struct Scratch {
     int2 *lbrick;         // [Bsrc][bricks] samples and items, then their sums before
     int4 *litems;         // [Bsrc][itemcap] items: (first entry, count, brick, part box)
     unsigned *llist;      // B*P*plane entries: output pixel index (b * P + p) * plane + row * Xo + kx
-    int2 *lkey;           // B*P*plane: each in-radius pixel's key and place in the key's list
+    unsigned *lrank;      // B*P*plane: each in-radius pixel's place in its key's list
     int2 *lblock;         // [Bsrc][brick blocks] the sums of k_list_sums' blocks
     int nchunks;          // 32-pose chunks per volume
     int itemcap;          // items per volume and kind
@@ -1151,9 +1151,48 @@ __global__ void k_list_begin(Scratch sc) {
 // time, the lanes of each run of equal keys (a key that recurs after a gap
 // starts another run): the run's first lane adds its length to the key's
 // count with one atomic, whose result places the run in the key's list, and
-// every pixel keeps its key and its place for the fill.  The atomics of
-// kListChunks chunks are issued before their results are used.
+// every pixel keeps its place for the fill (which recomputes the key).  The
+// atomics of kListChunks chunks are issued before their results are used.
 constexpr int kListChunks = 4;
+
+// One image row of the list passes: its first pixel, last in-radius kx,
+// the pose record and the key offset of its volume.  False when the row
+// lies wholly outside the radius.
+struct ListRow {
+    unsigned e0;        // output index of the row's pixel kx = 0
+    int xmax;           // last kx with kx^2 + ky^2 <= r2max
+    float4 A;           // pose record (a, b0)
+    float by[3];        // b qy, rounded first as in pose8_position
+    int vkey;           // key offset of the row's volume
+};
+
+__device__ __forceinline__ bool list_row(const Params &q, const Scratch &sc, int nb, int row,
+                                         ListRow &r) {
+    const int bp = row / q.N, iy = row - bp * q.N;
+    const int qy = row_freq(iy, q.N);
+    const int rr = q.r2max - qy * qy;
+    if (rr < 0) return false;
+    // The last kx with kx^2 + ky^2 <= r2max (sqrtf corrected to the exact bound).
+    int xmax = (int)sqrtf((float)rr);
+    if ((xmax + 1) * (xmax + 1) <= rr) ++xmax;
+    if (xmax * xmax > rr) --xmax;
+    r.xmax = min(xmax, q.Xo - 1);
+    r.e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
+    r.A = __ldg(sc.pose8 + 2 * bp);
+    const float4 Bv = __ldg(sc.pose8 + 2 * bp + 1);
+    r.vkey = (q.Bsrc == 1) ? 0 : (bp / q.P) * (nb * nb * nb * kParts);
+    r.by[0] = r.A.w * (float)qy;
+    r.by[1] = Bv.x * (float)qy;
+    r.by[2] = Bv.y * (float)qy;
+    return true;
+}
+
+// The key of pixel kx = f of the row (f a float holding kx).
+__device__ __forceinline__ int row_key(const int *__restrict__ tab, int nb, const ListRow &r,
+                                       float f) {
+    const float p[3] = {fmaf(r.A.x, f, r.by[0]), fmaf(r.A.y, f, r.by[1]), fmaf(r.A.z, f, r.by[2])};
+    return sample_key(tab, nb, r.vkey, p);
+}
 
 __global__ void __launch_bounds__(256) k_list_count(Params q, int nb, Scratch sc) {
     if (sc.lflag[1] == 0u) return;
@@ -1163,22 +1202,11 @@ __global__ void __launch_bounds__(256) k_list_count(Params q, int nb, Scratch sc
     const int lane = threadIdx.x & 31;
     const int rows = q.B * q.P * q.N;
     const unsigned upto = (2u << lane) - 1u;   // lanes 0 .. lane
-    const int nbr16 = nb * nb * nb * kParts;
     for (int row = (blockIdx.x * 256 + threadIdx.x) >> 5; row < rows; row += (gridDim.x * 256) >> 5) {
-        const int bp = row / q.N, iy = row - bp * q.N;
-        const int qy = row_freq(iy, q.N);
-        const int rr = q.r2max - qy * qy;
-        if (rr < 0) continue;
-        // The last kx with kx^2 + ky^2 <= r2max (sqrtf corrected to the exact bound).
-        int xmax = (int)sqrtf((float)rr);
-        if ((xmax + 1) * (xmax + 1) <= rr) ++xmax;
-        if (xmax * xmax > rr) --xmax;
-        xmax = min(xmax, q.Xo - 1);
-        const unsigned e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
-        const float4 A = __ldg(sc.pose8 + 2 * bp), Bv = __ldg(sc.pose8 + 2 * bp + 1);
-        const int vkey = (q.Bsrc == 1) ? 0 : (bp / q.P) * nbr16;
-        // p = a qx + (b qy), as in pose8_position (b qy rounded first).
-        const float by0 = A.w * (float)qy, by1 = Bv.x * (float)qy, by2 = Bv.y * (float)qy;
+        ListRow R;
+        if (!list_row(q, sc, nb, row, R)) continue;
+        const int xmax = R.xmax;
+        const unsigned e0 = R.e0;
         float fx = (float)lane;
         for (int xb = 0; xb <= xmax; xb += 32 * kListChunks, fx += 32.0f * kListChunks) {
             int key[kListChunks], leader[kListChunks];
@@ -1187,11 +1215,7 @@ __global__ void __launch_bounds__(256) k_list_count(Params q, int nb, Scratch sc
             for (int k = 0; k < kListChunks; ++k) {
                 const int qx = xb + 32 * k + lane;
                 key[k] = -1;
-                if (qx <= xmax) {
-                    const float f = fx + 32.0f * k;
-                    const float p[3] = {fmaf(A.x, f, by0), fmaf(A.y, f, by1), fmaf(A.z, f, by2)};
-                    key[k] = sample_key(s_tab, nb, vkey, p);
-                }
+                if (qx <= xmax) key[k] = row_key(s_tab, nb, R, fx + 32.0f * k);
                 const int prev = __shfl_up_sync(0xffffffffu, key[k], 1);
                 const unsigned starts = __ballot_sync(0xffffffffu, lane == 0 || key[k] != prev);
                 leader[k] = 31 - __clz(starts & upto);
@@ -1204,44 +1228,46 @@ __global__ void __launch_bounds__(256) k_list_count(Params q, int nb, Scratch sc
             for (int k = 0; k < kListChunks; ++k) {
                 const unsigned rank = __shfl_sync(0xffffffffu, at[k], leader[k]) + (unsigned)(lane - leader[k]);
                 const int qx = xb + 32 * k + lane;
-                if (qx <= xmax) sc.lkey[e0 + qx] = make_int2(key[k], (int)rank);
+                if (qx <= xmax && key[k] >= 0) sc.lrank[e0 + qx] = rank;
             }
         }
     }
 }
 
 // The fill pass (the counts are the parts' first entries now): every
-// in-radius pixel with a key is written at its key's first entry plus its
-// place.  A warp takes one image row, 32 pixels at a time.
-__global__ void __launch_bounds__(256) k_list_fill(Params q, Scratch sc) {
+// in-radius pixel with a key -- recomputed exactly as the count pass formed
+// it -- is written at its key's first entry plus its place.  A warp takes one
+// image row, 32 pixels at a time.
+__global__ void __launch_bounds__(256) k_list_fill(Params q, int nb, Scratch sc) {
     if (sc.lflag[1] == 0u) return;
+    extern __shared__ int s_tab[];
+    key_tables(s_tab, nb);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int rows = q.B * q.P * q.N;
     const unsigned entries = (unsigned)q.B * (unsigned)q.P * (unsigned)q.plane;
     for (int row = (blockIdx.x * 256 + threadIdx.x) >> 5; row < rows; row += (gridDim.x * 256) >> 5) {
-        const int bp = row / q.N, iy = row - bp * q.N;
-        const int qy = row_freq(iy, q.N);
-        const int rr = q.r2max - qy * qy;
-        if (rr < 0) continue;
-        int xmax = (int)sqrtf((float)rr);
-        if ((xmax + 1) * (xmax + 1) <= rr) ++xmax;
-        if (xmax * xmax > rr) --xmax;
-        xmax = min(xmax, q.Xo - 1);
-        const unsigned e0 = (unsigned)bp * (unsigned)q.plane + (unsigned)iy * (unsigned)q.Xo;
+        ListRow R;
+        if (!list_row(q, sc, nb, row, R)) continue;
+        const int xmax = R.xmax;
+        const unsigned e0 = R.e0;
         // kListChunks chunks at a time: their loads are all in flight before
         // the first store.
-        for (int xb = lane; xb <= xmax; xb += 32 * kListChunks) {
-            int2 kr[kListChunks];
-            unsigned first[kListChunks];
-#pragma unroll
-            for (int k = 0; k < kListChunks; ++k)
-                kr[k] = xb + 32 * k <= xmax ? __ldg(sc.lkey + e0 + xb + 32 * k) : make_int2(-1, 0);
-#pragma unroll
-            for (int k = 0; k < kListChunks; ++k) first[k] = kr[k].x >= 0 ? __ldg(sc.lcount + kr[k].x) : 0u;
+        float fx = (float)lane;
+        for (int xb = lane; xb <= xmax; xb += 32 * kListChunks, fx += 32.0f * kListChunks) {
+            int key[kListChunks];
+            unsigned rank[kListChunks], first[kListChunks];
 #pragma unroll
             for (int k = 0; k < kListChunks; ++k) {
-                const unsigned at = first[k] + (unsigned)kr[k].y;
-                if (kr[k].x >= 0 && TP_CHECK(q.dbg, at < entries, 8)) sc.llist[at] = e0 + (unsigned)(xb + 32 * k);
+                key[k] = xb + 32 * k <= xmax ? row_key(s_tab, nb, R, fx + 32.0f * k) : -1;
+                rank[k] = key[k] >= 0 ? __ldg(sc.lrank + e0 + xb + 32 * k) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < kListChunks; ++k) first[k] = key[k] >= 0 ? __ldg(sc.lcount + key[k]) : 0u;
+#pragma unroll
+            for (int k = 0; k < kListChunks; ++k) {
+                const unsigned at = first[k] + rank[k];
+                if (key[k] >= 0 && TP_CHECK(q.dbg, at < entries, 8)) sc.llist[at] = e0 + (unsigned)(xb + 32 * k);
             }
         }
     }
@@ -1810,7 +1836,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t counters, geo, pose8, reach, masks, hits, units, binning;   // the binning
-    size_t lcount, lbrick, litems, llist, lkey, lblock, total;        // + the sample lists
+    size_t lcount, lbrick, litems, llist, lrank, lblock, total;       // + the sample lists
     int nb, nchunks, itemcap;
     long long vol_entries;   // list entries per volume (its images' pixels)
 };
@@ -1834,7 +1860,7 @@ Layout layout(const Params &q, bool cubic) {
     L.binning = L.units + align256(sizeof(int4) * (size_t)q.Bsrc * nbr * L.nchunks);
     L.vol_entries = Pv * (long long)q.N * (q.N / 2 + 1);
     L.itemcap = 0;
-    L.lcount = L.lbrick = L.litems = L.llist = L.lkey = L.lblock = 0;
+    L.lcount = L.lbrick = L.litems = L.llist = L.lrank = L.lblock = 0;
     L.total = L.binning;
     {
         L.itemcap = (int)(nbr * kParts + L.vol_entries / kListChunk + 1);
@@ -1842,8 +1868,8 @@ Layout layout(const Params &q, bool cubic) {
         L.lbrick = L.lcount + align256(sizeof(unsigned) * (size_t)q.Bsrc * nbr * kParts);
         L.litems = L.lbrick + align256(sizeof(int2) * (size_t)q.Bsrc * nbr);
         L.llist = L.litems + align256(sizeof(int4) * (size_t)q.Bsrc * L.itemcap);
-        L.lkey = L.llist + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
-        L.lblock = L.lkey + align256(sizeof(int2) * (size_t)(L.vol_entries * q.Bsrc));
+        L.lrank = L.llist + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
+        L.lblock = L.lrank + align256(sizeof(unsigned) * (size_t)(L.vol_entries * q.Bsrc));
         L.total = L.lblock + align256(sizeof(int2) * (size_t)q.Bsrc * ((nbr + kSumBlock - 1) / kSumBlock));
     }
     return L;
@@ -1866,7 +1892,7 @@ Scratch scratch_in(void *ws, const Layout &L) {
     sc.lbrick = L.lbrick ? reinterpret_cast<int2 *>(base + L.lbrick) : nullptr;
     sc.litems = L.litems ? reinterpret_cast<int4 *>(base + L.litems) : nullptr;
     sc.llist = L.llist ? reinterpret_cast<unsigned *>(base + L.llist) : nullptr;
-    sc.lkey = L.lkey ? reinterpret_cast<int2 *>(base + L.lkey) : nullptr;
+    sc.lrank = L.lrank ? reinterpret_cast<unsigned *>(base + L.lrank) : nullptr;
     sc.lblock = L.lblock ? reinterpret_cast<int2 *>(base + L.lblock) : nullptr;
     sc.nchunks = L.nchunks;
     sc.itemcap = L.itemcap;
@@ -1990,12 +2016,14 @@ cudaError_t build_lists(const Params &q, const Layout &L, const Scratch &sc, cud
     if (blocks == 0) return cudaGetLastError();
     const size_t tab = sizeof(int) * 3 * (16 * L.nb + 2);
     if ((e = cudaFuncSetAttribute(k_list_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab)) !=
-        cudaSuccess)
+            cudaSuccess ||
+        (e = cudaFuncSetAttribute(k_list_fill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab)) !=
+            cudaSuccess)
         return e;
     k_list_count<<<blocks, 256, tab, st>>>(q, L.nb, sc);
     k_list_sums<<<dim3((unsigned)((nbr + kSumBlock - 1) / kSumBlock), (unsigned)q.Bsrc), kSumBlock, 0, st>>>(nbr, sc);
     k_list_items<<<8 * bricks, 256, 0, st>>>(nbr, sc, q.Bsrc, L.vol_entries);
-    k_list_fill<<<blocks, 256, 0, st>>>(q, sc);
+    k_list_fill<<<blocks, 256, tab, st>>>(q, L.nb, sc);
     return cudaGetLastError();
 }
 

@@ -93,10 +93,6 @@ __host__ __device__ inline PlaneGeo plane_geo(int M) {
     return g;
 }
 
-// Complex words of the phase tables of one pose (N/2 + 1 column and N row
-// factors), rounded up to an even count so that what follows stays 16-byte
-// aligned.
-__host__ __device__ inline int table_words(int N) { return (N + N / 2 + 1 + 1) & ~1; }
 
 // Shared memory of a launch: two planes and the phase tables (16-byte
 // aligned: the plane words are a multiple of 16).
@@ -163,20 +159,6 @@ __device__ __forceinline__ void friedel_columns(const PlaneGeo &g, float2 *plane
         if (!TP_CHECK(dbg, from >= 0 && from < g.words && to >= 0 && to < g.words, 1)) continue;
         const float2 v = plane[from];
         plane[to] = make_float2(v.x, -v.y);
-    }
-}
-
-// The two factors of the shift phase of one pose: phx[kx] = exp(-2 pi i kx sx / N)
-// for kx = 0 .. N/2 and phy[iy] = exp(-2 pi i ky(iy) sy / N) for iy = 0 .. N-1,
-// each from the exactly period-reduced cycle count (frac_cycles).
-__device__ __forceinline__ void phase_tables(const Params &q, float sx, float sy, float2 *phx,
-                                             float2 *phy) {
-    for (int i = threadIdx.x; i < q.N + q.Xo; i += kPlaneThreads) {
-        const bool col = i < q.Xo;
-        const int k = col ? i : row_freq(i - q.Xo, q.N);
-        float sn, cs;
-        sincospif(-2.0f * frac_cycles(k, col ? sx : sy, q.fN, q.invN), &sn, &cs);
-        (col ? phx[i] : phy[i - q.Xo]) = make_float2(cs, sn);
     }
 }
 

@@ -38,8 +38,11 @@ namespace {
 // several samples per round, one at a time in a round where two of their
 // stencils meet (stencils_meet).  The tile is then added to the stored
 // half-spectrum with one vector atomic per touched word (Friedel positions
-// conjugated at -n).
+// conjugated at -n).  With a shift (and N <= kMaxTableN) the block first
+// tabulates the two separable factors of the pose's phase, and a sample
+// multiplies two entries instead of evaluating a sine and a cosine.
 constexpr int kTile = 16;
+constexpr int kMaxTableN = 1024;
 constexpr int kTileWarps = 4;
 constexpr int kSplit = 4;   // blocks per image: shorter blocks, a smaller last wave
 constexpr float kTileMargin = 0.01f;
@@ -78,7 +81,8 @@ struct Queue2 {
 template <bool CUBIC>
 __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                                                                     const float2 *__restrict__ img,
-                                                                    float2 *__restrict__ dst) {
+                                                                    float2 *__restrict__ dst,
+                                                                    bool tables) {
     using T = Tile2<CUBIC>;
     using St = Stencil<CUBIC>;
     extern __shared__ float4 s_t2[];
@@ -120,6 +124,9 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
     const float2 *gimg = img + (size_t)bp * q.plane;
     float2 *V = dst + (q.Bsrc == 1 ? (size_t)0 : (size_t)b * q.src_stride);
     const float sx = ps.sx, sy = ps.sy;
+    float2 *phx = reinterpret_cast<float2 *>(reinterpret_cast<char *>(s_t2) + kTileWarps * T::WARP_BYTES);
+    float2 *phy = phx + q.Xo;
+    if (tables) phase_tables(q, sx, sy, phx, phy);   // read after the barrier below
 
     for (int e = lane; e < T::ELEMS * T::COPIES; e += 32) acc[e] = make_float2(0.f, 0.f);
     float2 *const mytile = acc + (T::COPIES == 2 ? (lane >> 4) * T::ELEMS : 0);   // this half-warp's tile
@@ -229,7 +236,10 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                         const int iy = qyr < 0 ? qyr + q.N : qyr;
                         const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo, 7);
                         float2 cv = in ? __ldg(gimg + iy * q.Xo + qx) : make_float2(0.f, 0.f);
-                        if (q.shift) cv = cmul_conj_a(shift_phase(qx, qyr, sx, sy, q.fN, q.invN), cv);
+                        if (q.shift && in)
+                            cv = cmul_conj_a(tables ? cmul(phx[qx], phy[iy])
+                                                    : shift_phase(qx, qyr, sx, sy, q.fN, q.invN),
+                                             cv);
                         float wy[4];
                         rot4(w[0], (lane - l0) & 3, wx);
                         rot4(w[1], ((lane >> 2) - l1) & 3, wy);
@@ -261,7 +271,10 @@ __global__ void __launch_bounds__(32 * kTileWarps) k_scatter2d_tiles(Params q,
                     const int iy = qyr < 0 ? qyr + q.N : qyr;
                     const bool in = TP_CHECK(q.dbg, iy >= 0 && iy < q.N && qx >= 0 && qx < q.Xo, 7);
                     float2 cv = in ? __ldg(gimg + iy * q.Xo + qx) : make_float2(0.f, 0.f);
-                    if (q.shift) cv = cmul_conj_a(shift_phase(qx, qyr, sx, sy, q.fN, q.invN), cv);
+                    if (q.shift && in)
+                        cv = cmul_conj_a(tables ? cmul(phx[qx], phy[iy])
+                                                : shift_phase(qx, qyr, sx, sy, q.fN, q.invN),
+                                         cv);
                     float *wq = Q.w[slot];
 #pragma unroll
                     for (int j = 0; j < St::TAPS; ++j) {
@@ -338,11 +351,12 @@ cudaError_t launch_scatter2d_tiles(const Params &q, const float2 *img, float2 *d
     using T = Tile2<CUBIC>;
     const long long images = (long long)q.B * q.P;
     if (images == 0) return cudaSuccess;
-    const size_t smem = kTileWarps * T::WARP_BYTES;
+    const bool tables = q.shift && q.N <= kMaxTableN;
+    const size_t smem = kTileWarps * T::WARP_BYTES + (tables ? sizeof(float2) * table_words(q.N) : 0);
     auto kern = k_scatter2d_tiles<CUBIC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(images * kSplit), 32 * kTileWarps, smem, st>>>(q, img, dst);
+    kern<<<(unsigned)(images * kSplit), 32 * kTileWarps, smem, st>>>(q, img, dst, tables);
     return cudaGetLastError();
 }
 

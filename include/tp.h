@@ -332,7 +332,7 @@ tp_status tp_hermitian_x0(float *spec, float *weight, int B, int N, int dim, voi
  * B (Bv is 1 or B), P poses per batch element, volume box Nv, image box N
  * and the interpolation of opts: enough for every 3D entry point on these
  * sizes (the backward uses it for both of its passes).  This includes
- * 12 bytes per output pixel (B * P * N * (N/2+1)) for the scatters' sample
+ * 8 bytes per output pixel (B * P * N * (N/2+1)) for the scatters' sample
  * lists.  Returns 0 for invalid sizes.
  */
 size_t tp_workspace_bytes(int Bv, int B, int P, int Nv, int N, tp_options opts);

@@ -126,3 +126,51 @@ def test_l2_box256_step_sampled(tp):
     ys, ds = tp.tp_project_3d_2d_save(dv, dR, dt, **kw)
     gs_r, _ = tp.tp_project_3d_2d_backward_saved(g, ys, ds, dR, dt, **kw)
     assert rel(host(gr), host(gs_r)) <= ATOMIC_TOL
+
+
+@pytest.mark.parametrize("interp,Bv", [("cubic", 1), ("linear", 1), ("cubic", 2)])
+def test_l2_forward_and_volume_gradient_share_a_workspace(tp, interp, Bv):
+    """The benchmark's pattern: the L2 forward and the volume gradient on one
+    workspace, which keeps the binning and the sample lists between calls.  The
+    volume gradient is compared with the oracle after: a forward and a backward
+    on the same poses; a second backward (lists kept); a forward on other poses
+    followed by a backward on the first ones (binning and lists rebuilt); a
+    forward on the poses whose lists are held; two forwards and a backward on
+    new poses."""
+    rng = np.random.default_rng(321 + Bv)
+    M = N = 32
+    P = 6
+    vol = crandn(rng, (Bv, M, M, M // 2 + 1))
+    R1 = synth.random_rotations(Bv * P, rng).reshape(Bv, P, 3, 3)
+    R2 = synth.random_rotations(Bv * P, rng).reshape(Bv, P, 3, 3)
+    t = rng.uniform(-3, 3, (Bv, P, 2)).astype(np.float32)
+    target = crandn(rng, (Bv, P, N, N // 2 + 1))
+    g = crandn(rng, (Bv, P, N, N // 2 + 1))
+    kw = dict(interp=interp, radius=-1.0)
+    ws = torch.zeros(tp.tp_workspace_bytes(Bv, Bv, P, M, interp, N), dtype=torch.uint8,
+                     device="cuda")
+    dv, dt, dT, dg = dev(vol), dev(t), dev(target), dev(g)
+
+    def ref(R):
+        return oracle.project_backward(3, g, vol, R, shift=t, need_rot=False,
+                                       need_shift=False, **kw)[0]
+
+    def backward(R):
+        gv, _, _ = tp.tp_project_3d_2d_backward(dg, dv, dev(R), dt, want_rot=False,
+                                                want_shift=False, workspace=ws, **kw)
+        return host(gv)
+
+    def forward(R):
+        tp.tp_project_3d_2d_l2(dv, dev(R), dt, dT, workspace=ws, **kw)
+
+    ref1, ref2 = ref(R1), ref(R2)
+    forward(R1)
+    assert rel(backward(R1), ref1) <= ATOMIC_TOL
+    assert rel(backward(R1), ref1) <= ATOMIC_TOL
+    forward(R2)
+    assert rel(backward(R1), ref1) <= ATOMIC_TOL
+    forward(R1)
+    assert rel(backward(R1), ref1) <= ATOMIC_TOL
+    forward(R2)
+    forward(R2)
+    assert rel(backward(R2), ref2) <= ATOMIC_TOL
