@@ -1641,6 +1641,47 @@ __global__ void __launch_bounds__(32 * OctLayout<WEIGHTS>::WARPS, OctLayout<WEIG
         __syncwarp();
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0] - 1, y0 = ob.o[1] - 1, z0 = ob.o[2] - 1;
+        if (x0 >= 0 || x0 + kOS - 1 < 0) {
+            // Every word on one side of n_x = 0 (all but the parts at the
+            // origin column): each lane takes four (x, y) columns of the tile,
+            // whose layer offsets and stored (x, y) positions it forms once,
+            // and walks them up the z layers.
+            const int sg = x0 >= 0 ? 1 : -1;   // -1: Friedel side, conjugated at -n
+            int toff[4], woff[4], gyx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = lane + 32 * j;
+                const int lx = c % kOS, ly = c / kOS;
+                const int tl = (ly >> 2) * (kCT / 4) + (lx >> 2), in = 4 * (ly & 3) + (lx & 3);
+                toff[j] = c < kOS * kOS ? tl * 16 + in : -1;
+                woff[j] = tl * 32 + in;
+                const int nx = sg * (x0 + lx), ny = sg * (y0 + ly);
+                gyx[j] = nx <= half && row_ok(ny, half) ? wrap_row(ny, q.M) * q.Xs + nx : -1;
+            }
+            for (int lz = 0; lz < OL::SZ; ++lz) {
+                const int nz = sg * (z0 + lz);
+                const bool zok = row_ok(nz, half);
+                const size_t zrow = (size_t)wrap_row(zok ? nz : 0, q.M) * q.M * q.Xs;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (toff[j] < 0) continue;
+                    const int k = lz * kCLayer + toff[j];
+                    const int kw = (lz >> 1) * kCWPair + woff[j] + 16 * (lz & 1);
+                    const float2 cv = acc[k];
+                    const float wv = WEIGHTS ? wacc[kw] : 0.f;
+                    if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
+                    acc[k] = make_float2(0.f, 0.f);
+                    if (WEIGHTS) wacc[kw] = 0.f;
+                    if (!zok || gyx[j] < 0) continue;
+                    const size_t idx = zrow + (size_t)gyx[j];
+                    if (!TP_CHECK(q.dbg, idx < (size_t)q.M * q.M * q.Xs, 6)) continue;
+                    if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, sg * cv.y));
+                    if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         for (int e = lane; e < kOS * kOS * OL::SZ; e += 32) {
             const int lx = e % kOS, ly = (e / kOS) % kOS, lz = e / (kOS * kOS);
             const int tl = (ly >> 2) * (kCT / 4) + (lx >> 2), in = 4 * (ly & 3) + (lx & 3);
