@@ -1841,6 +1841,42 @@ __global__ void __launch_bounds__(32 * LinLayout<WEIGHTS>::WARPS, 8)
         }
         // Fold the tile into the stored half-spectrum and clear it.
         const int x0 = ob.o[0], y0 = ob.o[1], z0 = ob.o[2];
+        if (x0 >= 0 || x0 + kLS - 1 < 0) {
+            // Every word on one side of n_x = 0: by (x, y) columns, as in
+            // the cubic scatter (three columns a lane).
+            const int sg = x0 >= 0 ? 1 : -1;   // -1: Friedel side, conjugated at -n
+            int toff[3], gyx[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int c = lane + 32 * j;
+                const int lx = c % kLS, ly = c / kLS;
+                toff[j] = c < kLS * kLS ? ly * kLPX + lx : -1;
+                const int nx = sg * (x0 + lx), ny = sg * (y0 + ly);
+                gyx[j] = nx <= half && row_ok(ny, half) ? wrap_row(ny, q.M) * q.Xs + nx : -1;
+            }
+            for (int lz = 0; lz < kLZ; ++lz) {
+                const int nz = sg * (z0 + lz);
+                const bool zok = row_ok(nz, half);
+                const size_t zrow = (size_t)wrap_row(zok ? nz : 0, q.M) * q.M * q.Xs;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    if (toff[j] < 0) continue;
+                    const int k = lz * kLPY * kLPX + toff[j];
+                    const float2 cv = acc[k];
+                    const float wv = WEIGHTS ? wacc[k] : 0.f;
+                    if (cv.x == 0.f && cv.y == 0.f && wv == 0.f) continue;
+                    acc[k] = make_float2(0.f, 0.f);
+                    if (WEIGHTS) wacc[k] = 0.f;
+                    if (!zok || gyx[j] < 0) continue;
+                    const size_t idx = zrow + (size_t)gyx[j];
+                    if (!TP_CHECK(q.dbg, idx < (size_t)q.M * q.M * q.Xs, 6)) continue;
+                    if (cv.x != 0.f || cv.y != 0.f) atomicAdd(Vd + idx, make_float2(cv.x, sg * cv.y));
+                    if (Wd && wv != 0.f) atomicAdd(Wd + idx, wv);
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         for (int e = lane; e < kLS * kLS * kLZ; e += 32) {
             const int lx = e % kLS, ly = (e / kLS) % kLS, lz = e / (kLS * kLS);
             const int k = (lz * kLPY + ly) * kLPX + lx;
